@@ -1,0 +1,247 @@
+/*
+ * thd_attn.h -- C ABI of libthdattn.so: causal softmax attention over packed
+ * variable-length THD tensors, decomposed the way P2P (ring) context
+ * parallelism decomposes it, with every CP rank emulated on one GPU.
+ *
+ * Sources (web pages), cited by page and section:
+ *   [P1] TransformerEngine issue #2208, "thd format is not supported with
+ *        hierarchical CP implementation yet" (traceback through
+ *        AttnFuncWithCPAndKVP2P; maintainer reply on P2P vs A2A).
+ *   [P2] TransformerEngine issue #3487, "THD P2P context-parallel regression
+ *        when padded cu_seqlens are value-equal but not object-identical"
+ *        ("Describe the bug", "Steps/Code to reproduce bug",
+ *        "Expected behavior").
+ *   [P3] "Hybrid / Hierarchical Context Parallel Skill" ("Contraintes
+ *        requises": seq_length % (2 * context_parallel_size) == 0;
+ *        "Pitfalls" item 5).
+ *
+ * Conventions for every entry point
+ *   - THD layout: tensor [T, H, D] is row-major and contiguous, token-major:
+ *     element (t, h, d) at ((t * H) + h) * D + d.  bf16 tensors are passed
+ *     as `void*` to 2-byte IEEE bfloat16 storage.
+ *   - cu_seqlens (int32, B+1 entries, cu[0] == 0) are exclusive prefix sums of
+ *     the VALID lengths L_b.  cu_seqlens_padded (int32, B+1, may be NULL) are
+ *     the buffer offsets: sequence b's valid tokens sit at rows
+ *     [pad[b], pad[b] + L_b) and rows [pad[b] + L_b, pad[b+1]) are pad.
+ *     NULL means no padding (pad = cu).
+ *   - Each padded length P_b must be divisible by 2 * cp_size [P3
+ *     "Contraintes requises"]; chunk length cb = P_b / (2 cp_size); emulated
+ *     rank r owns chunks r and 2 cp_size - 1 - r.
+ *   - All pointers are DEVICE pointers owned by the caller; the library never
+ *     allocates device memory and never synchronises the host.  All work is
+ *     enqueued on `stream` (a cudaStream_t; NULL = legacy default stream).
+ *   - Return value: a host-side status (THD_OK or THD_ERR_*) for argument
+ *     errors found without reading device memory, and launch failures.
+ *   - Metadata errors can only be seen on the device (cu_seqlens live in
+ *     device memory).  The first kernel of each call writes `*dev_status`
+ *     (int32, device): 0 when the metadata is valid, else a THD_DEV_*
+ *     code; every later kernel of the call reads it and returns without
+ *     touching the outputs when it is nonzero.  Read it after the stream has
+ *     synchronised.  Kernels that give up a bounded wait write
+ *     THD_ERR_TIMEOUT there.
+ *   - Workspace: caller-provided device memory of at least
+ *     thd_workspace_size(...) bytes, 256-byte aligned; its contents need not be
+ *     initialised and are not meaningful after the call.
+ *   - Nothing is captured across calls except read-only state (driver entry
+ *     points, per-device attributes); calls are safe to capture in a CUDA
+ *     graph as long as the pointers stay valid.
+ */
+#ifndef THD_ATTN_H
+#define THD_ATTN_H
+
+#include <stddef.h>
+#include <stdint.h>
+
+#ifdef __cplusplus
+extern "C" {
+#endif
+
+typedef struct CUstream_st* thd_stream_t; /* identical to cudaStream_t */
+
+#if defined(__GNUC__)
+#define THD_API __attribute__((visibility("default")))
+#else
+#define THD_API
+#endif
+
+/* host-side status codes */
+#define THD_OK 0
+#define THD_ERR_INVALID_ARG 1 /* null pointer, bad size, misaligned pointer */
+#define THD_ERR_UNSUPPORTED 2 /* head_dim not 64/128, unsupported mode */
+#define THD_ERR_CUDA 3        /* a CUDA call or launch failed */
+#define THD_ERR_TIMEOUT 4     /* (device) a bounded wait gave up */
+#define THD_ERR_WORKSPACE 5   /* workspace too small or misaligned */
+
+/* device-side status codes written to *dev_status */
+#define THD_DEV_ERR_NONZERO_START 101  /* cu_seqlens[0] or padded[0] != 0 */
+#define THD_DEV_ERR_NOT_MONOTONE 102   /* negative length */
+#define THD_DEV_ERR_VALID_GT_PAD 103   /* L_b > P_b */
+#define THD_DEV_ERR_NOT_DIVISIBLE 104  /* P_b % (2 cp_size) != 0 */
+#define THD_DEV_ERR_EXCEEDS_BUF 105    /* pad[B] larger than the buffer rows */
+#define THD_DEV_ERR_CAUSAL_LENGTHS 106 /* causal with q and kv lengths differing */
+#define THD_DEV_ERR_CAPACITY 107       /* internal schedule capacity exceeded */
+
+/* Kernel identifiers for the profiling hook. */
+#define THD_KERNEL_PLAN 1
+#define THD_KERNEL_FWD 2
+#define THD_KERNEL_BWD_PREP 3
+#define THD_KERNEL_BWD 4
+#define THD_KERNEL_BWD_DQ 5
+#define THD_KERNEL_LSE_MERGE 6
+#define THD_KERNEL_TAIL_ZERO 7
+#define THD_KERNEL_PARTITION 8
+
+/* Human-readable text for any status above (host or device). Never NULL. */
+THD_API const char* thd_status_string(int status);
+
+/* Library ABI version (major * 100 + minor). */
+THD_API int thd_version(void);
+
+/*
+ * Bytes of workspace thd_attn_fwd (for_bwd = 0) or thd_attn_bwd (for_bwd = 1)
+ * needs for these sizes.  T_q / T_kv are the buffer rows of q and k/v.
+ * Returns 0 for invalid sizes.
+ */
+THD_API size_t thd_workspace_size(int B, int64_t T_q, int64_t T_kv, int Hq, int Hkv, int D, int cp_size, int for_bwd);
+
+/*
+ * thd_cp_partition -- per-rank cu_seqlens for THD + P2P context parallelism,
+ * for every emulated rank in ONE launch.
+ *
+ * [P2 "Describe the bug"] names the helper get_cu_seqlens_on_cp_rank, which
+ * the padded path calls once per ring step; [P3 "Contraintes requises"]
+ * fixes the 2*cp_size split.  For rank r and sequence b, with
+ * cb = P_b / (2 cp_size):
+ *     v1 = clamp(L_b - r cb, 0, cb)                (valid rows of chunk r)
+ *     v2 = clamp(L_b - (2 cp_size - 1 - r) cb, 0, cb)
+ *     cu_rank[r][b+1]        = cu_rank[r][b] + v1 + v2
+ *     cu_rank_padded[r][b]   = pad[b] / cp_size
+ *     cu_rank_half[r][0][b+1] = cu_rank_half[r][0][b] + v1
+ *     cu_rank_half[r][1][b+1] = cu_rank_half[r][1][b] + v2
+ *     token_map[r * (T / cp_size) + p] = global padded row of rank-local row p
+ *       (rank-local rows of sequence b: chunk r then chunk 2cp-1-r), T = pad[B].
+ * Arguments:
+ *   cu_seqlens [B+1], cu_seqlens_padded [B+1] or NULL: device int32.
+ *   pad_between_seqs: -1 decide from VALUES (padded iff some entry differs,
+ *     never by pointer identity [P2 "Expected behavior"]), 0 ignore the
+ *     padded array, 1 use it.
+ *   cu_rank, cu_rank_padded: [cp_size][B+1] int32; cu_rank_half
+ *     [cp_size][2][B+1] int32; token_map [token_map_capacity] int32.  Any
+ *     output may be NULL (not written).  token_map needs capacity >= pad[B]
+ *     (else THD_DEV_ERR_EXCEEDS_BUF).
+ *   dev_status: device int32, always written.
+ * Bit-exact (integer).
+ */
+THD_API int thd_cp_partition(const int32_t* cu_seqlens, const int32_t* cu_seqlens_padded, int B, int cp_size,
+                     int pad_between_seqs, int32_t* cu_rank, int32_t* cu_rank_padded, int32_t* cu_rank_half,
+                     int32_t* token_map, int64_t token_map_capacity, int32_t* dev_status, thd_stream_t stream);
+
+/*
+ * thd_attn_fwd -- O = softmax(scale q k^T + mask) v per sequence and head,
+ * and lse = logsumexp of the masked scaled scores (natural log).
+ *
+ * Decomposition [P1 traceback: AttnFuncWithCPAndKVP2P; P3 "Contraintes
+ * requises"]: work is split per emulated rank r (local query rows = chunk r
+ * then chunk 2cp-1-r of each sequence) and ring step i, where rank r
+ * holds the KV of rank s = (r - i) mod cp_size; per-step partials are merged
+ * on chip by online-softmax (log-sum-exp) correction.  The merged result
+ * equals plain attention.  Causal uses the top-left mask (key position <=
+ * query position) and requires equal q and kv lengths per sequence.
+ *
+ *   q   [T_q, Hq, D] bf16;  k, v [T_kv, Hkv, D] bf16 (Hq % Hkv == 0; query
+ *       head h reads kv head h / (Hq/Hkv)).  16-byte aligned.
+ *   o   [T_q, Hq, D] bf16 output; lse [Hq, T_q] fp32 output.  Rows that hold
+ *       no valid token (pad rows and rows [pad_q[B], T_q)) get o = 0 and
+ *       lse = -inf.
+ *   D: 64 or 128.  causal: 1 (causal) or 0 (full).  softmax_scale > 0.
+ *   cp_size >= 1: the emulated CP degree.  pad_between_seqs as in
+ *   thd_cp_partition (decided per side from values when -1).
+ *   Pad rows inside tiles are read: they must hold finite values.
+ */
+THD_API int thd_attn_fwd(const void* q, const void* k, const void* v, void* o, float* lse, const int32_t* cu_seqlens_q,
+                 const int32_t* cu_seqlens_kv, const int32_t* cu_seqlens_q_padded,
+                 const int32_t* cu_seqlens_kv_padded, int B, int64_t T_q, int64_t T_kv, int Hq, int Hkv, int D,
+                 int causal, float softmax_scale, int cp_size, int pad_between_seqs, void* workspace,
+                 size_t workspace_bytes, int32_t* dev_status, thd_stream_t stream);
+
+/*
+ * thd_attn_fwd_step -- the partial of ONE ring step, materialised: for every
+ * emulated rank r, the attention of its local queries against the KV it
+ * holds at step `step` (rank s = (r - step) mod cp_size), written in fp32 at
+ * the queries' global rows:
+ *   o_part [T_q, Hq, D] fp32, lse_part [Hq, T_q] fp32 (natural log).
+ * Rows that get no contribution at this step get o = 0, lse = -inf.  Merging
+ * the cp_size step partials with thd_lse_merge gives thd_attn_fwd's result
+ * (the ring with communication replaced by reads of rank s's rows).
+ * Other arguments as thd_attn_fwd.
+ */
+THD_API int thd_attn_fwd_step(const void* q, const void* k, const void* v, float* o_part, float* lse_part,
+                      const int32_t* cu_seqlens_q, const int32_t* cu_seqlens_kv, const int32_t* cu_seqlens_q_padded,
+                      const int32_t* cu_seqlens_kv_padded, int B, int64_t T_q, int64_t T_kv, int Hq, int Hkv,
+                      int D, int causal, float softmax_scale, int cp_size, int pad_between_seqs, int step,
+                      void* workspace, size_t workspace_bytes, int32_t* dev_status, thd_stream_t stream);
+
+/*
+ * thd_attn_bwd -- gradients of thd_attn_fwd w.r.t. q, k, v.
+ * [P2 "Steps/Code to reproduce bug"] runs forward/backward on this layout.
+ *   q, k, v, o (forward output), dout: bf16 as in thd_attn_fwd; lse [Hq, T_q]
+ *   fp32 from thd_attn_fwd.
+ *   dq [dq_rows, Hq, D], dk/dv [dkv_rows, Hkv, D] bf16 outputs, with
+ *   dq_rows >= T_q and dkv_rows >= T_kv.  Every row without a valid token,
+ *   including the slack rows [pad[B], rows), is written with 0 (the THD
+ *   gradient tail-zero of [P2 "Describe the bug"], done on the device with
+ *   no extra launch and no work when there is no slack).
+ * dK/dV of each kv head sum over its query-head group.  dQ is accumulated in
+ * fp32 with atomic adds, so its rounding may differ between runs.
+ */
+THD_API int thd_attn_bwd(const void* q, const void* k, const void* v, const void* o, const float* lse, const void* dout,
+                 void* dq, void* dk, void* dv, int64_t dq_rows, int64_t dkv_rows, const int32_t* cu_seqlens_q,
+                 const int32_t* cu_seqlens_kv, const int32_t* cu_seqlens_q_padded,
+                 const int32_t* cu_seqlens_kv_padded, int B, int64_t T_q, int64_t T_kv, int Hq, int Hkv, int D,
+                 int causal, float softmax_scale, int cp_size, int pad_between_seqs, void* workspace,
+                 size_t workspace_bytes, int32_t* dev_status, thd_stream_t stream);
+
+/*
+ * thd_lse_merge -- in place: (o_acc, lse_acc) <- merge((o_acc, lse_acc),
+ * (o_part, lse_part)), the ring's per-step output correction
+ * [P1 traceback].  Per (t, h), with a = lse_acc, b = lse_part:
+ *     lse = max(a, b) + log1p(exp(-|a - b|))
+ *     o   = exp(a - lse) o_acc + exp(b - lse) o_part
+ * A side with lse = -inf contributes nothing; both -inf give (0, -inf).
+ *   o_acc, o_part [T, H, D] fp32; lse_acc, lse_part [H, T] fp32; 16-byte
+ *   aligned.  D a multiple of 4.
+ */
+THD_API int thd_lse_merge(float* o_acc, float* lse_acc, const float* o_part, const float* lse_part, int64_t T, int H,
+                  int D, thd_stream_t stream);
+
+/*
+ * thd_grad_tail_zero -- zero gradient rows past the last padded endpoint:
+ * rows [cu_seqlens_q_padded[B], dq_rows) of dq and [cu_seqlens_kv_padded[B],
+ * dkv_rows) of dk and dv (bf16, [rows, H, D]).  [P2 "Describe the bug"]:
+ * the THD tail-zero; [P2 "Expected behavior"]: no work when the valid
+ * endpoint equals the buffer end.  The endpoint is read ON THE DEVICE (no
+ * host sync, graph-safe); when the caller already knows there is no tail
+ * (host_knows_no_tail = 1) nothing is launched.  Any of dq/dk/dv may be NULL.
+ */
+THD_API int thd_grad_tail_zero(void* dq, void* dk, void* dv, int64_t dq_rows, int64_t dkv_rows, int Hq, int Hkv, int D,
+                       const int32_t* cu_seqlens_q_padded, const int32_t* cu_seqlens_kv_padded, int B,
+                       int host_knows_no_tail, thd_stream_t stream);
+
+/*
+ * Profiling hook (not needed for normal use): while enabled for `kernel_id`
+ * (a THD_KERNEL_* value), every launch of that kernel is bracketed by a pair
+ * of CUDA events recorded on its stream, up to `max_records` launches.
+ * thd_profile_read synchronises those events and returns the durations in
+ * milliseconds (oldest first) and their number.  kernel_id 0 disables.
+ */
+THD_API int thd_profile_enable(int kernel_id, int max_records);
+THD_API int thd_profile_read(float* ms_out, int max_out, int* count_out);
+
+/* Number of kernels this library has launched in this process. */
+THD_API uint64_t thd_launch_count(void);
+
+#ifdef __cplusplus
+}
+#endif
+
+#endif /* THD_ATTN_H */

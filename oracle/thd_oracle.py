@@ -323,6 +323,39 @@ def attn_bwd(q, k, v, do, cu_seqlens_q, cu_seqlens_kv, cu_seqlens_q_padded=None,
     return dq, dk, dv
 
 
+def attn_fwd_rows(q, k, v, cu_seqlens_q, cu_seqlens_kv, cu_seqlens_q_padded, cu_seqlens_kv_padded, b: int,
+                  h: int, positions, causal: bool = True, softmax_scale: float | None = None,
+                  pad_between_seqs: int = -1):
+    """The same definition as ``attn_fwd`` for a few query positions of one
+    sequence b and query head h only (so that full-size workloads can be
+    checked on samples).  Returns (O [n, D], lse [n]); positions at or past
+    the valid length give (0, -inf)."""
+    q, k, v = np.asarray(q), np.asarray(k), np.asarray(v)
+    Hq, D = q.shape[1], q.shape[2]
+    G = Hq // k.shape[1]
+    scale = 1.0 / math.sqrt(D) if softmax_scale is None else float(softmax_scale)
+    cu_q, cu_kv = _as_int_list(cu_seqlens_q), _as_int_list(cu_seqlens_kv)
+    pq = effective_padded(cu_q, cu_seqlens_q_padded, pad_between_seqs)
+    pkv = effective_padded(cu_kv, cu_seqlens_kv_padded, pad_between_seqs)
+    Lq, Lkv = cu_q[b + 1] - cu_q[b], cu_kv[b + 1] - cu_kv[b]
+    K = _f64(k[pkv[b]:pkv[b] + Lkv, h // G])
+    V = _f64(v[pkv[b]:pkv[b] + Lkv, h // G])
+    pos = [int(x) for x in positions]
+    O = np.zeros((len(pos), D))
+    lse = np.full(len(pos), NEG_INF)
+    for n, i in enumerate(pos):
+        if i >= Lq:
+            continue
+        S = scale * (K @ _f64(q[pq[b] + i, h]))
+        if causal:
+            S[i + 1:] = NEG_INF
+        l = _logsumexp_rows(S[None, :])[0]
+        lse[n] = l
+        if np.isfinite(l):
+            O[n] = np.exp(S - l) @ V
+    return O, lse
+
+
 # ---------------------------------------------------------------------------
 # a5: LSE merge
 # ---------------------------------------------------------------------------

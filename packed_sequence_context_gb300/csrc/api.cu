@@ -1,0 +1,379 @@
+// Host side of the C ABI declared in include/thd_attn.h: argument checks that
+// need no device reads, workspace carving, TMA tensor maps, launches and the
+// profiling hook.  The host never reads device memory and never synchronises.
+#include <atomic>
+#include <cmath>
+#include <cstring>
+#include <mutex>
+#include <vector>
+
+#include <cudaTypedefs.h>
+
+#include "common.cuh"
+
+namespace thd {
+
+// ------------------------------------------------------------------ bookkeeping
+static std::atomic<uint64_t> g_launches{0};
+void count_launch() { g_launches.fetch_add(1, std::memory_order_relaxed); }
+
+int num_sms() {
+  static int cache[64] = {0};
+  int dev = 0;
+  if (cudaGetDevice(&dev) != cudaSuccess) return 1;
+  if (dev >= 0 && dev < 64 && cache[dev]) return cache[dev];
+  int n = 0;
+  cudaDeviceGetAttribute(&n, cudaDevAttrMultiProcessorCount, dev);
+  if (n <= 0) n = 1;
+  if (dev >= 0 && dev < 64) cache[dev] = n;
+  return n;
+}
+
+struct Prof {
+  std::mutex mu;
+  int kernel = 0;
+  int max = 0;
+  int n = 0;
+  std::vector<cudaEvent_t> ev;
+};
+static Prof g_prof;
+
+void prof_before(int id, cudaStream_t st) {
+  if (g_prof.kernel != id) return;
+  std::lock_guard<std::mutex> lk(g_prof.mu);
+  if (g_prof.kernel == id && g_prof.n < g_prof.max) cudaEventRecord(g_prof.ev[2 * g_prof.n], st);
+}
+void prof_after(int id, cudaStream_t st) {
+  if (g_prof.kernel != id) return;
+  std::lock_guard<std::mutex> lk(g_prof.mu);
+  if (g_prof.kernel == id && g_prof.n < g_prof.max) {
+    cudaEventRecord(g_prof.ev[2 * g_prof.n + 1], st);
+    ++g_prof.n;
+  }
+}
+
+// ------------------------------------------------------------------ tensor maps
+static PFN_cuTensorMapEncodeTiled_v12000 encode_fn() {
+  static PFN_cuTensorMapEncodeTiled_v12000 fn = nullptr;
+  static std::once_flag once;
+  std::call_once(once, [] {
+    void* p = nullptr;
+    cudaDriverEntryPointQueryResult q;
+    if (cudaGetDriverEntryPointByVersion("cuTensorMapEncodeTiled", &p, 12000, cudaEnableDefault, &q) ==
+            cudaSuccess &&
+        q == cudaDriverEntryPointSuccess)
+      fn = reinterpret_cast<PFN_cuTensorMapEncodeTiled_v12000>(p);
+  });
+  return fn;
+}
+
+// 3-D map over a [rows, H, D] bf16 THD tensor; box = 128 rows x 1 head x 64
+// columns (128 bytes, the 128B-swizzle width).  Rows past the end read as 0.
+static bool make_thd_map(CUtensorMap* m, const void* base, int64_t rows, int H, int D) {
+  auto enc = encode_fn();
+  if (!enc) return false;
+  cuuint64_t dims[3] = {(cuuint64_t)D, (cuuint64_t)H, (cuuint64_t)(rows > 0 ? rows : 1)};
+  cuuint64_t strides[2] = {(cuuint64_t)D * 2, (cuuint64_t)H * D * 2};
+  cuuint32_t box[3] = {64, 1, (cuuint32_t)kTile};
+  cuuint32_t es[3] = {1, 1, 1};
+  return enc(m, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 3, const_cast<void*>(base), dims, strides, box, es,
+             CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
+             CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
+}
+
+static bool aligned(const void* p, uintptr_t a) { return (reinterpret_cast<uintptr_t>(p) & (a - 1)) == 0; }
+
+static int check_sizes(int B, int64_t T_q, int64_t T_kv, int Hq, int Hkv, int D, int cp, int pad_mode) {
+  if (B < 1 || T_q < 0 || T_kv < 0 || Hq < 1 || Hkv < 1 || cp < 1 || cp > 1024) return THD_ERR_INVALID_ARG;
+  if (Hq % Hkv != 0) return THD_ERR_INVALID_ARG;
+  if (pad_mode < -1 || pad_mode > 1) return THD_ERR_INVALID_ARG;
+  if (T_q >= (int64_t)1 << 31 || T_kv >= (int64_t)1 << 31 || B >= (1 << 24)) return THD_ERR_INVALID_ARG;
+  if (D != 64 && D != 128) return THD_ERR_UNSUPPORTED;
+  return THD_OK;
+}
+
+static int check_ws(const void* ws, size_t ws_bytes, size_t need) {
+  if (need == 0) return THD_ERR_INVALID_ARG;
+  if (!ws || ws_bytes < need || !aligned(ws, 256)) return THD_ERR_WORKSPACE;
+  return THD_OK;
+}
+
+static PlanParams plan_params(const int32_t* cu_q, const int32_t* cu_kv, const int32_t* pad_q,
+                              const int32_t* pad_kv, int B, int cp, int causal, int pad_mode, int64_t rows_q,
+                              int64_t rows_kv, int mode, char* ws, const WsLayout& L, int32_t* dev_status) {
+  PlanParams p;
+  std::memset(&p, 0, sizeof(p));
+  p.cu_q = cu_q;
+  p.cu_kv = cu_kv;
+  p.pad_q = pad_q;
+  p.pad_kv = pad_kv;
+  p.B = B;
+  p.cp = cp;
+  p.causal = causal;
+  p.pad_mode = pad_mode;
+  p.rows_q = rows_q;
+  p.rows_kv = rows_kv;
+  p.mode = mode;
+  p.step_lo = 0;
+  p.step_hi = cp;
+  p.eff = reinterpret_cast<int32_t*>(ws + L.eff);
+  p.tile_off = reinterpret_cast<int32_t*>(ws + L.tile_off);
+  p.counters = reinterpret_cast<int32_t*>(ws + L.counters);
+  p.items = reinterpret_cast<int4*>(ws + L.items);
+  p.item_cap = L.item_cap;
+  p.dev_status = dev_status;
+  return p;
+}
+
+static int cuda_status(cudaError_t e) { return e == cudaSuccess ? THD_OK : THD_ERR_CUDA; }
+
+static int fwd_common(const void* q, const void* k, const void* v, void* o, float* lse, const int32_t* cu_q,
+                      const int32_t* cu_kv, const int32_t* pad_q, const int32_t* pad_kv, int B, int64_t T_q,
+                      int64_t T_kv, int Hq, int Hkv, int D, int causal, float scale, int cp, int pad_mode,
+                      int step, void* ws, size_t ws_bytes, int32_t* dev_status, cudaStream_t st) {
+  int rc = check_sizes(B, T_q, T_kv, Hq, Hkv, D, cp, pad_mode);
+  if (rc) return rc;
+  if (!q || !k || !v || !o || !lse || !cu_q || !cu_kv || !dev_status) return THD_ERR_INVALID_ARG;
+  if (!aligned(q, 16) || !aligned(k, 16) || !aligned(v, 16) || !aligned(o, 16) || !aligned(lse, 4))
+    return THD_ERR_INVALID_ARG;
+  if (!(scale > 0.f) || !std::isfinite(scale) || (causal != 0 && causal != 1)) return THD_ERR_INVALID_ARG;
+  if (step >= cp) return THD_ERR_INVALID_ARG;
+  const WsLayout L = ws_layout(B, T_q, T_kv, Hq, D, cp, false);
+  rc = check_ws(ws, ws_bytes, L.total);
+  if (rc) return rc;
+  char* w = static_cast<char*>(ws);
+  PlanParams pp = plan_params(cu_q, cu_kv, pad_q, pad_kv, B, cp, causal, pad_mode, T_q, T_kv, 1, w, L, dev_status);
+  if (step >= 0) {
+    pp.step_lo = step;
+    pp.step_hi = step + 1;
+  }
+  rc = cuda_status(launch_plan(pp, st));
+  if (rc) return rc;
+  CUtensorMap tk, tv;
+  if (!make_thd_map(&tk, k, T_kv, Hkv, D) || !make_thd_map(&tv, v, T_kv, Hkv, D)) return THD_ERR_CUDA;
+  FwdParams fp;
+  std::memset(&fp, 0, sizeof(fp));
+  fp.q = static_cast<const uint16_t*>(q);
+  fp.o = o;
+  fp.lse = lse;
+  fp.eff = pp.eff;
+  fp.items = pp.items;
+  fp.counters = pp.counters;
+  fp.dev_status = dev_status;
+  fp.B = B;
+  fp.Hq = Hq;
+  fp.Hkv = Hkv;
+  fp.cp = cp;
+  fp.causal = causal;
+  fp.T_q = T_q;
+  fp.scale_log2 = scale * 1.4426950408889634f;
+  fp.step_lo = pp.step_lo;
+  fp.step_hi = pp.step_hi;
+  const int64_t bound = (int64_t)L.item_cap * Hq;
+  const int grid = (int)(bound < num_sms() ? (bound > 0 ? bound : 1) : num_sms());
+  return cuda_status(launch_fwd(fp, tk, tv, D, step >= 0, grid, st));
+}
+
+}  // namespace thd
+
+using namespace thd;
+
+extern "C" {
+
+const char* thd_status_string(int s) {
+  switch (s) {
+    case THD_OK: return "ok";
+    case THD_ERR_INVALID_ARG: return "invalid argument";
+    case THD_ERR_UNSUPPORTED: return "unsupported configuration";
+    case THD_ERR_CUDA: return "CUDA error";
+    case THD_ERR_TIMEOUT: return "device wait timed out";
+    case THD_ERR_WORKSPACE: return "workspace too small or misaligned";
+    case THD_DEV_ERR_NONZERO_START: return "cu_seqlens must start at 0";
+    case THD_DEV_ERR_NOT_MONOTONE: return "cu_seqlens not monotone";
+    case THD_DEV_ERR_VALID_GT_PAD: return "valid length exceeds padded length";
+    case THD_DEV_ERR_NOT_DIVISIBLE: return "padded length not divisible by 2*cp_size";
+    case THD_DEV_ERR_EXCEEDS_BUF: return "sequences exceed the buffer rows";
+    case THD_DEV_ERR_CAUSAL_LENGTHS: return "causal attention needs equal q/kv lengths per sequence";
+    case THD_DEV_ERR_CAPACITY: return "internal schedule capacity exceeded";
+    default: return "unknown status";
+  }
+}
+
+int thd_version(void) { return 100; }
+
+size_t thd_workspace_size(int B, int64_t T_q, int64_t T_kv, int Hq, int Hkv, int D, int cp_size, int for_bwd) {
+  if (check_sizes(B, T_q, T_kv, Hq, Hkv, D, cp_size, -1) != THD_OK) return 0;
+  return ws_layout(B, T_q, T_kv, Hq, D, cp_size, for_bwd != 0).total;
+}
+
+int thd_cp_partition(const int32_t* cu_seqlens, const int32_t* cu_seqlens_padded, int B, int cp_size,
+                     int pad_between_seqs, int32_t* cu_rank, int32_t* cu_rank_padded, int32_t* cu_rank_half,
+                     int32_t* token_map, int64_t token_map_capacity, int32_t* dev_status, thd_stream_t stream) {
+  if (!cu_seqlens || !dev_status || B < 1 || cp_size < 1 || cp_size > 1024 || pad_between_seqs < -1 ||
+      pad_between_seqs > 1)
+    return THD_ERR_INVALID_ARG;
+  if (token_map && token_map_capacity < 0) return THD_ERR_INVALID_ARG;
+  PlanParams p;
+  std::memset(&p, 0, sizeof(p));
+  p.cu_q = cu_seqlens;
+  p.cu_kv = cu_seqlens;
+  p.pad_q = cu_seqlens_padded;
+  p.pad_kv = cu_seqlens_padded;
+  p.B = B;
+  p.cp = cp_size;
+  p.causal = 0;
+  p.pad_mode = pad_between_seqs;
+  p.rows_q = INT64_MAX;
+  p.rows_kv = INT64_MAX;
+  p.mode = 0;
+  p.cu_rank = cu_rank;
+  p.cu_rank_padded = cu_rank_padded;
+  p.cu_rank_half = cu_rank_half;
+  p.token_map = token_map;
+  p.token_map_cap = token_map_capacity;
+  p.dev_status = dev_status;
+  return cuda_status(launch_plan(p, reinterpret_cast<cudaStream_t>(stream)));
+}
+
+int thd_attn_fwd(const void* q, const void* k, const void* v, void* o, float* lse, const int32_t* cu_seqlens_q,
+                 const int32_t* cu_seqlens_kv, const int32_t* cu_seqlens_q_padded,
+                 const int32_t* cu_seqlens_kv_padded, int B, int64_t T_q, int64_t T_kv, int Hq, int Hkv, int D,
+                 int causal, float softmax_scale, int cp_size, int pad_between_seqs, void* workspace,
+                 size_t workspace_bytes, int32_t* dev_status, thd_stream_t stream) {
+  return fwd_common(q, k, v, o, lse, cu_seqlens_q, cu_seqlens_kv, cu_seqlens_q_padded, cu_seqlens_kv_padded, B, T_q,
+                    T_kv, Hq, Hkv, D, causal, softmax_scale, cp_size, pad_between_seqs, -1, workspace,
+                    workspace_bytes, dev_status, reinterpret_cast<cudaStream_t>(stream));
+}
+
+int thd_attn_fwd_step(const void* q, const void* k, const void* v, float* o_part, float* lse_part,
+                      const int32_t* cu_seqlens_q, const int32_t* cu_seqlens_kv, const int32_t* cu_seqlens_q_padded,
+                      const int32_t* cu_seqlens_kv_padded, int B, int64_t T_q, int64_t T_kv, int Hq, int Hkv,
+                      int D, int causal, float softmax_scale, int cp_size, int pad_between_seqs, int step,
+                      void* workspace, size_t workspace_bytes, int32_t* dev_status, thd_stream_t stream) {
+  if (step < 0) return THD_ERR_INVALID_ARG;
+  return fwd_common(q, k, v, o_part, lse_part, cu_seqlens_q, cu_seqlens_kv, cu_seqlens_q_padded,
+                    cu_seqlens_kv_padded, B, T_q, T_kv, Hq, Hkv, D, causal, softmax_scale, cp_size,
+                    pad_between_seqs, step, workspace, workspace_bytes, dev_status,
+                    reinterpret_cast<cudaStream_t>(stream));
+}
+
+int thd_attn_bwd(const void* q, const void* k, const void* v, const void* o, const float* lse, const void* dout,
+                 void* dq, void* dk, void* dv, int64_t dq_rows, int64_t dkv_rows, const int32_t* cu_seqlens_q,
+                 const int32_t* cu_seqlens_kv, const int32_t* cu_seqlens_q_padded,
+                 const int32_t* cu_seqlens_kv_padded, int B, int64_t T_q, int64_t T_kv, int Hq, int Hkv, int D,
+                 int causal, float softmax_scale, int cp_size, int pad_between_seqs, void* workspace,
+                 size_t workspace_bytes, int32_t* dev_status, thd_stream_t stream) {
+  cudaStream_t st = reinterpret_cast<cudaStream_t>(stream);
+  int rc = check_sizes(B, T_q, T_kv, Hq, Hkv, D, cp_size, pad_between_seqs);
+  if (rc) return rc;
+  if (!q || !k || !v || !o || !lse || !dout || !dq || !dk || !dv || !cu_seqlens_q || !cu_seqlens_kv || !dev_status)
+    return THD_ERR_INVALID_ARG;
+  if (!aligned(q, 16) || !aligned(k, 16) || !aligned(v, 16) || !aligned(o, 16) || !aligned(dout, 16) ||
+      !aligned(dq, 16) || !aligned(dk, 16) || !aligned(dv, 16) || !aligned(lse, 4))
+    return THD_ERR_INVALID_ARG;
+  if (dq_rows < T_q || dkv_rows < T_kv || dq_rows >= ((int64_t)1 << 31) || dkv_rows >= ((int64_t)1 << 31))
+    return THD_ERR_INVALID_ARG;
+  if (!(softmax_scale > 0.f) || !std::isfinite(softmax_scale) || (causal != 0 && causal != 1))
+    return THD_ERR_INVALID_ARG;
+  const WsLayout L = ws_layout(B, T_q, T_kv, Hq, D, cp_size, true);
+  rc = check_ws(workspace, workspace_bytes, L.total);
+  if (rc) return rc;
+  char* w = static_cast<char*>(workspace);
+  PlanParams pp = plan_params(cu_seqlens_q, cu_seqlens_kv, cu_seqlens_q_padded, cu_seqlens_kv_padded, B, cp_size,
+                              causal, pad_between_seqs, T_q, T_kv, 2, w, L, dev_status);
+  rc = cuda_status(launch_plan(pp, st));
+  if (rc) return rc;
+  float* delta = reinterpret_cast<float*>(w + L.delta);
+  float* dq_acc = reinterpret_cast<float*>(w + L.dq_acc);
+  rc = cuda_status(launch_bwd_prep(static_cast<const uint16_t*>(o), static_cast<const uint16_t*>(dout), delta,
+                                   dq_acc, pp.eff, B, T_q, Hq, D, dev_status, st));
+  if (rc) return rc;
+  CUtensorMap tq, tdo, tk, tv;
+  if (!make_thd_map(&tq, q, T_q, Hq, D) || !make_thd_map(&tdo, dout, T_q, Hq, D) ||
+      !make_thd_map(&tk, k, T_kv, Hkv, D) || !make_thd_map(&tv, v, T_kv, Hkv, D))
+    return THD_ERR_CUDA;
+  BwdParams bp;
+  std::memset(&bp, 0, sizeof(bp));
+  bp.q = static_cast<const uint16_t*>(q);
+  bp.dout = static_cast<const uint16_t*>(dout);
+  bp.lse = lse;
+  bp.delta = delta;
+  bp.dq_acc = dq_acc;
+  bp.dk = static_cast<uint16_t*>(dk);
+  bp.dv = static_cast<uint16_t*>(dv);
+  bp.eff = pp.eff;
+  bp.items = pp.items;
+  bp.counters = pp.counters;
+  bp.dev_status = dev_status;
+  bp.B = B;
+  bp.Hq = Hq;
+  bp.Hkv = Hkv;
+  bp.cp = cp_size;
+  bp.causal = causal;
+  bp.T_q = T_q;
+  bp.dkv_rows = dkv_rows;
+  bp.scale = softmax_scale;
+  bp.scale_log2 = softmax_scale * 1.4426950408889634f;
+  const int64_t bound = (int64_t)L.item_cap * Hkv;
+  const int grid = (int)(bound < num_sms() ? (bound > 0 ? bound : 1) : num_sms());
+  rc = cuda_status(launch_bwd(bp, tq, tdo, tk, tv, D, grid, st));
+  if (rc) return rc;
+  return cuda_status(launch_bwd_dq(dq_acc, static_cast<uint16_t*>(dq), pp.eff, B, T_q, dq_rows, Hq, D,
+                                   softmax_scale, dev_status, st));
+}
+
+int thd_lse_merge(float* o_acc, float* lse_acc, const float* o_part, const float* lse_part, int64_t T, int H, int D,
+                  thd_stream_t stream) {
+  if (!o_acc || !lse_acc || !o_part || !lse_part || T < 0 || H < 1 || D < 4 || D % 4 != 0) return THD_ERR_INVALID_ARG;
+  if (!aligned(o_acc, 16) || !aligned(o_part, 16)) return THD_ERR_INVALID_ARG;
+  return cuda_status(launch_lse_merge(o_acc, lse_acc, o_part, lse_part, T, H, D, reinterpret_cast<cudaStream_t>(stream)));
+}
+
+int thd_grad_tail_zero(void* dq, void* dk, void* dv, int64_t dq_rows, int64_t dkv_rows, int Hq, int Hkv, int D,
+                       const int32_t* cu_seqlens_q_padded, const int32_t* cu_seqlens_kv_padded, int B,
+                       int host_knows_no_tail, thd_stream_t stream) {
+  if (B < 1 || Hq < 1 || Hkv < 1 || D < 8 || D % 8 != 0 || dq_rows < 0 || dkv_rows < 0) return THD_ERR_INVALID_ARG;
+  if (dq && !cu_seqlens_q_padded) return THD_ERR_INVALID_ARG;
+  if ((dk || dv) && !cu_seqlens_kv_padded) return THD_ERR_INVALID_ARG;
+  if (!aligned(dq, 16) || !aligned(dk, 16) || !aligned(dv, 16)) return THD_ERR_INVALID_ARG;
+  if (host_knows_no_tail) return THD_OK;  // nothing to clear: no launch at all
+  if (!dq && !dk && !dv) return THD_OK;
+  return cuda_status(launch_tail_zero(static_cast<uint16_t*>(dq), static_cast<uint16_t*>(dk),
+                                      static_cast<uint16_t*>(dv), dq_rows, dkv_rows, Hq, Hkv, D,
+                                      cu_seqlens_q_padded ? cu_seqlens_q_padded + B : nullptr,
+                                      cu_seqlens_kv_padded ? cu_seqlens_kv_padded + B : nullptr, nullptr,
+                                      reinterpret_cast<cudaStream_t>(stream)));
+}
+
+int thd_profile_enable(int kernel_id, int max_records) {
+  std::lock_guard<std::mutex> lk(g_prof.mu);
+  for (auto e : g_prof.ev) cudaEventDestroy(e);
+  g_prof.ev.clear();
+  g_prof.kernel = 0;
+  g_prof.n = 0;
+  g_prof.max = 0;
+  if (kernel_id == 0 || max_records <= 0) return THD_OK;
+  g_prof.ev.resize(2 * (size_t)max_records);
+  for (auto& e : g_prof.ev)
+    if (cudaEventCreate(&e) != cudaSuccess) return THD_ERR_CUDA;
+  g_prof.max = max_records;
+  g_prof.kernel = kernel_id;
+  return THD_OK;
+}
+
+int thd_profile_read(float* ms_out, int max_out, int* count_out) {
+  std::lock_guard<std::mutex> lk(g_prof.mu);
+  const int n = g_prof.n < max_out ? g_prof.n : max_out;
+  for (int i = 0; i < n; ++i) {
+    if (cudaEventSynchronize(g_prof.ev[2 * i + 1]) != cudaSuccess) return THD_ERR_CUDA;
+    float ms = 0.f;
+    if (cudaEventElapsedTime(&ms, g_prof.ev[2 * i], g_prof.ev[2 * i + 1]) != cudaSuccess) return THD_ERR_CUDA;
+    if (ms_out) ms_out[i] = ms;
+  }
+  if (count_out) *count_out = n;
+  return THD_OK;
+}
+
+uint64_t thd_launch_count(void) { return g_launches.load(std::memory_order_relaxed); }
+
+}  // extern "C"

@@ -1,0 +1,447 @@
+// Forward attention over packed THD tensors, decomposed like P2P (ring)
+// context parallelism and executed for every emulated rank on one GB300.
+//
+// [P1] TransformerEngine issue #2208 (traceback through
+// AttnFuncWithCPAndKVP2P.forward): per ring step, partial attention of the
+// rank's local queries against the KV it holds, corrected into the running
+// output.  [P3] "Hybrid / Hierarchical Context Parallel Skill" ("Contraintes
+// requises"): sequences split into 2*cp chunks; rank r owns chunks r and
+// 2cp-1-r.
+//
+// One work item = (rank r, sequence b, query head h, rank-local 128-row query
+// tile t).  The item walks ring steps i = 0..cp-1 (KV of rank s = (r-i) mod
+// cp: chunks s then 2cp-1-s) and, inside each, the 128-row key tiles that
+// hold any key a query of the tile may see; fully masked tiles are skipped.
+// The per-step LSE merge happens on chip: the running (max, sum, O) of the
+// online softmax is exactly the log-sum-exp correction applied at tile
+// granularity.  In one-step mode (thd_attn_fwd_step) only step `step_lo`
+// is walked and the step's partial (O_i, lse_i) is written in fp32.
+//
+// CTA layout (192 threads, one CTA per SM, persistent over the schedule):
+//   warps 0-3  softmax + epilogue, one query row per thread (TMEM lane)
+//   warp 4     TMA producer (K/V tiles, 3-D tensor maps over [T, Hkv, D])
+//   warp 5     TMEM allocator and single-thread tcgen05.mma issuer
+// TMEM: S double buffer in columns [0,128) and [128,256) (fp32); the
+// softmax writes P as packed bf16 over the first 64 columns of its S buffer,
+// and PV reads it from TMEM as the A operand; O accumulates in [256, 256+D).
+#include "common.cuh"
+#include "ptx.cuh"
+
+namespace thd {
+
+template <int D>
+struct FwdCfg {
+  static constexpr int kStages = D == 128 ? 2 : 4;
+  static constexpr int kQBytes = kTile * D * 2;
+  static constexpr int kKVBytes = kTile * D * 2;  // one K (or V) tile
+  static constexpr int kSmem = 1024 + kQBytes + kStages * 2 * kKVBytes;
+  static constexpr uint32_t kTmemCols = 512;
+  static constexpr uint32_t kColO = 256;
+  static constexpr int kThreads = 192;
+};
+
+struct FwdItem {
+  SeqGeom g;
+  int b, r, t, h, kvh, qmax;
+};
+
+__device__ inline FwdItem fwd_item(const FwdParams& p, int w) {
+  FwdItem it;
+  const int4 e = p.items[w / p.Hq];
+  it.h = w % p.Hq;
+  it.kvh = it.h / (p.Hq / p.Hkv);
+  it.b = e.x;
+  it.r = e.y;
+  it.t = e.z;
+  it.g = seq_geom(p.eff, p.B, it.b, p.cp);
+  it.qmax = fwd_tile_qmax(it.g, it.r, it.t, p.cp);
+  return it;
+}
+
+// Calls f(c, j) for every key tile the item visits, in ring order.
+template <typename F>
+__device__ inline void for_each_kv_tile(const FwdItem& it, const FwdParams& p, F&& f) {
+  for (int i = p.step_lo; i < p.step_hi; ++i) {
+    const int s = ring_src(it.r, i, p.cp);
+    for (int e = 0; e < 2; ++e) {
+      const int c = ring_chunk(s, e, p.cp);
+      const int n = fwd_chunk_tiles(it.g, c, it.qmax, p.causal != 0);
+      for (int j = 0; j < n; ++j) f(c, j);
+    }
+  }
+}
+
+// Bounded wait that ignores the abort flag (used to drain in-flight async
+// work before the CTA exits).
+__device__ inline void drain_wait(uint64_t* bar, uint32_t parity) {
+  const uint64_t t0 = globaltimer();
+  while (!mbar_try_wait(bar, parity)) {
+    if (globaltimer() - t0 > kWaitTimeoutNs) break;
+  }
+}
+
+template <int D, bool kStep>
+__global__ void __launch_bounds__(192, 1)
+    fwd_kernel(const FwdParams p, const __grid_constant__ CUtensorMap tmK, const __grid_constant__ CUtensorMap tmV) {
+  using C = FwdCfg<D>;
+  constexpr int S = C::kStages;
+  extern __shared__ uint8_t smem_raw[];
+  uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
+  uint8_t* sQ = smem;
+  uint8_t* sK = smem + C::kQBytes;
+  uint8_t* sV = sK + S * C::kKVBytes;
+  __shared__ __align__(8) uint64_t bar_kv_full[S];
+  __shared__ __align__(8) uint64_t bar_kv_empty[S];
+  __shared__ __align__(8) uint64_t bar_s_full[2];
+  __shared__ __align__(8) uint64_t bar_p_ready[2];
+  __shared__ __align__(8) uint64_t bar_pv_done;
+  __shared__ __align__(8) uint64_t bar_q_ready;
+  __shared__ __align__(8) uint64_t bar_drain;
+  __shared__ uint32_t s_tmem;
+  __shared__ int s_abort;
+
+  const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
+  if (*p.dev_status != 0) return;  // metadata rejected: outputs untouched
+  const int n_items = p.counters[0] * p.Hq;
+
+  if (tid == 0) {
+    for (int s = 0; s < S; ++s) {
+      mbar_init(&bar_kv_full[s], 1);
+      mbar_init(&bar_kv_empty[s], 1);
+    }
+    for (int s = 0; s < 2; ++s) {
+      mbar_init(&bar_s_full[s], 1);
+      mbar_init(&bar_p_ready[s], 128);
+    }
+    mbar_init(&bar_pv_done, 1);
+    mbar_init(&bar_q_ready, 128);
+    mbar_init(&bar_drain, 1);
+    s_abort = 0;
+    fence_mbar_init();
+  }
+  if (warp == 5) {
+    tmem_alloc(&s_tmem, C::kTmemCols);
+    tmem_relinquish();
+  }
+  if (warp == 4 && lane == 0) {
+    tma_prefetch_desc(&tmK);
+    tma_prefetch_desc(&tmV);
+  }
+  tc_fence_before();
+  __syncthreads();
+  tc_fence_after();
+  const uint32_t tmem = s_tmem;
+
+  if (warp == 4) {
+    // ------------------------------------------------------------ producer
+    if (lane == 0) {
+      int stage = 0;
+      uint32_t ph = 0;
+      int fills[S];
+      for (int s = 0; s < S; ++s) fills[s] = 0;
+      bool ok = true;
+      for (int w = blockIdx.x; w < n_items && ok; w += gridDim.x) {
+        const FwdItem it = fwd_item(p, w);
+        for_each_kv_tile(it, p, [&](int c, int j) {
+          if (!ok) return;
+          if (!mbar_wait(&bar_kv_empty[stage], ph ^ 1u, &s_abort)) {
+            ok = false;
+            return;
+          }
+          const int row = it.g.kv_off + c * it.g.cbkv + j * kTile;
+          mbar_arrive_expect_tx(&bar_kv_full[stage], 2 * C::kKVBytes);
+#pragma unroll
+          for (int hb = 0; hb < D / 64; ++hb) {
+            tma_load_3d(smem_u32(sK + stage * C::kKVBytes + hb * 16384), &tmK, &bar_kv_full[stage], hb * 64,
+                        it.kvh, row);
+            tma_load_3d(smem_u32(sV + stage * C::kKVBytes + hb * 16384), &tmV, &bar_kv_full[stage], hb * 64,
+                        it.kvh, row);
+          }
+          ++fills[stage];
+          if (++stage == S) {
+            stage = 0;
+            ph ^= 1u;
+          }
+        });
+      }
+      // every issued load must land before the CTA may exit
+      for (int s = 0; s < S; ++s)
+        if (fills[s] > 0) drain_wait(&bar_kv_full[s], (uint32_t)(fills[s] - 1) & 1u);
+    }
+    __syncwarp();
+  } else if (warp == 5) {
+    // ------------------------------------------------------------ MMA issuer
+    if (lane == 0) {
+      constexpr uint32_t idesc_qk = idesc_bf16(128, 128, false, false);
+      constexpr uint32_t idesc_pv = idesc_bf16(128, D, false, true);
+      const uint32_t qbase = smem_u32(sQ), kbase = smem_u32(sK), vbase = smem_u32(sV);
+      int stage = 0;
+      uint32_t ph = 0, g = 0, q_iter = 0;
+      bool ok = true;
+      auto issue_pv = [&](uint32_t gg, int st, bool first) -> bool {
+        if (!mbar_wait(&bar_p_ready[gg & 1u], (gg >> 1) & 1u, &s_abort)) return false;
+        tc_fence_after();
+        const uint32_t pcol = tmem + ((gg & 1u) ? 128u : 0u);
+#pragma unroll
+        for (int ks = 0; ks < kTile / 16; ++ks) {
+          const uint64_t bd = sdesc_sw128(vbase + st * C::kKVBytes + ks * 2048, 16384, 1024);
+          mma_ts(tmem + C::kColO, pcol + ks * 8, bd, idesc_pv, (first && ks == 0) ? 0u : 1u);
+        }
+        tc_commit(&bar_kv_empty[st]);
+        tc_commit(&bar_pv_done);
+        return true;
+      };
+      for (int w = blockIdx.x; w < n_items && ok; w += gridDim.x) {
+        const FwdItem it = fwd_item(p, w);
+        int n = 0;
+        for_each_kv_tile(it, p, [&](int, int) { ++n; });
+        if (!mbar_wait(&bar_q_ready, q_iter & 1u, &s_abort)) break;
+        ++q_iter;
+        tc_fence_after();
+        int prev_stage = 0;
+        uint32_t prev_g = 0;
+        for (int j = 0; j < n; ++j) {
+          if (!mbar_wait(&bar_kv_full[stage], ph, &s_abort)) {
+            ok = false;
+            break;
+          }
+          tc_fence_after();
+          const uint32_t scol = tmem + ((g & 1u) ? 128u : 0u);
+#pragma unroll
+          for (int ks = 0; ks < D / 16; ++ks) {
+            const uint32_t koff = (ks >> 2) * 16384 + (ks & 3) * 32;
+            const uint64_t ad = sdesc_sw128(qbase + koff, 16, 1024);
+            const uint64_t bd = sdesc_sw128(kbase + stage * C::kKVBytes + koff, 16, 1024);
+            mma_ss(scol, ad, bd, idesc_qk, ks > 0 ? 1u : 0u);
+          }
+          tc_commit(&bar_s_full[g & 1u]);
+          if (j > 0 && !issue_pv(prev_g, prev_stage, j == 1)) {
+            ok = false;
+            break;
+          }
+          prev_stage = stage;
+          prev_g = g;
+          if (++stage == S) {
+            stage = 0;
+            ph ^= 1u;
+          }
+          ++g;
+        }
+        if (ok && n > 0 && !issue_pv(prev_g, prev_stage, n == 1)) ok = false;
+      }
+      // all issued MMAs must complete before TMEM is released
+      tc_commit(&bar_drain);
+      drain_wait(&bar_drain, 0);
+    }
+    __syncwarp();
+  } else {
+    // ------------------------------------------------------------ softmax + epilogue
+    const uint32_t lane_base = (uint32_t)(warp * 32) << 16;
+    const float sl2 = p.scale_log2;
+    uint32_t g = 0;
+    bool ok = true;
+    for (int w = blockIdx.x; w < n_items && ok; w += gridDim.x) {
+      const FwdItem it = fwd_item(p, w);
+      const int prow = it.t * kTile + tid;
+      const bool in_rank = prow < 2 * it.g.cbq;
+      const int pos = in_rank ? local_to_pos(prow, it.r, it.g.cbq, p.cp) : 0;
+      const bool valid = in_rank && pos < it.g.Lq;
+      const int64_t grow = (int64_t)it.g.q_off + pos;
+      // ---- gather this row of the query tile into 128B-swizzled smem
+      {
+        const uint4* src = reinterpret_cast<const uint4*>(p.q + (grow * p.Hq + it.h) * D);
+#pragma unroll
+        for (int c = 0; c < D / 8; ++c) {
+          const uint4 v = valid ? __ldg(src + c) : make_uint4(0, 0, 0, 0);
+          *reinterpret_cast<uint4*>(sQ + sw128_offset(tid, c * 8, kTile)) = v;
+        }
+      }
+      fence_proxy_async_smem();
+      mbar_arrive(&bar_q_ready);
+      // ---- key tiles
+      float m = -INFINITY, l = 0.f;
+      int jl = 0;
+      for_each_kv_tile(it, p, [&](int c, int j) {
+        if (!ok) return;
+        const uint32_t sb = g & 1u;
+        if (!mbar_wait(&bar_s_full[sb], (g >> 1) & 1u, &s_abort)) {
+          ok = false;
+          return;
+        }
+        tc_fence_after();
+        const int j0 = c * it.g.cbkv + j * kTile;
+        int cnt = 0;
+        if (valid) {
+          cnt = imin(kTile, (c + 1) * it.g.cbkv - j0);
+          cnt = imin(cnt, it.g.Lkv - j0);
+          if (p.causal) cnt = imin(cnt, pos - j0 + 1);
+          cnt = imax(cnt, 0);
+        }
+        uint32_t sr[4][32];
+        const uint32_t scol = tmem + lane_base + sb * 128u;
+#pragma unroll
+        for (int k = 0; k < 4; ++k) tmem_ld32(scol + 32 * k, sr[k]);
+#pragma unroll
+        for (int k = 0; k < 4; ++k) tmem_ld_wait(sr[k]);
+        float mt = -INFINITY;
+        if (cnt >= kTile) {
+#pragma unroll
+          for (int k = 0; k < 4; ++k)
+#pragma unroll
+            for (int n = 0; n < 32; ++n) mt = fmaxf(mt, __uint_as_float(sr[k][n]));
+        } else {
+#pragma unroll
+          for (int k = 0; k < 4; ++k)
+#pragma unroll
+            for (int n = 0; n < 32; ++n) {
+              const float x = (32 * k + n < cnt) ? __uint_as_float(sr[k][n]) : -INFINITY;
+              sr[k][n] = __float_as_uint(x);
+              mt = fmaxf(mt, x);
+            }
+        }
+        mt *= sl2;
+        // lazy rescale: move the running max only when it grows by > 8 (log2 units)
+        const bool upd = mt > m + 8.0f;
+        const float alpha = upd ? ex2(m - mt) : 1.0f;
+        const bool need_o = upd && (m != -INFINITY) && (jl > 0);
+        if (upd) {
+          l *= alpha;
+          m = mt;
+        }
+        if (__any_sync(0xffffffffu, need_o)) {
+          // O must hold the previous tile's PV before it is rescaled
+          if (!mbar_wait(&bar_pv_done, (g - 1) & 1u, &s_abort)) {
+            ok = false;
+            return;
+          }
+          tc_fence_after();
+          const float f = need_o ? alpha : 1.0f;
+#pragma unroll
+          for (int k = 0; k < D / 32; ++k) {
+            uint32_t o[32];
+            tmem_ld32(tmem + lane_base + C::kColO + 32 * k, o);
+            tmem_ld_wait(o);
+#pragma unroll
+            for (int n = 0; n < 32; ++n) o[n] = __float_as_uint(__uint_as_float(o[n]) * f);
+            tmem_st32(tmem + lane_base + C::kColO + 32 * k, o);
+          }
+        }
+        const float mm = (m == -INFINITY) ? 0.f : m;
+        float rs = 0.f;
+#pragma unroll
+        for (int half = 0; half < 2; ++half) {
+          uint32_t pk[32];
+#pragma unroll
+          for (int kk = 0; kk < 2; ++kk) {
+            const int k = half * 2 + kk;
+#pragma unroll
+            for (int n = 0; n < 16; ++n) {
+              const float p0 = ex2(fmaf(__uint_as_float(sr[k][2 * n]), sl2, -mm));
+              const float p1 = ex2(fmaf(__uint_as_float(sr[k][2 * n + 1]), sl2, -mm));
+              rs += p0 + p1;
+              pk[kk * 16 + n] = pack_bf16x2(p0, p1);
+            }
+          }
+          tmem_st32(scol + 32 * half, pk);
+        }
+        l += rs;
+        tmem_st_wait();
+        tc_fence_before();
+        mbar_arrive(&bar_p_ready[sb]);
+        ++g;
+        ++jl;
+      });
+      if (!ok) break;
+      // ---- epilogue
+      if (jl > 0) {
+        if (!mbar_wait(&bar_pv_done, (g - 1) & 1u, &s_abort)) break;
+        tc_fence_after();
+      }
+      const bool live = valid && l > 0.f;
+      const float inv_l = live ? 1.0f / l : 0.f;
+      if (in_rank) {
+        const float lse = live ? (m + log2f(l)) * 0.69314718055994531f : -INFINITY;
+        p.lse[(int64_t)it.h * p.T_q + grow] = lse;
+      }
+#pragma unroll
+      for (int k = 0; k < D / 32; ++k) {
+        uint32_t o[32];
+        if (jl > 0) {
+          tmem_ld32(tmem + lane_base + C::kColO + 32 * k, o);
+          tmem_ld_wait(o);
+        } else {
+#pragma unroll
+          for (int n = 0; n < 32; ++n) o[n] = 0u;
+        }
+        if (in_rank) {
+          if constexpr (kStep) {
+            float4* dst = reinterpret_cast<float4*>(static_cast<float*>(p.o) + (grow * p.Hq + it.h) * D + 32 * k);
+#pragma unroll
+            for (int n = 0; n < 8; ++n)
+              dst[n] = make_float4(__uint_as_float(o[4 * n]) * inv_l, __uint_as_float(o[4 * n + 1]) * inv_l,
+                                   __uint_as_float(o[4 * n + 2]) * inv_l, __uint_as_float(o[4 * n + 3]) * inv_l);
+          } else {
+            uint4* dst = reinterpret_cast<uint4*>(static_cast<uint16_t*>(p.o) + (grow * p.Hq + it.h) * D + 32 * k);
+#pragma unroll
+            for (int n = 0; n < 4; ++n) {
+              uint4 v;
+              v.x = pack_bf16x2(__uint_as_float(o[8 * n + 0]) * inv_l, __uint_as_float(o[8 * n + 1]) * inv_l);
+              v.y = pack_bf16x2(__uint_as_float(o[8 * n + 2]) * inv_l, __uint_as_float(o[8 * n + 3]) * inv_l);
+              v.z = pack_bf16x2(__uint_as_float(o[8 * n + 4]) * inv_l, __uint_as_float(o[8 * n + 5]) * inv_l);
+              v.w = pack_bf16x2(__uint_as_float(o[8 * n + 6]) * inv_l, __uint_as_float(o[8 * n + 7]) * inv_l);
+              dst[n] = v;
+            }
+          }
+        }
+      }
+      tc_fence_before();
+    }
+    // ---- rows past the last sequence: O = 0, lse = -inf
+    if (ok) {
+      const int Tend = p.eff[(p.B + 1) + p.B];
+      const int64_t nrow = (p.T_q - Tend) * (int64_t)p.Hq;
+      for (int64_t i = (int64_t)blockIdx.x * 128 + tid; i < nrow; i += (int64_t)gridDim.x * 128) {
+        const int64_t t = Tend + i / p.Hq;
+        const int h = (int)(i % p.Hq);
+        if constexpr (kStep) {
+          float4* dst = reinterpret_cast<float4*>(static_cast<float*>(p.o) + (t * p.Hq + h) * D);
+          for (int n = 0; n < D / 4; ++n) dst[n] = make_float4(0.f, 0.f, 0.f, 0.f);
+        } else {
+          uint4* dst = reinterpret_cast<uint4*>(static_cast<uint16_t*>(p.o) + (t * p.Hq + h) * D);
+          for (int n = 0; n < D / 8; ++n) dst[n] = make_uint4(0, 0, 0, 0);
+        }
+        p.lse[(int64_t)h * p.T_q + t] = -INFINITY;
+      }
+    }
+  }
+
+  tc_fence_before();
+  __syncthreads();
+  if (warp == 5) {
+    tc_fence_after();
+    tmem_dealloc(tmem, C::kTmemCols);
+  }
+  if (tid == 0 && s_abort) atomicCAS(p.dev_status, 0, THD_ERR_TIMEOUT);
+}
+
+template <int D, bool kStep>
+static cudaError_t launch_fwd_t(const FwdParams& p, const CUtensorMap& tk, const CUtensorMap& tv, int grid,
+                                cudaStream_t st) {
+  using C = FwdCfg<D>;
+  cudaError_t ea = cudaFuncSetAttribute(fwd_kernel<D, kStep>, cudaFuncAttributeMaxDynamicSharedMemorySize, C::kSmem);
+  if (ea != cudaSuccess) return ea;
+  prof_before(THD_KERNEL_FWD, st);
+  fwd_kernel<D, kStep><<<grid, C::kThreads, C::kSmem, st>>>(p, tk, tv);
+  count_launch();
+  cudaError_t e = cudaGetLastError();
+  prof_after(THD_KERNEL_FWD, st);
+  return e;
+}
+
+cudaError_t launch_fwd(const FwdParams& p, const CUtensorMap& tk, const CUtensorMap& tv, int D, bool step_mode,
+                       int grid, cudaStream_t st) {
+  if (D == 128) return step_mode ? launch_fwd_t<128, true>(p, tk, tv, grid, st) : launch_fwd_t<128, false>(p, tk, tv, grid, st);
+  return step_mode ? launch_fwd_t<64, true>(p, tk, tv, grid, st) : launch_fwd_t<64, false>(p, tk, tv, grid, st);
+}
+
+}  // namespace thd

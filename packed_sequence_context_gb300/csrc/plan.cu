@@ -1,0 +1,451 @@
+// Metadata validation + pad detection (from values), the per-rank partition,
+// the longest-first tile schedule, and the small HBM-bound kernels: LSE
+// merge, gradient tail-zero, backward preprocess (Delta, dQ accumulator
+// reset) and dQ conversion.
+//
+// Pages: [P2] TransformerEngine issue #3487 ("Describe the bug": the
+// padding detector decides by object identity and get_cu_seqlens_on_cp_rank
+// is called per ring step; THD dQ/dK/dV tail-zeroing launches work even with
+// no tail; "Expected behavior": decide from values, stay graph-safe),
+// [P3] "Hybrid / Hierarchical Context Parallel Skill" ("Contraintes
+// requises": padded length divisible by 2 * cp_size).
+#include <climits>
+#include <cuda_bf16.h>
+
+#include "common.cuh"
+
+namespace thd {
+
+// ------------------------------------------------------------------ helpers
+// Exclusive scan over the 1024 threads of the block; `total` receives the sum.
+__device__ int block_exclusive_scan(int v, int* s_warp, int& total) {
+  const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5, nwarps = blockDim.x >> 5;
+  int x = v;
+#pragma unroll
+  for (int o = 1; o < 32; o <<= 1) {
+    int y = __shfl_up_sync(0xffffffffu, x, o);
+    if (lane >= o) x += y;
+  }
+  if (lane == 31) s_warp[warp] = x;
+  __syncthreads();
+  if (warp == 0) {
+    int w = lane < nwarps ? s_warp[lane] : 0;
+#pragma unroll
+    for (int o = 1; o < 32; o <<= 1) {
+      int y = __shfl_up_sync(0xffffffffu, w, o);
+      if (lane >= o) w += y;
+    }
+    s_warp[lane] = w;
+  }
+  __syncthreads();
+  const int prefix = warp ? s_warp[warp - 1] : 0;
+  total = s_warp[nwarps - 1];
+  __syncthreads();
+  return prefix + x - v;
+}
+
+// Largest b in [0, n] with a[b] <= x (a non-decreasing, a[0] <= x).
+__device__ inline int upper_index(const int32_t* a, int n, int x) {
+  int lo = 0, hi = n;
+  while (lo < hi) {
+    int mid = (lo + hi + 1) >> 1;
+    if (a[mid] <= x) lo = mid;
+    else hi = mid - 1;
+  }
+  return lo;
+}
+
+__device__ inline void set_err(int* s_err, int code) { atomicMin(s_err, code); }
+
+// ------------------------------------------------------------------ planner
+__global__ void __launch_bounds__(kPlanThreads) plan_kernel(PlanParams p) {
+  __shared__ int s_err;
+  __shared__ int s_pad[2];
+  __shared__ int s_warp[32];
+  __shared__ int s_hist[kCostBins];
+  const int tid = threadIdx.x, nt = blockDim.x;
+  const int B = p.B, cp = p.cp;
+  if (tid == 0) {
+    s_err = INT_MAX;
+    s_pad[0] = 0;
+    s_pad[1] = 0;
+  }
+  __syncthreads();
+  // a1: padding between sequences, decided from VALUES.
+  if (p.pad_mode == -1) {
+    for (int b = tid; b <= B; b += nt) {
+      if (p.pad_q && p.pad_q[b] != p.cu_q[b]) s_pad[0] = 1;
+      if (p.pad_kv && p.pad_kv[b] != p.cu_kv[b]) s_pad[1] = 1;
+    }
+  }
+  __syncthreads();
+  const int padq = p.pad_q ? (p.pad_mode == -1 ? s_pad[0] : p.pad_mode) : 0;
+  const int padkv = p.pad_kv ? (p.pad_mode == -1 ? s_pad[1] : p.pad_mode) : 0;
+  const int32_t* PQ = padq ? p.pad_q : p.cu_q;
+  const int32_t* PK = padkv ? p.pad_kv : p.cu_kv;
+  int32_t* eff = p.eff;
+  for (int b = tid; b <= B; b += nt) {
+    const int cq = p.cu_q[b], pq = PQ[b], ck = p.cu_kv[b], pk = PK[b];
+    if (eff) {
+      eff[b] = cq;
+      eff[(B + 1) + b] = pq;
+      eff[2 * (B + 1) + b] = ck;
+      eff[3 * (B + 1) + b] = pk;
+    }
+    if (b == 0 && (cq != 0 || pq != 0 || ck != 0 || pk != 0)) set_err(&s_err, THD_DEV_ERR_NONZERO_START);
+    if (b < B) {
+      const int Lq = p.cu_q[b + 1] - cq, Pq = PQ[b + 1] - pq;
+      const int Lk = p.cu_kv[b + 1] - ck, Pk = PK[b + 1] - pk;
+      if (Lq < 0 || Pq < 0 || Lk < 0 || Pk < 0) set_err(&s_err, THD_DEV_ERR_NOT_MONOTONE);
+      else if (Lq > Pq || Lk > Pk) set_err(&s_err, THD_DEV_ERR_VALID_GT_PAD);
+      else if (Pq % (2 * cp) != 0 || Pk % (2 * cp) != 0) set_err(&s_err, THD_DEV_ERR_NOT_DIVISIBLE);
+      else if (p.causal && (Lq != Lk || Pq != Pk)) set_err(&s_err, THD_DEV_ERR_CAUSAL_LENGTHS);
+    } else {
+      if ((int64_t)pq > p.rows_q || (int64_t)pk > p.rows_kv) set_err(&s_err, THD_DEV_ERR_EXCEEDS_BUF);
+      if (p.token_map && (int64_t)pq > p.token_map_cap) set_err(&s_err, THD_DEV_ERR_EXCEEDS_BUF);
+    }
+  }
+  __syncthreads();
+  const int err = s_err == INT_MAX ? 0 : s_err;
+  if (err) {
+    if (tid == 0) *p.dev_status = err;
+    return;
+  }
+  if (tid == 0) *p.dev_status = 0;
+
+  // a2: per-rank partition (query side), every rank in this one launch.
+  if (p.cu_rank || p.cu_rank_padded || p.cu_rank_half) {
+    for (int r = tid; r < cp; r += nt) {
+      int acc = 0, acc1 = 0, acc2 = 0;
+      if (p.cu_rank) p.cu_rank[r * (B + 1)] = 0;
+      if (p.cu_rank_half) {
+        p.cu_rank_half[(r * 2 + 0) * (B + 1)] = 0;
+        p.cu_rank_half[(r * 2 + 1) * (B + 1)] = 0;
+      }
+      for (int b = 0; b < B; ++b) {
+        const int L = p.cu_q[b + 1] - p.cu_q[b];
+        const int cb = (PQ[b + 1] - PQ[b]) / (2 * cp);
+        const int v1 = imin(imax(L - r * cb, 0), cb);
+        const int v2 = imin(imax(L - (2 * cp - 1 - r) * cb, 0), cb);
+        acc += v1 + v2;
+        acc1 += v1;
+        acc2 += v2;
+        if (p.cu_rank) p.cu_rank[r * (B + 1) + b + 1] = acc;
+        if (p.cu_rank_half) {
+          p.cu_rank_half[(r * 2 + 0) * (B + 1) + b + 1] = acc1;
+          p.cu_rank_half[(r * 2 + 1) * (B + 1) + b + 1] = acc2;
+        }
+      }
+      if (p.cu_rank_padded)
+        for (int b = 0; b <= B; ++b) p.cu_rank_padded[r * (B + 1) + b] = PQ[b] / cp;
+    }
+  }
+  if (p.token_map) {
+    const int T = PQ[B];
+    const int per = T / cp;
+    for (int g = tid; g < T; g += nt) {
+      const int b = upper_index(PQ, B, g);
+      const int pos = g - PQ[b];
+      const int cb = (PQ[b + 1] - PQ[b]) / (2 * cp);
+      const int chunk = pos / cb;
+      const int owner = chunk < cp ? chunk : 2 * cp - 1 - chunk;
+      const int local = chunk == owner ? pos - owner * cb : cb + (pos - chunk * cb);
+      p.token_map[owner * per + PQ[b] / cp + local] = g;
+    }
+  }
+  if (p.mode == 0) return;
+
+  // a3: the schedule.  Forward entries are rank-local query tiles (b, r, t);
+  // backward entries are chunk-aligned key tiles (b, c, jk).  Both are
+  // ordered longest-first (counting sort on the number of tiles visited).
+  int carry = 0;
+  for (int base = 0; base < B; base += nt) {
+    const int b = base + tid;
+    int n = 0;
+    if (b < B) {
+      SeqGeom g = seq_geom(eff, B, b, cp);
+      n = p.mode == 1 ? cp * ceil_div(2 * g.cbq, kTile) : 2 * cp * ceil_div(g.cbkv, kTile);
+    }
+    int tot;
+    const int ex = block_exclusive_scan(n, s_warp, tot);
+    if (b < B) p.tile_off[b] = carry + ex;
+    carry += tot;
+  }
+  if (tid == 0) p.tile_off[B] = carry;
+  const int total = carry;
+  if (total > p.item_cap) {
+    if (tid == 0) *p.dev_status = THD_DEV_ERR_CAPACITY;
+    return;
+  }
+  for (int i = tid; i < kCostBins; i += nt) s_hist[i] = 0;
+  __syncthreads();
+  auto entry = [&](int w, int& b, int& x, int& y, int& cost) {
+    b = upper_index(p.tile_off, B, w);
+    // skip empty sequences that share the same offset
+    while (b < B && p.tile_off[b + 1] <= w) ++b;
+    SeqGeom g = seq_geom(eff, B, b, cp);
+    const int rem = w - p.tile_off[b];
+    if (p.mode == 1) {
+      const int per_r = ceil_div(2 * g.cbq, kTile);
+      x = rem / per_r;
+      y = rem % per_r;
+      cost = fwd_item_tiles(g, x, y, cp, p.causal != 0, p.step_lo, p.step_hi);
+    } else {
+      const int per_c = ceil_div(g.cbkv, kTile);
+      x = rem / per_c;
+      y = rem % per_c;
+      cost = bwd_item_qtiles(g, x, y, cp, p.causal != 0);
+    }
+  };
+  for (int w = tid; w < total; w += nt) {
+    int b, x, y, cost;
+    entry(w, b, x, y, cost);
+    atomicAdd(&s_hist[kCostBins - 1 - imin(cost, kCostBins - 1)], 1);
+  }
+  __syncthreads();
+  // exclusive scan of the histogram: 4 bins per thread
+  {
+    constexpr int per = kCostBins / kPlanThreads;
+    int loc[per];
+    int sum = 0;
+#pragma unroll
+    for (int j = 0; j < per; ++j) {
+      loc[j] = s_hist[tid * per + j];
+      sum += loc[j];
+    }
+    int tot;
+    int ex = block_exclusive_scan(sum, s_warp, tot);
+#pragma unroll
+    for (int j = 0; j < per; ++j) {
+      s_hist[tid * per + j] = ex;
+      ex += loc[j];
+    }
+  }
+  __syncthreads();
+  for (int w = tid; w < total; w += nt) {
+    int b, x, y, cost;
+    entry(w, b, x, y, cost);
+    const int pos = atomicAdd(&s_hist[kCostBins - 1 - imin(cost, kCostBins - 1)], 1);
+    p.items[pos] = make_int4(b, x, y, cost);
+  }
+  if (tid == 0) p.counters[0] = total;
+}
+
+cudaError_t launch_plan(const PlanParams& p, cudaStream_t st) {
+  prof_before(p.mode == 0 ? THD_KERNEL_PARTITION : THD_KERNEL_PLAN, st);
+  plan_kernel<<<1, kPlanThreads, 0, st>>>(p);
+  count_launch();
+  cudaError_t e = cudaGetLastError();
+  prof_after(p.mode == 0 ? THD_KERNEL_PARTITION : THD_KERNEL_PLAN, st);
+  return e;
+}
+
+// ------------------------------------------------------------------ LSE merge
+// (o_acc, lse_acc) <- merge with (o_part, lse_part), one float4 per thread.
+__global__ void __launch_bounds__(256) lse_merge_kernel(float4* __restrict__ o_acc, float* __restrict__ lse_acc,
+                                                        const float4* __restrict__ o_part,
+                                                        const float* __restrict__ lse_part, int64_t T, int H,
+                                                        int D4) {
+  const int64_t n = T * H * (int64_t)D4;
+  for (int64_t i = blockIdx.x * (int64_t)blockDim.x + threadIdx.x; i < n; i += (int64_t)gridDim.x * blockDim.x) {
+    const int64_t row = i / D4;  // row = t * H + h
+    const int d4 = (int)(i - row * D4);
+    const int64_t t = row / H;
+    const int h = (int)(row - t * H);
+    const int64_t li = (int64_t)h * T + t;
+    const float a = lse_acc[li], b = lse_part[li];
+    const float hi = fmaxf(a, b), lo = fminf(a, b);
+    float lse, wa, wb;
+    if (hi == -INFINITY) {
+      lse = -INFINITY;
+      wa = 0.f;
+      wb = 0.f;
+    } else {
+      lse = hi + log1pf(expf(lo - hi));
+      wa = a == -INFINITY ? 0.f : expf(a - lse);
+      wb = b == -INFINITY ? 0.f : expf(b - lse);
+    }
+    const float4 x = o_acc[i], y = o_part[i];
+    o_acc[i] = make_float4(wa * x.x + wb * y.x, wa * x.y + wb * y.y, wa * x.z + wb * y.z, wa * x.w + wb * y.w);
+    if (d4 == 0) lse_acc[li] = lse;
+  }
+}
+
+cudaError_t launch_lse_merge(float* o_acc, float* lse_acc, const float* o_part, const float* lse_part, int64_t T,
+                             int H, int D, cudaStream_t st) {
+  const int64_t n = T * H * (int64_t)(D / 4);
+  if (n == 0) return cudaSuccess;
+  const int64_t want = (n + 255) / 256;
+  const int grid = (int)(want < 8LL * num_sms() ? want : 8LL * num_sms());
+  prof_before(THD_KERNEL_LSE_MERGE, st);
+  lse_merge_kernel<<<grid, 256, 0, st>>>((float4*)o_acc, lse_acc, (const float4*)o_part, lse_part, T, H, D / 4);
+  count_launch();
+  cudaError_t e = cudaGetLastError();
+  prof_after(THD_KERNEL_LSE_MERGE, st);
+  return e;
+}
+
+// ------------------------------------------------------------------ tail-zero
+// Zero rows [*end, rows) of up to three [rows, H, D] bf16 buffers; reads the
+// endpoint on the device, so it does nothing when there is no tail.
+struct TailJob {
+  uint16_t* buf;
+  int64_t rows;
+  int hd;  // H * D
+  const int32_t* end;
+};
+
+__global__ void __launch_bounds__(256) tail_zero_kernel(TailJob j0, TailJob j1, TailJob j2,
+                                                        const int32_t* dev_status) {
+  if (dev_status && *dev_status != 0) return;
+  TailJob jobs[3] = {j0, j1, j2};
+#pragma unroll
+  for (int k = 0; k < 3; ++k) {
+    const TailJob& j = jobs[k];
+    if (!j.buf) continue;
+    const int64_t start = (int64_t)(*j.end) * j.hd;
+    const int64_t stop = j.rows * (int64_t)j.hd;
+    // 16-byte stores (H * D is a multiple of 8)
+    for (int64_t i = start + (blockIdx.x * (int64_t)blockDim.x + threadIdx.x) * 8; i < stop;
+         i += (int64_t)gridDim.x * blockDim.x * 8)
+      *reinterpret_cast<uint4*>(j.buf + i) = make_uint4(0, 0, 0, 0);
+  }
+}
+
+cudaError_t launch_tail_zero(uint16_t* dq, uint16_t* dk, uint16_t* dv, int64_t dq_rows, int64_t dkv_rows, int Hq,
+                             int Hkv, int D, const int32_t* pad_q_end, const int32_t* pad_kv_end,
+                             const int32_t* dev_status, cudaStream_t st) {
+  TailJob a{dq, dq_rows, Hq * D, pad_q_end}, b{dk, dkv_rows, Hkv * D, pad_kv_end},
+      c{dv, dkv_rows, Hkv * D, pad_kv_end};
+  const int64_t biggest = (dq_rows * Hq > dkv_rows * Hkv ? dq_rows * Hq : dkv_rows * Hkv) * (int64_t)D / 8;
+  const int64_t want = (biggest + 255) / 256;
+  const int grid = (int)(want < 2LL * num_sms() ? (want > 0 ? want : 1) : 2LL * num_sms());
+  prof_before(THD_KERNEL_TAIL_ZERO, st);
+  tail_zero_kernel<<<grid, 256, 0, st>>>(a, b, c, dev_status);
+  count_launch();
+  cudaError_t e = cudaGetLastError();
+  prof_after(THD_KERNEL_TAIL_ZERO, st);
+  return e;
+}
+
+// ------------------------------------------------------------------ backward preprocess
+// Delta[h][t] = sum_d dO[t,h,d] * O[t,h,d] on valid rows (0 elsewhere), and
+// the fp32 dQ accumulator reset.  One warp per (t, h) row.
+__device__ inline bool row_valid(const int32_t* eff, int B, int t) {
+  const int32_t* cu = eff;
+  const int32_t* pad = eff + (B + 1);
+  if (t >= pad[B]) return false;
+  const int b = upper_index(pad, B, t);
+  return b < B && t - pad[b] < cu[b + 1] - cu[b];
+}
+
+template <int D>
+__global__ void __launch_bounds__(256) bwd_prep_kernel(const uint16_t* __restrict__ o,
+                                                       const uint16_t* __restrict__ dout, float* __restrict__ delta,
+                                                       float* __restrict__ dq_acc, const int32_t* __restrict__ eff,
+                                                       int B, int64_t T, int Hq, const int32_t* dev_status) {
+  if (*dev_status != 0) return;
+  constexpr int PER = D / 32;  // elements per lane (4 or 2)
+  const int lane = threadIdx.x & 31;
+  const int64_t nrows = T * Hq;
+  for (int64_t row = (blockIdx.x * (int64_t)blockDim.x + threadIdx.x) >> 5; row < nrows;
+       row += ((int64_t)gridDim.x * blockDim.x) >> 5) {
+    const int64_t t = row / Hq;
+    const int h = (int)(row - t * Hq);
+    float acc = 0.f;
+    if (row_valid(eff, B, (int)t)) {
+      const uint16_t* po = o + row * D + lane * PER;
+      const uint16_t* pd = dout + row * D + lane * PER;
+      if (PER == 4) {
+        uint2 a = *reinterpret_cast<const uint2*>(po), b = *reinterpret_cast<const uint2*>(pd);
+        __nv_bfloat162 a0 = *reinterpret_cast<__nv_bfloat162*>(&a.x), a1 = *reinterpret_cast<__nv_bfloat162*>(&a.y);
+        __nv_bfloat162 b0 = *reinterpret_cast<__nv_bfloat162*>(&b.x), b1 = *reinterpret_cast<__nv_bfloat162*>(&b.y);
+        float2 fa0 = __bfloat1622float2(a0), fa1 = __bfloat1622float2(a1);
+        float2 fb0 = __bfloat1622float2(b0), fb1 = __bfloat1622float2(b1);
+        acc = fa0.x * fb0.x + fa0.y * fb0.y + fa1.x * fb1.x + fa1.y * fb1.y;
+      } else {
+        uint32_t a = *reinterpret_cast<const uint32_t*>(po), b = *reinterpret_cast<const uint32_t*>(pd);
+        float2 fa = __bfloat1622float2(*reinterpret_cast<__nv_bfloat162*>(&a));
+        float2 fb = __bfloat1622float2(*reinterpret_cast<__nv_bfloat162*>(&b));
+        acc = fa.x * fb.x + fa.y * fb.y;
+      }
+    }
+#pragma unroll
+    for (int off = 16; off > 0; off >>= 1) acc += __shfl_xor_sync(0xffffffffu, acc, off);
+    if (lane == 0) delta[(int64_t)h * T + t] = acc;
+    float* pq = dq_acc + row * D + lane * PER;
+    if (PER == 4) *reinterpret_cast<float4*>(pq) = make_float4(0.f, 0.f, 0.f, 0.f);
+    else *reinterpret_cast<float2*>(pq) = make_float2(0.f, 0.f);
+  }
+}
+
+cudaError_t launch_bwd_prep(const uint16_t* o, const uint16_t* dout, float* delta, float* dq_acc,
+                            const int32_t* eff, int B, int64_t T_q, int Hq, int D, const int32_t* dev_status,
+                            cudaStream_t st) {
+  const int64_t warps = T_q * Hq;
+  if (warps == 0) return cudaSuccess;
+  const int64_t want = (warps + 7) / 8;
+  const int grid = (int)(want < 8LL * num_sms() ? want : 8LL * num_sms());
+  prof_before(THD_KERNEL_BWD_PREP, st);
+  if (D == 128) bwd_prep_kernel<128><<<grid, 256, 0, st>>>(o, dout, delta, dq_acc, eff, B, T_q, Hq, dev_status);
+  else bwd_prep_kernel<64><<<grid, 256, 0, st>>>(o, dout, delta, dq_acc, eff, B, T_q, Hq, dev_status);
+  count_launch();
+  cudaError_t e = cudaGetLastError();
+  prof_after(THD_KERNEL_BWD_PREP, st);
+  return e;
+}
+
+// ------------------------------------------------------------------ dQ convert
+// dq[t,h,:] = bf16(scale * acc[t,h,:]) on valid rows; 0 on pad rows and on the
+// slack rows [pad[B], dq_rows) (the tail-zero, with no extra launch).
+template <int D>
+__global__ void __launch_bounds__(256) bwd_dq_kernel(const float* __restrict__ acc, uint16_t* __restrict__ dq,
+                                                     const int32_t* __restrict__ eff, int B, int64_t T,
+                                                     int64_t rows, int Hq, float scale, const int32_t* dev_status) {
+  if (*dev_status != 0) return;
+  constexpr int PER = D / 32;
+  const int lane = threadIdx.x & 31;
+  const int64_t nrows = rows * Hq;
+  for (int64_t row = (blockIdx.x * (int64_t)blockDim.x + threadIdx.x) >> 5; row < nrows;
+       row += ((int64_t)gridDim.x * blockDim.x) >> 5) {
+    const int64_t t = row / Hq;
+    const bool valid = t < T && row_valid(eff, B, (int)t);
+    uint16_t* out = dq + row * D + lane * PER;
+    if (PER == 4) {
+      uint2 w = make_uint2(0, 0);
+      if (valid) {
+        float4 a = *reinterpret_cast<const float4*>(acc + row * D + lane * PER);
+        __nv_bfloat162 lo = __floats2bfloat162_rn(a.x * scale, a.y * scale);
+        __nv_bfloat162 hi = __floats2bfloat162_rn(a.z * scale, a.w * scale);
+        w.x = *reinterpret_cast<uint32_t*>(&lo);
+        w.y = *reinterpret_cast<uint32_t*>(&hi);
+      }
+      *reinterpret_cast<uint2*>(out) = w;
+    } else {
+      uint32_t w = 0;
+      if (valid) {
+        float2 a = *reinterpret_cast<const float2*>(acc + row * D + lane * PER);
+        __nv_bfloat162 v = __floats2bfloat162_rn(a.x * scale, a.y * scale);
+        w = *reinterpret_cast<uint32_t*>(&v);
+      }
+      *reinterpret_cast<uint32_t*>(out) = w;
+    }
+  }
+}
+
+cudaError_t launch_bwd_dq(const float* dq_acc, uint16_t* dq, const int32_t* eff, int B, int64_t T_q,
+                          int64_t dq_rows, int Hq, int D, float scale, const int32_t* dev_status, cudaStream_t st) {
+  const int64_t warps = dq_rows * Hq;
+  if (warps == 0) return cudaSuccess;
+  const int64_t want = (warps + 7) / 8;
+  const int grid = (int)(want < 8LL * num_sms() ? want : 8LL * num_sms());
+  prof_before(THD_KERNEL_BWD_DQ, st);
+  if (D == 128) bwd_dq_kernel<128><<<grid, 256, 0, st>>>(dq_acc, dq, eff, B, T_q, dq_rows, Hq, scale, dev_status);
+  else bwd_dq_kernel<64><<<grid, 256, 0, st>>>(dq_acc, dq, eff, B, T_q, dq_rows, Hq, scale, dev_status);
+  count_launch();
+  cudaError_t e = cudaGetLastError();
+  prof_after(THD_KERNEL_BWD_DQ, st);
+  return e;
+}
+
+}  // namespace thd

@@ -290,6 +290,24 @@ def test_fwd_first_row_attends_only_itself():
     np.testing.assert_allclose(O[9, 0], 0.5 * (v[8, 0] + v[9, 0]), atol=1e-14)
 
 
+@pytest.mark.parametrize("seed", range(3))
+def test_fwd_rows_equals_full_definition(seed):
+    rng = np.random.default_rng(600 + seed)
+    cu, cu_pad, q, k, v, lens, valid = _rand_case(rng, 3, 40, 2, pad_mult=seed % 2, Hq=4, Hkv=2, D=8,
+                                                  zero_len_ok=False)
+    O, lse = orc.attn_fwd(q, k, v, cu, cu, cu_pad, cu_pad, causal=bool(seed % 2 == 0), softmax_scale=0.4)
+    for b in range(len(lens)):
+        for h in (0, 3):
+            pos = list(range(int(cu_pad[b + 1] - cu_pad[b])))
+            Or, lr = orc.attn_fwd_rows(q, k, v, cu, cu, cu_pad, cu_pad, b, h, pos,
+                                       causal=bool(seed % 2 == 0), softmax_scale=0.4)
+            rows = int(cu_pad[b]) + np.arange(len(pos))
+            np.testing.assert_allclose(Or, O[rows, h], rtol=0, atol=1e-13)
+            assert np.array_equal(np.isfinite(lr), np.isfinite(lse[h, rows]))
+            fin = np.isfinite(lr)
+            np.testing.assert_allclose(lr[fin], lse[h, rows][fin], rtol=0, atol=1e-13)
+
+
 # ---------------------------------------------------------------- padding
 
 def test_value_equal_padded_metadata_is_bit_identical():
