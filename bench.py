@@ -1,0 +1,410 @@
+#!/usr/bin/env python3
+"""Benchmark: THD causal attention TFLOPS, forward and forward+backward, on GB300.
+
+One step = one pass of the whole hot path over one synthetic packed batch:
+metadata validation + pad detection + per-rank partition + schedule (one
+planner launch), the fused ring-decomposed forward (thd_attn_fwd), and the
+backward (thd_attn_bwd: Delta preprocess, key-stationary backward, dQ
+conversion with tail-zero).  Inputs are resident in HBM before the timed
+region; L2 is flushed (256 MiB write) between timed steps, outside the
+events.  Each step is timed with CUDA events on the launching stream.
+
+    python bench.py [--gpus N] [--steps K] [--warmup W] [--config packed]
+    python bench.py --impl reference ...   # the CPU fp64 oracle on host cores
+
+Under torchrun each rank runs its own replica of the workload (weak scaling,
+no collective on the data path); rank 0 prints one JSON line.
+"""
+
+from __future__ import annotations
+
+import argparse
+import json
+import math
+import os
+import subprocess
+import sys
+import time
+
+ROOT = os.path.dirname(os.path.abspath(__file__))
+if ROOT not in sys.path:
+    sys.path.insert(0, ROOT)
+
+METRIC = "THD causal attn TFLOPS fwd & fwd+bwd, 1 GB300; % of BF16 tensor peak"
+UNIT = "TFLOPS"
+
+
+def _args():
+    ap = argparse.ArgumentParser()
+    ap.add_argument("--gpus", type=int, default=1)
+    ap.add_argument("--steps", type=int, default=100)
+    ap.add_argument("--warmup", type=int, default=10)
+    ap.add_argument("--config", default="packed", help="tiny|packed|padded|long|fwdbwd (or C1..C5)")
+    ap.add_argument("--impl", default="ours", choices=["ours", "reference"])
+    ap.add_argument("--no-cpu-baseline", action="store_true")
+    ap.add_argument("--no-e2e", action="store_true")
+    ap.add_argument("--fwd-only", action="store_true", help="time the forward alone as the step")
+    return ap.parse_args()
+
+
+def _peaks():
+    try:
+        with open(os.path.join(ROOT, "MEASURED_PEAKS.json")) as f:
+            p = json.load(f)
+        return float(p["bf16_tflops"]), float(p["bf16_tflops_sustained"]), float(p["hbm_gbs"]), "measured"
+    except Exception:
+        return 1900.0, 1700.0, 6800.0, "fallback"
+
+
+# ----------------------------------------------------------------- clocks
+class ClockSampler:
+    """nvidia-smi clocks / throttle reasons sampled every 200 ms while running."""
+
+    FIELDS = ("index,clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.active,"
+              "clocks_event_reasons.hw_slowdown,clocks_event_reasons.hw_thermal_slowdown,"
+              "clocks_event_reasons.sw_thermal_slowdown,clocks_event_reasons.sw_power_cap")
+
+    def __init__(self, index: int):
+        self.index = index
+        self.proc = None
+
+    def __enter__(self):
+        try:
+            self.proc = subprocess.Popen(["nvidia-smi", f"--query-gpu={self.FIELDS}", "--format=csv,noheader,nounits",
+                                          "-lms", "200", "-i", str(self.index)], stdout=subprocess.PIPE,
+                                         stderr=subprocess.DEVNULL, text=True)
+        except Exception:
+            self.proc = None
+        return self
+
+    def __exit__(self, *exc):
+        self.lines = []
+        if self.proc is not None:
+            self.proc.terminate()
+            try:
+                out, _ = self.proc.communicate(timeout=5)
+            except Exception:
+                self.proc.kill()
+                out, _ = self.proc.communicate()
+            self.lines = [ln for ln in out.splitlines() if ln.strip()]
+
+    def summary(self):
+        sm, mx, reasons = [], None, set()
+        names = ["hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap"]
+        for ln in getattr(self, "lines", []):
+            f = [x.strip() for x in ln.split(",")]
+            if len(f) < 9:
+                continue
+            try:
+                sm.append(float(f[1]))
+                mx = float(f[2])
+            except ValueError:
+                continue
+            for n, v in zip(names, f[5:9]):
+                if v.lower() == "active":
+                    reasons.add(n)
+        if not sm:
+            return None
+        sm.sort()
+        return {"sm_mhz": sm[len(sm) // 2], "sm_max_mhz": mx, "reasons": sorted(reasons), "samples": len(sm)}
+
+
+# ----------------------------------------------------------------- CPU oracle leg
+def _oracle_item(args):
+    """One (sequence, head) fwd+bwd of the oracle; runs in a spawned worker."""
+    q, k, v, do, scale = args
+    from oracle import thd_oracle as orc
+    import numpy as np
+    L = q.shape[0]
+    cu = np.array([0, L], np.int32)
+    t0 = time.perf_counter()
+    orc.attn_fwd(q, k, v, cu, cu, softmax_scale=scale)
+    orc.attn_bwd(q, k, v, do, cu, cu, softmax_scale=scale)
+    return time.perf_counter() - t0
+
+
+def _oracle_items(w, t, heads):
+    G = w.Hq // w.Hkv
+    items = []
+    for b in range(w.B):
+        off = int(w.cu_seqlens_padded[b])
+        L = w.lengths[b]
+        if L == 0:
+            continue
+        for h in heads:
+            sl = slice(off, off + L)
+            items.append((t["q"][sl, h:h + 1].float().numpy(), t["k"][sl, h // G:h // G + 1].float().numpy(),
+                          t["v"][sl, h // G:h // G + 1].float().numpy(), t["do"][sl, h:h + 1].float().numpy(),
+                          w.softmax_scale))
+    return items
+
+
+def _sample_flops(w, heads):
+    from packed_sequence_context_gb300 import inputs
+    _, both = inputs.algorithmic_flops(w.lengths, 1, w.D)
+    return both * len(heads)
+
+
+def _spawn_pool(n):
+    import multiprocessing as mp
+    for k in ("OMP_NUM_THREADS", "OPENBLAS_NUM_THREADS", "MKL_NUM_THREADS"):
+        os.environ[k] = "1"
+    return mp.get_context("spawn").Pool(n)
+
+
+def cpu_baseline(w, t, target_s=15.0):
+    """Time the oracle (as it stands) on a bounded sample of the workload:
+    fwd+bwd of query heads 0, 1, 2, ... over every sequence, adding batches of
+    heads until about `target_s` seconds of host time (or the whole workload)."""
+    cores = os.cpu_count() or 1
+    n_seq = max(1, sum(1 for L in w.lengths if L))
+    per_batch = max(1, cores // n_seq)
+    done, spent = 0, 0.0
+    with _spawn_pool(cores) as pool:
+        while done < w.Hq and spent < target_s:
+            heads = list(range(done, min(w.Hq, done + per_batch)))
+            items = _oracle_items(w, t, heads)
+            t0 = time.perf_counter()
+            pool.map(_oracle_item, items)
+            spent += time.perf_counter() - t0
+            done += len(heads)
+    flops = _sample_flops(w, list(range(done)))
+    scope = "all" if done == w.Hq else f"0..{done - 1} of {w.Hq}"
+    return {"value": flops / spent / 1e12, "unit": UNIT, "cores": cores, "kind": "oracle",
+            "sample": f"fp64 oracle fwd+bwd of query heads {scope} over all {w.B} sequences of the "
+                      f"'{w.name}' workload ({spent:.1f} s, process pool of {cores}, one BLAS thread each)",
+            "seconds": spent}
+
+
+# ----------------------------------------------------------------- reference arm
+def run_reference(a):
+    rank = int(os.environ.get("RANK", "0"))
+    if rank != 0:
+        return 0
+    from packed_sequence_context_gb300 import inputs
+    w = inputs.make_workload(a.config)
+    t = inputs.make_tensors(w, with_grad=True)
+    cores = os.cpu_count() or 1
+    fwd_only = a.fwd_only
+    with _spawn_pool(cores) as pool:
+        times = []
+        for i in range(a.warmup + a.steps):
+            h = i % w.Hq
+            items = _oracle_items(w, t, [h])
+            t0 = time.perf_counter()
+            pool.map(_oracle_item, items)
+            dt = time.perf_counter() - t0
+            if i >= a.warmup:
+                times.append(dt)
+    flops = _sample_flops(w, [0])
+    mean = sum(times) / len(times)
+    value = flops / mean / 1e12
+    line = {"impl": "reference", "metric": METRIC, "value": value, "unit": UNIT, "n_gpus": a.gpus,
+            "steps": a.steps, "warmup": a.warmup, "ms_per_step": mean * 1e3, "higher_is_better": True,
+            "scaling": "weak", "vs_baseline": None, "dtype": "f64", "data": "synthetic",
+            "config": {"workload": w.name, "sequences": w.B, "tokens": w.T, "Hq": w.Hq, "Hkv": w.Hkv, "D": w.D,
+                       "cp_size": w.cp_size, "causal": True, "step": "fwd+bwd" if not fwd_only else "fwd",
+                       "sample": "one query head (rotating) over all sequences per step"},
+            "cpu_baseline": {"value": value, "unit": UNIT, "cores": cores, "kind": "oracle",
+                             "sample": "fp64 oracle fwd+bwd, one query head over all sequences per step"},
+            "e2e": {"value": value, "unit": UNIT, "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0}}
+    print(json.dumps(line), flush=True)
+    return 0
+
+
+# ----------------------------------------------------------------- GPU arm
+def run_ours(a):
+    import torch
+    import torch.distributed as dist
+
+    from packed_sequence_context_gb300 import inputs
+    from packed_sequence_context_gb300 import thd_attn as T
+
+    world = int(os.environ.get("WORLD_SIZE", "1"))
+    rank = int(os.environ.get("RANK", "0"))
+    local = int(os.environ.get("LOCAL_RANK", "0"))
+    if not torch.cuda.is_available():
+        raise SystemExit("bench.py needs a CUDA GPU")
+    torch.cuda.set_device(local)
+    if world > 1:
+        dist.init_process_group("nccl", device_id=torch.device("cuda", local))
+    T.lib()
+    peak, peak_sus, hbm, peak_kind = _peaks()
+
+    w = inputs.make_workload(a.config)
+    t = inputs.make_tensors(w, with_grad=True)
+    # the CPU leg runs first, before this process touches the GPU with work
+    cpu = None
+    if rank == 0 and world == 1 and not a.no_cpu_baseline:
+        cpu = cpu_baseline(w, t)
+
+    dev = torch.device("cuda", local)
+    q, k, v, do = (t[x].to(dev) for x in ("q", "k", "v", "do"))
+    cu = torch.from_numpy(w.cu_seqlens).to(dev)
+    cu_pad = torch.from_numpy(w.cu_seqlens_padded).to(dev)
+    B, Tq = w.B, w.T
+    o = torch.empty_like(q)
+    lse = torch.empty((w.Hq, Tq), dtype=torch.float32, device=dev)
+    dq = torch.empty((w.dq_rows, w.Hq, w.D), dtype=torch.bfloat16, device=dev)
+    dk = torch.empty((w.dkv_rows, w.Hkv, w.D), dtype=torch.bfloat16, device=dev)
+    dv = torch.empty_like(dk)
+    st = torch.zeros(1, dtype=torch.int32, device=dev)
+    wsf = torch.empty(T.thd_workspace_size(B, Tq, Tq, w.Hq, w.Hkv, w.D, w.cp_size, 0), dtype=torch.uint8, device=dev)
+    wsb = torch.empty(T.thd_workspace_size(B, Tq, Tq, w.Hq, w.Hkv, w.D, w.cp_size, 1), dtype=torch.uint8, device=dev)
+    flush_buf = torch.empty(256 << 20, dtype=torch.uint8, device=dev)
+    stream = torch.cuda.current_stream()
+    sptr = stream.cuda_stream
+
+    def fwd():
+        rc = T.thd_attn_fwd(q, k, v, o, lse, cu, cu, cu_pad, cu_pad, B, Tq, Tq, w.Hq, w.Hkv, w.D, 1,
+                            w.softmax_scale, w.cp_size, -1, wsf, wsf.numel(), st, sptr)
+        assert rc == 0, T.thd_status_string(rc)
+
+    def bwd():
+        rc = T.thd_attn_bwd(q, k, v, o, lse, do, dq, dk, dv, w.dq_rows, w.dkv_rows, cu, cu, cu_pad, cu_pad, B, Tq,
+                            Tq, w.Hq, w.Hkv, w.D, 1, w.softmax_scale, w.cp_size, -1, wsb, wsb.numel(), st, sptr)
+        assert rc == 0, T.thd_status_string(rc)
+
+    def step():
+        fwd()
+        if not a.fwd_only:
+            bwd()
+
+    def timed(fn, n, kernel_id):
+        evs = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)) for _ in range(n)]
+        T.thd_profile_enable(kernel_id, n)
+        n0 = T.thd_launch_count()
+        if world > 1:
+            dist.barrier()
+        torch.cuda.synchronize()
+        for e0, e1 in evs:
+            flush_buf.zero_()
+            e0.record(stream)
+            fn()
+            e1.record(stream)
+        torch.cuda.synchronize()
+        if world > 1:
+            dist.barrier()
+        launches = T.thd_launch_count() - n0
+        kms = T.thd_profile_read(n)
+        T.thd_profile_enable(0, 0)
+        return [e0.elapsed_time(e1) for e0, e1 in evs], kms, launches
+
+    fwd_flops, both_flops = inputs.algorithmic_flops(w.lengths, w.Hq, w.D)
+    step_flops = fwd_flops if a.fwd_only else both_flops
+    for _ in range(max(a.warmup, 3)):
+        flush_buf.zero_()
+        step()
+    torch.cuda.synchronize()
+    assert int(st.item()) == 0, T.thd_status_string(int(st.item()))
+
+    main_kernel = T.THD_KERNEL_FWD if a.fwd_only else T.THD_KERNEL_BWD
+    with ClockSampler(local) as clk:
+        times, kms, launches = timed(step, a.steps, main_kernel)
+        fwd_times, fwd_kms, _ = timed(fwd, a.steps, T.THD_KERNEL_FWD)
+    assert int(st.item()) == 0, T.thd_status_string(int(st.item()))
+
+    ms = sum(times) / len(times)
+    ms_t = torch.tensor([ms], device=dev)
+    if world > 1:
+        dist.all_reduce(ms_t, op=dist.ReduceOp.MAX)
+    ms_max = float(ms_t.item())
+    value = step_flops * world / (ms_max * 1e-3) / 1e12
+    fwd_ms = sum(fwd_times) / len(fwd_times)
+    fwd_tflops = fwd_flops / (fwd_ms * 1e-3) / 1e12
+
+    main_flops = fwd_flops if a.fwd_only else 2.5 * fwd_flops
+    kavg = sum(kms) / len(kms) if kms else float("nan")
+    achieved = main_flops / (kavg * 1e-3) / 1e12
+    fk = sum(fwd_kms) / len(fwd_kms) if fwd_kms else float("nan")
+    fwd_kernel_tflops = fwd_flops / (fk * 1e-3) / 1e12
+
+    e2e = None
+    if not a.no_e2e:
+        e2e = e2e_measure(a, w, t, dev, stream, step_flops)
+
+    if rank == 0:
+        line = {
+            "metric": METRIC, "value": value, "unit": UNIT, "n_gpus": world, "steps": a.steps, "warmup": a.warmup,
+            "ms_per_step": ms_max, "higher_is_better": True, "scaling": "weak", "vs_baseline": None,
+            "dtype": "bf16", "data": "synthetic",
+            "config": {"workload": w.name, "sequences": w.B, "tokens": w.T, "Hq": w.Hq, "Hkv": w.Hkv, "D": w.D,
+                       "cp_size": w.cp_size, "causal": True, "step": "fwd" if a.fwd_only else "fwd+bwd",
+                       "grad_rows": w.dq_rows, "l2": "flushed between timed steps (256 MiB write)",
+                       "parallelism": f"replicas x{world}"},
+            "fwd_tflops": fwd_tflops, "fwd_ms": fwd_ms, "fwd_frac_of_peak": fwd_tflops / peak,
+            "roofline": {"bound": "tensor", "kernel": "bwd_kernel" if not a.fwd_only else "fwd_kernel",
+                         "achieved": achieved, "peak": peak, "unit": "TFLOP/s", "frac": achieved / peak,
+                         "peak_kind": f"bf16 burst ({peak_kind})", "frac_of_sustained": achieved / peak_sus,
+                         "kernel_ms": kavg, "traffic": None},
+            "fwd_roofline": {"bound": "tensor", "kernel": "fwd_kernel", "achieved": fwd_kernel_tflops, "peak": peak,
+                             "unit": "TFLOP/s", "frac": fwd_kernel_tflops / peak, "kernel_ms": fk},
+            "gpu_launches": launches,
+            "clocks": clk.summary(),
+            "cpu_baseline": cpu,
+            "e2e": e2e,
+        }
+        print(json.dumps(line), flush=True)
+    if world > 1:
+        dist.destroy_process_group()
+    return 0
+
+
+def e2e_measure(a, w, t, dev, stream, step_flops):
+    """Same metric through the public API with host buffers: pinned H2D of the
+    step's inputs and metadata, the calls, and D2H of O, lse, dQ, dK, dV."""
+    import torch
+
+    from packed_sequence_context_gb300 import thd_attn as T
+
+    host = {x: t[x].pin_memory() for x in ("q", "k", "v", "do")}
+    cu_h = torch.from_numpy(w.cu_seqlens).pin_memory()
+    cup_h = torch.from_numpy(w.cu_seqlens_padded).pin_memory()
+    dev_in = {x: torch.empty_like(host[x], device=dev) for x in host}
+    cu_d = torch.empty_like(cu_h, device=dev)
+    cup_d = torch.empty_like(cup_h, device=dev)
+    outs = None
+    h2d = sum(x.numel() * x.element_size() for x in host.values()) + 2 * cu_h.numel() * 4
+    n = max(3, min(a.steps, 20))
+    evs = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)) for _ in range(n + 2)]
+    host_out = None
+    times = []
+    for i, (e0, e1) in enumerate(evs):
+        e0.record(stream)
+        for x in host:
+            dev_in[x].copy_(host[x], non_blocking=True)
+        cu_d.copy_(cu_h, non_blocking=True)
+        cup_d.copy_(cup_h, non_blocking=True)
+        o, lse, st = T.attn_fwd(dev_in["q"], dev_in["k"], dev_in["v"], cu_d, cu_d, cup_d, cup_d,
+                                cp_size=w.cp_size, softmax_scale=w.softmax_scale)
+        res = [o, lse]
+        if not a.fwd_only:
+            dq, dk, dv, st2 = T.attn_bwd(dev_in["q"], dev_in["k"], dev_in["v"], o, lse, dev_in["do"], cu_d, cu_d,
+                                         cup_d, cup_d, cp_size=w.cp_size, softmax_scale=w.softmax_scale,
+                                         dq_rows=w.dq_rows, dkv_rows=w.dkv_rows)
+            res += [dq, dk, dv]
+        if host_out is None:
+            host_out = [torch.empty(r.shape, dtype=r.dtype, pin_memory=True) for r in res]
+        for hd, r in zip(host_out, res):
+            hd.copy_(r, non_blocking=True)
+        e1.record(stream)
+        stream.synchronize()
+        if i >= 2:
+            times.append(e0.elapsed_time(e1))
+    d2h = sum(x.numel() * x.element_size() for x in host_out)
+    ms = sum(times) / len(times)
+    return {"value": step_flops / (ms * 1e-3) / 1e12, "unit": UNIT, "ms_per_step": ms,
+            "h2d_bytes_per_step": int(h2d), "d2h_bytes_per_step": int(d2h)}
+
+
+def main():
+    a = _args()
+    from packed_sequence_context_gb300.inputs import CONFIG_ALIASES
+    a.config = CONFIG_ALIASES.get(a.config, a.config)
+    if a.impl == "reference":
+        return run_reference(a)
+    return run_ours(a)
+
+
+if __name__ == "__main__":
+    sys.exit(main())

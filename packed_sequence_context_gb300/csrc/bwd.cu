@@ -1,8 +1,466 @@
-// Backward attention (placeholder until the tcgen05 kernel lands).
+// Backward attention over packed THD tensors, key/value-stationary, walked in
+// P2P ring order and executed for every emulated rank on one GB300.
+//
+// [P2] TransformerEngine issue #3487 ("Steps/Code to reproduce bug": BF16
+// attention forward/backward on this layout with four-rank P2P context
+// parallelism; "Describe the bug": THD dQ/dK/dV tail-zeroing).  [P1]
+// TransformerEngine issue #2208 (traceback through AttnFuncWithCPAndKVP2P):
+// in the ring, the KV of owner rank s is seen by rank r = (s + i) mod cp at
+// step i, and dK/dV travel back around the ring to their owner.  Here the
+// owner keeps its key tile in shared memory and visits, in ring order, the
+// query tiles of every rank that sees it; dK/dV accumulate in TMEM (no
+// travel), dQ goes to an fp32 accumulator with vector atomics.
+//
+// One work item = (sequence b, key chunk c, key tile jk within the chunk, kv
+// head hk).  For each query tile (chunk qc, tile jq) that sees it and each
+// query head h of the GQA group:
+//   S^T  = K Q^T            (TMEM X)     dP^T = V dO^T         (TMEM Y)
+//   P^T  = exp(S^T scale - lse)          dS^T = P^T (dP^T - Delta)
+//   dV  += P^T dO   (A = P^T from TMEM)  dK  += dS^T Q   (A = dS^T, smem)
+//   dQ   = dS K     (A = dS, the same smem read MN-major; into TMEM Y)
+// CTA: warps 0-3 compute (one key row per thread = TMEM lane; one query row
+// per thread when draining dQ), warp 4 TMA producer (+ lse/Delta staging),
+// warp 5 TMEM allocator and single-thread MMA issuer.
 #include "common.cuh"
+#include "ptx.cuh"
+
 namespace thd {
-cudaError_t launch_bwd(const BwdParams&, const CUtensorMap&, const CUtensorMap&, const CUtensorMap&,
-                       const CUtensorMap&, int, int, cudaStream_t) {
-  return cudaErrorNotSupported;
+
+template <int D>
+struct BwdCfg {
+  static constexpr int kStages = 2;
+  static constexpr int kTileBytes = kTile * D * 2;  // one [128, D] bf16 tile
+  static constexpr int kOffK = 0;
+  static constexpr int kOffV = kTileBytes;
+  static constexpr int kOffQ = 2 * kTileBytes;                 // stage s: Q at kOffQ + s * 2 * kTileBytes
+  static constexpr int kOffDS = kOffQ + kStages * 2 * kTileBytes;
+  static constexpr int kOffLse = kOffDS + kTile * kTile * 2;   // stage s: lse2[128], delta[128]
+  static constexpr int kOffBar = kOffLse + kStages * 2 * kTile * 4;
+  static constexpr int kSmem = kOffBar + 256;
+  static constexpr uint32_t kTmemCols = 512;
+  static constexpr uint32_t kColDV = 0, kColDK = D, kColX = 2 * D, kColY = 2 * D + 128;
+};
+
+struct BwdItem {
+  SeqGeom g;
+  int b, c, jk, hk;
+  int kv_first, kv_last;  // valid key positions of the tile (first > last: none)
+};
+
+__device__ inline BwdItem bwd_item(const BwdParams& p, int w) {
+  BwdItem it;
+  const int4 e = p.items[w / p.Hkv];
+  it.hk = w % p.Hkv;
+  it.b = e.x;
+  it.c = e.y;
+  it.jk = e.z;
+  it.g = seq_geom(p.eff, p.B, it.b, p.cp);
+  bwd_kv_range(it.g, it.c, it.jk, it.kv_first, it.kv_last);
+  return it;
 }
+
+// Calls f(qc, jq, h) for every (query tile, query head) that sees the item's
+// key tile, in ring order of the ranks holding the key tile.
+template <typename F>
+__device__ inline void for_each_q_step(const BwdItem& it, const BwdParams& p, F&& f) {
+  if (it.kv_first > it.kv_last) return;
+  const int G = p.Hq / p.Hkv;
+  const int s = chunk_owner(it.c, p.cp);
+  const int nq = ceil_div(it.g.cbq, kTile);
+  for (int i = 0; i < p.cp; ++i) {
+    const int r = (s + i) % p.cp;
+    for (int e = 0; e < 2; ++e) {
+      const int qc = e == 0 ? r : 2 * p.cp - 1 - r;
+      for (int jq = 0; jq < nq; ++jq) {
+        if (!bwd_q_tile_visits(it.g, qc, jq, it.kv_first, it.kv_last, p.causal != 0)) continue;
+        for (int hh = 0; hh < G; ++hh) f(qc, jq, it.hk * G + hh);
+      }
+    }
+  }
+}
+
+__device__ inline void drain_wait_b(uint64_t* bar, uint32_t parity) {
+  const uint64_t t0 = globaltimer();
+  while (!mbar_try_wait(bar, parity)) {
+    if (globaltimer() - t0 > kWaitTimeoutNs) break;
+  }
+}
+
+template <int D>
+__global__ void __launch_bounds__(192, 1)
+    bwd_kernel(const BwdParams p, const __grid_constant__ CUtensorMap tmQ, const __grid_constant__ CUtensorMap tmDO,
+               const __grid_constant__ CUtensorMap tmK, const __grid_constant__ CUtensorMap tmV) {
+  using C = BwdCfg<D>;
+  constexpr int S = C::kStages;
+  extern __shared__ __align__(1024) uint8_t smem[];
+  uint8_t* sK = smem + C::kOffK;
+  uint8_t* sV = smem + C::kOffV;
+  uint8_t* sDS = smem + C::kOffDS;
+  float* sLse = reinterpret_cast<float*>(smem + C::kOffLse);  // stage s: [s*256, s*256+128) lse2, then delta
+  uint64_t* bars = reinterpret_cast<uint64_t*>(smem + C::kOffBar);
+  uint64_t* bar_kv_full = bars + 0;
+  uint64_t* bar_kv_empty = bars + 1;
+  uint64_t* bar_qdo_full = bars + 2;       // [S]
+  uint64_t* bar_qdo_empty = bars + 2 + S;  // [S]
+  uint64_t* bar_st_full = bars + 2 + 2 * S;
+  uint64_t* bar_p_ready = bars + 3 + 2 * S;
+  uint64_t* bar_dq_full = bars + 4 + 2 * S;
+  uint64_t* bar_y_free = bars + 5 + 2 * S;
+  uint64_t* bar_drain = bars + 6 + 2 * S;
+  uint32_t* s_tmem = reinterpret_cast<uint32_t*>(bars + 8 + 2 * S);
+  int* s_abort = reinterpret_cast<int*>(bars + 9 + 2 * S);
+
+  const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
+  if (*p.dev_status != 0) return;
+  if ((smem_u32(smem) & 1023u) != 0) {  // the swizzled tiles need a 1024-byte aligned base
+    if (tid == 0) atomicCAS(p.dev_status, 0, THD_ERR_UNSUPPORTED);
+    return;
+  }
+  const int n_items = p.counters[0] * p.Hkv;
+
+  if (tid == 0) {
+    mbar_init(bar_kv_full, 1);
+    mbar_init(bar_kv_empty, 1);
+    for (int s = 0; s < S; ++s) {
+      mbar_init(&bar_qdo_full[s], 32);
+      mbar_init(&bar_qdo_empty[s], 1);
+    }
+    mbar_init(bar_st_full, 1);
+    mbar_init(bar_p_ready, 128);
+    mbar_init(bar_dq_full, 1);
+    mbar_init(bar_y_free, 128);
+    mbar_init(bar_drain, 1);
+    *s_abort = 0;
+    fence_mbar_init();
+  }
+  if (warp == 5) {
+    tmem_alloc(s_tmem, C::kTmemCols);
+    tmem_relinquish();
+  }
+  if (warp == 4 && lane == 0) {
+    tma_prefetch_desc(&tmQ);
+    tma_prefetch_desc(&tmDO);
+    tma_prefetch_desc(&tmK);
+    tma_prefetch_desc(&tmV);
+  }
+  tc_fence_before();
+  __syncthreads();
+  tc_fence_after();
+  const uint32_t tmem = *s_tmem;
+  constexpr float kLog2e = 1.4426950408889634f;
+
+  if (warp == 4) {
+    // ------------------------------------------------------------ producer (whole warp)
+    int stage = 0;
+    uint32_t ph = 0, kv_iter = 0;
+    int fills[S];
+    for (int s = 0; s < S; ++s) fills[s] = 0;
+    int kv_fills = 0;
+    bool ok = true;
+    for (int w = blockIdx.x; w < n_items && ok; w += gridDim.x) {
+      const BwdItem it = bwd_item(p, w);
+      if (it.kv_first > it.kv_last) continue;  // no valid key: nothing to load
+      const int kv_row = it.g.kv_off + it.c * it.g.cbkv + it.jk * kTile;
+      if (!mbar_wait(bar_kv_empty, (kv_iter & 1u) ^ 1u, s_abort)) break;
+      if (lane == 0) {
+        mbar_arrive_expect_tx(bar_kv_full, 2 * C::kTileBytes);
+#pragma unroll
+        for (int hb = 0; hb < D / 64; ++hb) {
+          tma_load_3d(smem_u32(sK + hb * 16384), &tmK, bar_kv_full, hb * 64, it.hk, kv_row);
+          tma_load_3d(smem_u32(sV + hb * 16384), &tmV, bar_kv_full, hb * 64, it.hk, kv_row);
+        }
+      }
+      ++kv_fills;
+      ++kv_iter;
+      for_each_q_step(it, p, [&](int qc, int jq, int h) {
+        if (!ok) return;
+        if (!mbar_wait(&bar_qdo_empty[stage], ph ^ 1u, s_abort)) {
+          ok = false;
+          return;
+        }
+        const int q0 = qc * it.g.cbq + jq * kTile;
+        const int nqv = imin(imin(kTile, it.g.cbq - jq * kTile), it.g.Lq - q0);
+        const int q_row = it.g.q_off + q0;
+        float* lse2 = sLse + stage * 256;
+        float* dl = lse2 + 128;
+#pragma unroll
+        for (int k = 0; k < 4; ++k) {
+          const int n = lane + 32 * k;
+          const bool v = n < nqv;
+          const int64_t idx = (int64_t)h * p.T_q + q_row + n;
+          lse2[n] = v ? p.lse[idx] * kLog2e : 0.f;
+          dl[n] = v ? p.delta[idx] : 0.f;
+        }
+        __syncwarp();
+        if (lane == 0) {
+          mbar_arrive_expect_tx(&bar_qdo_full[stage], 2 * C::kTileBytes);
+          uint8_t* sQ = smem + C::kOffQ + stage * 2 * C::kTileBytes;
+          uint8_t* sDO = sQ + C::kTileBytes;
+#pragma unroll
+          for (int hb = 0; hb < D / 64; ++hb) {
+            tma_load_3d(smem_u32(sQ + hb * 16384), &tmQ, &bar_qdo_full[stage], hb * 64, h, q_row);
+            tma_load_3d(smem_u32(sDO + hb * 16384), &tmDO, &bar_qdo_full[stage], hb * 64, h, q_row);
+          }
+        } else {
+          mbar_arrive(&bar_qdo_full[stage]);
+        }
+        ++fills[stage];
+        if (++stage == S) {
+          stage = 0;
+          ph ^= 1u;
+        }
+      });
+    }
+    if (lane == 0) {
+      if (kv_fills > 0) drain_wait_b(bar_kv_full, (uint32_t)(kv_fills - 1) & 1u);
+      for (int s = 0; s < S; ++s)
+        if (fills[s] > 0) drain_wait_b(&bar_qdo_full[s], (uint32_t)(fills[s] - 1) & 1u);
+    }
+    __syncwarp();
+  } else if (warp == 5) {
+    // ------------------------------------------------------------ MMA issuer
+    if (lane == 0) {
+      constexpr uint32_t idesc_t = idesc_bf16(128, 128, false, false);  // S^T, dP^T
+      constexpr uint32_t idesc_kv = idesc_bf16(128, D, false, true);    // dV, dK (B MN-major)
+      constexpr uint32_t idesc_q = idesc_bf16(128, D, true, true);      // dQ (A and B MN-major)
+      const uint32_t kb = smem_u32(sK), vb = smem_u32(sV), dsb = smem_u32(sDS);
+      int stage = 0;
+      uint32_t ph = 0, su = 0, kv_iter = 0;
+      bool ok = true;
+      for (int w = blockIdx.x; w < n_items && ok; w += gridDim.x) {
+        const BwdItem it = bwd_item(p, w);
+        if (it.kv_first > it.kv_last) continue;
+        if (!mbar_wait(bar_kv_full, kv_iter & 1u, s_abort)) break;
+        ++kv_iter;
+        tc_fence_after();
+        bool first = true;
+        for_each_q_step(it, p, [&](int, int, int) {
+          if (!ok) return;
+          if (!mbar_wait(&bar_qdo_full[stage], ph, s_abort)) {
+            ok = false;
+            return;
+          }
+          tc_fence_after();
+          const uint32_t qb = smem_u32(smem + C::kOffQ + stage * 2 * C::kTileBytes);
+          const uint32_t dob = qb + C::kTileBytes;
+          // S^T = K Q^T -> X
+#pragma unroll
+          for (int ks = 0; ks < D / 16; ++ks) {
+            const uint32_t off = (ks >> 2) * 16384 + (ks & 3) * 32;
+            mma_ss(tmem + C::kColX, sdesc_sw128(kb + off, 16, 1024), sdesc_sw128(qb + off, 16, 1024), idesc_t,
+                   ks > 0);
+          }
+          // dP^T = V dO^T -> Y, once the previous step's dQ has been drained from Y
+          if (su > 0 && !mbar_wait(bar_y_free, (su - 1) & 1u, s_abort)) {
+            ok = false;
+            return;
+          }
+          tc_fence_after();
+#pragma unroll
+          for (int ks = 0; ks < D / 16; ++ks) {
+            const uint32_t off = (ks >> 2) * 16384 + (ks & 3) * 32;
+            mma_ss(tmem + C::kColY, sdesc_sw128(vb + off, 16, 1024), sdesc_sw128(dob + off, 16, 1024), idesc_t,
+                   ks > 0);
+          }
+          tc_commit(bar_st_full);
+          if (!mbar_wait(bar_p_ready, su & 1u, s_abort)) {
+            ok = false;
+            return;
+          }
+          tc_fence_after();
+          // dV += P^T dO  (P^T packed bf16 in X)
+#pragma unroll
+          for (int ks = 0; ks < kTile / 16; ++ks)
+            mma_ts(tmem + C::kColDV, tmem + C::kColX + ks * 8, sdesc_sw128(dob + ks * 2048, 16384, 1024), idesc_kv,
+                   (first && ks == 0) ? 0u : 1u);
+          // dK += dS^T Q
+#pragma unroll
+          for (int ks = 0; ks < kTile / 16; ++ks)
+            mma_ss(tmem + C::kColDK, sdesc_sw128(dsb + (ks >> 2) * 16384 + (ks & 3) * 32, 16, 1024),
+                   sdesc_sw128(qb + ks * 2048, 16384, 1024), idesc_kv, (first && ks == 0) ? 0u : 1u);
+          // dQ = dS K -> Y
+#pragma unroll
+          for (int ks = 0; ks < kTile / 16; ++ks)
+            mma_ss(tmem + C::kColY, sdesc_sw128(dsb + ks * 2048, 16384, 1024),
+                   sdesc_sw128(kb + ks * 2048, 16384, 1024), idesc_q, ks > 0);
+          tc_commit(bar_dq_full);
+          tc_commit(&bar_qdo_empty[stage]);
+          first = false;
+          ++su;
+          if (++stage == S) {
+            stage = 0;
+            ph ^= 1u;
+          }
+        });
+        if (ok) tc_commit(bar_kv_empty);
+      }
+      tc_commit(bar_drain);
+      drain_wait_b(bar_drain, 0);
+    }
+    __syncwarp();
+  } else {
+    // ------------------------------------------------------------ compute warps
+    const uint32_t lane_base = (uint32_t)(warp * 32) << 16;
+    const float sl2 = p.scale_log2;
+    uint32_t su = 0;
+    bool ok = true;
+    for (int w = blockIdx.x; w < n_items && ok; w += gridDim.x) {
+      const BwdItem it = bwd_item(p, w);
+      const int kv_local = it.jk * kTile + tid;  // row within the chunk
+      const int j_pos = it.c * it.g.cbkv + kv_local;
+      const bool in_chunk = kv_local < it.g.cbkv;
+      const bool valid_kv = in_chunk && j_pos < it.g.Lkv;
+      int nsteps = 0;
+      for_each_q_step(it, p, [&](int qc, int jq, int h) {
+        if (!ok) return;
+        if (!mbar_wait(bar_st_full, su & 1u, s_abort)) {
+          ok = false;
+          return;
+        }
+        tc_fence_after();
+        const int q0 = qc * it.g.cbq + jq * kTile;
+        const int nqv = imin(imin(kTile, it.g.cbq - jq * kTile), it.g.Lq - q0);
+        int n_lo = 0, n_hi = valid_kv ? nqv : 0;
+        if (p.causal) n_lo = imin(imax(j_pos - q0, 0), kTile);
+        const float* lse2 = sLse + (su % S) * 256;
+        const float* dl = lse2 + 128;
+#pragma unroll 1
+        for (int kk = 0; kk < 4; ++kk) {
+          uint32_t sr[32], dr[32];
+          tmem_ld32(tmem + lane_base + C::kColX + 32 * kk, sr);
+          tmem_ld32(tmem + lane_base + C::kColY + 32 * kk, dr);
+          tmem_ld_wait(sr);
+          tmem_ld_wait(dr);
+          uint32_t pk[16], dk[16];
+#pragma unroll
+          for (int n2 = 0; n2 < 16; ++n2) {
+            float pp[2], dd[2];
+#pragma unroll
+            for (int e = 0; e < 2; ++e) {
+              const int n = 32 * kk + 2 * n2 + e;
+              const bool a = n >= n_lo && n < n_hi;
+              const float pv = a ? ex2(fmaf(__uint_as_float(sr[2 * n2 + e]), sl2, -lse2[n])) : 0.f;
+              pp[e] = pv;
+              dd[e] = pv * (__uint_as_float(dr[2 * n2 + e]) - dl[n]);
+            }
+            pk[n2] = pack_bf16x2(pp[0], pp[1]);
+            dk[n2] = pack_bf16x2(dd[0], dd[1]);
+          }
+          tmem_st16(tmem + lane_base + C::kColX + 16 * kk, pk);
+#pragma unroll
+          for (int i = 0; i < 4; ++i)
+            *reinterpret_cast<uint4*>(sDS + sw128_offset(tid, 32 * kk + 8 * i, kTile)) =
+                make_uint4(dk[4 * i], dk[4 * i + 1], dk[4 * i + 2], dk[4 * i + 3]);
+        }
+        tmem_st_wait();
+        fence_proxy_async_smem();
+        tc_fence_before();
+        mbar_arrive(bar_p_ready);
+        // drain dQ (one query row per thread) into the fp32 accumulator
+        if (!mbar_wait(bar_dq_full, su & 1u, s_abort)) {
+          ok = false;
+          return;
+        }
+        tc_fence_after();
+        const bool q_live = tid < nqv && (!p.causal || q0 + tid >= it.kv_first);
+        float* dst = p.dq_acc + (((int64_t)it.g.q_off + q0 + tid) * p.Hq + h) * D;
+#pragma unroll 1
+        for (int kk = 0; kk < D / 32; ++kk) {
+          uint32_t r[32];
+          tmem_ld32(tmem + lane_base + C::kColY + 32 * kk, r);
+          tmem_ld_wait(r);
+          if (q_live) {
+#pragma unroll
+            for (int i = 0; i < 8; ++i)
+              atomicAdd(reinterpret_cast<float4*>(dst + 32 * kk + 4 * i),
+                        make_float4(__uint_as_float(r[4 * i]), __uint_as_float(r[4 * i + 1]),
+                                    __uint_as_float(r[4 * i + 2]), __uint_as_float(r[4 * i + 3])));
+          }
+        }
+        tc_fence_before();
+        mbar_arrive(bar_y_free);
+        ++su;
+        ++nsteps;
+      });
+      if (!ok) break;
+      // ---- epilogue: dK (scaled) and dV of this key tile, zeros on pad rows
+#pragma unroll 1
+      for (int kk = 0; kk < D / 32; ++kk) {
+        uint32_t a[32], bq[32];
+        if (nsteps > 0) {
+          tmem_ld32(tmem + lane_base + C::kColDK + 32 * kk, a);
+          tmem_ld32(tmem + lane_base + C::kColDV + 32 * kk, bq);
+          tmem_ld_wait(a);
+          tmem_ld_wait(bq);
+        } else {
+#pragma unroll
+          for (int n = 0; n < 32; ++n) {
+            a[n] = 0u;
+            bq[n] = 0u;
+          }
+        }
+        if (in_chunk) {
+          const float fk = valid_kv ? p.scale : 0.f;
+          const float fv = valid_kv ? 1.f : 0.f;
+          const int64_t grow = (int64_t)it.g.kv_off + j_pos;
+          uint4* dkp = reinterpret_cast<uint4*>(p.dk + (grow * p.Hkv + it.hk) * D + 32 * kk);
+          uint4* dvp = reinterpret_cast<uint4*>(p.dv + (grow * p.Hkv + it.hk) * D + 32 * kk);
+#pragma unroll
+          for (int n = 0; n < 4; ++n) {
+            uint4 x, y;
+            x.x = pack_bf16x2(__uint_as_float(a[8 * n + 0]) * fk, __uint_as_float(a[8 * n + 1]) * fk);
+            x.y = pack_bf16x2(__uint_as_float(a[8 * n + 2]) * fk, __uint_as_float(a[8 * n + 3]) * fk);
+            x.z = pack_bf16x2(__uint_as_float(a[8 * n + 4]) * fk, __uint_as_float(a[8 * n + 5]) * fk);
+            x.w = pack_bf16x2(__uint_as_float(a[8 * n + 6]) * fk, __uint_as_float(a[8 * n + 7]) * fk);
+            y.x = pack_bf16x2(__uint_as_float(bq[8 * n + 0]) * fv, __uint_as_float(bq[8 * n + 1]) * fv);
+            y.y = pack_bf16x2(__uint_as_float(bq[8 * n + 2]) * fv, __uint_as_float(bq[8 * n + 3]) * fv);
+            y.z = pack_bf16x2(__uint_as_float(bq[8 * n + 4]) * fv, __uint_as_float(bq[8 * n + 5]) * fv);
+            y.w = pack_bf16x2(__uint_as_float(bq[8 * n + 6]) * fv, __uint_as_float(bq[8 * n + 7]) * fv);
+            dkp[n] = x;
+            dvp[n] = y;
+          }
+        }
+      }
+      tc_fence_before();
+    }
+    // ---- dK/dV rows past the last sequence: zero
+    if (ok) {
+      const int Tend = p.eff[3 * (p.B + 1) + p.B];
+      const int64_t nvec = (p.dkv_rows - Tend) * (int64_t)p.Hkv * (D / 8);
+      const int64_t base = (int64_t)Tend * p.Hkv * D;
+      for (int64_t i = (int64_t)blockIdx.x * 128 + tid; i < nvec; i += (int64_t)gridDim.x * 128) {
+        reinterpret_cast<uint4*>(p.dk + base)[i] = make_uint4(0, 0, 0, 0);
+        reinterpret_cast<uint4*>(p.dv + base)[i] = make_uint4(0, 0, 0, 0);
+      }
+    }
+  }
+
+  tc_fence_before();
+  __syncthreads();
+  if (warp == 5) {
+    tc_fence_after();
+    tmem_dealloc(tmem, C::kTmemCols);
+  }
+  if (tid == 0 && *s_abort) atomicCAS(p.dev_status, 0, THD_ERR_TIMEOUT);
+}
+
+template <int D>
+static cudaError_t launch_bwd_t(const BwdParams& p, const CUtensorMap& tq, const CUtensorMap& tdo,
+                                const CUtensorMap& tk, const CUtensorMap& tv, int grid, cudaStream_t st) {
+  using C = BwdCfg<D>;
+  cudaError_t e = cudaFuncSetAttribute(bwd_kernel<D>, cudaFuncAttributeMaxDynamicSharedMemorySize, C::kSmem);
+  if (e != cudaSuccess) return e;
+  prof_before(THD_KERNEL_BWD, st);
+  bwd_kernel<D><<<grid, 192, C::kSmem, st>>>(p, tq, tdo, tk, tv);
+  count_launch();
+  e = cudaGetLastError();
+  prof_after(THD_KERNEL_BWD, st);
+  return e;
+}
+
+cudaError_t launch_bwd(const BwdParams& p, const CUtensorMap& tq, const CUtensorMap& tdo, const CUtensorMap& tk,
+                       const CUtensorMap& tv, int D, int grid, cudaStream_t st) {
+  return D == 128 ? launch_bwd_t<128>(p, tq, tdo, tk, tv, grid, st) : launch_bwd_t<64>(p, tq, tdo, tk, tv, grid, st);
+}
+
 }  // namespace thd
