@@ -182,6 +182,39 @@ THD_API int thd_attn_fwd_step(const void* q, const void* k, const void* v, float
                       void* workspace, size_t workspace_bytes, int32_t* dev_status, thd_stream_t stream);
 
 /*
+ * thd_attn_fwd_noalloc -- thd_attn_fwd for callers that cannot allocate device
+ * memory where they call the library.  The pages have no counterpart to
+ * this entry point; it exists for deployment.  Examples of such callers: a
+ * plug-in that only receives input and output pointers from a host framework
+ * whose own pool allocator owns the device memory; a serving loop with a
+ * fixed, pre-planned memory budget; code that must not call cudaMalloc,
+ * which can synchronise the device and is not allowed inside stream capture.
+ *
+ * Same arguments and results as thd_attn_fwd, minus the workspace: the
+ * scratch lives in a static device array of THD_NOALLOC_SCRATCH_BYTES (1 MiB)
+ * inside the library, which every GPU that loads the library keeps until the
+ * process exits.  The entry point calls no cudaMalloc/cudaFree and no
+ * allocating library routine.
+ *   - Limit: returns THD_ERR_WORKSPACE, launching nothing, when
+ *     thd_workspace_size(B, T_q, T_kv, Hq, Hkv, D, cp_size, 0) exceeds
+ *     THD_NOALLOC_SCRATCH_BYTES (about T_q / 128 + cp_size * B < 65000 schedule
+ *     entries, e.g. up to ~8M tokens for a few sequences).
+ *   - Set-up: the first call on each device looks up the array's device
+ *     address (cudaGetSymbolAddress) with that device current; make that first
+ *     call before any stream capture.
+ *   - Sharing: every call on a device uses the same array, which keeps the
+ *     last call's contents (nothing in it needs clearing; each call rewrites
+ *     what it reads).  Calls whose kernels overlap on the GPU (different
+ *     streams, or host threads without ordering) race on it: serialise them.
+ */
+#define THD_NOALLOC_SCRATCH_BYTES (1 << 20)
+THD_API int thd_attn_fwd_noalloc(const void* q, const void* k, const void* v, void* o, float* lse,
+                                 const int32_t* cu_seqlens_q, const int32_t* cu_seqlens_kv,
+                                 const int32_t* cu_seqlens_q_padded, const int32_t* cu_seqlens_kv_padded, int B,
+                                 int64_t T_q, int64_t T_kv, int Hq, int Hkv, int D, int causal, float softmax_scale,
+                                 int cp_size, int pad_between_seqs, int32_t* dev_status, thd_stream_t stream);
+
+/*
  * thd_attn_bwd -- gradients of thd_attn_fwd w.r.t. q, k, v.
  * [P2 "Steps/Code to reproduce bug"] runs forward/backward on this layout.
  *   q, k, v, o (forward output), dout: bf16 as in thd_attn_fwd; lse [Hq, T_q]

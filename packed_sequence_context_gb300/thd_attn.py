@@ -59,6 +59,8 @@ SIGNATURES = {
                             _i32, _f32, _i32, _i32, _vp, _sz, _vp, _vp]),
     "thd_attn_fwd_step": (_i32, [_vp, _vp, _vp, _vp, _vp, _vp, _vp, _vp, _vp, _i32, _i64, _i64, _i32, _i32, _i32,
                                  _i32, _f32, _i32, _i32, _i32, _vp, _sz, _vp, _vp]),
+    "thd_attn_fwd_noalloc": (_i32, [_vp, _vp, _vp, _vp, _vp, _vp, _vp, _vp, _vp, _i32, _i64, _i64, _i32, _i32,
+                                    _i32, _i32, _f32, _i32, _i32, _vp, _vp]),
     "thd_attn_bwd": (_i32, [_vp, _vp, _vp, _vp, _vp, _vp, _vp, _vp, _vp, _i64, _i64, _vp, _vp, _vp, _vp, _i32,
                             _i64, _i64, _i32, _i32, _i32, _i32, _f32, _i32, _i32, _vp, _sz, _vp, _vp]),
     "thd_lse_merge": (_i32, [_vp, _vp, _vp, _vp, _i64, _i32, _i32, _vp]),
@@ -140,6 +142,14 @@ def thd_attn_fwd_step(q, k, v, o_part, lse_part, cu_seqlens_q, cu_seqlens_kv, cu
                                    _p(cu_seqlens_kv), _p(cu_seqlens_q_padded), _p(cu_seqlens_kv_padded), B, T_q,
                                    T_kv, Hq, Hkv, D, causal, softmax_scale, cp_size, pad_between_seqs, step,
                                    _p(workspace), workspace_bytes, _p(dev_status), _s(stream))
+
+
+def thd_attn_fwd_noalloc(q, k, v, o, lse, cu_seqlens_q, cu_seqlens_kv, cu_seqlens_q_padded, cu_seqlens_kv_padded,
+                         B, T_q, T_kv, Hq, Hkv, D, causal, softmax_scale, cp_size, pad_between_seqs, dev_status,
+                         stream=None) -> int:
+    return lib().thd_attn_fwd_noalloc(_p(q), _p(k), _p(v), _p(o), _p(lse), _p(cu_seqlens_q), _p(cu_seqlens_kv),
+                                      _p(cu_seqlens_q_padded), _p(cu_seqlens_kv_padded), B, T_q, T_kv, Hq, Hkv, D,
+                                      causal, softmax_scale, cp_size, pad_between_seqs, _p(dev_status), _s(stream))
 
 
 def thd_attn_bwd(q, k, v, o, lse, dout, dq, dk, dv, dq_rows, dkv_rows, cu_seqlens_q, cu_seqlens_kv,
