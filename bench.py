@@ -47,6 +47,28 @@ def _args():
     return ap.parse_args()
 
 
+def _kernel_traffic(kernel: str, workload: str):
+    """DRAM bytes per launch from the committed ncu capture of this kernel on
+    this workload (profiles/traffic.txt), or None when there is none or the
+    kernel's source changed since the counters were taken."""
+    import hashlib
+    try:
+        with open(os.path.join(ROOT, "profiles", "traffic.txt")) as f:
+            rec = json.load(f).get(kernel)
+    except Exception:
+        return None
+    if not rec or rec.get("workload") != workload:
+        return None
+    cs = os.path.join(ROOT, "packed_sequence_context_gb300", "csrc")
+    h = hashlib.sha256()
+    for name in (kernel.split("_")[0] + ".cu", "common.cuh", "ptx.cuh"):
+        with open(os.path.join(cs, name), "rb") as f:
+            h.update(f.read())
+    if h.hexdigest()[:16] != rec.get("source_sha"):
+        return None
+    return rec.get("bytes_per_launch")
+
+
 def _peaks():
     try:
         with open(os.path.join(ROOT, "MEASURED_PEAKS.json")) as f:
@@ -336,9 +358,11 @@ def run_ours(a):
             "roofline": {"bound": "tensor", "kernel": "bwd_kernel" if not a.fwd_only else "fwd_kernel",
                          "achieved": achieved, "peak": peak, "unit": "TFLOP/s", "frac": achieved / peak,
                          "peak_kind": f"bf16 burst ({peak_kind})", "frac_of_sustained": achieved / peak_sus,
-                         "kernel_ms": kavg, "traffic": None},
+                         "kernel_ms": kavg,
+                         "traffic": _kernel_traffic("fwd_kernel" if a.fwd_only else "bwd_kernel", w.name)},
             "fwd_roofline": {"bound": "tensor", "kernel": "fwd_kernel", "achieved": fwd_kernel_tflops, "peak": peak,
-                             "unit": "TFLOP/s", "frac": fwd_kernel_tflops / peak, "kernel_ms": fk},
+                             "unit": "TFLOP/s", "frac": fwd_kernel_tflops / peak, "kernel_ms": fk,
+                             "traffic": _kernel_traffic("fwd_kernel", w.name)},
             "gpu_launches": launches,
             "clocks": clk.summary(),
             "cpu_baseline": cpu,
