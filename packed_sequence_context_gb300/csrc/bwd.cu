@@ -17,7 +17,8 @@
 //   S^T  = K Q^T            (TMEM X)     dP^T = V dO^T         (TMEM Y)
 //   P^T  = exp(S^T scale - lse)          dS^T = P^T (dP^T - Delta)
 //   dV  += P^T dO   (A = P^T from TMEM)  dK  += dS^T Q   (A = dS^T, smem)
-//   dQ   = dS K     (A = dS, the same smem read MN-major; into TMEM Y)
+//   dQ   = dS K     (A = dS, the same smem read MN-major; into TMEM X once
+//                    dV has consumed P^T, so the next dP^T need not wait for the dQ drain)
 // CTA: warps 0-3 compute (one key row per thread = TMEM lane; one query row
 // per thread when draining dQ), warp 4 TMA producer (+ lse/Delta staging),
 // warp 5 TMEM allocator and single-thread MMA issuer.
@@ -105,8 +106,9 @@ __global__ void __launch_bounds__(192, 1)
   uint64_t* bar_st_full = bars + 2 + 2 * S;
   uint64_t* bar_p_ready = bars + 3 + 2 * S;
   uint64_t* bar_dq_full = bars + 4 + 2 * S;
-  uint64_t* bar_y_free = bars + 5 + 2 * S;
+  uint64_t* bar_x_free = bars + 5 + 2 * S;
   uint64_t* bar_drain = bars + 6 + 2 * S;
+  uint64_t* bar_dv_done = bars + 7 + 2 * S;
   uint32_t* s_tmem = reinterpret_cast<uint32_t*>(bars + 8 + 2 * S);
   int* s_abort = reinterpret_cast<int*>(bars + 9 + 2 * S);
 
@@ -122,14 +124,15 @@ __global__ void __launch_bounds__(192, 1)
     mbar_init(bar_kv_full, 1);
     mbar_init(bar_kv_empty, 1);
     for (int s = 0; s < S; ++s) {
-      mbar_init(&bar_qdo_full[s], 32);
+      mbar_init(&bar_qdo_full[s], 33);  // 32 cp.async arrivals + the TMA expect-tx arrival
       mbar_init(&bar_qdo_empty[s], 1);
     }
     mbar_init(bar_st_full, 1);
     mbar_init(bar_p_ready, 128);
     mbar_init(bar_dq_full, 1);
-    mbar_init(bar_y_free, 128);
+    mbar_init(bar_x_free, 128);
     mbar_init(bar_drain, 1);
+    mbar_init(bar_dv_done, 1);
     *s_abort = 0;
     fence_mbar_init();
   }
@@ -147,15 +150,11 @@ __global__ void __launch_bounds__(192, 1)
   __syncthreads();
   tc_fence_after();
   const uint32_t tmem = *s_tmem;
-  constexpr float kLog2e = 1.4426950408889634f;
 
   if (warp == 4) {
     // ------------------------------------------------------------ producer (whole warp)
     int stage = 0;
-    uint32_t ph = 0, kv_iter = 0;
-    int fills[S];
-    for (int s = 0; s < S; ++s) fills[s] = 0;
-    int kv_fills = 0;
+    uint32_t ph = 0, kv_iter = 0, n_fill = 0;
     bool ok = true;
     for (int w = blockIdx.x; w < n_items && ok; w += gridDim.x) {
       const BwdItem it = bwd_item(p, w);
@@ -170,7 +169,6 @@ __global__ void __launch_bounds__(192, 1)
           tma_load_3d(smem_u32(sV + hb * 16384), &tmV, bar_kv_full, hb * 64, it.hk, kv_row);
         }
       }
-      ++kv_fills;
       ++kv_iter;
       for_each_q_step(it, p, [&](int qc, int jq, int h) {
         if (!ok) return;
@@ -181,17 +179,19 @@ __global__ void __launch_bounds__(192, 1)
         const int q0 = qc * it.g.cbq + jq * kTile;
         const int nqv = imin(imin(kTile, it.g.cbq - jq * kTile), it.g.Lq - q0);
         const int q_row = it.g.q_off + q0;
-        float* lse2 = sLse + stage * 256;
-        float* dl = lse2 + 128;
+        const uint32_t lse2 = smem_u32(sLse + stage * 256);
+        // lse and Delta of the valid query rows, copied asynchronously (entries
+        // past nqv are left stale: the compute warps never read them unmasked)
 #pragma unroll
         for (int k = 0; k < 4; ++k) {
           const int n = lane + 32 * k;
-          const bool v = n < nqv;
-          const int64_t idx = (int64_t)h * p.T_q + q_row + n;
-          lse2[n] = v ? p.lse[idx] * kLog2e : 0.f;
-          dl[n] = v ? p.delta[idx] : 0.f;
+          if (n < nqv) {
+            const int64_t idx = (int64_t)h * p.T_q + q_row + n;
+            cp_async_4(lse2 + 4 * n, p.lse + idx);
+            cp_async_4(lse2 + 512 + 4 * n, p.delta + idx);
+          }
         }
-        __syncwarp();
+        cp_async_arrive_noinc(&bar_qdo_full[stage]);
         if (lane == 0) {
           mbar_arrive_expect_tx(&bar_qdo_full[stage], 2 * C::kTileBytes);
           uint8_t* sQ = smem + C::kOffQ + stage * 2 * C::kTileBytes;
@@ -201,26 +201,24 @@ __global__ void __launch_bounds__(192, 1)
             tma_load_3d(smem_u32(sQ + hb * 16384), &tmQ, &bar_qdo_full[stage], hb * 64, h, q_row);
             tma_load_3d(smem_u32(sDO + hb * 16384), &tmDO, &bar_qdo_full[stage], hb * 64, h, q_row);
           }
-        } else {
-          mbar_arrive(&bar_qdo_full[stage]);
         }
-        ++fills[stage];
+        ++n_fill;
         if (++stage == S) {
           stage = 0;
           ph ^= 1u;
         }
       });
     }
-    if (lane == 0) {
-      if (kv_fills > 0) drain_wait_b(bar_kv_full, (uint32_t)(kv_fills - 1) & 1u);
-      for (int s = 0; s < S; ++s)
-        if (fills[s] > 0) drain_wait_b(&bar_qdo_full[s], (uint32_t)(fills[s] - 1) & 1u);
+    // every issued copy must land before the CTA may exit
+    if (kv_iter > 0) drain_wait_b(bar_kv_full, (kv_iter - 1) & 1u);
+    for (int s = 0; s < S; ++s) {
+      const uint32_t fills = n_fill > (uint32_t)s ? (n_fill - 1 - s) / S + 1 : 0;
+      if (fills > 0) drain_wait_b(&bar_qdo_full[s], (fills - 1) & 1u);
     }
     __syncwarp();
   } else if (warp == 5) {
     // ------------------------------------------------------------ MMA issuer
     if (lane == 0) {
-      constexpr uint32_t idesc_t = idesc_bf16(128, 128, false, false);  // S^T, dP^T
       constexpr uint32_t idesc_kv = idesc_bf16(128, D, false, true);    // dV, dK (B MN-major)
       constexpr uint32_t idesc_q = idesc_bf16(128, D, true, true);      // dQ (A and B MN-major)
       const uint32_t kb = smem_u32(sK), vb = smem_u32(sV), dsb = smem_u32(sDS);
@@ -233,9 +231,13 @@ __global__ void __launch_bounds__(192, 1)
         if (!mbar_wait(bar_kv_full, kv_iter & 1u, s_abort)) break;
         ++kv_iter;
         tc_fence_after();
+        const int kv_steps = ceil_div(it.kv_last - it.kv_first + 1, 16);  // K of the dQ product
         bool first = true;
-        for_each_q_step(it, p, [&](int, int, int) {
+        for_each_q_step(it, p, [&](int qc, int jq, int) {
           if (!ok) return;
+          const int nqv = imin(imin(kTile, it.g.cbq - jq * kTile), it.g.Lq - (qc * it.g.cbq + jq * kTile));
+          const int n16 = ceil_div(nqv, 16);  // query rows in MMA units of 16
+          const uint32_t idesc_t = idesc_bf16(128, 16 * n16, false, false);  // S^T, dP^T
           if (!mbar_wait(&bar_qdo_full[stage], ph, s_abort)) {
             ok = false;
             return;
@@ -243,15 +245,15 @@ __global__ void __launch_bounds__(192, 1)
           tc_fence_after();
           const uint32_t qb = smem_u32(smem + C::kOffQ + stage * 2 * C::kTileBytes);
           const uint32_t dob = qb + C::kTileBytes;
-          // S^T = K Q^T -> X
+          // dP^T = V dO^T -> Y (Y was read by the compute warps before the last p_ready)
 #pragma unroll
           for (int ks = 0; ks < D / 16; ++ks) {
             const uint32_t off = (ks >> 2) * 16384 + (ks & 3) * 32;
-            mma_ss(tmem + C::kColX, sdesc_sw128(kb + off, 16, 1024), sdesc_sw128(qb + off, 16, 1024), idesc_t,
+            mma_ss(tmem + C::kColY, sdesc_sw128(vb + off, 16, 1024), sdesc_sw128(dob + off, 16, 1024), idesc_t,
                    ks > 0);
           }
-          // dP^T = V dO^T -> Y, once the previous step's dQ has been drained from Y
-          if (su > 0 && !mbar_wait(bar_y_free, (su - 1) & 1u, s_abort)) {
+          // S^T = K Q^T -> X, once the previous dQ has been drained from X
+          if (su > 0 && !mbar_wait(bar_x_free, (su - 1) & 1u, s_abort)) {
             ok = false;
             return;
           }
@@ -259,7 +261,7 @@ __global__ void __launch_bounds__(192, 1)
 #pragma unroll
           for (int ks = 0; ks < D / 16; ++ks) {
             const uint32_t off = (ks >> 2) * 16384 + (ks & 3) * 32;
-            mma_ss(tmem + C::kColY, sdesc_sw128(vb + off, 16, 1024), sdesc_sw128(dob + off, 16, 1024), idesc_t,
+            mma_ss(tmem + C::kColX, sdesc_sw128(kb + off, 16, 1024), sdesc_sw128(qb + off, 16, 1024), idesc_t,
                    ks > 0);
           }
           tc_commit(bar_st_full);
@@ -268,20 +270,24 @@ __global__ void __launch_bounds__(192, 1)
             return;
           }
           tc_fence_after();
-          // dV += P^T dO  (P^T packed bf16 in X)
-#pragma unroll
-          for (int ks = 0; ks < kTile / 16; ++ks)
+          // dV += P^T dO  (P^T packed bf16 in X; K = the valid query rows)
+          for (int ks = 0; ks < n16; ++ks)
             mma_ts(tmem + C::kColDV, tmem + C::kColX + ks * 8, sdesc_sw128(dob + ks * 2048, 16384, 1024), idesc_kv,
                    (first && ks == 0) ? 0u : 1u);
+          tc_commit(bar_dv_done);
           // dK += dS^T Q
-#pragma unroll
-          for (int ks = 0; ks < kTile / 16; ++ks)
+          for (int ks = 0; ks < n16; ++ks)
             mma_ss(tmem + C::kColDK, sdesc_sw128(dsb + (ks >> 2) * 16384 + (ks & 3) * 32, 16, 1024),
                    sdesc_sw128(qb + ks * 2048, 16384, 1024), idesc_kv, (first && ks == 0) ? 0u : 1u);
-          // dQ = dS K -> Y
-#pragma unroll
-          for (int ks = 0; ks < kTile / 16; ++ks)
-            mma_ss(tmem + C::kColY, sdesc_sw128(dsb + ks * 2048, 16384, 1024),
+          // dQ = dS K -> X.  MMAs into different accumulators are not ordered,
+          // so dQ may overwrite X only once dV has finished reading P^T there.
+          if (!mbar_wait(bar_dv_done, su & 1u, s_abort)) {
+            ok = false;
+            return;
+          }
+          tc_fence_after();
+          for (int ks = 0; ks < kv_steps; ++ks)
+            mma_ss(tmem + C::kColX, sdesc_sw128(dsb + ks * 2048, 16384, 1024),
                    sdesc_sw128(kb + ks * 2048, 16384, 1024), idesc_q, ks > 0);
           tc_commit(bar_dq_full);
           tc_commit(&bar_qdo_empty[stage]);
@@ -302,6 +308,7 @@ __global__ void __launch_bounds__(192, 1)
     // ------------------------------------------------------------ compute warps
     const uint32_t lane_base = (uint32_t)(warp * 32) << 16;
     const float sl2 = p.scale_log2;
+    const uint32_t ds_s = smem_u32(sDS);
     uint32_t su = 0;
     bool ok = true;
     for (int w = blockIdx.x; w < n_items && ok; w += gridDim.x) {
@@ -322,10 +329,21 @@ __global__ void __launch_bounds__(192, 1)
         const int nqv = imin(imin(kTile, it.g.cbq - jq * kTile), it.g.Lq - q0);
         int n_lo = 0, n_hi = valid_kv ? nqv : 0;
         if (p.causal) n_lo = imin(imax(j_pos - q0, 0), kTile);
-        const float* lse2 = sLse + (su % S) * 256;
-        const float* dl = lse2 + 128;
+        // the cp.async writes of lse/Delta are visible to the threads that
+        // observe the stage barrier's phase, so observe it here (it cannot have
+        // moved on: the stage is refilled only after this step's p_ready)
+        if (!mbar_wait(&bar_qdo_full[su % S], (su / S) & 1u, s_abort)) {
+          ok = false;
+          return;
+        }
+        float* lse2 = sLse + (su % S) * 256;
+        // lse arrives in natural log; the exponent below is in log2 units
+        if (tid < nqv) lse2[tid] *= 1.4426950408889634f;
+        named_bar_sync(1, 128);
+        const uint32_t lse_s = smem_u32(lse2), dl_s = lse_s + 512;
+        const int nch = ceil_div(nqv, 32);
 #pragma unroll 1
-        for (int kk = 0; kk < 4; ++kk) {
+        for (int kk = 0; kk < nch; ++kk) {
           uint32_t sr[32], dr[32];
           tmem_ld32(tmem + lane_base + C::kColX + 32 * kk, sr);
           tmem_ld32(tmem + lane_base + C::kColY + 32 * kk, dr);
@@ -333,30 +351,36 @@ __global__ void __launch_bounds__(192, 1)
           tmem_ld_wait(dr);
           uint32_t pk[16], dk[16];
 #pragma unroll
-          for (int n2 = 0; n2 < 16; ++n2) {
-            float pp[2], dd[2];
+          for (int q4 = 0; q4 < 8; ++q4) {  // four query columns at a time
+            const float4 l4 = lds128f(lse_s + 4 * (32 * kk + 4 * q4));
+            const float4 d4 = lds128f(dl_s + 4 * (32 * kk + 4 * q4));
+            const float lv[4] = {l4.x, l4.y, l4.z, l4.w}, dv4[4] = {d4.x, d4.y, d4.z, d4.w};
+            float pp[4], dd[4];
 #pragma unroll
-            for (int e = 0; e < 2; ++e) {
-              const int n = 32 * kk + 2 * n2 + e;
+            for (int e = 0; e < 4; ++e) {
+              const int n = 32 * kk + 4 * q4 + e;
               const bool a = n >= n_lo && n < n_hi;
-              const float pv = a ? ex2(fmaf(__uint_as_float(sr[2 * n2 + e]), sl2, -lse2[n])) : 0.f;
+              const float pv = a ? ex2(fmaf(__uint_as_float(sr[4 * q4 + e]), sl2, -lv[e])) : 0.f;
               pp[e] = pv;
-              dd[e] = pv * (__uint_as_float(dr[2 * n2 + e]) - dl[n]);
+              dd[e] = a ? pv * (__uint_as_float(dr[4 * q4 + e]) - dv4[e]) : 0.f;
             }
-            pk[n2] = pack_bf16x2(pp[0], pp[1]);
-            dk[n2] = pack_bf16x2(dd[0], dd[1]);
+            pk[2 * q4] = pack_bf16x2(pp[0], pp[1]);
+            pk[2 * q4 + 1] = pack_bf16x2(pp[2], pp[3]);
+            dk[2 * q4] = pack_bf16x2(dd[0], dd[1]);
+            dk[2 * q4 + 1] = pack_bf16x2(dd[2], dd[3]);
           }
           tmem_st16(tmem + lane_base + C::kColX + 16 * kk, pk);
 #pragma unroll
           for (int i = 0; i < 4; ++i)
-            *reinterpret_cast<uint4*>(sDS + sw128_offset(tid, 32 * kk + 8 * i, kTile)) =
-                make_uint4(dk[4 * i], dk[4 * i + 1], dk[4 * i + 2], dk[4 * i + 3]);
+            sts128(ds_s + sw128_offset(tid, 32 * kk + 8 * i, kTile), dk[4 * i], dk[4 * i + 1], dk[4 * i + 2],
+                   dk[4 * i + 3]);
         }
         tmem_st_wait();
         fence_proxy_async_smem();
         tc_fence_before();
         mbar_arrive(bar_p_ready);
-        // drain dQ (one query row per thread) into the fp32 accumulator
+        // drain dQ (TMEM lane = query row) into the fp32 accumulator with
+        // fire-and-forget vector reductions straight from registers
         if (!mbar_wait(bar_dq_full, su & 1u, s_abort)) {
           ok = false;
           return;
@@ -367,18 +391,17 @@ __global__ void __launch_bounds__(192, 1)
 #pragma unroll 1
         for (int kk = 0; kk < D / 32; ++kk) {
           uint32_t r[32];
-          tmem_ld32(tmem + lane_base + C::kColY + 32 * kk, r);
+          tmem_ld32(tmem + lane_base + C::kColX + 32 * kk, r);
           tmem_ld_wait(r);
           if (q_live) {
 #pragma unroll
             for (int i = 0; i < 8; ++i)
-              atomicAdd(reinterpret_cast<float4*>(dst + 32 * kk + 4 * i),
-                        make_float4(__uint_as_float(r[4 * i]), __uint_as_float(r[4 * i + 1]),
-                                    __uint_as_float(r[4 * i + 2]), __uint_as_float(r[4 * i + 3])));
+              red_add_v4(dst + 32 * kk + 4 * i, __uint_as_float(r[4 * i]), __uint_as_float(r[4 * i + 1]),
+                         __uint_as_float(r[4 * i + 2]), __uint_as_float(r[4 * i + 3]));
           }
         }
         tc_fence_before();
-        mbar_arrive(bar_y_free);
+        mbar_arrive(bar_x_free);
         ++su;
         ++nsteps;
       });

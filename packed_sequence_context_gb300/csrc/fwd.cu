@@ -19,11 +19,15 @@
 //
 // CTA layout (192 threads, one CTA per SM, persistent over the schedule):
 //   warps 0-3  softmax + epilogue, one query row per thread (TMEM lane)
-//   warp 4     TMA producer (K/V tiles, 3-D tensor maps over [T, Hkv, D])
+//   warp 4     producer: gathers the next item's query tile (its rows come
+//              from two chunks, so cp.async row gathers, double-buffered) and
+//              issues the K/V tile TMA loads (3-D tensor maps over [T, Hkv, D])
 //   warp 5     TMEM allocator and single-thread tcgen05.mma issuer
-// TMEM: S double buffer in columns [0,128) and [128,256) (fp32); the
-// softmax writes P as packed bf16 over the first 64 columns of its S buffer,
-// and PV reads it from TMEM as the A operand; O accumulates in [256, 256+D).
+// TMEM: three S buffers of 128 fp32 columns ([0,384)); the softmax writes P
+// as packed bf16 over the first columns of its S buffer, and PV reads it from
+// TMEM as the A operand; O accumulates in [384, 384+D).  MMAs into different
+// accumulators are not ordered among themselves, so a buffer is reused for a
+// later QK^T only after the PV that read its P has completed (s_free).
 #include "common.cuh"
 #include "ptx.cuh"
 
@@ -34,9 +38,10 @@ struct FwdCfg {
   static constexpr int kStages = D == 128 ? 2 : 4;
   static constexpr int kQBytes = kTile * D * 2;
   static constexpr int kKVBytes = kTile * D * 2;  // one K (or V) tile
-  static constexpr int kSmem = 1024 + kQBytes + kStages * 2 * kKVBytes;
+  static constexpr int kSmem = 1024 + 2 * kQBytes + kStages * 2 * kKVBytes;  // query tile double-buffered
   static constexpr uint32_t kTmemCols = 512;
-  static constexpr uint32_t kColO = 256;
+  static constexpr int kSBufs = 3;          // S/P buffers of 128 columns
+  static constexpr uint32_t kColO = 384;
   static constexpr int kThreads = 192;
 };
 
@@ -71,6 +76,15 @@ __device__ inline void for_each_kv_tile(const FwdItem& it, const FwdParams& p, F
   }
 }
 
+// Columns (keys) of tile (c, j) any query of the item may see, rounded up to
+// the MMA granularity of 16: the N of its QK^T product and the K of its PV.
+__device__ inline int fwd_tile_ncols(const FwdItem& it, const FwdParams& p, int c, int j) {
+  const int j0 = c * it.g.cbkv + j * kTile;
+  int n = imin(kTile, imin((c + 1) * it.g.cbkv - j0, it.g.Lkv - j0));
+  if (p.causal) n = imin(n, it.qmax - j0 + 1);
+  return 16 * ceil_div(imax(n, 1), 16);
+}
+
 // Bounded wait that ignores the abort flag (used to drain in-flight async
 // work before the CTA exits).
 __device__ inline void drain_wait(uint64_t* bar, uint32_t parity) {
@@ -87,15 +101,16 @@ __global__ void __launch_bounds__(192, 1)
   constexpr int S = C::kStages;
   extern __shared__ uint8_t smem_raw[];
   uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
-  uint8_t* sQ = smem;
-  uint8_t* sK = smem + C::kQBytes;
+  uint8_t* sQ = smem;  // two buffers of kQBytes
+  uint8_t* sK = smem + 2 * C::kQBytes;
   uint8_t* sV = sK + S * C::kKVBytes;
   __shared__ __align__(8) uint64_t bar_kv_full[S];
   __shared__ __align__(8) uint64_t bar_kv_empty[S];
-  __shared__ __align__(8) uint64_t bar_s_full[2];
-  __shared__ __align__(8) uint64_t bar_p_ready[2];
-  __shared__ __align__(8) uint64_t bar_pv_done;
-  __shared__ __align__(8) uint64_t bar_q_ready;
+  __shared__ __align__(8) uint64_t bar_s_full[C::kSBufs];
+  __shared__ __align__(8) uint64_t bar_p_ready[C::kSBufs];
+  __shared__ __align__(8) uint64_t bar_s_free[C::kSBufs];
+  __shared__ __align__(8) uint64_t bar_q_full[2];
+  __shared__ __align__(8) uint64_t bar_q_empty[2];
   __shared__ __align__(8) uint64_t bar_drain;
   __shared__ uint32_t s_tmem;
   __shared__ int s_abort;
@@ -109,12 +124,15 @@ __global__ void __launch_bounds__(192, 1)
       mbar_init(&bar_kv_full[s], 1);
       mbar_init(&bar_kv_empty[s], 1);
     }
-    for (int s = 0; s < 2; ++s) {
+    for (int s = 0; s < C::kSBufs; ++s) {
       mbar_init(&bar_s_full[s], 1);
       mbar_init(&bar_p_ready[s], 128);
+      mbar_init(&bar_s_free[s], 1);
     }
-    mbar_init(&bar_pv_done, 1);
-    mbar_init(&bar_q_ready, 128);
+    for (int s = 0; s < 2; ++s) {
+      mbar_init(&bar_q_full[s], 32);
+      mbar_init(&bar_q_empty[s], 1);
+    }
     mbar_init(&bar_drain, 1);
     s_abort = 0;
     fence_mbar_init();
@@ -133,21 +151,43 @@ __global__ void __launch_bounds__(192, 1)
   const uint32_t tmem = s_tmem;
 
   if (warp == 4) {
-    // ------------------------------------------------------------ producer
-    if (lane == 0) {
-      int stage = 0;
-      uint32_t ph = 0;
-      int fills[S];
-      for (int s = 0; s < S; ++s) fills[s] = 0;
-      bool ok = true;
-      for (int w = blockIdx.x; w < n_items && ok; w += gridDim.x) {
-        const FwdItem it = fwd_item(p, w);
-        for_each_kv_tile(it, p, [&](int c, int j) {
-          if (!ok) return;
-          if (!mbar_wait(&bar_kv_empty[stage], ph ^ 1u, &s_abort)) {
-            ok = false;
-            return;
-          }
+    // ------------------------------------------------------------ producer (whole warp)
+    int stage = 0;
+    uint32_t ph = 0, n_fill = 0, q_iter = 0;
+    bool ok = true;
+    for (int w = blockIdx.x; w < n_items && ok; w += gridDim.x) {
+      const FwdItem it = fwd_item(p, w);
+      // ---- the query tile: rank-local rows [128 t, 128 t + 128) of rank r,
+      // gathered into 128B-swizzled smem; rows without a valid query are zero
+      const uint32_t qb = q_iter & 1u;
+      if (!mbar_wait(&bar_q_empty[qb], ((q_iter >> 1) & 1u) ^ 1u, &s_abort)) break;
+      const uint32_t qdst = smem_u32(sQ + qb * C::kQBytes);
+#pragma unroll
+      for (int rr = 0; rr < 4; ++rr) {
+        const int row = lane + 32 * rr;
+        const int prow = it.t * kTile + row;
+        const bool in_rank = prow < 2 * it.g.cbq;
+        const int pos = in_rank ? local_to_pos(prow, it.r, it.g.cbq, p.cp) : 0;
+        const bool valid = in_rank && pos < it.g.Lq;
+        const uint16_t* src = valid ? p.q + (((int64_t)it.g.q_off + pos) * p.Hq + it.h) * D : p.q;
+#pragma unroll
+        for (int c = 0; c < D / 8; ++c)
+          cp_async_16(qdst + sw128_offset(row, 8 * c, kTile), src + (valid ? 8 * c : 0), valid ? 16u : 0u);
+      }
+      // the copies must have landed and be visible to the tensor core's
+      // (async) proxy before the MMA thread may read them
+      cp_async_wait_all();
+      fence_proxy_async_smem();
+      mbar_arrive(&bar_q_full[qb]);
+      ++q_iter;
+      // ---- the key/value tiles of the item, in ring order
+      for_each_kv_tile(it, p, [&](int c, int j) {
+        if (!ok) return;
+        if (!mbar_wait(&bar_kv_empty[stage], ph ^ 1u, &s_abort)) {
+          ok = false;
+          return;
+        }
+        if (lane == 0) {
           const int row = it.g.kv_off + c * it.g.cbkv + j * kTile;
           mbar_arrive_expect_tx(&bar_kv_full[stage], 2 * C::kKVBytes);
 #pragma unroll
@@ -157,56 +197,67 @@ __global__ void __launch_bounds__(192, 1)
             tma_load_3d(smem_u32(sV + stage * C::kKVBytes + hb * 16384), &tmV, &bar_kv_full[stage], hb * 64,
                         it.kvh, row);
           }
-          ++fills[stage];
-          if (++stage == S) {
-            stage = 0;
-            ph ^= 1u;
-          }
-        });
+        }
+        ++n_fill;
+        if (++stage == S) {
+          stage = 0;
+          ph ^= 1u;
+        }
+      });
+    }
+    // every issued load must land before the CTA may exit
+    if (lane == 0) {
+      for (int s = 0; s < S; ++s) {
+        const uint32_t fills = n_fill > (uint32_t)s ? (n_fill - 1 - s) / S + 1 : 0;
+        if (fills > 0) drain_wait(&bar_kv_full[s], (fills - 1) & 1u);
       }
-      // every issued load must land before the CTA may exit
-      for (int s = 0; s < S; ++s)
-        if (fills[s] > 0) drain_wait(&bar_kv_full[s], (uint32_t)(fills[s] - 1) & 1u);
     }
     __syncwarp();
   } else if (warp == 5) {
     // ------------------------------------------------------------ MMA issuer
     if (lane == 0) {
-      constexpr uint32_t idesc_qk = idesc_bf16(128, 128, false, false);
       constexpr uint32_t idesc_pv = idesc_bf16(128, D, false, true);
-      const uint32_t qbase = smem_u32(sQ), kbase = smem_u32(sK), vbase = smem_u32(sV);
+      const uint32_t kbase = smem_u32(sK), vbase = smem_u32(sV);
       int stage = 0;
       uint32_t ph = 0, g = 0, q_iter = 0;
       bool ok = true;
-      auto issue_pv = [&](uint32_t gg, int st, bool first) -> bool {
-        if (!mbar_wait(&bar_p_ready[gg & 1u], (gg >> 1) & 1u, &s_abort)) return false;
+      auto issue_pv = [&](uint32_t gg, int st, bool first, int ncols) -> bool {
+        const uint32_t b = gg % C::kSBufs;
+        if (!mbar_wait(&bar_p_ready[b], (gg / C::kSBufs) & 1u, &s_abort)) return false;
         tc_fence_after();
-        const uint32_t pcol = tmem + ((gg & 1u) ? 128u : 0u);
-#pragma unroll
-        for (int ks = 0; ks < kTile / 16; ++ks) {
+        const uint32_t pcol = tmem + b * 128u;
+        for (int ks = 0; ks < ncols / 16; ++ks) {
           const uint64_t bd = sdesc_sw128(vbase + st * C::kKVBytes + ks * 2048, 16384, 1024);
           mma_ts(tmem + C::kColO, pcol + ks * 8, bd, idesc_pv, (first && ks == 0) ? 0u : 1u);
         }
         tc_commit(&bar_kv_empty[st]);
-        tc_commit(&bar_pv_done);
+        tc_commit(&bar_s_free[b]);  // PV on buffer b done: P consumed, O holds tile gg
         return true;
       };
       for (int w = blockIdx.x; w < n_items && ok; w += gridDim.x) {
         const FwdItem it = fwd_item(p, w);
-        int n = 0;
-        for_each_kv_tile(it, p, [&](int, int) { ++n; });
-        if (!mbar_wait(&bar_q_ready, q_iter & 1u, &s_abort)) break;
+        const uint32_t qb = q_iter & 1u;
+        if (!mbar_wait(&bar_q_full[qb], (q_iter >> 1) & 1u, &s_abort)) break;
         ++q_iter;
         tc_fence_after();
-        int prev_stage = 0;
+        const uint32_t qbase = smem_u32(sQ + qb * C::kQBytes);
+        int prev_stage = 0, prev_cols = 0, j = 0;
         uint32_t prev_g = 0;
-        for (int j = 0; j < n; ++j) {
+        for_each_kv_tile(it, p, [&](int c, int jt) {
+          if (!ok) return;
+          const int ncols = fwd_tile_ncols(it, p, c, jt);
           if (!mbar_wait(&bar_kv_full[stage], ph, &s_abort)) {
             ok = false;
-            break;
+            return;
+          }
+          const uint32_t b = g % C::kSBufs;
+          if (g >= (uint32_t)C::kSBufs && !mbar_wait(&bar_s_free[b], (g / C::kSBufs - 1) & 1u, &s_abort)) {
+            ok = false;
+            return;
           }
           tc_fence_after();
-          const uint32_t scol = tmem + ((g & 1u) ? 128u : 0u);
+          const uint32_t scol = tmem + b * 128u;
+          const uint32_t idesc_qk = idesc_bf16(128, ncols, false, false);
 #pragma unroll
           for (int ks = 0; ks < D / 16; ++ks) {
             const uint32_t koff = (ks >> 2) * 16384 + (ks & 3) * 32;
@@ -214,20 +265,23 @@ __global__ void __launch_bounds__(192, 1)
             const uint64_t bd = sdesc_sw128(kbase + stage * C::kKVBytes + koff, 16, 1024);
             mma_ss(scol, ad, bd, idesc_qk, ks > 0 ? 1u : 0u);
           }
-          tc_commit(&bar_s_full[g & 1u]);
-          if (j > 0 && !issue_pv(prev_g, prev_stage, j == 1)) {
+          tc_commit(&bar_s_full[b]);
+          if (j > 0 && !issue_pv(prev_g, prev_stage, j == 1, prev_cols)) {
             ok = false;
-            break;
+            return;
           }
           prev_stage = stage;
           prev_g = g;
+          prev_cols = ncols;
           if (++stage == S) {
             stage = 0;
             ph ^= 1u;
           }
           ++g;
-        }
-        if (ok && n > 0 && !issue_pv(prev_g, prev_stage, n == 1)) ok = false;
+          ++j;
+        });
+        if (ok && j > 0 && !issue_pv(prev_g, prev_stage, j == 1, prev_cols)) ok = false;
+        tc_commit(&bar_q_empty[qb]);  // the query buffer is free once this item's MMAs complete
       }
       // all issued MMAs must complete before TMEM is released
       tc_commit(&bar_drain);
@@ -247,24 +301,13 @@ __global__ void __launch_bounds__(192, 1)
       const int pos = in_rank ? local_to_pos(prow, it.r, it.g.cbq, p.cp) : 0;
       const bool valid = in_rank && pos < it.g.Lq;
       const int64_t grow = (int64_t)it.g.q_off + pos;
-      // ---- gather this row of the query tile into 128B-swizzled smem
-      {
-        const uint4* src = reinterpret_cast<const uint4*>(p.q + (grow * p.Hq + it.h) * D);
-#pragma unroll
-        for (int c = 0; c < D / 8; ++c) {
-          const uint4 v = valid ? __ldg(src + c) : make_uint4(0, 0, 0, 0);
-          *reinterpret_cast<uint4*>(sQ + sw128_offset(tid, c * 8, kTile)) = v;
-        }
-      }
-      fence_proxy_async_smem();
-      mbar_arrive(&bar_q_ready);
       // ---- key tiles
       float m = -INFINITY, l = 0.f;
       int jl = 0;
       for_each_kv_tile(it, p, [&](int c, int j) {
         if (!ok) return;
-        const uint32_t sb = g & 1u;
-        if (!mbar_wait(&bar_s_full[sb], (g >> 1) & 1u, &s_abort)) {
+        const uint32_t sb = g % C::kSBufs;
+        if (!mbar_wait(&bar_s_full[sb], (g / C::kSBufs) & 1u, &s_abort)) {
           ok = false;
           return;
         }
@@ -277,12 +320,16 @@ __global__ void __launch_bounds__(192, 1)
           if (p.causal) cnt = imin(cnt, pos - j0 + 1);
           cnt = imax(cnt, 0);
         }
+        const int ncols = fwd_tile_ncols(it, p, c, j);   // the N this tile's QK^T computed
+        const int nch = ceil_div(ncols, 32);
         uint32_t sr[4][32];
         const uint32_t scol = tmem + lane_base + sb * 128u;
 #pragma unroll
-        for (int k = 0; k < 4; ++k) tmem_ld32(scol + 32 * k, sr[k]);
+        for (int k = 0; k < 4; ++k)
+          if (k < nch) tmem_ld32(scol + 32 * k, sr[k]);
 #pragma unroll
-        for (int k = 0; k < 4; ++k) tmem_ld_wait(sr[k]);
+        for (int k = 0; k < 4; ++k)
+          if (k < nch) tmem_ld_wait(sr[k]);
         float mt = -INFINITY;
         if (cnt >= kTile) {
 #pragma unroll
@@ -292,11 +339,13 @@ __global__ void __launch_bounds__(192, 1)
         } else {
 #pragma unroll
           for (int k = 0; k < 4; ++k)
+            if (k < nch) {
 #pragma unroll
-            for (int n = 0; n < 32; ++n) {
-              const float x = (32 * k + n < cnt) ? __uint_as_float(sr[k][n]) : -INFINITY;
-              sr[k][n] = __float_as_uint(x);
-              mt = fmaxf(mt, x);
+              for (int n = 0; n < 32; ++n) {
+                const float x = (32 * k + n < cnt) ? __uint_as_float(sr[k][n]) : -INFINITY;
+                sr[k][n] = __float_as_uint(x);
+                mt = fmaxf(mt, x);
+              }
             }
         }
         mt *= sl2;
@@ -309,8 +358,11 @@ __global__ void __launch_bounds__(192, 1)
           m = mt;
         }
         if (__any_sync(0xffffffffu, need_o)) {
-          // O must hold the previous tile's PV before it is rescaled
-          if (!mbar_wait(&bar_pv_done, (g - 1) & 1u, &s_abort)) {
+          // O must hold the previous tile's PV before it is rescaled.  Its
+          // buffer's s_free barrier is at most one phase behind (the PV before
+          // it on that buffer completed before this item's QK reused it), so a
+          // parity wait is exact there; a single barrier for all PVs is not.
+          if (!mbar_wait(&bar_s_free[(g - 1) % C::kSBufs], ((g - 1) / C::kSBufs) & 1u, &s_abort)) {
             ok = false;
             return;
           }
@@ -329,20 +381,18 @@ __global__ void __launch_bounds__(192, 1)
         const float mm = (m == -INFINITY) ? 0.f : m;
         float rs = 0.f;
 #pragma unroll
-        for (int half = 0; half < 2; ++half) {
-          uint32_t pk[32];
-#pragma unroll
-          for (int kk = 0; kk < 2; ++kk) {
-            const int k = half * 2 + kk;
+        for (int k = 0; k < 4; ++k) {
+          if (k < nch) {
+            uint32_t pk[16];
 #pragma unroll
             for (int n = 0; n < 16; ++n) {
               const float p0 = ex2(fmaf(__uint_as_float(sr[k][2 * n]), sl2, -mm));
               const float p1 = ex2(fmaf(__uint_as_float(sr[k][2 * n + 1]), sl2, -mm));
               rs += p0 + p1;
-              pk[kk * 16 + n] = pack_bf16x2(p0, p1);
+              pk[n] = pack_bf16x2(p0, p1);
             }
+            tmem_st16(scol + 16 * k, pk);
           }
-          tmem_st32(scol + 32 * half, pk);
         }
         l += rs;
         tmem_st_wait();
@@ -353,8 +403,8 @@ __global__ void __launch_bounds__(192, 1)
       });
       if (!ok) break;
       // ---- epilogue
-      if (jl > 0) {
-        if (!mbar_wait(&bar_pv_done, (g - 1) & 1u, &s_abort)) break;
+      if (jl > 0) {  // the last PV (and, in order, every earlier one) has completed
+        if (!mbar_wait(&bar_s_free[(g - 1) % C::kSBufs], ((g - 1) / C::kSBufs) & 1u, &s_abort)) break;
         tc_fence_after();
       }
       const bool live = valid && l > 0.f;

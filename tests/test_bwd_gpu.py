@@ -171,3 +171,19 @@ def test_full_size_backward_sampled(name, heads, n_seq):
         if inv.any():
             assert torch.all(g[:w.T][inv] == 0)
         assert torch.isfinite(g.float()).all()
+
+
+def test_backward_dk_dv_bit_reproducible_over_repeats():
+    """dK/dV accumulate in TMEM in a fixed order: repeated calls agree bit for
+    bit (dQ is summed with atomics and may differ in its last bits)."""
+    w = inputs.make_workload("packed")
+    t = inputs.make_tensors(w, with_grad=True)
+    d = device_inputs(w, t)
+    o, lse, dq0, dk0, dv0 = _run(w, d)
+    for _ in range(10):
+        dq, dk, dv, st = T.attn_bwd(d["q"], d["k"], d["v"], o, lse, d["do"], d["cu"], d["cu"], d["cu_pad"],
+                                    d["cu_pad"], cp_size=w.cp_size, softmax_scale=w.softmax_scale)
+        torch.cuda.synchronize()
+        assert int(st.item()) == 0
+        assert torch.equal(dk, dk0) and torch.equal(dv, dv0)
+        assert (dq.float() - dq0.float()).abs().max().item() <= 1e-2
