@@ -19,9 +19,11 @@
 //   dV  += P^T dO   (A = P^T from TMEM)  dK  += dS^T Q   (A = dS^T, smem)
 //   dQ   = dS K     (A = dS, the same smem read MN-major; into TMEM X once
 //                    dV has consumed P^T, so the next dP^T need not wait for the dQ drain)
-// CTA: warps 0-3 compute (one key row per thread = TMEM lane; one query row
-// per thread when draining dQ), warp 4 TMA producer (+ lse/Delta staging),
-// warp 5 TMEM allocator and single-thread MMA issuer.
+// CTA (320 threads): warps 0-7 compute in two warpgroups -- a thread owns one
+// key row (its TMEM lane) and half of the columns: query columns [0,64) or
+// [64,128) for P/dS, and half of the head dimension when draining dQ (one
+// query row per thread) and writing dK/dV; warp 8 TMA producer (+ lse/Delta
+// staging); warp 9 TMEM allocator and single-thread MMA issuer.
 #include "common.cuh"
 #include "ptx.cuh"
 
@@ -88,7 +90,7 @@ __device__ inline void drain_wait_b(uint64_t* bar, uint32_t parity) {
 }
 
 template <int D>
-__global__ void __launch_bounds__(192, 1)
+__global__ void __launch_bounds__(320, 1)
     bwd_kernel(const BwdParams p, const __grid_constant__ CUtensorMap tmQ, const __grid_constant__ CUtensorMap tmDO,
                const __grid_constant__ CUtensorMap tmK, const __grid_constant__ CUtensorMap tmV) {
   using C = BwdCfg<D>;
@@ -128,19 +130,19 @@ __global__ void __launch_bounds__(192, 1)
       mbar_init(&bar_qdo_empty[s], 1);
     }
     mbar_init(bar_st_full, 1);
-    mbar_init(bar_p_ready, 128);
+    mbar_init(bar_p_ready, 256);
     mbar_init(bar_dq_full, 1);
-    mbar_init(bar_x_free, 128);
+    mbar_init(bar_x_free, 256);
     mbar_init(bar_drain, 1);
     mbar_init(bar_dv_done, 1);
     *s_abort = 0;
     fence_mbar_init();
   }
-  if (warp == 5) {
+  if (warp == 9) {
     tmem_alloc(s_tmem, C::kTmemCols);
     tmem_relinquish();
   }
-  if (warp == 4 && lane == 0) {
+  if (warp == 8 && lane == 0) {
     tma_prefetch_desc(&tmQ);
     tma_prefetch_desc(&tmDO);
     tma_prefetch_desc(&tmK);
@@ -151,7 +153,7 @@ __global__ void __launch_bounds__(192, 1)
   tc_fence_after();
   const uint32_t tmem = *s_tmem;
 
-  if (warp == 4) {
+  if (warp == 8) {
     // ------------------------------------------------------------ producer (whole warp)
     int stage = 0;
     uint32_t ph = 0, kv_iter = 0, n_fill = 0;
@@ -216,7 +218,7 @@ __global__ void __launch_bounds__(192, 1)
       if (fills > 0) drain_wait_b(&bar_qdo_full[s], (fills - 1) & 1u);
     }
     __syncwarp();
-  } else if (warp == 5) {
+  } else if (warp == 9) {
     // ------------------------------------------------------------ MMA issuer
     if (lane == 0) {
       constexpr uint32_t idesc_kv = idesc_bf16(128, D, false, true);    // dV, dK (B MN-major)
@@ -270,10 +272,11 @@ __global__ void __launch_bounds__(192, 1)
             return;
           }
           tc_fence_after();
-          // dV += P^T dO  (P^T packed bf16 in X; K = the valid query rows)
+          // dV += P^T dO  (P^T packed bf16 in X: query columns 16 ks.. of K-step ks
+          // sit at column 64 (ks/4) + 8 (ks%4); K = the valid query rows)
           for (int ks = 0; ks < n16; ++ks)
-            mma_ts(tmem + C::kColDV, tmem + C::kColX + ks * 8, sdesc_sw128(dob + ks * 2048, 16384, 1024), idesc_kv,
-                   (first && ks == 0) ? 0u : 1u);
+            mma_ts(tmem + C::kColDV, tmem + C::kColX + 64 * (ks >> 2) + 8 * (ks & 3),
+                   sdesc_sw128(dob + ks * 2048, 16384, 1024), idesc_kv, (first && ks == 0) ? 0u : 1u);
           tc_commit(bar_dv_done);
           // dK += dS^T Q
           for (int ks = 0; ks < n16; ++ks)
@@ -306,14 +309,16 @@ __global__ void __launch_bounds__(192, 1)
     __syncwarp();
   } else {
     // ------------------------------------------------------------ compute warps
-    const uint32_t lane_base = (uint32_t)(warp * 32) << 16;
+    const int half = warp >> 2;     // which half of the columns this thread owns
+    const int row = tid & 127;      // its key row (TMEM lane) / query row when draining dQ
+    const uint32_t lane_base = (uint32_t)((warp & 3) * 32) << 16;
     const float sl2 = p.scale_log2;
     const uint32_t ds_s = smem_u32(sDS);
     uint32_t su = 0;
     bool ok = true;
     for (int w = blockIdx.x; w < n_items && ok; w += gridDim.x) {
       const BwdItem it = bwd_item(p, w);
-      const int kv_local = it.jk * kTile + tid;  // row within the chunk
+      const int kv_local = it.jk * kTile + row;  // row within the chunk
       const int j_pos = it.c * it.g.cbkv + kv_local;
       const bool in_chunk = kv_local < it.g.cbkv;
       const bool valid_kv = in_chunk && j_pos < it.g.Lkv;
@@ -338,12 +343,12 @@ __global__ void __launch_bounds__(192, 1)
         }
         float* lse2 = sLse + (su % S) * 256;
         // lse arrives in natural log; the exponent below is in log2 units
-        if (tid < nqv) lse2[tid] *= 1.4426950408889634f;
-        named_bar_sync(1, 128);
+        if (half == 0 && row < nqv) lse2[row] *= 1.4426950408889634f;
+        named_bar_sync(1, 256);
         const uint32_t lse_s = smem_u32(lse2), dl_s = lse_s + 512;
         const int nch = ceil_div(nqv, 32);
 #pragma unroll 1
-        for (int kk = 0; kk < nch; ++kk) {
+        for (int kk = 2 * half; kk < imin(nch, 2 * half + 2); ++kk) {
           uint32_t sr[32], dr[32];
           tmem_ld32(tmem + lane_base + C::kColX + 32 * kk, sr);
           tmem_ld32(tmem + lane_base + C::kColY + 32 * kk, dr);
@@ -369,10 +374,12 @@ __global__ void __launch_bounds__(192, 1)
             dk[2 * q4] = pack_bf16x2(dd[0], dd[1]);
             dk[2 * q4 + 1] = pack_bf16x2(dd[2], dd[3]);
           }
-          tmem_st16(tmem + lane_base + C::kColX + 16 * kk, pk);
+          // packed P^T stays inside this warpgroup's own S^T columns (the other
+          // warpgroup may still be reading its half): chunk kk -> 64 (kk/2) + 16 (kk%2)
+          tmem_st16(tmem + lane_base + C::kColX + 64 * (kk >> 1) + 16 * (kk & 1), pk);
 #pragma unroll
           for (int i = 0; i < 4; ++i)
-            sts128(ds_s + sw128_offset(tid, 32 * kk + 8 * i, kTile), dk[4 * i], dk[4 * i + 1], dk[4 * i + 2],
+            sts128(ds_s + sw128_offset(row, 32 * kk + 8 * i, kTile), dk[4 * i], dk[4 * i + 1], dk[4 * i + 2],
                    dk[4 * i + 3]);
         }
         tmem_st_wait();
@@ -386,10 +393,10 @@ __global__ void __launch_bounds__(192, 1)
           return;
         }
         tc_fence_after();
-        const bool q_live = tid < nqv && (!p.causal || q0 + tid >= it.kv_first);
-        float* dst = p.dq_acc + (((int64_t)it.g.q_off + q0 + tid) * p.Hq + h) * D;
+        const bool q_live = row < nqv && (!p.causal || q0 + row >= it.kv_first);
+        float* dst = p.dq_acc + (((int64_t)it.g.q_off + q0 + row) * p.Hq + h) * D;
 #pragma unroll 1
-        for (int kk = 0; kk < D / 32; ++kk) {
+        for (int kk = half * (D / 64); kk < (half + 1) * (D / 64); ++kk) {
           uint32_t r[32];
           tmem_ld32(tmem + lane_base + C::kColX + 32 * kk, r);
           tmem_ld_wait(r);
@@ -408,7 +415,7 @@ __global__ void __launch_bounds__(192, 1)
       if (!ok) break;
       // ---- epilogue: dK (scaled) and dV of this key tile, zeros on pad rows
 #pragma unroll 1
-      for (int kk = 0; kk < D / 32; ++kk) {
+      for (int kk = half * (D / 64); kk < (half + 1) * (D / 64); ++kk) {
         uint32_t a[32], bq[32];
         if (nsteps > 0) {
           tmem_ld32(tmem + lane_base + C::kColDK + 32 * kk, a);
@@ -451,7 +458,7 @@ __global__ void __launch_bounds__(192, 1)
       const int Tend = p.eff[3 * (p.B + 1) + p.B];
       const int64_t nvec = (p.dkv_rows - Tend) * (int64_t)p.Hkv * (D / 8);
       const int64_t base = (int64_t)Tend * p.Hkv * D;
-      for (int64_t i = (int64_t)blockIdx.x * 128 + tid; i < nvec; i += (int64_t)gridDim.x * 128) {
+      for (int64_t i = (int64_t)blockIdx.x * 256 + tid; i < nvec; i += (int64_t)gridDim.x * 256) {
         reinterpret_cast<uint4*>(p.dk + base)[i] = make_uint4(0, 0, 0, 0);
         reinterpret_cast<uint4*>(p.dv + base)[i] = make_uint4(0, 0, 0, 0);
       }
@@ -460,7 +467,7 @@ __global__ void __launch_bounds__(192, 1)
 
   tc_fence_before();
   __syncthreads();
-  if (warp == 5) {
+  if (warp == 9) {
     tc_fence_after();
     tmem_dealloc(tmem, C::kTmemCols);
   }
@@ -474,7 +481,7 @@ static cudaError_t launch_bwd_t(const BwdParams& p, const CUtensorMap& tq, const
   cudaError_t e = cudaFuncSetAttribute(bwd_kernel<D>, cudaFuncAttributeMaxDynamicSharedMemorySize, C::kSmem);
   if (e != cudaSuccess) return e;
   prof_before(THD_KERNEL_BWD, st);
-  bwd_kernel<D><<<grid, 192, C::kSmem, st>>>(p, tq, tdo, tk, tv);
+  bwd_kernel<D><<<grid, 320, C::kSmem, st>>>(p, tq, tdo, tk, tv);
   count_launch();
   e = cudaGetLastError();
   prof_after(THD_KERNEL_BWD, st);

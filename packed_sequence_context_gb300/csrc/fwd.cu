@@ -17,12 +17,13 @@
 // granularity.  In one-step mode (thd_attn_fwd_step) only step `step_lo`
 // is walked and the step's partial (O_i, lse_i) is written in fp32.
 //
-// CTA layout (192 threads, one CTA per SM, persistent over the schedule):
-//   warps 0-3  softmax + epilogue, one query row per thread (TMEM lane)
-//   warp 4     producer: gathers the next item's query tile (its rows come
+// CTA layout (320 threads, one CTA per SM, persistent over the schedule):
+//   warps 0-7  softmax + epilogue in two warpgroups: a thread owns one query
+//              row (its TMEM lane) and half of the key columns of each tile
+//   warp 8     producer: gathers the next item's query tile (its rows come
 //              from two chunks, so cp.async row gathers, double-buffered) and
 //              issues the K/V tile TMA loads (3-D tensor maps over [T, Hkv, D])
-//   warp 5     TMEM allocator and single-thread tcgen05.mma issuer
+//   warp 9     TMEM allocator and single-thread tcgen05.mma issuer
 // TMEM: three S buffers of 128 fp32 columns ([0,384)); the softmax writes P
 // as packed bf16 over the first columns of its S buffer, and PV reads it from
 // TMEM as the A operand; O accumulates in [384, 384+D).  MMAs into different
@@ -42,7 +43,7 @@ struct FwdCfg {
   static constexpr uint32_t kTmemCols = 512;
   static constexpr int kSBufs = 3;          // S/P buffers of 128 columns
   static constexpr uint32_t kColO = 384;
-  static constexpr int kThreads = 192;
+  static constexpr int kThreads = 320;
 };
 
 struct FwdItem {
@@ -95,7 +96,7 @@ __device__ inline void drain_wait(uint64_t* bar, uint32_t parity) {
 }
 
 template <int D, bool kStep>
-__global__ void __launch_bounds__(192, 1)
+__global__ void __launch_bounds__(320, 1)
     fwd_kernel(const FwdParams p, const __grid_constant__ CUtensorMap tmK, const __grid_constant__ CUtensorMap tmV) {
   using C = FwdCfg<D>;
   constexpr int S = C::kStages;
@@ -114,6 +115,8 @@ __global__ void __launch_bounds__(192, 1)
   __shared__ __align__(8) uint64_t bar_drain;
   __shared__ uint32_t s_tmem;
   __shared__ int s_abort;
+  __shared__ float s_mx[2][2][kTile];   // partial row maxima, [tile parity][half][row]
+  __shared__ float s_sum[2][2][kTile];  // partial row sums, [item parity][half][row]
 
   const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
   if (*p.dev_status != 0) return;  // metadata rejected: outputs untouched
@@ -126,7 +129,7 @@ __global__ void __launch_bounds__(192, 1)
     }
     for (int s = 0; s < C::kSBufs; ++s) {
       mbar_init(&bar_s_full[s], 1);
-      mbar_init(&bar_p_ready[s], 128);
+      mbar_init(&bar_p_ready[s], 256);
       mbar_init(&bar_s_free[s], 1);
     }
     for (int s = 0; s < 2; ++s) {
@@ -137,11 +140,11 @@ __global__ void __launch_bounds__(192, 1)
     s_abort = 0;
     fence_mbar_init();
   }
-  if (warp == 5) {
+  if (warp == 9) {
     tmem_alloc(&s_tmem, C::kTmemCols);
     tmem_relinquish();
   }
-  if (warp == 4 && lane == 0) {
+  if (warp == 8 && lane == 0) {
     tma_prefetch_desc(&tmK);
     tma_prefetch_desc(&tmV);
   }
@@ -150,7 +153,7 @@ __global__ void __launch_bounds__(192, 1)
   tc_fence_after();
   const uint32_t tmem = s_tmem;
 
-  if (warp == 4) {
+  if (warp == 8) {
     // ------------------------------------------------------------ producer (whole warp)
     int stage = 0;
     uint32_t ph = 0, n_fill = 0, q_iter = 0;
@@ -213,7 +216,7 @@ __global__ void __launch_bounds__(192, 1)
       }
     }
     __syncwarp();
-  } else if (warp == 5) {
+  } else if (warp == 9) {
     // ------------------------------------------------------------ MMA issuer
     if (lane == 0) {
       constexpr uint32_t idesc_pv = idesc_bf16(128, D, false, true);
@@ -228,7 +231,8 @@ __global__ void __launch_bounds__(192, 1)
         const uint32_t pcol = tmem + b * 128u;
         for (int ks = 0; ks < ncols / 16; ++ks) {
           const uint64_t bd = sdesc_sw128(vbase + st * C::kKVBytes + ks * 2048, 16384, 1024);
-          mma_ts(tmem + C::kColO, pcol + ks * 8, bd, idesc_pv, (first && ks == 0) ? 0u : 1u);
+          // packed P of key columns 16 ks.. sits at column 64 (ks/4) + 8 (ks%4)
+          mma_ts(tmem + C::kColO, pcol + 64 * (ks >> 2) + 8 * (ks & 3), bd, idesc_pv, (first && ks == 0) ? 0u : 1u);
         }
         tc_commit(&bar_kv_empty[st]);
         tc_commit(&bar_s_free[b]);  // PV on buffer b done: P consumed, O holds tile gg
@@ -290,19 +294,28 @@ __global__ void __launch_bounds__(192, 1)
     __syncwarp();
   } else {
     // ------------------------------------------------------------ softmax + epilogue
-    const uint32_t lane_base = (uint32_t)(warp * 32) << 16;
+    // Two warpgroups: thread (half, row) owns query row `row` (its TMEM lane)
+    // and key columns [64 half, 64 half + 64) of every tile, plus head-dim
+    // columns [D/2 half, D/2 half + D/2) of O.  The two threads of a row swap
+    // partial row maxima once per tile through shared memory (pair barrier)
+    // and their partial row sums once per item.
+    const int half = warp >> 2;
+    const int row = tid & 127;
+    const int pair_bar = 2 + (warp & 3);  // named barrier of warps w and w + 4
+    const uint32_t lane_base = (uint32_t)((warp & 3) * 32) << 16;
+    constexpr int DH = D / 2;
     const float sl2 = p.scale_log2;
-    uint32_t g = 0;
+    uint32_t g = 0, n_item = 0;
     bool ok = true;
     for (int w = blockIdx.x; w < n_items && ok; w += gridDim.x) {
       const FwdItem it = fwd_item(p, w);
-      const int prow = it.t * kTile + tid;
+      const int prow = it.t * kTile + row;
       const bool in_rank = prow < 2 * it.g.cbq;
       const int pos = in_rank ? local_to_pos(prow, it.r, it.g.cbq, p.cp) : 0;
       const bool valid = in_rank && pos < it.g.Lq;
       const int64_t grow = (int64_t)it.g.q_off + pos;
       // ---- key tiles
-      float m = -INFINITY, l = 0.f;
+      float m = -INFINITY, l = 0.f;  // running max (log2 units, shared value) and this half's sum
       int jl = 0;
       for_each_kv_tile(it, p, [&](int c, int j) {
         if (!ok) return;
@@ -320,35 +333,32 @@ __global__ void __launch_bounds__(192, 1)
           if (p.causal) cnt = imin(cnt, pos - j0 + 1);
           cnt = imax(cnt, 0);
         }
-        const int ncols = fwd_tile_ncols(it, p, c, j);   // the N this tile's QK^T computed
+        const int ncols = fwd_tile_ncols(it, p, c, j);  // the N this tile's QK^T computed
         const int nch = ceil_div(ncols, 32);
-        uint32_t sr[4][32];
+        const int k0 = 2 * half;  // this thread's 32-column chunks: k0, k0 + 1
+        uint32_t sr[2][32];
         const uint32_t scol = tmem + lane_base + sb * 128u;
 #pragma unroll
-        for (int k = 0; k < 4; ++k)
-          if (k < nch) tmem_ld32(scol + 32 * k, sr[k]);
+        for (int kk = 0; kk < 2; ++kk)
+          if (k0 + kk < nch) tmem_ld32(scol + 32 * (k0 + kk), sr[kk]);
 #pragma unroll
-        for (int k = 0; k < 4; ++k)
-          if (k < nch) tmem_ld_wait(sr[k]);
-        float mt = -INFINITY;
-        if (cnt >= kTile) {
+        for (int kk = 0; kk < 2; ++kk)
+          if (k0 + kk < nch) tmem_ld_wait(sr[kk]);
+        float mloc = -INFINITY;
+        const bool full = cnt >= kTile;
 #pragma unroll
-          for (int k = 0; k < 4; ++k)
+        for (int kk = 0; kk < 2; ++kk)
+          if (k0 + kk < nch) {
 #pragma unroll
-            for (int n = 0; n < 32; ++n) mt = fmaxf(mt, __uint_as_float(sr[k][n]));
-        } else {
-#pragma unroll
-          for (int k = 0; k < 4; ++k)
-            if (k < nch) {
-#pragma unroll
-              for (int n = 0; n < 32; ++n) {
-                const float x = (32 * k + n < cnt) ? __uint_as_float(sr[k][n]) : -INFINITY;
-                sr[k][n] = __float_as_uint(x);
-                mt = fmaxf(mt, x);
-              }
+            for (int n = 0; n < 32; ++n) {
+              const float x = (full || 32 * (k0 + kk) + n < cnt) ? __uint_as_float(sr[kk][n]) : -INFINITY;
+              sr[kk][n] = __float_as_uint(x);
+              mloc = fmaxf(mloc, x);
             }
-        }
-        mt *= sl2;
+          }
+        s_mx[g & 1u][half][row] = mloc;
+        named_bar_sync(pair_bar, 64);
+        const float mt = fmaxf(mloc, s_mx[g & 1u][half ^ 1][row]) * sl2;
         // lazy rescale: move the running max only when it grows by > 8 (log2 units)
         const bool upd = mt > m + 8.0f;
         const float alpha = upd ? ex2(m - mt) : 1.0f;
@@ -369,29 +379,32 @@ __global__ void __launch_bounds__(192, 1)
           tc_fence_after();
           const float f = need_o ? alpha : 1.0f;
 #pragma unroll
-          for (int k = 0; k < D / 32; ++k) {
+          for (int k = 0; k < DH / 32; ++k) {
             uint32_t o[32];
-            tmem_ld32(tmem + lane_base + C::kColO + 32 * k, o);
+            const uint32_t oc = tmem + lane_base + C::kColO + half * DH + 32 * k;
+            tmem_ld32(oc, o);
             tmem_ld_wait(o);
 #pragma unroll
             for (int n = 0; n < 32; ++n) o[n] = __float_as_uint(__uint_as_float(o[n]) * f);
-            tmem_st32(tmem + lane_base + C::kColO + 32 * k, o);
+            tmem_st32(oc, o);
           }
         }
         const float mm = (m == -INFINITY) ? 0.f : m;
         float rs = 0.f;
 #pragma unroll
-        for (int k = 0; k < 4; ++k) {
-          if (k < nch) {
+        for (int kk = 0; kk < 2; ++kk) {
+          if (k0 + kk < nch) {
             uint32_t pk[16];
 #pragma unroll
             for (int n = 0; n < 16; ++n) {
-              const float p0 = ex2(fmaf(__uint_as_float(sr[k][2 * n]), sl2, -mm));
-              const float p1 = ex2(fmaf(__uint_as_float(sr[k][2 * n + 1]), sl2, -mm));
+              const float p0 = ex2(fmaf(__uint_as_float(sr[kk][2 * n]), sl2, -mm));
+              const float p1 = ex2(fmaf(__uint_as_float(sr[kk][2 * n + 1]), sl2, -mm));
               rs += p0 + p1;
               pk[n] = pack_bf16x2(p0, p1);
             }
-            tmem_st16(scol + 16 * k, pk);
+            // packed P stays inside this half's own S columns (the partner may
+            // still be reading its half): chunk k -> column 64 (k/2) + 16 (k%2)
+            tmem_st16(scol + 64 * half + 16 * kk, pk);
           }
         }
         l += rs;
@@ -407,31 +420,36 @@ __global__ void __launch_bounds__(192, 1)
         if (!mbar_wait(&bar_s_free[(g - 1) % C::kSBufs], ((g - 1) / C::kSBufs) & 1u, &s_abort)) break;
         tc_fence_after();
       }
-      const bool live = valid && l > 0.f;
-      const float inv_l = live ? 1.0f / l : 0.f;
-      if (in_rank) {
-        const float lse = live ? (m + log2f(l)) * 0.69314718055994531f : -INFINITY;
+      s_sum[n_item & 1u][half][row] = l;
+      named_bar_sync(pair_bar, 64);
+      const float ltot = l + s_sum[n_item & 1u][half ^ 1][row];
+      ++n_item;
+      const bool live = valid && ltot > 0.f;
+      const float inv_l = live ? 1.0f / ltot : 0.f;
+      if (in_rank && half == 0) {
+        const float lse = live ? (m + log2f(ltot)) * 0.69314718055994531f : -INFINITY;
         p.lse[(int64_t)it.h * p.T_q + grow] = lse;
       }
 #pragma unroll
-      for (int k = 0; k < D / 32; ++k) {
+      for (int k = 0; k < DH / 32; ++k) {
         uint32_t o[32];
         if (jl > 0) {
-          tmem_ld32(tmem + lane_base + C::kColO + 32 * k, o);
+          tmem_ld32(tmem + lane_base + C::kColO + half * DH + 32 * k, o);
           tmem_ld_wait(o);
         } else {
 #pragma unroll
           for (int n = 0; n < 32; ++n) o[n] = 0u;
         }
         if (in_rank) {
+          const int64_t col = (grow * p.Hq + it.h) * D + half * DH + 32 * k;
           if constexpr (kStep) {
-            float4* dst = reinterpret_cast<float4*>(static_cast<float*>(p.o) + (grow * p.Hq + it.h) * D + 32 * k);
+            float4* dst = reinterpret_cast<float4*>(static_cast<float*>(p.o) + col);
 #pragma unroll
             for (int n = 0; n < 8; ++n)
               dst[n] = make_float4(__uint_as_float(o[4 * n]) * inv_l, __uint_as_float(o[4 * n + 1]) * inv_l,
                                    __uint_as_float(o[4 * n + 2]) * inv_l, __uint_as_float(o[4 * n + 3]) * inv_l);
           } else {
-            uint4* dst = reinterpret_cast<uint4*>(static_cast<uint16_t*>(p.o) + (grow * p.Hq + it.h) * D + 32 * k);
+            uint4* dst = reinterpret_cast<uint4*>(static_cast<uint16_t*>(p.o) + col);
 #pragma unroll
             for (int n = 0; n < 4; ++n) {
               uint4 v;
@@ -450,7 +468,7 @@ __global__ void __launch_bounds__(192, 1)
     if (ok) {
       const int Tend = p.eff[(p.B + 1) + p.B];
       const int64_t nrow = (p.T_q - Tend) * (int64_t)p.Hq;
-      for (int64_t i = (int64_t)blockIdx.x * 128 + tid; i < nrow; i += (int64_t)gridDim.x * 128) {
+      for (int64_t i = (int64_t)blockIdx.x * 256 + tid; i < nrow; i += (int64_t)gridDim.x * 256) {
         const int64_t t = Tend + i / p.Hq;
         const int h = (int)(i % p.Hq);
         if constexpr (kStep) {
@@ -467,7 +485,7 @@ __global__ void __launch_bounds__(192, 1)
 
   tc_fence_before();
   __syncthreads();
-  if (warp == 5) {
+  if (warp == 9) {
     tc_fence_after();
     tmem_dealloc(tmem, C::kTmemCols);
   }
