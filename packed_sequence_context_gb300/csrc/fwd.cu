@@ -17,12 +17,14 @@
 // granularity.  In one-step mode (thd_attn_fwd_step) only step `step_lo`
 // is walked and the step's partial (O_i, lse_i) is written in fp32.
 //
-// CTA layout (320 threads, one CTA per SM, persistent over the schedule):
+// CTA layout (352 threads, one CTA per SM, persistent over the schedule):
 //   warps 0-7  softmax + epilogue in two warpgroups: a thread owns one query
 //              row (its TMEM lane) and half of the key columns of each tile
-//   warp 8     producer: gathers the next item's query tile (its rows come
-//              from two chunks, so cp.async row gathers, double-buffered) and
-//              issues the K/V tile TMA loads (3-D tensor maps over [T, Hkv, D])
+//   warp 8     producer: gathers each item's query tile (its rows come from
+//              two chunks, so cp.async row gathers) and issues the K tile TMA
+//              loads (3-D tensor maps over [T, Hkv, D]) into a 3-slot ring
+//   warp 10    producer of the V tiles (2-slot ring: a V slot frees only when
+//              its PV completes, a K slot already when its QK^T does)
 //   warp 9     TMEM allocator and single-thread tcgen05.mma issuer
 // TMEM: three S buffers of 128 fp32 columns ([0,384)); the softmax writes P
 // as packed bf16 over the first columns of its S buffer, and PV reads it from
@@ -36,14 +38,15 @@ namespace thd {
 
 template <int D>
 struct FwdCfg {
-  static constexpr int kStages = D == 128 ? 2 : 4;
+  static constexpr int kKStages = D == 128 ? 3 : 4;  // K ring: a slot frees when its QK^T completes
+  static constexpr int kVStages = D == 128 ? 2 : 3;  // V ring: a slot frees when its PV completes
   static constexpr int kQBytes = kTile * D * 2;
   static constexpr int kKVBytes = kTile * D * 2;  // one K (or V) tile
-  static constexpr int kSmem = 1024 + 2 * kQBytes + kStages * 2 * kKVBytes;  // query tile double-buffered
+  static constexpr int kSmem = 1024 + kQBytes + (kKStages + kVStages) * kKVBytes;
   static constexpr uint32_t kTmemCols = 512;
   static constexpr int kSBufs = 3;          // S/P buffers of 128 columns
   static constexpr uint32_t kColO = 384;
-  static constexpr int kThreads = 320;
+  static constexpr int kThreads = 352;
 };
 
 struct FwdItem {
@@ -96,22 +99,24 @@ __device__ inline void drain_wait(uint64_t* bar, uint32_t parity) {
 }
 
 template <int D, bool kStep>
-__global__ void __launch_bounds__(320, 1)
+__global__ void __launch_bounds__(352, 1)
     fwd_kernel(const FwdParams p, const __grid_constant__ CUtensorMap tmK, const __grid_constant__ CUtensorMap tmV) {
   using C = FwdCfg<D>;
-  constexpr int S = C::kStages;
+  constexpr int KS = C::kKStages, VS = C::kVStages;
   extern __shared__ uint8_t smem_raw[];
   uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
-  uint8_t* sQ = smem;  // two buffers of kQBytes
-  uint8_t* sK = smem + 2 * C::kQBytes;
-  uint8_t* sV = sK + S * C::kKVBytes;
-  __shared__ __align__(8) uint64_t bar_kv_full[S];
-  __shared__ __align__(8) uint64_t bar_kv_empty[S];
+  uint8_t* sQ = smem;
+  uint8_t* sK = smem + C::kQBytes;
+  uint8_t* sV = sK + KS * C::kKVBytes;
+  __shared__ __align__(8) uint64_t bar_k_full[KS];
+  __shared__ __align__(8) uint64_t bar_k_empty[KS];
+  __shared__ __align__(8) uint64_t bar_v_full[VS];
+  __shared__ __align__(8) uint64_t bar_v_empty[VS];
   __shared__ __align__(8) uint64_t bar_s_full[C::kSBufs];
   __shared__ __align__(8) uint64_t bar_p_ready[C::kSBufs];
   __shared__ __align__(8) uint64_t bar_s_free[C::kSBufs];
-  __shared__ __align__(8) uint64_t bar_q_full[2];
-  __shared__ __align__(8) uint64_t bar_q_empty[2];
+  __shared__ __align__(8) uint64_t bar_q_full;
+  __shared__ __align__(8) uint64_t bar_q_empty;
   __shared__ __align__(8) uint64_t bar_drain;
   __shared__ uint32_t s_tmem;
   __shared__ int s_abort;
@@ -123,19 +128,21 @@ __global__ void __launch_bounds__(320, 1)
   const int n_items = p.counters[0] * p.Hq;
 
   if (tid == 0) {
-    for (int s = 0; s < S; ++s) {
-      mbar_init(&bar_kv_full[s], 1);
-      mbar_init(&bar_kv_empty[s], 1);
+    for (int s = 0; s < KS; ++s) {
+      mbar_init(&bar_k_full[s], 1);
+      mbar_init(&bar_k_empty[s], 1);
+    }
+    for (int s = 0; s < VS; ++s) {
+      mbar_init(&bar_v_full[s], 1);
+      mbar_init(&bar_v_empty[s], 1);
     }
     for (int s = 0; s < C::kSBufs; ++s) {
       mbar_init(&bar_s_full[s], 1);
       mbar_init(&bar_p_ready[s], 256);
       mbar_init(&bar_s_free[s], 1);
     }
-    for (int s = 0; s < 2; ++s) {
-      mbar_init(&bar_q_full[s], 32);
-      mbar_init(&bar_q_empty[s], 1);
-    }
+    mbar_init(&bar_q_full, 32);
+    mbar_init(&bar_q_empty, 1);
     mbar_init(&bar_drain, 1);
     s_abort = 0;
     fence_mbar_init();
@@ -154,17 +161,17 @@ __global__ void __launch_bounds__(320, 1)
   const uint32_t tmem = s_tmem;
 
   if (warp == 8) {
-    // ------------------------------------------------------------ producer (whole warp)
-    int stage = 0;
-    uint32_t ph = 0, n_fill = 0, q_iter = 0;
+    // ------------------------------------------------------------ query + key producer (whole warp)
+    int ks = 0;
+    uint32_t kph = 0, n_fill = 0, q_iter = 0;
     bool ok = true;
     for (int w = blockIdx.x; w < n_items && ok; w += gridDim.x) {
       const FwdItem it = fwd_item(p, w);
       // ---- the query tile: rank-local rows [128 t, 128 t + 128) of rank r,
-      // gathered into 128B-swizzled smem; rows without a valid query are zero
-      const uint32_t qb = q_iter & 1u;
-      if (!mbar_wait(&bar_q_empty[qb], ((q_iter >> 1) & 1u) ^ 1u, &s_abort)) break;
-      const uint32_t qdst = smem_u32(sQ + qb * C::kQBytes);
+      // gathered into 128B-swizzled smem once the previous item's last QK^T
+      // has completed; rows without a valid query are zero
+      if (!mbar_wait(&bar_q_empty, (q_iter & 1u) ^ 1u, &s_abort)) break;
+      const uint32_t qdst = smem_u32(sQ);
 #pragma unroll
       for (int rr = 0; rr < 4; ++rr) {
         const int row = lane + 32 * rr;
@@ -181,38 +188,66 @@ __global__ void __launch_bounds__(320, 1)
       // (async) proxy before the MMA thread may read them
       cp_async_wait_all();
       fence_proxy_async_smem();
-      mbar_arrive(&bar_q_full[qb]);
+      mbar_arrive(&bar_q_full);
       ++q_iter;
-      // ---- the key/value tiles of the item, in ring order
+      // ---- the key tiles of the item, in ring order
       for_each_kv_tile(it, p, [&](int c, int j) {
         if (!ok) return;
-        if (!mbar_wait(&bar_kv_empty[stage], ph ^ 1u, &s_abort)) {
+        if (!mbar_wait(&bar_k_empty[ks], kph ^ 1u, &s_abort)) {
           ok = false;
           return;
         }
         if (lane == 0) {
           const int row = it.g.kv_off + c * it.g.cbkv + j * kTile;
-          mbar_arrive_expect_tx(&bar_kv_full[stage], 2 * C::kKVBytes);
+          mbar_arrive_expect_tx(&bar_k_full[ks], C::kKVBytes);
 #pragma unroll
-          for (int hb = 0; hb < D / 64; ++hb) {
-            tma_load_3d(smem_u32(sK + stage * C::kKVBytes + hb * 16384), &tmK, &bar_kv_full[stage], hb * 64,
-                        it.kvh, row);
-            tma_load_3d(smem_u32(sV + stage * C::kKVBytes + hb * 16384), &tmV, &bar_kv_full[stage], hb * 64,
-                        it.kvh, row);
-          }
+          for (int hb = 0; hb < D / 64; ++hb)
+            tma_load_3d(smem_u32(sK + ks * C::kKVBytes + hb * 16384), &tmK, &bar_k_full[ks], hb * 64, it.kvh, row);
         }
         ++n_fill;
-        if (++stage == S) {
-          stage = 0;
-          ph ^= 1u;
+        if (++ks == KS) {
+          ks = 0;
+          kph ^= 1u;
         }
       });
     }
     // every issued load must land before the CTA may exit
     if (lane == 0) {
-      for (int s = 0; s < S; ++s) {
-        const uint32_t fills = n_fill > (uint32_t)s ? (n_fill - 1 - s) / S + 1 : 0;
-        if (fills > 0) drain_wait(&bar_kv_full[s], (fills - 1) & 1u);
+      for (int s = 0; s < KS; ++s) {
+        const uint32_t fills = n_fill > (uint32_t)s ? (n_fill - 1 - s) / KS + 1 : 0;
+        if (fills > 0) drain_wait(&bar_k_full[s], (fills - 1) & 1u);
+      }
+    }
+    __syncwarp();
+  } else if (warp == 10) {
+    // ------------------------------------------------------------ value producer
+    if (lane == 0) {
+      int vs = 0;
+      uint32_t vph = 0, n_fill = 0;
+      bool ok = true;
+      for (int w = blockIdx.x; w < n_items && ok; w += gridDim.x) {
+        const FwdItem it = fwd_item(p, w);
+        for_each_kv_tile(it, p, [&](int c, int j) {
+          if (!ok) return;
+          if (!mbar_wait(&bar_v_empty[vs], vph ^ 1u, &s_abort)) {
+            ok = false;
+            return;
+          }
+          const int row = it.g.kv_off + c * it.g.cbkv + j * kTile;
+          mbar_arrive_expect_tx(&bar_v_full[vs], C::kKVBytes);
+#pragma unroll
+          for (int hb = 0; hb < D / 64; ++hb)
+            tma_load_3d(smem_u32(sV + vs * C::kKVBytes + hb * 16384), &tmV, &bar_v_full[vs], hb * 64, it.kvh, row);
+          ++n_fill;
+          if (++vs == VS) {
+            vs = 0;
+            vph ^= 1u;
+          }
+        });
+      }
+      for (int s = 0; s < VS; ++s) {
+        const uint32_t fills = n_fill > (uint32_t)s ? (n_fill - 1 - s) / VS + 1 : 0;
+        if (fills > 0) drain_wait(&bar_v_full[s], (fills - 1) & 1u);
       }
     }
     __syncwarp();
@@ -220,37 +255,43 @@ __global__ void __launch_bounds__(320, 1)
     // ------------------------------------------------------------ MMA issuer
     if (lane == 0) {
       constexpr uint32_t idesc_pv = idesc_bf16(128, D, false, true);
-      const uint32_t kbase = smem_u32(sK), vbase = smem_u32(sV);
-      int stage = 0;
-      uint32_t ph = 0, g = 0, q_iter = 0;
+      const uint32_t qbase = smem_u32(sQ), kbase = smem_u32(sK), vbase = smem_u32(sV);
+      int ks = 0, vs = 0;
+      uint32_t kph = 0, vph = 0, g = 0, q_iter = 0;
       bool ok = true;
-      auto issue_pv = [&](uint32_t gg, int st, bool first, int ncols) -> bool {
+      auto issue_pv = [&](uint32_t gg, bool first, int ncols) -> bool {
         const uint32_t b = gg % C::kSBufs;
         if (!mbar_wait(&bar_p_ready[b], (gg / C::kSBufs) & 1u, &s_abort)) return false;
+        if (!mbar_wait(&bar_v_full[vs], vph, &s_abort)) return false;
         tc_fence_after();
         const uint32_t pcol = tmem + b * 128u;
-        for (int ks = 0; ks < ncols / 16; ++ks) {
-          const uint64_t bd = sdesc_sw128(vbase + st * C::kKVBytes + ks * 2048, 16384, 1024);
-          // packed P of key columns 16 ks.. sits at column 64 (ks/4) + 8 (ks%4)
-          mma_ts(tmem + C::kColO, pcol + 64 * (ks >> 2) + 8 * (ks & 3), bd, idesc_pv, (first && ks == 0) ? 0u : 1u);
+        for (int kk = 0; kk < ncols / 16; ++kk) {
+          const uint64_t bd = sdesc_sw128(vbase + vs * C::kKVBytes + kk * 2048, 16384, 1024);
+          // packed P of key columns 16 kk.. sits at column 64 (kk/4) + 8 (kk%4)
+          mma_ts(tmem + C::kColO, pcol + 64 * (kk >> 2) + 8 * (kk & 3), bd, idesc_pv, (first && kk == 0) ? 0u : 1u);
         }
-        tc_commit(&bar_kv_empty[st]);
+        tc_commit(&bar_v_empty[vs]);
         tc_commit(&bar_s_free[b]);  // PV on buffer b done: P consumed, O holds tile gg
+        if (++vs == VS) {
+          vs = 0;
+          vph ^= 1u;
+        }
         return true;
       };
       for (int w = blockIdx.x; w < n_items && ok; w += gridDim.x) {
         const FwdItem it = fwd_item(p, w);
-        const uint32_t qb = q_iter & 1u;
-        if (!mbar_wait(&bar_q_full[qb], (q_iter >> 1) & 1u, &s_abort)) break;
+        int n = 0;
+        for_each_kv_tile(it, p, [&](int, int) { ++n; });
+        if (!mbar_wait(&bar_q_full, q_iter & 1u, &s_abort)) break;
         ++q_iter;
         tc_fence_after();
-        const uint32_t qbase = smem_u32(sQ + qb * C::kQBytes);
-        int prev_stage = 0, prev_cols = 0, j = 0;
+        if (n == 0) tc_commit(&bar_q_empty);
+        int prev_cols = 0, j = 0;
         uint32_t prev_g = 0;
         for_each_kv_tile(it, p, [&](int c, int jt) {
           if (!ok) return;
           const int ncols = fwd_tile_ncols(it, p, c, jt);
-          if (!mbar_wait(&bar_kv_full[stage], ph, &s_abort)) {
+          if (!mbar_wait(&bar_k_full[ks], kph, &s_abort)) {
             ok = false;
             return;
           }
@@ -263,29 +304,29 @@ __global__ void __launch_bounds__(320, 1)
           const uint32_t scol = tmem + b * 128u;
           const uint32_t idesc_qk = idesc_bf16(128, ncols, false, false);
 #pragma unroll
-          for (int ks = 0; ks < D / 16; ++ks) {
-            const uint32_t koff = (ks >> 2) * 16384 + (ks & 3) * 32;
+          for (int kk = 0; kk < D / 16; ++kk) {
+            const uint32_t koff = (kk >> 2) * 16384 + (kk & 3) * 32;
             const uint64_t ad = sdesc_sw128(qbase + koff, 16, 1024);
-            const uint64_t bd = sdesc_sw128(kbase + stage * C::kKVBytes + koff, 16, 1024);
-            mma_ss(scol, ad, bd, idesc_qk, ks > 0 ? 1u : 0u);
+            const uint64_t bd = sdesc_sw128(kbase + ks * C::kKVBytes + koff, 16, 1024);
+            mma_ss(scol, ad, bd, idesc_qk, kk > 0 ? 1u : 0u);
           }
           tc_commit(&bar_s_full[b]);
-          if (j > 0 && !issue_pv(prev_g, prev_stage, j == 1, prev_cols)) {
+          tc_commit(&bar_k_empty[ks]);              // the K slot frees once this QK^T completes
+          if (j == n - 1) tc_commit(&bar_q_empty);  // and the query tile after the item's last QK^T
+          if (++ks == KS) {
+            ks = 0;
+            kph ^= 1u;
+          }
+          if (j > 0 && !issue_pv(prev_g, j == 1, prev_cols)) {
             ok = false;
             return;
           }
-          prev_stage = stage;
           prev_g = g;
           prev_cols = ncols;
-          if (++stage == S) {
-            stage = 0;
-            ph ^= 1u;
-          }
           ++g;
           ++j;
         });
-        if (ok && j > 0 && !issue_pv(prev_g, prev_stage, j == 1, prev_cols)) ok = false;
-        tc_commit(&bar_q_empty[qb]);  // the query buffer is free once this item's MMAs complete
+        if (ok && j > 0 && !issue_pv(prev_g, j == 1, prev_cols)) ok = false;
       }
       // all issued MMAs must complete before TMEM is released
       tc_commit(&bar_drain);
@@ -378,7 +419,7 @@ __global__ void __launch_bounds__(320, 1)
           }
           tc_fence_after();
           const float f = need_o ? alpha : 1.0f;
-#pragma unroll
+#pragma unroll 1
           for (int k = 0; k < DH / 32; ++k) {
             uint32_t o[32];
             const uint32_t oc = tmem + lane_base + C::kColO + half * DH + 32 * k;
@@ -430,7 +471,7 @@ __global__ void __launch_bounds__(320, 1)
         const float lse = live ? (m + log2f(ltot)) * 0.69314718055994531f : -INFINITY;
         p.lse[(int64_t)it.h * p.T_q + grow] = lse;
       }
-#pragma unroll
+#pragma unroll 1
       for (int k = 0; k < DH / 32; ++k) {
         uint32_t o[32];
         if (jl > 0) {
