@@ -81,6 +81,20 @@ static bool make_thd_map(CUtensorMap* m, const void* base, int64_t rows, int H, 
              CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
 }
 
+// 3-D map over the fp32 dQ accumulator [rows, H, D]; box = 32 rows x 1 head
+// x 32 columns (128 bytes, the 128B-swizzle width), used for reduce-add.
+static bool make_f32_map(CUtensorMap* m, const float* base, int64_t rows, int H, int D) {
+  auto enc = encode_fn();
+  if (!enc) return false;
+  cuuint64_t dims[3] = {(cuuint64_t)D, (cuuint64_t)H, (cuuint64_t)(rows > 0 ? rows : 1)};
+  cuuint64_t strides[2] = {(cuuint64_t)D * 4, (cuuint64_t)H * D * 4};
+  cuuint32_t box[3] = {32, 1, 32};
+  cuuint32_t es[3] = {1, 1, 1};
+  return enc(m, CU_TENSOR_MAP_DATA_TYPE_FLOAT32, 3, const_cast<float*>(base), dims, strides, box, es,
+             CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
+             CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
+}
+
 static bool aligned(const void* p, uintptr_t a) { return (reinterpret_cast<uintptr_t>(p) & (a - 1)) == 0; }
 
 static int check_sizes(int B, int64_t T_q, int64_t T_kv, int Hq, int Hkv, int D, int cp, int pad_mode) {
@@ -288,9 +302,10 @@ int thd_attn_bwd(const void* q, const void* k, const void* v, const void* o, con
   rc = cuda_status(launch_bwd_prep(static_cast<const uint16_t*>(o), static_cast<const uint16_t*>(dout), delta,
                                    dq_acc, pp.eff, B, T_q, Hq, D, dev_status, st));
   if (rc) return rc;
-  CUtensorMap tq, tdo, tk, tv;
+  CUtensorMap tq, tdo, tk, tv, tdq;
   if (!make_thd_map(&tq, q, T_q, Hq, D) || !make_thd_map(&tdo, dout, T_q, Hq, D) ||
-      !make_thd_map(&tk, k, T_kv, Hkv, D) || !make_thd_map(&tv, v, T_kv, Hkv, D))
+      !make_thd_map(&tk, k, T_kv, Hkv, D) || !make_thd_map(&tv, v, T_kv, Hkv, D) ||
+      !make_f32_map(&tdq, dq_acc, T_q, Hq, D))
     return THD_ERR_CUDA;
   BwdParams bp;
   std::memset(&bp, 0, sizeof(bp));
@@ -316,7 +331,7 @@ int thd_attn_bwd(const void* q, const void* k, const void* v, const void* o, con
   bp.scale_log2 = softmax_scale * 1.4426950408889634f;
   const int64_t bound = (int64_t)L.item_cap * Hkv;
   const int grid = (int)(bound < num_sms() ? (bound > 0 ? bound : 1) : num_sms());
-  rc = cuda_status(launch_bwd(bp, tq, tdo, tk, tv, D, grid, st));
+  rc = cuda_status(launch_bwd(bp, tq, tdo, tk, tv, tdq, D, grid, st));
   if (rc) return rc;
   return cuda_status(launch_bwd_dq(dq_acc, static_cast<uint16_t*>(dq), pp.eff, B, T_q, dq_rows, Hq, D,
                                    softmax_scale, dev_status, st));

@@ -9,7 +9,8 @@
 // step i, and dK/dV travel back around the ring to their owner.  Here the
 // owner keeps its key tile in shared memory and visits, in ring order, the
 // query tiles of every rank that sees it; dK/dV accumulate in TMEM (no
-// travel), dQ goes to an fp32 accumulator with vector atomics.
+// travel), dQ goes to an fp32 accumulator with TMA reduce-adds (one bulk
+// operation per warp and 32-column block, element-wise atomic).
 //
 // One work item = (sequence b, key chunk c, key tile jk within the chunk, kv
 // head hk).  For each query tile (chunk qc, tile jq) that sees it and each
@@ -92,7 +93,8 @@ __device__ inline void drain_wait_b(uint64_t* bar, uint32_t parity) {
 template <int D>
 __global__ void __launch_bounds__(320, 1)
     bwd_kernel(const BwdParams p, const __grid_constant__ CUtensorMap tmQ, const __grid_constant__ CUtensorMap tmDO,
-               const __grid_constant__ CUtensorMap tmK, const __grid_constant__ CUtensorMap tmV) {
+               const __grid_constant__ CUtensorMap tmK, const __grid_constant__ CUtensorMap tmV,
+               const __grid_constant__ CUtensorMap tmDQ) {
   using C = BwdCfg<D>;
   constexpr int S = C::kStages;
   extern __shared__ __align__(1024) uint8_t smem[];
@@ -147,6 +149,7 @@ __global__ void __launch_bounds__(320, 1)
     tma_prefetch_desc(&tmDO);
     tma_prefetch_desc(&tmK);
     tma_prefetch_desc(&tmV);
+    tma_prefetch_desc(&tmDQ);
   }
   tc_fence_before();
   __syncthreads();
@@ -347,6 +350,10 @@ __global__ void __launch_bounds__(320, 1)
         named_bar_sync(1, 256);
         const uint32_t lse_s = smem_u32(lse2), dl_s = lse_s + 512;
         const int nch = ceil_div(nqv, 32);
+        // this warp's last dQ reduction must have read its staging bytes (this
+        // warp's own dS rows) before they are overwritten below
+        if (lane == 0) bulk_wait_read_all();
+        __syncwarp();
 #pragma unroll 1
         for (int kk = 2 * half; kk < imin(nch, 2 * half + 2); ++kk) {
           uint32_t sr[32], dr[32];
@@ -386,25 +393,42 @@ __global__ void __launch_bounds__(320, 1)
         fence_proxy_async_smem();
         tc_fence_before();
         mbar_arrive(bar_p_ready);
-        // drain dQ (TMEM lane = query row) into the fp32 accumulator with
-        // fire-and-forget vector reductions straight from registers
+        // drain dQ (TMEM lane = query row) into the fp32 accumulator: each warp
+        // stages its own 32 rows x 32 columns in the 4 KB of the dS buffer that
+        // hold its own dS rows (idle now: this step's dK/dQ products have
+        // completed), and its lane 0 adds the block to global memory with a TMA
+        // reduce-add.  Warps whose rows received nothing skip; dead rows in a
+        // live warp are staged as zeros.
         if (!mbar_wait(bar_dq_full, su & 1u, s_abort)) {
           ok = false;
           return;
         }
         tc_fence_after();
         const bool q_live = row < nqv && (!p.causal || q0 + row >= it.kv_first);
-        float* dst = p.dq_acc + (((int64_t)it.g.q_off + q0 + row) * p.Hq + h) * D;
+        if (__any_sync(0xffffffffu, q_live)) {
+          const uint32_t stg = ds_s + 16384 * half + 4096 * (warp & 3);
 #pragma unroll 1
-        for (int kk = half * (D / 64); kk < (half + 1) * (D / 64); ++kk) {
-          uint32_t r[32];
-          tmem_ld32(tmem + lane_base + C::kColX + 32 * kk, r);
-          tmem_ld_wait(r);
-          if (q_live) {
+          for (int kk = 0; kk < D / 64; ++kk) {
+            const int dcol = half * (D / 2) + 32 * kk;
+            uint32_t r[32];
+            tmem_ld32(tmem + lane_base + C::kColX + dcol, r);
+            tmem_ld_wait(r);
 #pragma unroll
-            for (int i = 0; i < 8; ++i)
-              red_add_v4(dst + 32 * kk + 4 * i, __uint_as_float(r[4 * i]), __uint_as_float(r[4 * i + 1]),
-                         __uint_as_float(r[4 * i + 2]), __uint_as_float(r[4 * i + 3]));
+            for (int c = 0; c < 8; ++c) {
+              const uint32_t a = q_live ? r[4 * c] : 0u, b = q_live ? r[4 * c + 1] : 0u;
+              const uint32_t e = q_live ? r[4 * c + 2] : 0u, f = q_live ? r[4 * c + 3] : 0u;
+              sts128(stg + lane * 128 + ((c ^ (lane & 7)) << 4), a, b, e, f);
+            }
+            fence_proxy_async_smem();
+            __syncwarp();
+            if (lane == 0) {
+              tma_reduce_add_3d(&tmDQ, stg, dcol, h, it.g.q_off + q0 + 32 * (warp & 3));
+              bulk_commit_group();
+              // the next block reuses the staging bytes; after the last one the
+              // wait moves to just before this warp's next dS write
+              if (kk + 1 < D / 64) bulk_wait_read_all();
+            }
+            __syncwarp();
           }
         }
         tc_fence_before();
@@ -453,6 +477,7 @@ __global__ void __launch_bounds__(320, 1)
       }
       tc_fence_before();
     }
+    if (lane == 0) bulk_wait_all();  // this warp's dQ reductions complete before the kernel ends
     // ---- dK/dV rows past the last sequence: zero
     if (ok) {
       const int Tend = p.eff[3 * (p.B + 1) + p.B];
@@ -476,12 +501,13 @@ __global__ void __launch_bounds__(320, 1)
 
 template <int D>
 static cudaError_t launch_bwd_t(const BwdParams& p, const CUtensorMap& tq, const CUtensorMap& tdo,
-                                const CUtensorMap& tk, const CUtensorMap& tv, int grid, cudaStream_t st) {
+                                const CUtensorMap& tk, const CUtensorMap& tv, const CUtensorMap& tdq, int grid,
+                                cudaStream_t st) {
   using C = BwdCfg<D>;
   cudaError_t e = cudaFuncSetAttribute(bwd_kernel<D>, cudaFuncAttributeMaxDynamicSharedMemorySize, C::kSmem);
   if (e != cudaSuccess) return e;
   prof_before(THD_KERNEL_BWD, st);
-  bwd_kernel<D><<<grid, 320, C::kSmem, st>>>(p, tq, tdo, tk, tv);
+  bwd_kernel<D><<<grid, 320, C::kSmem, st>>>(p, tq, tdo, tk, tv, tdq);
   count_launch();
   e = cudaGetLastError();
   prof_after(THD_KERNEL_BWD, st);
@@ -489,8 +515,9 @@ static cudaError_t launch_bwd_t(const BwdParams& p, const CUtensorMap& tq, const
 }
 
 cudaError_t launch_bwd(const BwdParams& p, const CUtensorMap& tq, const CUtensorMap& tdo, const CUtensorMap& tk,
-                       const CUtensorMap& tv, int D, int grid, cudaStream_t st) {
-  return D == 128 ? launch_bwd_t<128>(p, tq, tdo, tk, tv, grid, st) : launch_bwd_t<64>(p, tq, tdo, tk, tv, grid, st);
+                       const CUtensorMap& tv, const CUtensorMap& tdq, int D, int grid, cudaStream_t st) {
+  return D == 128 ? launch_bwd_t<128>(p, tq, tdo, tk, tv, tdq, grid, st)
+                  : launch_bwd_t<64>(p, tq, tdo, tk, tv, tdq, grid, st);
 }
 
 }  // namespace thd

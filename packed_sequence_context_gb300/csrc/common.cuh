@@ -234,7 +234,7 @@ cudaError_t launch_plan(const PlanParams& p, cudaStream_t st);
 cudaError_t launch_fwd(const FwdParams& p, const CUtensorMap& tk, const CUtensorMap& tv, int D, bool step_mode,
                        int grid, cudaStream_t st);
 cudaError_t launch_bwd(const BwdParams& p, const CUtensorMap& tq, const CUtensorMap& tdo, const CUtensorMap& tk,
-                       const CUtensorMap& tv, int D, int grid, cudaStream_t st);
+                       const CUtensorMap& tv, const CUtensorMap& tdq, int D, int grid, cudaStream_t st);
 cudaError_t launch_lse_merge(float* o_acc, float* lse_acc, const float* o_part, const float* lse_part, int64_t T,
                              int H, int D, cudaStream_t st);
 cudaError_t launch_tail_zero(uint16_t* dq, uint16_t* dk, uint16_t* dv, int64_t dq_rows, int64_t dkv_rows, int Hq,
