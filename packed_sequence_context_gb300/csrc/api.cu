@@ -298,9 +298,10 @@ int thd_attn_bwd(const void* q, const void* k, const void* v, const void* o, con
   rc = cuda_status(launch_plan(pp, st));
   if (rc) return rc;
   float* delta = reinterpret_cast<float*>(w + L.delta);
+  float* lse2 = reinterpret_cast<float*>(w + L.lse2);
   float* dq_acc = reinterpret_cast<float*>(w + L.dq_acc);
-  rc = cuda_status(launch_bwd_prep(static_cast<const uint16_t*>(o), static_cast<const uint16_t*>(dout), delta,
-                                   dq_acc, pp.eff, B, T_q, Hq, D, dev_status, st));
+  rc = cuda_status(launch_bwd_prep(static_cast<const uint16_t*>(o), static_cast<const uint16_t*>(dout), lse, delta,
+                                   lse2, dq_acc, pp.eff, B, T_q, Hq, D, dev_status, st));
   if (rc) return rc;
   CUtensorMap tq, tdo, tk, tv, tdq;
   if (!make_thd_map(&tq, q, T_q, Hq, D) || !make_thd_map(&tdo, dout, T_q, Hq, D) ||
@@ -311,7 +312,7 @@ int thd_attn_bwd(const void* q, const void* k, const void* v, const void* o, con
   std::memset(&bp, 0, sizeof(bp));
   bp.q = static_cast<const uint16_t*>(q);
   bp.dout = static_cast<const uint16_t*>(dout);
-  bp.lse = lse;
+  bp.lse2 = lse2;
   bp.delta = delta;
   bp.dq_acc = dq_acc;
   bp.dk = static_cast<uint16_t*>(dk);

@@ -192,7 +192,7 @@ __global__ void __launch_bounds__(320, 1)
           const int n = lane + 32 * k;
           if (n < nqv) {
             const int64_t idx = (int64_t)h * p.T_q + q_row + n;
-            cp_async_4(lse2 + 4 * n, p.lse + idx);
+            cp_async_4(lse2 + 4 * n, p.lse2 + idx);
             cp_async_4(lse2 + 512 + 4 * n, p.delta + idx);
           }
         }
@@ -344,11 +344,8 @@ __global__ void __launch_bounds__(320, 1)
           ok = false;
           return;
         }
-        float* lse2 = sLse + (su % S) * 256;
-        // lse arrives in natural log; the exponent below is in log2 units
-        if (half == 0 && row < nqv) lse2[row] *= 1.4426950408889634f;
-        named_bar_sync(1, 256);
-        const uint32_t lse_s = smem_u32(lse2), dl_s = lse_s + 512;
+        // lse arrives pre-scaled to log2 units by the preprocess kernel
+        const uint32_t lse_s = smem_u32(sLse + (su % S) * 256), dl_s = lse_s + 512;
         const int nch = ceil_div(nqv, 32);
         // this warp's last dQ reduction must have read its staging bytes (this
         // warp's own dS rows) before they are overwritten below
@@ -407,28 +404,29 @@ __global__ void __launch_bounds__(320, 1)
         const bool q_live = row < nqv && (!p.causal || q0 + row >= it.kv_first);
         if (__any_sync(0xffffffffu, q_live)) {
           const uint32_t stg = ds_s + 16384 * half + 4096 * (warp & 3);
+          uint32_t r[32];
+          tmem_ld32(tmem + lane_base + C::kColX + half * (D / 2), r);
 #pragma unroll 1
           for (int kk = 0; kk < D / 64; ++kk) {
             const int dcol = half * (D / 2) + 32 * kk;
-            uint32_t r[32];
-            tmem_ld32(tmem + lane_base + C::kColX + dcol, r);
             tmem_ld_wait(r);
+            // the previous block's reduction must have read the staging bytes
+            if (lane == 0 && kk > 0) bulk_wait_read_all();
+            __syncwarp();
 #pragma unroll
             for (int c = 0; c < 8; ++c) {
               const uint32_t a = q_live ? r[4 * c] : 0u, b = q_live ? r[4 * c + 1] : 0u;
               const uint32_t e = q_live ? r[4 * c + 2] : 0u, f = q_live ? r[4 * c + 3] : 0u;
               sts128(stg + lane * 128 + ((c ^ (lane & 7)) << 4), a, b, e, f);
             }
+            // the next block's TMEM load overlaps this block's reduction
+            if (kk + 1 < D / 64) tmem_ld32(tmem + lane_base + C::kColX + dcol + 32, r);
             fence_proxy_async_smem();
             __syncwarp();
             if (lane == 0) {
               tma_reduce_add_3d(&tmDQ, stg, dcol, h, it.g.q_off + q0 + 32 * (warp & 3));
               bulk_commit_group();
-              // the next block reuses the staging bytes; after the last one the
-              // wait moves to just before this warp's next dS write
-              if (kk + 1 < D / 64) bulk_wait_read_all();
             }
-            __syncwarp();
           }
         }
         tc_fence_before();

@@ -29,6 +29,7 @@ struct WsLayout {
   size_t counters = 0;  // int32 [64]: [0] number of schedule entries
   size_t items = 0;     // int4 [item_cap]
   size_t delta = 0;     // fp32 [Hq][T_q]          (backward)
+  size_t lse2 = 0;      // fp32 [Hq][T_q], lse * log2(e)  (backward)
   size_t dq_acc = 0;    // fp32 [T_q][Hq][D]       (backward)
   size_t total = 0;
   int item_cap = 0;
@@ -54,6 +55,7 @@ inline WsLayout ws_layout(int B, int64_t T_q, int64_t T_kv, int Hq, int D, int c
   w.items = take(sizeof(int32_t) * 4 * (size_t)cap);
   if (bwd) {
     w.delta = take(sizeof(float) * (size_t)Hq * (size_t)T_q);
+    w.lse2 = take(sizeof(float) * (size_t)Hq * (size_t)T_q);
     w.dq_acc = take(sizeof(float) * (size_t)T_q * (size_t)Hq * (size_t)D);
   }
   w.total = off;
@@ -215,7 +217,7 @@ struct FwdParams {
 struct BwdParams {
   const uint16_t* q;
   const uint16_t* dout;
-  const float* lse;
+  const float* lse2;  // lse * log2(e), [Hq][T_q]
   const float* delta;
   float* dq_acc;
   uint16_t* dk;
@@ -240,9 +242,9 @@ cudaError_t launch_lse_merge(float* o_acc, float* lse_acc, const float* o_part, 
 cudaError_t launch_tail_zero(uint16_t* dq, uint16_t* dk, uint16_t* dv, int64_t dq_rows, int64_t dkv_rows, int Hq,
                              int Hkv, int D, const int32_t* pad_q_end, const int32_t* pad_kv_end,
                              const int32_t* dev_status, cudaStream_t st);
-cudaError_t launch_bwd_prep(const uint16_t* o, const uint16_t* dout, float* delta, float* dq_acc,
-                            const int32_t* eff, int B, int64_t T_q, int Hq, int D, const int32_t* dev_status,
-                            cudaStream_t st);
+cudaError_t launch_bwd_prep(const uint16_t* o, const uint16_t* dout, const float* lse, float* delta, float* lse2,
+                            float* dq_acc, const int32_t* eff, int B, int64_t T_q, int Hq, int D,
+                            const int32_t* dev_status, cudaStream_t st);
 cudaError_t launch_bwd_dq(const float* dq_acc, uint16_t* dq, const int32_t* eff, int B, int64_t T_q,
                           int64_t dq_rows, int Hq, int D, float scale, const int32_t* dev_status, cudaStream_t st);
 

@@ -329,8 +329,9 @@ cudaError_t launch_tail_zero(uint16_t* dq, uint16_t* dk, uint16_t* dv, int64_t d
 }
 
 // ------------------------------------------------------------------ backward preprocess
-// Delta[h][t] = sum_d dO[t,h,d] * O[t,h,d] on valid rows (0 elsewhere), and
-// the fp32 dQ accumulator reset.  One warp per (t, h) row.
+// Delta[h][t] = sum_d dO[t,h,d] * O[t,h,d] and lse2[h][t] = lse * log2(e) on
+// valid rows (0 elsewhere), and the fp32 dQ accumulator reset.  One warp per
+// (t, h) row.
 __device__ inline bool row_valid(const int32_t* eff, int B, int t) {
   const int32_t* cu = eff;
   const int32_t* pad = eff + (B + 1);
@@ -341,9 +342,11 @@ __device__ inline bool row_valid(const int32_t* eff, int B, int t) {
 
 template <int D>
 __global__ void __launch_bounds__(256) bwd_prep_kernel(const uint16_t* __restrict__ o,
-                                                       const uint16_t* __restrict__ dout, float* __restrict__ delta,
-                                                       float* __restrict__ dq_acc, const int32_t* __restrict__ eff,
-                                                       int B, int64_t T, int Hq, const int32_t* dev_status) {
+                                                       const uint16_t* __restrict__ dout,
+                                                       const float* __restrict__ lse, float* __restrict__ delta,
+                                                       float* __restrict__ lse2, float* __restrict__ dq_acc,
+                                                       const int32_t* __restrict__ eff, int B, int64_t T, int Hq,
+                                                       const int32_t* dev_status) {
   if (*dev_status != 0) return;
   constexpr int PER = D / 32;  // elements per lane (4 or 2)
   const int lane = threadIdx.x & 31;
@@ -353,7 +356,8 @@ __global__ void __launch_bounds__(256) bwd_prep_kernel(const uint16_t* __restric
     const int64_t t = row / Hq;
     const int h = (int)(row - t * Hq);
     float acc = 0.f;
-    if (row_valid(eff, B, (int)t)) {
+    const bool valid = row_valid(eff, B, (int)t);
+    if (valid) {
       const uint16_t* po = o + row * D + lane * PER;
       const uint16_t* pd = dout + row * D + lane * PER;
       if (PER == 4) {
@@ -372,23 +376,28 @@ __global__ void __launch_bounds__(256) bwd_prep_kernel(const uint16_t* __restric
     }
 #pragma unroll
     for (int off = 16; off > 0; off >>= 1) acc += __shfl_xor_sync(0xffffffffu, acc, off);
-    if (lane == 0) delta[(int64_t)h * T + t] = acc;
+    if (lane == 0) {
+      delta[(int64_t)h * T + t] = acc;
+      lse2[(int64_t)h * T + t] = valid ? lse[(int64_t)h * T + t] * 1.4426950408889634f : 0.f;
+    }
     float* pq = dq_acc + row * D + lane * PER;
     if (PER == 4) *reinterpret_cast<float4*>(pq) = make_float4(0.f, 0.f, 0.f, 0.f);
     else *reinterpret_cast<float2*>(pq) = make_float2(0.f, 0.f);
   }
 }
 
-cudaError_t launch_bwd_prep(const uint16_t* o, const uint16_t* dout, float* delta, float* dq_acc,
-                            const int32_t* eff, int B, int64_t T_q, int Hq, int D, const int32_t* dev_status,
-                            cudaStream_t st) {
+cudaError_t launch_bwd_prep(const uint16_t* o, const uint16_t* dout, const float* lse, float* delta, float* lse2,
+                            float* dq_acc, const int32_t* eff, int B, int64_t T_q, int Hq, int D,
+                            const int32_t* dev_status, cudaStream_t st) {
   const int64_t warps = T_q * Hq;
   if (warps == 0) return cudaSuccess;
   const int64_t want = (warps + 7) / 8;
   const int grid = (int)(want < 8LL * num_sms() ? want : 8LL * num_sms());
   prof_before(THD_KERNEL_BWD_PREP, st);
-  if (D == 128) bwd_prep_kernel<128><<<grid, 256, 0, st>>>(o, dout, delta, dq_acc, eff, B, T_q, Hq, dev_status);
-  else bwd_prep_kernel<64><<<grid, 256, 0, st>>>(o, dout, delta, dq_acc, eff, B, T_q, Hq, dev_status);
+  if (D == 128)
+    bwd_prep_kernel<128><<<grid, 256, 0, st>>>(o, dout, lse, delta, lse2, dq_acc, eff, B, T_q, Hq, dev_status);
+  else
+    bwd_prep_kernel<64><<<grid, 256, 0, st>>>(o, dout, lse, delta, lse2, dq_acc, eff, B, T_q, Hq, dev_status);
   count_launch();
   cudaError_t e = cudaGetLastError();
   prof_after(THD_KERNEL_BWD_PREP, st);
