@@ -17,7 +17,7 @@
 // granularity.  In one-step mode (thd_attn_fwd_step) only step `step_lo`
 // is walked and the step's partial (O_i, lse_i) is written in fp32.
 //
-// CTA layout (352 threads, one CTA per SM, persistent over the schedule):
+// CTA layout (384 threads, one CTA per SM, persistent over the schedule):
 //   warps 0-7  softmax + epilogue in two warpgroups: a thread owns one query
 //              row (its TMEM lane) and half of the key columns of each tile
 //   warp 8     producer: gathers each item's query tile (its rows come from
@@ -25,7 +25,8 @@
 //              loads (3-D tensor maps over [T, Hkv, D]) into a 3-slot ring
 //   warp 10    producer of the V tiles (2-slot ring: a V slot frees only when
 //              its PV completes, a K slot already when its QK^T does)
-//   warp 9     TMEM allocator and single-thread tcgen05.mma issuer
+//   warp 9     TMEM allocator and QK^T issuer (one thread)
+//   warp 11    PV issuer (one thread)
 // TMEM: three S buffers of 128 fp32 columns ([0,384)); the softmax writes P
 // as packed bf16 over the first columns of its S buffer, and PV reads it from
 // TMEM as the A operand; O accumulates in [384, 384+D).  MMAs into different
@@ -46,7 +47,7 @@ struct FwdCfg {
   static constexpr uint32_t kTmemCols = 512;
   static constexpr int kSBufs = 3;          // S/P buffers of 128 columns
   static constexpr uint32_t kColO = 384;
-  static constexpr int kThreads = 352;
+  static constexpr int kThreads = 384;
 };
 
 struct FwdItem {
@@ -99,7 +100,7 @@ __device__ inline void drain_wait(uint64_t* bar, uint32_t parity) {
 }
 
 template <int D, bool kStep>
-__global__ void __launch_bounds__(352, 1)
+__global__ void __launch_bounds__(384, 1)
     fwd_kernel(const FwdParams p, const __grid_constant__ CUtensorMap tmK, const __grid_constant__ CUtensorMap tmV) {
   using C = FwdCfg<D>;
   constexpr int KS = C::kKStages, VS = C::kVStages;
@@ -118,6 +119,7 @@ __global__ void __launch_bounds__(352, 1)
   __shared__ __align__(8) uint64_t bar_q_full;
   __shared__ __align__(8) uint64_t bar_q_empty;
   __shared__ __align__(8) uint64_t bar_drain;
+  __shared__ __align__(8) uint64_t bar_drain2;
   __shared__ uint32_t s_tmem;
   __shared__ int s_abort;
   __shared__ float s_mx[2][2][kTile];   // partial row maxima, [tile parity][half][row]
@@ -144,6 +146,7 @@ __global__ void __launch_bounds__(352, 1)
     mbar_init(&bar_q_full, 32);
     mbar_init(&bar_q_empty, 1);
     mbar_init(&bar_drain, 1);
+    mbar_init(&bar_drain2, 1);
     s_abort = 0;
     fence_mbar_init();
   }
@@ -252,32 +255,20 @@ __global__ void __launch_bounds__(352, 1)
     }
     __syncwarp();
   } else if (warp == 9) {
-    // ------------------------------------------------------------ MMA issuer
+    // ------------------------------------------------------------ QK^T issuer
+    // The tensor pipe accepts an MMA only about as fast as it executes one,
+    // so every barrier wait or commit in an issuing thread leaves it idle for
+    // that long.  QK^T and PV are therefore issued by two threads (warps 9
+    // and 11): while one waits on a barrier, the other keeps the pipe fed.
+    // Ordering between the two streams comes only from the barriers: a QK^T
+    // overwrites S buffer b once the PV that read P from it has completed
+    // (s_free), and a PV reads P only after the softmax wrote it (p_ready).
     if (lane == 0) {
-      constexpr uint32_t idesc_pv = idesc_bf16(128, D, false, true);
-      const uint32_t qbase = smem_u32(sQ), kbase = smem_u32(sK), vbase = smem_u32(sV);
-      int ks = 0, vs = 0;
-      uint32_t kph = 0, vph = 0, g = 0, q_iter = 0;
+      const uint64_t qdesc = sdesc_sw128(smem_u32(sQ), 16, 1024);
+      const uint64_t kdesc = sdesc_sw128(smem_u32(sK), 16, 1024);
+      int ks = 0;
+      uint32_t kph = 0, g = 0, q_iter = 0;
       bool ok = true;
-      auto issue_pv = [&](uint32_t gg, bool first, int ncols) -> bool {
-        const uint32_t b = gg % C::kSBufs;
-        if (!mbar_wait(&bar_p_ready[b], (gg / C::kSBufs) & 1u, &s_abort)) return false;
-        if (!mbar_wait(&bar_v_full[vs], vph, &s_abort)) return false;
-        tc_fence_after();
-        const uint32_t pcol = tmem + b * 128u;
-        for (int kk = 0; kk < ncols / 16; ++kk) {
-          const uint64_t bd = sdesc_sw128(vbase + vs * C::kKVBytes + kk * 2048, 16384, 1024);
-          // packed P of key columns 16 kk.. sits at column 64 (kk/4) + 8 (kk%4)
-          mma_ts(tmem + C::kColO, pcol + 64 * (kk >> 2) + 8 * (kk & 3), bd, idesc_pv, (first && kk == 0) ? 0u : 1u);
-        }
-        tc_commit(&bar_v_empty[vs]);
-        tc_commit(&bar_s_free[b]);  // PV on buffer b done: P consumed, O holds tile gg
-        if (++vs == VS) {
-          vs = 0;
-          vph ^= 1u;
-        }
-        return true;
-      };
       for (int w = blockIdx.x; w < n_items && ok; w += gridDim.x) {
         const FwdItem it = fwd_item(p, w);
         int n = 0;
@@ -286,51 +277,77 @@ __global__ void __launch_bounds__(352, 1)
         ++q_iter;
         tc_fence_after();
         if (n == 0) tc_commit(&bar_q_empty);
-        int prev_cols = 0, j = 0;
-        uint32_t prev_g = 0;
+        int j = 0;
         for_each_kv_tile(it, p, [&](int c, int jt) {
           if (!ok) return;
           const int ncols = fwd_tile_ncols(it, p, c, jt);
-          if (!mbar_wait(&bar_k_full[ks], kph, &s_abort)) {
-            ok = false;
-            return;
-          }
           const uint32_t b = g % C::kSBufs;
-          if (g >= (uint32_t)C::kSBufs && !mbar_wait(&bar_s_free[b], (g / C::kSBufs - 1) & 1u, &s_abort)) {
+          if (!mbar_wait(&bar_k_full[ks], kph, &s_abort) ||
+              (g >= (uint32_t)C::kSBufs && !mbar_wait(&bar_s_free[b], (g / C::kSBufs - 1) & 1u, &s_abort))) {
             ok = false;
             return;
           }
           tc_fence_after();
-          const uint32_t scol = tmem + b * 128u;
           const uint32_t idesc_qk = idesc_bf16(128, ncols, false, false);
+          const uint64_t kd = kdesc + (uint64_t)((ks * C::kKVBytes) >> 4);
 #pragma unroll
           for (int kk = 0; kk < D / 16; ++kk) {
-            const uint32_t koff = (kk >> 2) * 16384 + (kk & 3) * 32;
-            const uint64_t ad = sdesc_sw128(qbase + koff, 16, 1024);
-            const uint64_t bd = sdesc_sw128(kbase + ks * C::kKVBytes + koff, 16, 1024);
-            mma_ss(scol, ad, bd, idesc_qk, kk > 0 ? 1u : 0u);
+            const uint64_t off = (uint64_t)(((kk >> 2) * 16384 + (kk & 3) * 32) >> 4);
+            mma_ss(tmem + b * 128u, qdesc + off, kd + off, idesc_qk, kk > 0 ? 1u : 0u);
           }
           tc_commit(&bar_s_full[b]);
-          tc_commit(&bar_k_empty[ks]);              // the K slot frees once this QK^T completes
-          if (j == n - 1) tc_commit(&bar_q_empty);  // and the query tile after the item's last QK^T
+          tc_commit(&bar_k_empty[ks]);                  // the K slot frees once this QK^T completes
+          if (++j == n) tc_commit(&bar_q_empty);        // and the query tile after the item's last QK^T
           if (++ks == KS) {
             ks = 0;
             kph ^= 1u;
           }
-          if (j > 0 && !issue_pv(prev_g, j == 1, prev_cols)) {
-            ok = false;
-            return;
-          }
-          prev_g = g;
-          prev_cols = ncols;
           ++g;
-          ++j;
         });
-        if (ok && j > 0 && !issue_pv(prev_g, j == 1, prev_cols)) ok = false;
       }
       // all issued MMAs must complete before TMEM is released
       tc_commit(&bar_drain);
       drain_wait(&bar_drain, 0);
+    }
+    __syncwarp();
+  } else if (warp == 11) {
+    // ------------------------------------------------------------ PV issuer
+    if (lane == 0) {
+      constexpr uint32_t idesc_pv = idesc_bf16(128, D, false, true);
+      const uint64_t vdesc = sdesc_sw128(smem_u32(sV), 16384, 1024);
+      int vs = 0;
+      uint32_t vph = 0, g = 0;
+      bool ok = true;
+      for (int w = blockIdx.x; w < n_items && ok; w += gridDim.x) {
+        const FwdItem it = fwd_item(p, w);
+        int j = 0;
+        for_each_kv_tile(it, p, [&](int c, int jt) {
+          if (!ok) return;
+          const int ncols = fwd_tile_ncols(it, p, c, jt);
+          const uint32_t b = g % C::kSBufs;
+          if (!mbar_wait(&bar_p_ready[b], (g / C::kSBufs) & 1u, &s_abort) ||
+              !mbar_wait(&bar_v_full[vs], vph, &s_abort)) {
+            ok = false;
+            return;
+          }
+          tc_fence_after();
+          const uint32_t pcol = tmem + b * 128u;
+          const uint64_t vd = vdesc + (uint64_t)((vs * C::kKVBytes) >> 4);
+          for (int kk = 0; kk < ncols / 16; ++kk)  // packed P of key columns 16 kk.. at 64 (kk/4) + 8 (kk%4)
+            mma_ts(tmem + C::kColO, pcol + 64 * (kk >> 2) + 8 * (kk & 3), vd + (uint64_t)(kk * (2048 >> 4)), idesc_pv,
+                   (j == 0 && kk == 0) ? 0u : 1u);
+          tc_commit(&bar_v_empty[vs]);
+          tc_commit(&bar_s_free[b]);  // PV on buffer b done: P consumed, O holds tile g
+          if (++vs == VS) {
+            vs = 0;
+            vph ^= 1u;
+          }
+          ++g;
+          ++j;
+        });
+      }
+      tc_commit(&bar_drain2);
+      drain_wait(&bar_drain2, 0);
     }
     __syncwarp();
   } else {
