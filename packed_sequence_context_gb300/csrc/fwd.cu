@@ -402,18 +402,35 @@ __global__ void __launch_bounds__(384, 1)
 #pragma unroll
         for (int kk = 0; kk < 2; ++kk)
           if (k0 + kk < nch) tmem_ld_wait(sr[kk]);
-        float mloc = -INFINITY;
-        const bool full = cnt >= kTile;
+        // keys past the row's last visible one count as -inf; whole warps of
+        // fully visible rows (every tile off the causal diagonal) skip the selects
+        const int nvalid = (k0 + 1 < nch) ? 64 : (k0 < nch ? 32 : 0);  // this thread's loaded columns
+        if (__any_sync(0xffffffffu, cnt - 32 * k0 < nvalid)) {
 #pragma unroll
-        for (int kk = 0; kk < 2; ++kk)
-          if (k0 + kk < nch) {
+          for (int kk = 0; kk < 2; ++kk)
 #pragma unroll
-            for (int n = 0; n < 32; ++n) {
-              const float x = (full || 32 * (k0 + kk) + n < cnt) ? __uint_as_float(sr[kk][n]) : -INFINITY;
-              sr[kk][n] = __float_as_uint(x);
-              mloc = fmaxf(mloc, x);
-            }
+            for (int n = 0; n < 32; ++n)
+              if (32 * (k0 + kk) + n >= cnt) sr[kk][n] = __float_as_uint(-INFINITY);
+        }
+        if (k0 + 1 >= nch) {  // chunks this thread did not load (narrow tile)
+#pragma unroll
+          for (int n = 0; n < 32; ++n) sr[1][n] = __float_as_uint(-INFINITY);
+          if (k0 >= nch) {
+#pragma unroll
+            for (int n = 0; n < 32; ++n) sr[0][n] = __float_as_uint(-INFINITY);
           }
+        }
+        // tree maximum: eight independent partial maxima of 8 values each
+        float pm[8];
+#pragma unroll
+        for (int i = 0; i < 8; ++i) {
+          const uint32_t* v = &sr[i >> 2][8 * (i & 3)];
+          float a = fmax3(__uint_as_float(v[0]), __uint_as_float(v[1]), __uint_as_float(v[2]));
+          a = fmax3(a, __uint_as_float(v[3]), __uint_as_float(v[4]));
+          a = fmax3(a, __uint_as_float(v[5]), __uint_as_float(v[6]));
+          pm[i] = fmaxf(a, __uint_as_float(v[7]));
+        }
+        const float mloc = fmax3(fmax3(pm[0], pm[1], pm[2]), fmax3(pm[3], pm[4], pm[5]), fmaxf(pm[6], pm[7]));
         s_mx[g & 1u][half][row] = mloc;
         named_bar_sync(pair_bar, 64);
         const float mt = fmaxf(mloc, s_mx[g & 1u][half ^ 1][row]) * sl2;
@@ -448,16 +465,20 @@ __global__ void __launch_bounds__(384, 1)
           }
         }
         const float mm = (m == -INFINITY) ? 0.f : m;
-        float rs = 0.f;
+        // P = 2^(S scale_log2 - m): the scale-and-shift as packed pair FMAs,
+        // the row sum in four packed accumulators (short dependency chains)
+        float sa[8] = {0.f, 0.f, 0.f, 0.f, 0.f, 0.f, 0.f, 0.f};
 #pragma unroll
         for (int kk = 0; kk < 2; ++kk) {
           if (k0 + kk < nch) {
             uint32_t pk[16];
 #pragma unroll
             for (int n = 0; n < 16; ++n) {
-              const float p0 = ex2(fmaf(__uint_as_float(sr[kk][2 * n]), sl2, -mm));
-              const float p1 = ex2(fmaf(__uint_as_float(sr[kk][2 * n + 1]), sl2, -mm));
-              rs += p0 + p1;
+              float x0, x1;
+              ffma2(x0, x1, __uint_as_float(sr[kk][2 * n]), __uint_as_float(sr[kk][2 * n + 1]), sl2, sl2, -mm, -mm);
+              const float p0 = ex2(x0), p1 = ex2(x1);
+              const int a = 2 * (n & 3);
+              fadd2(sa[a], sa[a + 1], sa[a], sa[a + 1], p0, p1);
               pk[n] = pack_bf16x2(p0, p1);
             }
             // packed P stays inside this half's own S columns (the partner may
@@ -465,6 +486,10 @@ __global__ void __launch_bounds__(384, 1)
             tmem_st16(scol + 64 * half + 16 * kk, pk);
           }
         }
+        fadd2(sa[0], sa[1], sa[0], sa[1], sa[2], sa[3]);
+        fadd2(sa[4], sa[5], sa[4], sa[5], sa[6], sa[7]);
+        fadd2(sa[0], sa[1], sa[0], sa[1], sa[4], sa[5]);
+        const float rs = sa[0] + sa[1];
         l += rs;
         tmem_st_wait();
         tc_fence_before();
