@@ -132,9 +132,9 @@ __global__ void __launch_bounds__(320, 1)
       mbar_init(&bar_qdo_empty[s], 1);
     }
     mbar_init(bar_st_full, 1);
-    mbar_init(bar_p_ready, 256);
+    mbar_init(bar_p_ready, 8);  // one arrival per compute warp
     mbar_init(bar_dq_full, 1);
-    mbar_init(bar_x_free, 256);
+    mbar_init(bar_x_free, 8);
     mbar_init(bar_drain, 1);
     mbar_init(bar_dv_done, 1);
     *s_abort = 0;
@@ -389,7 +389,8 @@ __global__ void __launch_bounds__(320, 1)
         tmem_st_wait();
         fence_proxy_async_smem();
         tc_fence_before();
-        mbar_arrive(bar_p_ready);
+        __syncwarp();  // every lane's P^T and dS are written: one arrival speaks for the warp
+        if (lane == 0) mbar_arrive(bar_p_ready);
         // drain dQ (TMEM lane = query row) into the fp32 accumulator: each warp
         // stages its own 32 rows x 32 columns in the 4 KB of the dS buffer that
         // hold its own dS rows (idle now: this step's dK/dQ products have
@@ -430,7 +431,8 @@ __global__ void __launch_bounds__(320, 1)
           }
         }
         tc_fence_before();
-        mbar_arrive(bar_x_free);
+        __syncwarp();
+        if (lane == 0) mbar_arrive(bar_x_free);
         ++su;
         ++nsteps;
       });

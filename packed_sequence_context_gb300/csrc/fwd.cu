@@ -140,7 +140,7 @@ __global__ void __launch_bounds__(384, 1)
     }
     for (int s = 0; s < C::kSBufs; ++s) {
       mbar_init(&bar_s_full[s], 1);
-      mbar_init(&bar_p_ready[s], 256);
+      mbar_init(&bar_p_ready[s], 8);  // one arrival per softmax warp
       mbar_init(&bar_s_free[s], 1);
     }
     mbar_init(&bar_q_full, 32);
@@ -493,7 +493,8 @@ __global__ void __launch_bounds__(384, 1)
         l += rs;
         tmem_st_wait();
         tc_fence_before();
-        mbar_arrive(&bar_p_ready[sb]);
+        __syncwarp();  // every lane's P is in TMEM: one arrival speaks for the warp
+        if (lane == 0) mbar_arrive(&bar_p_ready[sb]);
         ++g;
         ++jl;
       });
