@@ -358,25 +358,33 @@ __global__ void __launch_bounds__(320, 1)
           tmem_ld32(tmem + lane_base + C::kColY + 32 * kk, dr);
           tmem_ld_wait(sr);
           tmem_ld_wait(dr);
+          // query columns outside [n_lo, n_hi) (causal, or past the valid rows)
+          // get S = -inf, hence P = 0 and dS = 0; warps whose rows see the
+          // whole chunk (every step off the causal diagonal) skip the selects
+          if (__any_sync(0xffffffffu, n_lo > 32 * kk || n_hi < 32 * kk + 32)) {
+#pragma unroll
+            for (int e = 0; e < 32; ++e) {
+              const int n = 32 * kk + e;
+              if (n < n_lo || n >= n_hi) sr[e] = __float_as_uint(-INFINITY);
+            }
+          }
           uint32_t pk[16], dk[16];
 #pragma unroll
-          for (int q4 = 0; q4 < 8; ++q4) {  // four query columns at a time
+          for (int q4 = 0; q4 < 8; ++q4) {  // four query columns at a time, as packed pairs
             const float4 l4 = lds128f(lse_s + 4 * (32 * kk + 4 * q4));
             const float4 d4 = lds128f(dl_s + 4 * (32 * kk + 4 * q4));
-            const float lv[4] = {l4.x, l4.y, l4.z, l4.w}, dv4[4] = {d4.x, d4.y, d4.z, d4.w};
-            float pp[4], dd[4];
-#pragma unroll
-            for (int e = 0; e < 4; ++e) {
-              const int n = 32 * kk + 4 * q4 + e;
-              const bool a = n >= n_lo && n < n_hi;
-              const float pv = a ? ex2(fmaf(__uint_as_float(sr[4 * q4 + e]), sl2, -lv[e])) : 0.f;
-              pp[e] = pv;
-              dd[e] = a ? pv * (__uint_as_float(dr[4 * q4 + e]) - dv4[e]) : 0.f;
-            }
-            pk[2 * q4] = pack_bf16x2(pp[0], pp[1]);
-            pk[2 * q4 + 1] = pack_bf16x2(pp[2], pp[3]);
-            dk[2 * q4] = pack_bf16x2(dd[0], dd[1]);
-            dk[2 * q4 + 1] = pack_bf16x2(dd[2], dd[3]);
+            float x0, x1, x2, x3, t0, t1, t2, t3, g0, g1, g2, g3;
+            ffma2(x0, x1, __uint_as_float(sr[4 * q4]), __uint_as_float(sr[4 * q4 + 1]), sl2, sl2, -l4.x, -l4.y);
+            ffma2(x2, x3, __uint_as_float(sr[4 * q4 + 2]), __uint_as_float(sr[4 * q4 + 3]), sl2, sl2, -l4.z, -l4.w);
+            const float p0 = ex2(x0), p1 = ex2(x1), p2 = ex2(x2), p3 = ex2(x3);
+            fadd2(t0, t1, __uint_as_float(dr[4 * q4]), __uint_as_float(dr[4 * q4 + 1]), -d4.x, -d4.y);
+            fadd2(t2, t3, __uint_as_float(dr[4 * q4 + 2]), __uint_as_float(dr[4 * q4 + 3]), -d4.z, -d4.w);
+            fmul2(g0, g1, p0, p1, t0, t1);
+            fmul2(g2, g3, p2, p3, t2, t3);
+            pk[2 * q4] = pack_bf16x2(p0, p1);
+            pk[2 * q4 + 1] = pack_bf16x2(p2, p3);
+            dk[2 * q4] = pack_bf16x2(g0, g1);
+            dk[2 * q4 + 1] = pack_bf16x2(g2, g3);
           }
           // packed P^T stays inside this warpgroup's own S^T columns (the other
           // warpgroup may still be reading its half): chunk kk -> 64 (kk/2) + 16 (kk%2)
