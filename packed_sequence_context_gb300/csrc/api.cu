@@ -83,18 +83,6 @@ static bool make_thd_map(CUtensorMap* m, const void* base, int64_t rows, int H, 
 
 // 3-D map over the fp32 dQ accumulator [rows, H, D]; box = 32 rows x 1 head
 // x 32 columns (128 bytes, the 128B-swizzle width), used for reduce-add.
-static bool make_f32_map(CUtensorMap* m, const float* base, int64_t rows, int H, int D) {
-  auto enc = encode_fn();
-  if (!enc) return false;
-  cuuint64_t dims[3] = {(cuuint64_t)D, (cuuint64_t)H, (cuuint64_t)(rows > 0 ? rows : 1)};
-  cuuint64_t strides[2] = {(cuuint64_t)D * 4, (cuuint64_t)H * D * 4};
-  cuuint32_t box[3] = {32, 1, 32};
-  cuuint32_t es[3] = {1, 1, 1};
-  return enc(m, CU_TENSOR_MAP_DATA_TYPE_FLOAT32, 3, const_cast<float*>(base), dims, strides, box, es,
-             CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
-             CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
-}
-
 static bool aligned(const void* p, uintptr_t a) { return (reinterpret_cast<uintptr_t>(p) & (a - 1)) == 0; }
 
 static int check_sizes(int B, int64_t T_q, int64_t T_kv, int Hq, int Hkv, int D, int cp, int pad_mode) {
@@ -293,20 +281,27 @@ int thd_attn_bwd(const void* q, const void* k, const void* v, const void* o, con
   rc = check_ws(workspace, workspace_bytes, L.total);
   if (rc) return rc;
   char* w = static_cast<char*>(workspace);
+  // two schedules: key tiles for the dK/dV pass, query tiles for the dQ pass
   PlanParams pp = plan_params(cu_seqlens_q, cu_seqlens_kv, cu_seqlens_q_padded, cu_seqlens_kv_padded, B, cp_size,
                               causal, pad_between_seqs, T_q, T_kv, 2, w, L, dev_status);
   rc = cuda_status(launch_plan(pp, st));
   if (rc) return rc;
+  PlanParams pq = pp;
+  pq.mode = 1;
+  pq.tile_off = reinterpret_cast<int32_t*>(w + L.tile_off_q);
+  pq.counters = reinterpret_cast<int32_t*>(w + L.counters_q);
+  pq.items = reinterpret_cast<int4*>(w + L.items_q);
+  pq.item_cap = L.item_cap_q;
+  rc = cuda_status(launch_plan(pq, st));
+  if (rc) return rc;
   float* delta = reinterpret_cast<float*>(w + L.delta);
   float* lse2 = reinterpret_cast<float*>(w + L.lse2);
-  float* dq_acc = reinterpret_cast<float*>(w + L.dq_acc);
   rc = cuda_status(launch_bwd_prep(static_cast<const uint16_t*>(o), static_cast<const uint16_t*>(dout), lse, delta,
-                                   lse2, dq_acc, pp.eff, B, T_q, Hq, D, dev_status, st));
+                                   lse2, pp.eff, B, T_q, Hq, D, dev_status, st));
   if (rc) return rc;
-  CUtensorMap tq, tdo, tk, tv, tdq;
+  CUtensorMap tq, tdo, tk, tv;
   if (!make_thd_map(&tq, q, T_q, Hq, D) || !make_thd_map(&tdo, dout, T_q, Hq, D) ||
-      !make_thd_map(&tk, k, T_kv, Hkv, D) || !make_thd_map(&tv, v, T_kv, Hkv, D) ||
-      !make_f32_map(&tdq, dq_acc, T_q, Hq, D))
+      !make_thd_map(&tk, k, T_kv, Hkv, D) || !make_thd_map(&tv, v, T_kv, Hkv, D))
     return THD_ERR_CUDA;
   BwdParams bp;
   std::memset(&bp, 0, sizeof(bp));
@@ -314,7 +309,6 @@ int thd_attn_bwd(const void* q, const void* k, const void* v, const void* o, con
   bp.dout = static_cast<const uint16_t*>(dout);
   bp.lse2 = lse2;
   bp.delta = delta;
-  bp.dq_acc = dq_acc;
   bp.dk = static_cast<uint16_t*>(dk);
   bp.dv = static_cast<uint16_t*>(dv);
   bp.eff = pp.eff;
@@ -332,10 +326,33 @@ int thd_attn_bwd(const void* q, const void* k, const void* v, const void* o, con
   bp.scale_log2 = softmax_scale * 1.4426950408889634f;
   const int64_t bound = (int64_t)L.item_cap * Hkv;
   const int grid = (int)(bound < num_sms() ? (bound > 0 ? bound : 1) : num_sms());
-  rc = cuda_status(launch_bwd(bp, tq, tdo, tk, tv, tdq, D, grid, st));
+  rc = cuda_status(launch_bwd(bp, tq, tdo, tk, tv, D, grid, st));
   if (rc) return rc;
-  return cuda_status(launch_bwd_dq(dq_acc, static_cast<uint16_t*>(dq), pp.eff, B, T_q, dq_rows, Hq, D,
-                                   softmax_scale, dev_status, st));
+  DqParams dp;
+  std::memset(&dp, 0, sizeof(dp));
+  dp.q = static_cast<const uint16_t*>(q);
+  dp.dout = static_cast<const uint16_t*>(dout);
+  dp.lse2 = lse2;
+  dp.delta = delta;
+  dp.dq = static_cast<uint16_t*>(dq);
+  dp.eff = pq.eff;
+  dp.items = pq.items;
+  dp.counters = pq.counters;
+  dp.dev_status = dev_status;
+  dp.B = B;
+  dp.Hq = Hq;
+  dp.Hkv = Hkv;
+  dp.cp = cp_size;
+  dp.causal = causal;
+  dp.T_q = T_q;
+  dp.dq_rows = dq_rows;
+  dp.scale = softmax_scale;
+  dp.scale_log2 = softmax_scale * 1.4426950408889634f;
+  dp.step_lo = 0;
+  dp.step_hi = cp_size;
+  const int64_t bound_q = (int64_t)L.item_cap_q * Hq;
+  const int grid_q = (int)(bound_q < num_sms() ? (bound_q > 0 ? bound_q : 1) : num_sms());
+  return cuda_status(launch_dq(dp, tk, tv, D, grid_q, st));
 }
 
 int thd_lse_merge(float* o_acc, float* lse_acc, const float* o_part, const float* lse_part, int64_t T, int H, int D,

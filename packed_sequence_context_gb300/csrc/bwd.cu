@@ -1,5 +1,5 @@
-// Backward attention over packed THD tensors, key/value-stationary, walked in
-// P2P ring order and executed for every emulated rank on one GB300.
+// dK and dV of attention over packed THD tensors, key/value-stationary,
+// walked in P2P ring order and executed for every emulated rank on one GB300.
 //
 // [P2] TransformerEngine issue #3487 ("Steps/Code to reproduce bug": BF16
 // attention forward/backward on this layout with four-rank P2P context
@@ -9,8 +9,7 @@
 // step i, and dK/dV travel back around the ring to their owner.  Here the
 // owner keeps its key tile in shared memory and visits, in ring order, the
 // query tiles of every rank that sees it; dK/dV accumulate in TMEM (no
-// travel), dQ goes to an fp32 accumulator with TMA reduce-adds (one bulk
-// operation per warp and 32-column block, element-wise atomic).
+// travel).  dQ is the query-stationary pass of dq.cu.
 //
 // One work item = (sequence b, key chunk c, key tile jk within the chunk, kv
 // head hk).  For each query tile (chunk qc, tile jq) that sees it and each
@@ -18,12 +17,9 @@
 //   S^T  = K Q^T            (TMEM X)     dP^T = V dO^T         (TMEM Y)
 //   P^T  = exp(S^T scale - lse)          dS^T = P^T (dP^T - Delta)
 //   dV  += P^T dO   (A = P^T from TMEM)  dK  += dS^T Q   (A = dS^T, smem)
-//   dQ   = dS K     (A = dS, the same smem read MN-major; into TMEM X once
-//                    dV has consumed P^T, so the next dP^T need not wait for the dQ drain)
 // CTA (320 threads): warps 0-7 compute in two warpgroups -- a thread owns one
-// key row (its TMEM lane) and half of the columns: query columns [0,64) or
-// [64,128) for P/dS, and half of the head dimension when draining dQ (one
-// query row per thread) and writing dK/dV; warp 8 TMA producer (+ lse/Delta
+// key row (its TMEM lane) and half of the query columns for P/dS, and half of
+// the head dimension when writing dK/dV; warp 8 TMA producer (+ lse/Delta
 // staging); warp 9 TMEM allocator and single-thread MMA issuer.
 #include "common.cuh"
 #include "ptx.cuh"
@@ -93,8 +89,7 @@ __device__ inline void drain_wait_b(uint64_t* bar, uint32_t parity) {
 template <int D>
 __global__ void __launch_bounds__(320, 1)
     bwd_kernel(const BwdParams p, const __grid_constant__ CUtensorMap tmQ, const __grid_constant__ CUtensorMap tmDO,
-               const __grid_constant__ CUtensorMap tmK, const __grid_constant__ CUtensorMap tmV,
-               const __grid_constant__ CUtensorMap tmDQ) {
+               const __grid_constant__ CUtensorMap tmK, const __grid_constant__ CUtensorMap tmV) {
   using C = BwdCfg<D>;
   constexpr int S = C::kStages;
   extern __shared__ __align__(1024) uint8_t smem[];
@@ -109,8 +104,7 @@ __global__ void __launch_bounds__(320, 1)
   uint64_t* bar_qdo_empty = bars + 2 + S;  // [S]
   uint64_t* bar_st_full = bars + 2 + 2 * S;
   uint64_t* bar_p_ready = bars + 3 + 2 * S;
-  uint64_t* bar_dq_full = bars + 4 + 2 * S;
-  uint64_t* bar_x_free = bars + 5 + 2 * S;
+  uint64_t* bar_dk_done = bars + 4 + 2 * S;
   uint64_t* bar_drain = bars + 6 + 2 * S;
   uint64_t* bar_dv_done = bars + 7 + 2 * S;
   uint32_t* s_tmem = reinterpret_cast<uint32_t*>(bars + 8 + 2 * S);
@@ -133,8 +127,7 @@ __global__ void __launch_bounds__(320, 1)
     }
     mbar_init(bar_st_full, 1);
     mbar_init(bar_p_ready, 8);  // one arrival per compute warp
-    mbar_init(bar_dq_full, 1);
-    mbar_init(bar_x_free, 8);
+    mbar_init(bar_dk_done, 1);
     mbar_init(bar_drain, 1);
     mbar_init(bar_dv_done, 1);
     *s_abort = 0;
@@ -149,7 +142,6 @@ __global__ void __launch_bounds__(320, 1)
     tma_prefetch_desc(&tmDO);
     tma_prefetch_desc(&tmK);
     tma_prefetch_desc(&tmV);
-    tma_prefetch_desc(&tmDQ);
   }
   tc_fence_before();
   __syncthreads();
@@ -223,9 +215,15 @@ __global__ void __launch_bounds__(320, 1)
     __syncwarp();
   } else if (warp == 9) {
     // ------------------------------------------------------------ MMA issuer
+    // Per step s: dP^T(s) -> Y, S^T(s) -> X (once dV(s-1) has read P^T(s-1)
+    // from X), then -- once the compute warps have written P^T(s) and dS(s)
+    // -- dV(s) and dK(s).  The commit behind S^T(s+1) covers dK(s), so the
+    // compute warps of step s+1 see S^T(s+1) only after dK(s) has read the
+    // dS buffer they are about to overwrite.  (Letting step s+1's compute
+    // start while dK(s) still ran, with an explicit dK-done wait before the
+    // dS writes, gave wrong dK and dV on GB300: the overlap is avoided.)
     if (lane == 0) {
-      constexpr uint32_t idesc_kv = idesc_bf16(128, D, false, true);    // dV, dK (B MN-major)
-      constexpr uint32_t idesc_q = idesc_bf16(128, D, true, true);      // dQ (A and B MN-major)
+      constexpr uint32_t idesc_kv = idesc_bf16(128, D, false, true);  // dV, dK (B MN-major)
       const uint32_t kb = smem_u32(sK), vb = smem_u32(sV), dsb = smem_u32(sDS);
       int stage = 0;
       uint32_t ph = 0, su = 0, kv_iter = 0;
@@ -236,7 +234,6 @@ __global__ void __launch_bounds__(320, 1)
         if (!mbar_wait(bar_kv_full, kv_iter & 1u, s_abort)) break;
         ++kv_iter;
         tc_fence_after();
-        const int kv_steps = ceil_div(it.kv_last - it.kv_first + 1, 16);  // K of the dQ product
         bool first = true;
         for_each_q_step(it, p, [&](int qc, int jq, int) {
           if (!ok) return;
@@ -257,8 +254,8 @@ __global__ void __launch_bounds__(320, 1)
             mma_ss(tmem + C::kColY, sdesc_sw128(vb + off, 16, 1024), sdesc_sw128(dob + off, 16, 1024), idesc_t,
                    ks > 0);
           }
-          // S^T = K Q^T -> X, once the previous dQ has been drained from X
-          if (su > 0 && !mbar_wait(bar_x_free, (su - 1) & 1u, s_abort)) {
+          // S^T = K Q^T -> X, once dV of the previous step has read P^T there
+          if (su > 0 && !mbar_wait(bar_dv_done, (su - 1) & 1u, s_abort)) {
             ok = false;
             return;
           }
@@ -285,17 +282,7 @@ __global__ void __launch_bounds__(320, 1)
           for (int ks = 0; ks < n16; ++ks)
             mma_ss(tmem + C::kColDK, sdesc_sw128(dsb + (ks >> 2) * 16384 + (ks & 3) * 32, 16, 1024),
                    sdesc_sw128(qb + ks * 2048, 16384, 1024), idesc_kv, (first && ks == 0) ? 0u : 1u);
-          // dQ = dS K -> X.  MMAs into different accumulators are not ordered,
-          // so dQ may overwrite X only once dV has finished reading P^T there.
-          if (!mbar_wait(bar_dv_done, su & 1u, s_abort)) {
-            ok = false;
-            return;
-          }
-          tc_fence_after();
-          for (int ks = 0; ks < kv_steps; ++ks)
-            mma_ss(tmem + C::kColX, sdesc_sw128(dsb + ks * 2048, 16384, 1024),
-                   sdesc_sw128(kb + ks * 2048, 16384, 1024), idesc_q, ks > 0);
-          tc_commit(bar_dq_full);
+          tc_commit(bar_dk_done);
           tc_commit(&bar_qdo_empty[stage]);
           first = false;
           ++su;
@@ -304,7 +291,8 @@ __global__ void __launch_bounds__(320, 1)
             ph ^= 1u;
           }
         });
-        if (ok) tc_commit(bar_kv_empty);
+        if (!ok) break;
+        tc_commit(bar_kv_empty);
       }
       tc_commit(bar_drain);
       drain_wait_b(bar_drain, 0);
@@ -347,10 +335,6 @@ __global__ void __launch_bounds__(320, 1)
         // lse arrives pre-scaled to log2 units by the preprocess kernel
         const uint32_t lse_s = smem_u32(sLse + (su % S) * 256), dl_s = lse_s + 512;
         const int nch = ceil_div(nqv, 32);
-        // this warp's last dQ reduction must have read its staging bytes (this
-        // warp's own dS rows) before they are overwritten below
-        if (lane == 0) bulk_wait_read_all();
-        __syncwarp();
 #pragma unroll 1
         for (int kk = 2 * half; kk < imin(nch, 2 * half + 2); ++kk) {
           uint32_t sr[32], dr[32];
@@ -399,53 +383,16 @@ __global__ void __launch_bounds__(320, 1)
         tc_fence_before();
         __syncwarp();  // every lane's P^T and dS are written: one arrival speaks for the warp
         if (lane == 0) mbar_arrive(bar_p_ready);
-        // drain dQ (TMEM lane = query row) into the fp32 accumulator: each warp
-        // stages its own 32 rows x 32 columns in the 4 KB of the dS buffer that
-        // hold its own dS rows (idle now: this step's dK/dQ products have
-        // completed), and its lane 0 adds the block to global memory with a TMA
-        // reduce-add.  Warps whose rows received nothing skip; dead rows in a
-        // live warp are staged as zeros.
-        if (!mbar_wait(bar_dq_full, su & 1u, s_abort)) {
-          ok = false;
-          return;
-        }
-        tc_fence_after();
-        const bool q_live = row < nqv && (!p.causal || q0 + row >= it.kv_first);
-        if (__any_sync(0xffffffffu, q_live)) {
-          const uint32_t stg = ds_s + 16384 * half + 4096 * (warp & 3);
-          uint32_t r[32];
-          tmem_ld32(tmem + lane_base + C::kColX + half * (D / 2), r);
-#pragma unroll 1
-          for (int kk = 0; kk < D / 64; ++kk) {
-            const int dcol = half * (D / 2) + 32 * kk;
-            tmem_ld_wait(r);
-            // the previous block's reduction must have read the staging bytes
-            if (lane == 0 && kk > 0) bulk_wait_read_all();
-            __syncwarp();
-#pragma unroll
-            for (int c = 0; c < 8; ++c) {
-              const uint32_t a = q_live ? r[4 * c] : 0u, b = q_live ? r[4 * c + 1] : 0u;
-              const uint32_t e = q_live ? r[4 * c + 2] : 0u, f = q_live ? r[4 * c + 3] : 0u;
-              sts128(stg + lane * 128 + ((c ^ (lane & 7)) << 4), a, b, e, f);
-            }
-            // the next block's TMEM load overlaps this block's reduction
-            if (kk + 1 < D / 64) tmem_ld32(tmem + lane_base + C::kColX + dcol + 32, r);
-            fence_proxy_async_smem();
-            __syncwarp();
-            if (lane == 0) {
-              tma_reduce_add_3d(&tmDQ, stg, dcol, h, it.g.q_off + q0 + 32 * (warp & 3));
-              bulk_commit_group();
-            }
-          }
-        }
-        tc_fence_before();
-        __syncwarp();
-        if (lane == 0) mbar_arrive(bar_x_free);
         ++su;
         ++nsteps;
       });
       if (!ok) break;
-      // ---- epilogue: dK (scaled) and dV of this key tile, zeros on pad rows
+      // ---- epilogue: dK (scaled) and dV of this key tile, zeros on pad rows,
+      // once the item's last dK (and with it every product before) completed
+      if (nsteps > 0) {
+        if (!mbar_wait(bar_dk_done, (su - 1) & 1u, s_abort)) break;
+        tc_fence_after();
+      }
 #pragma unroll 1
       for (int kk = half * (D / 64); kk < (half + 1) * (D / 64); ++kk) {
         uint32_t a[32], bq[32];
@@ -485,7 +432,6 @@ __global__ void __launch_bounds__(320, 1)
       }
       tc_fence_before();
     }
-    if (lane == 0) bulk_wait_all();  // this warp's dQ reductions complete before the kernel ends
     // ---- dK/dV rows past the last sequence: zero
     if (ok) {
       const int Tend = p.eff[3 * (p.B + 1) + p.B];
@@ -509,13 +455,12 @@ __global__ void __launch_bounds__(320, 1)
 
 template <int D>
 static cudaError_t launch_bwd_t(const BwdParams& p, const CUtensorMap& tq, const CUtensorMap& tdo,
-                                const CUtensorMap& tk, const CUtensorMap& tv, const CUtensorMap& tdq, int grid,
-                                cudaStream_t st) {
+                                const CUtensorMap& tk, const CUtensorMap& tv, int grid, cudaStream_t st) {
   using C = BwdCfg<D>;
   cudaError_t e = cudaFuncSetAttribute(bwd_kernel<D>, cudaFuncAttributeMaxDynamicSharedMemorySize, C::kSmem);
   if (e != cudaSuccess) return e;
   prof_before(THD_KERNEL_BWD, st);
-  bwd_kernel<D><<<grid, 320, C::kSmem, st>>>(p, tq, tdo, tk, tv, tdq);
+  bwd_kernel<D><<<grid, 320, C::kSmem, st>>>(p, tq, tdo, tk, tv);
   count_launch();
   e = cudaGetLastError();
   prof_after(THD_KERNEL_BWD, st);
@@ -523,9 +468,8 @@ static cudaError_t launch_bwd_t(const BwdParams& p, const CUtensorMap& tq, const
 }
 
 cudaError_t launch_bwd(const BwdParams& p, const CUtensorMap& tq, const CUtensorMap& tdo, const CUtensorMap& tk,
-                       const CUtensorMap& tv, const CUtensorMap& tdq, int D, int grid, cudaStream_t st) {
-  return D == 128 ? launch_bwd_t<128>(p, tq, tdo, tk, tv, tdq, grid, st)
-                  : launch_bwd_t<64>(p, tq, tdo, tk, tv, tdq, grid, st);
+                       const CUtensorMap& tv, int D, int grid, cudaStream_t st) {
+  return D == 128 ? launch_bwd_t<128>(p, tq, tdo, tk, tv, grid, st) : launch_bwd_t<64>(p, tq, tdo, tk, tv, grid, st);
 }
 
 }  // namespace thd

@@ -28,11 +28,16 @@ struct WsLayout {
   size_t tile_off = 0;  // int32 [B+1]
   size_t counters = 0;  // int32 [64]: [0] number of schedule entries
   size_t items = 0;     // int4 [item_cap]
-  size_t delta = 0;     // fp32 [Hq][T_q]          (backward)
-  size_t lse2 = 0;      // fp32 [Hq][T_q], lse * log2(e)  (backward)
-  size_t dq_acc = 0;    // fp32 [T_q][Hq][D]       (backward)
+  // backward only: the query-tile schedule of the dQ pass (its own planner
+  // outputs), Delta and lse in log2 units
+  size_t tile_off_q = 0;  // int32 [B+1]
+  size_t counters_q = 0;  // int32 [64]
+  size_t items_q = 0;     // int4 [item_cap_q]
+  size_t delta = 0;       // fp32 [Hq][T_q]
+  size_t lse2 = 0;        // fp32 [Hq][T_q], lse * log2(e)
   size_t total = 0;
   int item_cap = 0;
+  int item_cap_q = 0;
 };
 
 inline size_t align_up(size_t x, size_t a) { return (x + a - 1) / a * a; }
@@ -48,16 +53,21 @@ inline WsLayout ws_layout(int B, int64_t T_q, int64_t T_kv, int Hq, int D, int c
   w.eff = take(sizeof(int32_t) * 4 * (size_t)(B + 1));
   w.tile_off = take(sizeof(int32_t) * (size_t)(B + 1));
   w.counters = take(sizeof(int32_t) * 64);
-  // forward: rank-local query tiles; backward: chunk-aligned key tiles.  Both
-  // are bounded by rows/128 + (one partial tile per chunk).
-  int64_t cap = bwd ? (T_kv / kTile + (int64_t)2 * cp * B + 1) : (T_q / kTile + (int64_t)cp * B + 1);
-  w.item_cap = (int)cap;
-  w.items = take(sizeof(int32_t) * 4 * (size_t)cap);
+  // query schedule: rank-local query tiles; key schedule: chunk-aligned key
+  // tiles.  Both are bounded by rows/128 + (one partial tile per chunk).
+  const int64_t cap_q = T_q / kTile + (int64_t)cp * B + 1;
+  const int64_t cap_kv = T_kv / kTile + (int64_t)2 * cp * B + 1;
+  w.item_cap = (int)(bwd ? cap_kv : cap_q);
+  w.items = take(sizeof(int32_t) * 4 * (size_t)w.item_cap);
   if (bwd) {
+    w.item_cap_q = (int)cap_q;
+    w.tile_off_q = take(sizeof(int32_t) * (size_t)(B + 1));
+    w.counters_q = take(sizeof(int32_t) * 64);
+    w.items_q = take(sizeof(int32_t) * 4 * (size_t)cap_q);
     w.delta = take(sizeof(float) * (size_t)Hq * (size_t)T_q);
     w.lse2 = take(sizeof(float) * (size_t)Hq * (size_t)T_q);
-    w.dq_acc = take(sizeof(float) * (size_t)T_q * (size_t)Hq * (size_t)D);
   }
+  (void)D;
   w.total = off;
   return w;
 }
@@ -137,6 +147,53 @@ __host__ __device__ inline int fwd_item_tiles(const SeqGeom& g, int r, int t, in
     for (int e = 0; e < 2; ++e) n += fwd_chunk_tiles(g, ring_chunk(s, e, cp), qmax, causal);
   }
   return n;
+}
+
+// ---- one query tile's walk (forward and the dQ pass).  P is any params
+// struct with items, eff, B, Hq, Hkv, cp, causal, step_lo, step_hi.
+struct QItem {
+  SeqGeom g;
+  int b, r, t, h, kvh, qmax;
+};
+
+// Work item w = (schedule entry w / Hq, query head w % Hq).
+template <class P>
+__device__ inline QItem q_item(const P& p, int w) {
+  QItem it;
+  const int4 e = p.items[w / p.Hq];
+  it.h = w % p.Hq;
+  it.kvh = it.h / (p.Hq / p.Hkv);
+  it.b = e.x;
+  it.r = e.y;
+  it.t = e.z;
+  it.g = seq_geom(p.eff, p.B, it.b, p.cp);
+  it.qmax = fwd_tile_qmax(it.g, it.r, it.t, p.cp);
+  return it;
+}
+
+// Calls f(c, j) for every key tile the item visits, in ring order: step i
+// holds the KV of rank s = (r - i) mod cp, chunks s then 2cp-1-s.
+template <class P, typename F>
+__device__ inline void for_each_kv_tile(const QItem& it, const P& p, F&& f) {
+  for (int i = p.step_lo; i < p.step_hi; ++i) {
+    const int s = ring_src(it.r, i, p.cp);
+    for (int e = 0; e < 2; ++e) {
+      const int c = ring_chunk(s, e, p.cp);
+      const int n = fwd_chunk_tiles(it.g, c, it.qmax, p.causal != 0);
+      for (int j = 0; j < n; ++j) f(c, j);
+    }
+  }
+}
+
+// Columns (keys) of tile (c, j) any query of the item may see, rounded up to
+// the MMA granularity of 16: the N of the item's S product and the K of the
+// product that contracts over keys.
+template <class P>
+__device__ inline int q_tile_ncols(const QItem& it, const P& p, int c, int j) {
+  const int j0 = c * it.g.cbkv + j * kTile;
+  int n = imin(kTile, imin((c + 1) * it.g.cbkv - j0, it.g.Lkv - j0));
+  if (p.causal) n = imin(n, it.qmax - j0 + 1);
+  return 16 * ceil_div(imax(n, 1), 16);
 }
 
 // ---- backward: key tile (chunk c, tile jk) of sequence b, and the query
@@ -219,7 +276,6 @@ struct BwdParams {
   const uint16_t* dout;
   const float* lse2;  // lse * log2(e), [Hq][T_q]
   const float* delta;
-  float* dq_acc;
   uint16_t* dk;
   uint16_t* dv;
   const int32_t* eff;
@@ -231,22 +287,38 @@ struct BwdParams {
   float scale, scale_log2;
 };
 
+struct DqParams {
+  const uint16_t* q;
+  const uint16_t* dout;
+  const float* lse2;  // lse * log2(e), [Hq][T_q]
+  const float* delta;
+  uint16_t* dq;       // bf16 [dq_rows][Hq][D]
+  const int32_t* eff;
+  const int4* items;  // the query-tile schedule
+  const int32_t* counters;
+  int32_t* dev_status;
+  int B, Hq, Hkv, cp, causal;
+  int64_t T_q, dq_rows;
+  float scale, scale_log2;
+  int step_lo, step_hi;  // always the whole ring
+};
+
 // host launchers (each returns a cudaError_t)
 cudaError_t launch_plan(const PlanParams& p, cudaStream_t st);
 cudaError_t launch_fwd(const FwdParams& p, const CUtensorMap& tk, const CUtensorMap& tv, int D, bool step_mode,
                        int grid, cudaStream_t st);
 cudaError_t launch_bwd(const BwdParams& p, const CUtensorMap& tq, const CUtensorMap& tdo, const CUtensorMap& tk,
-                       const CUtensorMap& tv, const CUtensorMap& tdq, int D, int grid, cudaStream_t st);
+                       const CUtensorMap& tv, int D, int grid, cudaStream_t st);
+cudaError_t launch_dq(const DqParams& p, const CUtensorMap& tk, const CUtensorMap& tv, int D, int grid,
+                      cudaStream_t st);
 cudaError_t launch_lse_merge(float* o_acc, float* lse_acc, const float* o_part, const float* lse_part, int64_t T,
                              int H, int D, cudaStream_t st);
 cudaError_t launch_tail_zero(uint16_t* dq, uint16_t* dk, uint16_t* dv, int64_t dq_rows, int64_t dkv_rows, int Hq,
                              int Hkv, int D, const int32_t* pad_q_end, const int32_t* pad_kv_end,
                              const int32_t* dev_status, cudaStream_t st);
 cudaError_t launch_bwd_prep(const uint16_t* o, const uint16_t* dout, const float* lse, float* delta, float* lse2,
-                            float* dq_acc, const int32_t* eff, int B, int64_t T_q, int Hq, int D,
-                            const int32_t* dev_status, cudaStream_t st);
-cudaError_t launch_bwd_dq(const float* dq_acc, uint16_t* dq, const int32_t* eff, int B, int64_t T_q,
-                          int64_t dq_rows, int Hq, int D, float scale, const int32_t* dev_status, cudaStream_t st);
+                            const int32_t* eff, int B, int64_t T_q, int Hq, int D, const int32_t* dev_status,
+                            cudaStream_t st);
 
 int num_sms();
 void prof_before(int kernel_id, cudaStream_t st);

@@ -50,54 +50,7 @@ struct FwdCfg {
   static constexpr int kThreads = 384;
 };
 
-struct FwdItem {
-  SeqGeom g;
-  int b, r, t, h, kvh, qmax;
-};
-
-__device__ inline FwdItem fwd_item(const FwdParams& p, int w) {
-  FwdItem it;
-  const int4 e = p.items[w / p.Hq];
-  it.h = w % p.Hq;
-  it.kvh = it.h / (p.Hq / p.Hkv);
-  it.b = e.x;
-  it.r = e.y;
-  it.t = e.z;
-  it.g = seq_geom(p.eff, p.B, it.b, p.cp);
-  it.qmax = fwd_tile_qmax(it.g, it.r, it.t, p.cp);
-  return it;
-}
-
-// Calls f(c, j) for every key tile the item visits, in ring order.
-template <typename F>
-__device__ inline void for_each_kv_tile(const FwdItem& it, const FwdParams& p, F&& f) {
-  for (int i = p.step_lo; i < p.step_hi; ++i) {
-    const int s = ring_src(it.r, i, p.cp);
-    for (int e = 0; e < 2; ++e) {
-      const int c = ring_chunk(s, e, p.cp);
-      const int n = fwd_chunk_tiles(it.g, c, it.qmax, p.causal != 0);
-      for (int j = 0; j < n; ++j) f(c, j);
-    }
-  }
-}
-
-// Columns (keys) of tile (c, j) any query of the item may see, rounded up to
-// the MMA granularity of 16: the N of its QK^T product and the K of its PV.
-__device__ inline int fwd_tile_ncols(const FwdItem& it, const FwdParams& p, int c, int j) {
-  const int j0 = c * it.g.cbkv + j * kTile;
-  int n = imin(kTile, imin((c + 1) * it.g.cbkv - j0, it.g.Lkv - j0));
-  if (p.causal) n = imin(n, it.qmax - j0 + 1);
-  return 16 * ceil_div(imax(n, 1), 16);
-}
-
-// Bounded wait that ignores the abort flag (used to drain in-flight async
-// work before the CTA exits).
-__device__ inline void drain_wait(uint64_t* bar, uint32_t parity) {
-  const uint64_t t0 = globaltimer();
-  while (!mbar_try_wait(bar, parity)) {
-    if (globaltimer() - t0 > kWaitTimeoutNs) break;
-  }
-}
+using FwdItem = QItem;
 
 template <int D, bool kStep>
 __global__ void __launch_bounds__(384, 1)
@@ -169,7 +122,7 @@ __global__ void __launch_bounds__(384, 1)
     uint32_t kph = 0, n_fill = 0, q_iter = 0;
     bool ok = true;
     for (int w = blockIdx.x; w < n_items && ok; w += gridDim.x) {
-      const FwdItem it = fwd_item(p, w);
+      const FwdItem it = q_item(p, w);
       // ---- the query tile: rank-local rows [128 t, 128 t + 128) of rank r,
       // gathered into 128B-swizzled smem once the previous item's last QK^T
       // has completed; rows without a valid query are zero
@@ -229,7 +182,7 @@ __global__ void __launch_bounds__(384, 1)
       uint32_t vph = 0, n_fill = 0;
       bool ok = true;
       for (int w = blockIdx.x; w < n_items && ok; w += gridDim.x) {
-        const FwdItem it = fwd_item(p, w);
+        const FwdItem it = q_item(p, w);
         for_each_kv_tile(it, p, [&](int c, int j) {
           if (!ok) return;
           if (!mbar_wait(&bar_v_empty[vs], vph ^ 1u, &s_abort)) {
@@ -270,7 +223,7 @@ __global__ void __launch_bounds__(384, 1)
       uint32_t kph = 0, g = 0, q_iter = 0;
       bool ok = true;
       for (int w = blockIdx.x; w < n_items && ok; w += gridDim.x) {
-        const FwdItem it = fwd_item(p, w);
+        const FwdItem it = q_item(p, w);
         int n = 0;
         for_each_kv_tile(it, p, [&](int, int) { ++n; });
         if (!mbar_wait(&bar_q_full, q_iter & 1u, &s_abort)) break;
@@ -280,7 +233,7 @@ __global__ void __launch_bounds__(384, 1)
         int j = 0;
         for_each_kv_tile(it, p, [&](int c, int jt) {
           if (!ok) return;
-          const int ncols = fwd_tile_ncols(it, p, c, jt);
+          const int ncols = q_tile_ncols(it, p, c, jt);
           const uint32_t b = g % C::kSBufs;
           if (!mbar_wait(&bar_k_full[ks], kph, &s_abort) ||
               (g >= (uint32_t)C::kSBufs && !mbar_wait(&bar_s_free[b], (g / C::kSBufs - 1) & 1u, &s_abort))) {
@@ -319,11 +272,11 @@ __global__ void __launch_bounds__(384, 1)
       uint32_t vph = 0, g = 0;
       bool ok = true;
       for (int w = blockIdx.x; w < n_items && ok; w += gridDim.x) {
-        const FwdItem it = fwd_item(p, w);
+        const FwdItem it = q_item(p, w);
         int j = 0;
         for_each_kv_tile(it, p, [&](int c, int jt) {
           if (!ok) return;
-          const int ncols = fwd_tile_ncols(it, p, c, jt);
+          const int ncols = q_tile_ncols(it, p, c, jt);
           const uint32_t b = g % C::kSBufs;
           if (!mbar_wait(&bar_p_ready[b], (g / C::kSBufs) & 1u, &s_abort) ||
               !mbar_wait(&bar_v_full[vs], vph, &s_abort)) {
@@ -366,7 +319,7 @@ __global__ void __launch_bounds__(384, 1)
     uint32_t g = 0, n_item = 0;
     bool ok = true;
     for (int w = blockIdx.x; w < n_items && ok; w += gridDim.x) {
-      const FwdItem it = fwd_item(p, w);
+      const FwdItem it = q_item(p, w);
       const int prow = it.t * kTile + row;
       const bool in_rank = prow < 2 * it.g.cbq;
       const int pos = in_rank ? local_to_pos(prow, it.r, it.g.cbq, p.cp) : 0;
@@ -391,7 +344,7 @@ __global__ void __launch_bounds__(384, 1)
           if (p.causal) cnt = imin(cnt, pos - j0 + 1);
           cnt = imax(cnt, 0);
         }
-        const int ncols = fwd_tile_ncols(it, p, c, j);  // the N this tile's QK^T computed
+        const int ncols = q_tile_ncols(it, p, c, j);  // the N this tile's QK^T computed
         const int nch = ceil_div(ncols, 32);
         const int k0 = 2 * half;  // this thread's 32-column chunks: k0, k0 + 1
         uint32_t sr[2][32];

@@ -330,8 +330,7 @@ cudaError_t launch_tail_zero(uint16_t* dq, uint16_t* dk, uint16_t* dv, int64_t d
 
 // ------------------------------------------------------------------ backward preprocess
 // Delta[h][t] = sum_d dO[t,h,d] * O[t,h,d] and lse2[h][t] = lse * log2(e) on
-// valid rows (0 elsewhere), and the fp32 dQ accumulator reset.  One warp per
-// (t, h) row.
+// valid rows (0 elsewhere).  One warp per (t, h) row.
 __device__ inline bool row_valid(const int32_t* eff, int B, int t) {
   const int32_t* cu = eff;
   const int32_t* pad = eff + (B + 1);
@@ -344,7 +343,7 @@ template <int D>
 __global__ void __launch_bounds__(256) bwd_prep_kernel(const uint16_t* __restrict__ o,
                                                        const uint16_t* __restrict__ dout,
                                                        const float* __restrict__ lse, float* __restrict__ delta,
-                                                       float* __restrict__ lse2, float* __restrict__ dq_acc,
+                                                       float* __restrict__ lse2,
                                                        const int32_t* __restrict__ eff, int B, int64_t T, int Hq,
                                                        const int32_t* dev_status) {
   if (*dev_status != 0) return;
@@ -380,80 +379,24 @@ __global__ void __launch_bounds__(256) bwd_prep_kernel(const uint16_t* __restric
       delta[(int64_t)h * T + t] = acc;
       lse2[(int64_t)h * T + t] = valid ? lse[(int64_t)h * T + t] * 1.4426950408889634f : 0.f;
     }
-    float* pq = dq_acc + row * D + lane * PER;
-    if (PER == 4) *reinterpret_cast<float4*>(pq) = make_float4(0.f, 0.f, 0.f, 0.f);
-    else *reinterpret_cast<float2*>(pq) = make_float2(0.f, 0.f);
   }
 }
 
 cudaError_t launch_bwd_prep(const uint16_t* o, const uint16_t* dout, const float* lse, float* delta, float* lse2,
-                            float* dq_acc, const int32_t* eff, int B, int64_t T_q, int Hq, int D,
-                            const int32_t* dev_status, cudaStream_t st) {
+                            const int32_t* eff, int B, int64_t T_q, int Hq, int D, const int32_t* dev_status,
+                            cudaStream_t st) {
   const int64_t warps = T_q * Hq;
   if (warps == 0) return cudaSuccess;
   const int64_t want = (warps + 7) / 8;
   const int grid = (int)(want < 8LL * num_sms() ? want : 8LL * num_sms());
   prof_before(THD_KERNEL_BWD_PREP, st);
   if (D == 128)
-    bwd_prep_kernel<128><<<grid, 256, 0, st>>>(o, dout, lse, delta, lse2, dq_acc, eff, B, T_q, Hq, dev_status);
+    bwd_prep_kernel<128><<<grid, 256, 0, st>>>(o, dout, lse, delta, lse2, eff, B, T_q, Hq, dev_status);
   else
-    bwd_prep_kernel<64><<<grid, 256, 0, st>>>(o, dout, lse, delta, lse2, dq_acc, eff, B, T_q, Hq, dev_status);
+    bwd_prep_kernel<64><<<grid, 256, 0, st>>>(o, dout, lse, delta, lse2, eff, B, T_q, Hq, dev_status);
   count_launch();
   cudaError_t e = cudaGetLastError();
   prof_after(THD_KERNEL_BWD_PREP, st);
-  return e;
-}
-
-// ------------------------------------------------------------------ dQ convert
-// dq[t,h,:] = bf16(scale * acc[t,h,:]) on valid rows; 0 on pad rows and on the
-// slack rows [pad[B], dq_rows) (the tail-zero, with no extra launch).
-template <int D>
-__global__ void __launch_bounds__(256) bwd_dq_kernel(const float* __restrict__ acc, uint16_t* __restrict__ dq,
-                                                     const int32_t* __restrict__ eff, int B, int64_t T,
-                                                     int64_t rows, int Hq, float scale, const int32_t* dev_status) {
-  if (*dev_status != 0) return;
-  constexpr int PER = D / 32;
-  const int lane = threadIdx.x & 31;
-  const int64_t nrows = rows * Hq;
-  for (int64_t row = (blockIdx.x * (int64_t)blockDim.x + threadIdx.x) >> 5; row < nrows;
-       row += ((int64_t)gridDim.x * blockDim.x) >> 5) {
-    const int64_t t = row / Hq;
-    const bool valid = t < T && row_valid(eff, B, (int)t);
-    uint16_t* out = dq + row * D + lane * PER;
-    if (PER == 4) {
-      uint2 w = make_uint2(0, 0);
-      if (valid) {
-        float4 a = *reinterpret_cast<const float4*>(acc + row * D + lane * PER);
-        __nv_bfloat162 lo = __floats2bfloat162_rn(a.x * scale, a.y * scale);
-        __nv_bfloat162 hi = __floats2bfloat162_rn(a.z * scale, a.w * scale);
-        w.x = *reinterpret_cast<uint32_t*>(&lo);
-        w.y = *reinterpret_cast<uint32_t*>(&hi);
-      }
-      *reinterpret_cast<uint2*>(out) = w;
-    } else {
-      uint32_t w = 0;
-      if (valid) {
-        float2 a = *reinterpret_cast<const float2*>(acc + row * D + lane * PER);
-        __nv_bfloat162 v = __floats2bfloat162_rn(a.x * scale, a.y * scale);
-        w = *reinterpret_cast<uint32_t*>(&v);
-      }
-      *reinterpret_cast<uint32_t*>(out) = w;
-    }
-  }
-}
-
-cudaError_t launch_bwd_dq(const float* dq_acc, uint16_t* dq, const int32_t* eff, int B, int64_t T_q,
-                          int64_t dq_rows, int Hq, int D, float scale, const int32_t* dev_status, cudaStream_t st) {
-  const int64_t warps = dq_rows * Hq;
-  if (warps == 0) return cudaSuccess;
-  const int64_t want = (warps + 7) / 8;
-  const int grid = (int)(want < 8LL * num_sms() ? want : 8LL * num_sms());
-  prof_before(THD_KERNEL_BWD_DQ, st);
-  if (D == 128) bwd_dq_kernel<128><<<grid, 256, 0, st>>>(dq_acc, dq, eff, B, T_q, dq_rows, Hq, scale, dev_status);
-  else bwd_dq_kernel<64><<<grid, 256, 0, st>>>(dq_acc, dq, eff, B, T_q, dq_rows, Hq, scale, dev_status);
-  count_launch();
-  cudaError_t e = cudaGetLastError();
-  prof_after(THD_KERNEL_BWD_DQ, st);
   return e;
 }
 

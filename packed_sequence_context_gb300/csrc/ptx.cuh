@@ -66,6 +66,15 @@ THD_DEV bool mbar_wait(uint64_t* bar, uint32_t parity, volatile int* abort_flag)
   }
 }
 
+// Bounded wait that ignores the abort flag (used to drain in-flight async
+// work before a CTA exits).
+THD_DEV void drain_wait(uint64_t* bar, uint32_t parity) {
+  const uint64_t t0 = globaltimer();
+  while (!mbar_try_wait(bar, parity)) {
+    if (globaltimer() - t0 > kWaitTimeoutNs) break;
+  }
+}
+
 // ------------------------------------------------------------------ fences
 THD_DEV void fence_proxy_async_smem() { asm volatile("fence.proxy.async.shared::cta;" ::: "memory"); }
 THD_DEV void named_bar_sync(uint32_t id, uint32_t nthreads) {
