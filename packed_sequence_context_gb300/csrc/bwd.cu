@@ -105,6 +105,7 @@ __global__ void __launch_bounds__(320, 1)
   uint64_t* bar_st_full = bars + 2 + 2 * S;
   uint64_t* bar_p_ready = bars + 3 + 2 * S;
   uint64_t* bar_dk_done = bars + 4 + 2 * S;
+  uint64_t* bar_y_free = bars + 5 + 2 * S;  // the compute warps hold dP^T in registers
   uint64_t* bar_drain = bars + 6 + 2 * S;
   uint64_t* bar_dv_done = bars + 7 + 2 * S;
   uint32_t* s_tmem = reinterpret_cast<uint32_t*>(bars + 8 + 2 * S);
@@ -128,6 +129,7 @@ __global__ void __launch_bounds__(320, 1)
     mbar_init(bar_st_full, 1);
     mbar_init(bar_p_ready, 8);  // one arrival per compute warp
     mbar_init(bar_dk_done, 1);
+    mbar_init(bar_y_free, 8);  // one arrival per compute warp
     mbar_init(bar_drain, 1);
     mbar_init(bar_dv_done, 1);
     *s_abort = 0;
@@ -215,19 +217,41 @@ __global__ void __launch_bounds__(320, 1)
     __syncwarp();
   } else if (warp == 9) {
     // ------------------------------------------------------------ MMA issuer
-    // Per step s: dP^T(s) -> Y, S^T(s) -> X (once dV(s-1) has read P^T(s-1)
-    // from X), then -- once the compute warps have written P^T(s) and dS(s)
-    // -- dV(s) and dK(s).  The commit behind S^T(s+1) covers dK(s), so the
-    // compute warps of step s+1 see S^T(s+1) only after dK(s) has read the
-    // dS buffer they are about to overwrite.  (Letting step s+1's compute
-    // start while dK(s) still ran, with an explicit dK-done wait before the
-    // dS writes, gave wrong dK and dV on GB300: the overlap is avoided.)
+    // Per step s: dP^T(s) -> Y as soon as the compute warps hold dP^T(s-1) in
+    // registers (y_free, early in their step s-1); then, once they have
+    // written P^T(s-1) and dS(s-1), dV(s-1) and dK(s-1); then S^T(s) -> X
+    // once dV(s-1) has read P^T(s-1).  The commit behind S^T(s) covers
+    // dK(s-1), so step s's compute warps see S^T(s) only after dK(s-1) has
+    // read the dS buffer they will overwrite.
     if (lane == 0) {
       constexpr uint32_t idesc_kv = idesc_bf16(128, D, false, true);  // dV, dK (B MN-major)
       const uint32_t kb = smem_u32(sK), vb = smem_u32(sV), dsb = smem_u32(sDS);
       int stage = 0;
       uint32_t ph = 0, su = 0, kv_iter = 0;
       bool ok = true;
+      // the step whose dV / dK are still to be issued
+      int pv_stage = -1, pv_n16 = 0;
+      bool pv_first = false;
+      auto tail = [&]() -> bool {
+        if (!mbar_wait(bar_p_ready, (su - 1) & 1u, s_abort)) return false;
+        tc_fence_after();
+        const uint32_t qb = smem_u32(smem + C::kOffQ + pv_stage * 2 * C::kTileBytes);
+        const uint32_t dob = qb + C::kTileBytes;
+        // dV += P^T dO  (P^T packed bf16 in X: query columns 16 ks.. of K-step ks
+        // sit at column 64 (ks/4) + 8 (ks%4); K = the valid query rows)
+        for (int ks = 0; ks < pv_n16; ++ks)
+          mma_ts(tmem + C::kColDV, tmem + C::kColX + 64 * (ks >> 2) + 8 * (ks & 3),
+                 sdesc_sw128(dob + ks * 2048, 16384, 1024), idesc_kv, (pv_first && ks == 0) ? 0u : 1u);
+        tc_commit(bar_dv_done);
+        // dK += dS^T Q
+        for (int ks = 0; ks < pv_n16; ++ks)
+          mma_ss(tmem + C::kColDK, sdesc_sw128(dsb + (ks >> 2) * 16384 + (ks & 3) * 32, 16, 1024),
+                 sdesc_sw128(qb + ks * 2048, 16384, 1024), idesc_kv, (pv_first && ks == 0) ? 0u : 1u);
+        tc_commit(bar_dk_done);
+        tc_commit(&bar_qdo_empty[pv_stage]);
+        pv_stage = -1;
+        return true;
+      };
       for (int w = blockIdx.x; w < n_items && ok; w += gridDim.x) {
         const BwdItem it = bwd_item(p, w);
         if (it.kv_first > it.kv_last) continue;
@@ -240,19 +264,25 @@ __global__ void __launch_bounds__(320, 1)
           const int nqv = imin(imin(kTile, it.g.cbq - jq * kTile), it.g.Lq - (qc * it.g.cbq + jq * kTile));
           const int n16 = ceil_div(nqv, 16);  // query rows in MMA units of 16
           const uint32_t idesc_t = idesc_bf16(128, 16 * n16, false, false);  // S^T, dP^T
-          if (!mbar_wait(&bar_qdo_full[stage], ph, s_abort)) {
+          if (!mbar_wait(&bar_qdo_full[stage], ph, s_abort) ||
+              (su > 0 && !mbar_wait(bar_y_free, (su - 1) & 1u, s_abort))) {
             ok = false;
             return;
           }
           tc_fence_after();
           const uint32_t qb = smem_u32(smem + C::kOffQ + stage * 2 * C::kTileBytes);
           const uint32_t dob = qb + C::kTileBytes;
-          // dP^T = V dO^T -> Y (Y was read by the compute warps before the last p_ready)
+          // dP^T = V dO^T -> Y
 #pragma unroll
           for (int ks = 0; ks < D / 16; ++ks) {
             const uint32_t off = (ks >> 2) * 16384 + (ks & 3) * 32;
             mma_ss(tmem + C::kColY, sdesc_sw128(vb + off, 16, 1024), sdesc_sw128(dob + off, 16, 1024), idesc_t,
                    ks > 0);
+          }
+          // dV, dK of the previous step of this item
+          if (pv_stage >= 0 && !tail()) {
+            ok = false;
+            return;
           }
           // S^T = K Q^T -> X, once dV of the previous step has read P^T there
           if (su > 0 && !mbar_wait(bar_dv_done, (su - 1) & 1u, s_abort)) {
@@ -267,23 +297,9 @@ __global__ void __launch_bounds__(320, 1)
                    ks > 0);
           }
           tc_commit(bar_st_full);
-          if (!mbar_wait(bar_p_ready, su & 1u, s_abort)) {
-            ok = false;
-            return;
-          }
-          tc_fence_after();
-          // dV += P^T dO  (P^T packed bf16 in X: query columns 16 ks.. of K-step ks
-          // sit at column 64 (ks/4) + 8 (ks%4); K = the valid query rows)
-          for (int ks = 0; ks < n16; ++ks)
-            mma_ts(tmem + C::kColDV, tmem + C::kColX + 64 * (ks >> 2) + 8 * (ks & 3),
-                   sdesc_sw128(dob + ks * 2048, 16384, 1024), idesc_kv, (first && ks == 0) ? 0u : 1u);
-          tc_commit(bar_dv_done);
-          // dK += dS^T Q
-          for (int ks = 0; ks < n16; ++ks)
-            mma_ss(tmem + C::kColDK, sdesc_sw128(dsb + (ks >> 2) * 16384 + (ks & 3) * 32, 16, 1024),
-                   sdesc_sw128(qb + ks * 2048, 16384, 1024), idesc_kv, (first && ks == 0) ? 0u : 1u);
-          tc_commit(bar_dk_done);
-          tc_commit(&bar_qdo_empty[stage]);
+          pv_stage = stage;
+          pv_n16 = n16;
+          pv_first = first;
           first = false;
           ++su;
           if (++stage == S) {
@@ -292,6 +308,7 @@ __global__ void __launch_bounds__(320, 1)
           }
         });
         if (!ok) break;
+        if (pv_stage >= 0 && !tail()) break;  // the item's last step; dk_done then covers all its products
         tc_commit(bar_kv_empty);
       }
       tc_commit(bar_drain);
@@ -335,13 +352,26 @@ __global__ void __launch_bounds__(320, 1)
         // lse arrives pre-scaled to log2 units by the preprocess kernel
         const uint32_t lse_s = smem_u32(sLse + (su % S) * 256), dl_s = lse_s + 512;
         const int nch = ceil_div(nqv, 32);
-#pragma unroll 1
-        for (int kk = 2 * half; kk < imin(nch, 2 * half + 2); ++kk) {
-          uint32_t sr[32], dr[32];
+        // dP^T of this thread's chunks first, so Y can take the next step's
+        // dP^T while P and dS are computed
+        uint32_t dq2[2][32];
+#pragma unroll
+        for (int i = 0; i < 2; ++i)
+          if (2 * half + i < nch) tmem_ld32(tmem + lane_base + C::kColY + 32 * (2 * half + i), dq2[i]);
+#pragma unroll
+        for (int i = 0; i < 2; ++i)
+          if (2 * half + i < nch) tmem_ld_wait(dq2[i]);
+        tc_fence_before();
+        __syncwarp();
+        if (lane == 0) mbar_arrive(bar_y_free);
+#pragma unroll
+        for (int i = 0; i < 2; ++i) {
+          const int kk = 2 * half + i;
+          if (kk >= nch) break;
+          uint32_t sr[32];
+          const uint32_t* dr = dq2[i];
           tmem_ld32(tmem + lane_base + C::kColX + 32 * kk, sr);
-          tmem_ld32(tmem + lane_base + C::kColY + 32 * kk, dr);
           tmem_ld_wait(sr);
-          tmem_ld_wait(dr);
           // query columns outside [n_lo, n_hi) (causal, or past the valid rows)
           // get S = -inf, hence P = 0 and dS = 0; warps whose rows see the
           // whole chunk (every step off the causal diagonal) skip the selects

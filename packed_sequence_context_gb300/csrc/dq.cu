@@ -14,7 +14,8 @@
 // One work item = (rank r, sequence b, query head h, rank-local 128-row query
 // tile t), the forward's schedule.  For each key tile (chunk c, tile j) the
 // item visits:
-//   S  = Q K^T   (TMEM S buffer g % 2)     dP = dO V^T   (TMEM dP)
+//   S  = Q K^T   (TMEM S buffer g % 2)     dP = dO V^T   (TMEM dP, released
+//                                           as soon as the dS warps hold it)
 //   P  = 2^(S scale log2(e) - lse log2(e))  dS = P (dP - Delta)  -> bf16 into S
 //   dQ += dS K   (A = dS from TMEM, B = the K tile read MN-major)
 // and dQ * scale is written as bf16 at the end of the item.
@@ -67,6 +68,7 @@ __global__ void __launch_bounds__(384, 1)
   __shared__ __align__(8) uint64_t bar_s_free[2];
   __shared__ __align__(8) uint64_t bar_ds_ready[2];
   __shared__ __align__(8) uint64_t bar_dp_full;
+  __shared__ __align__(8) uint64_t bar_dp_free;  // the dS warps have read dP into registers
   __shared__ __align__(8) uint64_t bar_q_full;
   __shared__ __align__(8) uint64_t bar_q_empty;
   __shared__ __align__(8) uint64_t bar_dq_done;
@@ -94,6 +96,7 @@ __global__ void __launch_bounds__(384, 1)
       mbar_init(&bar_ds_ready[s], 8);  // one arrival per dS warp
     }
     mbar_init(&bar_dp_full, 1);
+    mbar_init(&bar_dp_free, 8);  // one arrival per dS warp
     mbar_init(&bar_q_full, 32);
     mbar_init(&bar_q_empty, 2);  // the S issuer's last read of Q and the dP issuer's last read of dO
     mbar_init(&bar_dq_done, 1);
@@ -255,9 +258,10 @@ __global__ void __launch_bounds__(384, 1)
     __syncwarp();
   } else if (warp == 11) {
     // ------------------------------------------------------------ dP = dO V^T and dQ += dS K issuer
-    // Per tile g: once the dS warps are done with tile g-1 (its dS is in TMEM
-    // and the dP buffer has been read), dP of tile g first (the dS warps wait
-    // for it), then dQ of tile g-1.  The item's last dQ follows its last dS.
+    // Per tile g: once the dS warps have read dP of tile g-1 into registers
+    // (dp_free: early in their work on g-1), dP of tile g -- so it is ready
+    // when they come to g -- then, once their dS of g-1 is in TMEM, dQ of
+    // tile g-1.  The item's last dQ follows its last dS.
     if (lane == 0) {
       constexpr uint32_t idesc_dq = idesc_bf16(128, D, false, true);
       const uint64_t dodesc = sdesc_sw128(smem_u32(sDO), 16, 1024);
@@ -296,9 +300,8 @@ __global__ void __launch_bounds__(384, 1)
         for_each_kv_tile(it, p, [&](int c, int jt) {
           if (!ok) return;
           const int ncols = q_tile_ncols(it, p, c, jt);
-          // the dP buffer is free once the dS warps finished tile g-1 (for
-          // j = 0 that wait was made before the previous item's last dQ)
-          if (j > 0 && !mbar_wait(&bar_ds_ready[(g - 1) & 1u], ((g - 1) >> 1) & 1u, &s_abort)) {
+          // the dP buffer is free once the dS warps have read tile g-1's dP
+          if (g > 0 && !mbar_wait(&bar_dp_free, (g - 1) & 1u, &s_abort)) {
             ok = false;
             return;
           }
@@ -380,15 +383,25 @@ __global__ void __launch_bounds__(384, 1)
         const int nch = ceil_div(q_tile_ncols(it, p, c, j), 32);
         const uint32_t scol = tmem + lane_base + b * 128u;
         const uint32_t pcol = tmem + lane_base + C::kColDP;
+        // dP of this thread's two chunks first, so the buffer can take the
+        // next tile's dP while dS is computed
+        uint32_t dr[2][32];
+#pragma unroll
+        for (int kk = 0; kk < 2; ++kk)
+          if (2 * half + kk < nch) tmem_ld32(pcol + 32 * (2 * half + kk), dr[kk]);
+#pragma unroll
+        for (int kk = 0; kk < 2; ++kk)
+          if (2 * half + kk < nch) tmem_ld_wait(dr[kk]);
+        tc_fence_before();
+        __syncwarp();
+        if (lane == 0) mbar_arrive(&bar_dp_free);
 #pragma unroll
         for (int kk = 0; kk < 2; ++kk) {
           const int ch = 2 * half + kk;  // this thread's 32-column chunk
           if (ch < nch) {
-            uint32_t sr[32], dr[32];
+            uint32_t sr[32];
             tmem_ld32(scol + 32 * ch, sr);
-            tmem_ld32(pcol + 32 * ch, dr);
             tmem_ld_wait(sr);
-            tmem_ld_wait(dr);
             // keys this row may not see get S = -inf: P = 0 and dS = 0
             if (__any_sync(0xffffffffu, cnt < 32 * ch + 32)) {
 #pragma unroll
@@ -401,7 +414,7 @@ __global__ void __launch_bounds__(384, 1)
               float x0, x1, t0, t1, g0, g1;
               ffma2(x0, x1, __uint_as_float(sr[2 * n]), __uint_as_float(sr[2 * n + 1]), sl2, sl2, -lse2, -lse2);
               const float p0 = ex2(x0), p1 = ex2(x1);
-              fadd2(t0, t1, __uint_as_float(dr[2 * n]), __uint_as_float(dr[2 * n + 1]), -dlt, -dlt);
+              fadd2(t0, t1, __uint_as_float(dr[kk][2 * n]), __uint_as_float(dr[kk][2 * n + 1]), -dlt, -dlt);
               fmul2(g0, g1, p0, p1, t0, t1);
               pk[n] = pack_bf16x2(g0, g1);
             }
@@ -413,7 +426,7 @@ __global__ void __launch_bounds__(384, 1)
         tmem_st_wait();
         tc_fence_before();
         __syncwarp();  // every lane's dS is in TMEM and dP was read: one arrival speaks for the warp
-        if (lane == 0) mbar_arrive(&bar_ds_ready[b]);
+        if (lane == 0) mbar_arrive(&bar_ds_ready[b]);  // dS of tile g is in TMEM
         ++g;
         ++jl;
       });
