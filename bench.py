@@ -4,8 +4,8 @@
 One step = one pass of the whole hot path over one synthetic packed batch:
 metadata validation + pad detection + per-rank partition + schedule (one
 planner launch), the fused ring-decomposed forward (thd_attn_fwd), and the
-backward (thd_attn_bwd: Delta preprocess, key-stationary backward, dQ
-conversion with tail-zero).  Inputs are resident in HBM before the timed
+backward (thd_attn_bwd: two planner passes, Delta preprocess, the
+key-stationary dK/dV kernel, the query-stationary dQ kernel).  Inputs are resident in HBM before the timed
 region; L2 is flushed (256 MiB write) between timed steps, outside the
 events.  Each step is timed with CUDA events on the launching stream.
 
@@ -324,6 +324,9 @@ def run_ours(a):
     with ClockSampler(local) as clk:
         times, kms, launches = timed(step, a.steps, main_kernel)
         fwd_times, fwd_kms, _ = timed(fwd, a.steps, T.THD_KERNEL_FWD)
+        dq_kms = None
+        if not a.fwd_only:
+            _, dq_kms, _ = timed(bwd, max(3, min(a.steps, 20)), T.THD_KERNEL_BWD_DQ)
     assert int(st.item()) == 0, T.thd_status_string(int(st.item()))
 
     ms = sum(times) / len(times)
@@ -335,7 +338,9 @@ def run_ours(a):
     fwd_ms = sum(fwd_times) / len(fwd_times)
     fwd_tflops = fwd_flops / (fwd_ms * 1e-3) / 1e12
 
-    main_flops = fwd_flops if a.fwd_only else 2.5 * fwd_flops
+    # algorithmic work of the dominant kernel: the forward's two matmuls, or
+    # the dK/dV kernel's four (S^T, dP^T, dV, dK: twice the forward)
+    main_flops = fwd_flops if a.fwd_only else 2.0 * fwd_flops
     kavg = sum(kms) / len(kms) if kms else float("nan")
     achieved = main_flops / (kavg * 1e-3) / 1e12
     fk = sum(fwd_kms) / len(fwd_kms) if fwd_kms else float("nan")
@@ -363,6 +368,14 @@ def run_ours(a):
             "fwd_roofline": {"bound": "tensor", "kernel": "fwd_kernel", "achieved": fwd_kernel_tflops, "peak": peak,
                              "unit": "TFLOP/s", "frac": fwd_kernel_tflops / peak, "kernel_ms": fk,
                              "traffic": _kernel_traffic("fwd_kernel", w.name)},
+            "dq_roofline": None if not dq_kms else {
+                "bound": "tensor", "kernel": "dq_kernel", "unit": "TFLOP/s", "peak": peak,
+                "kernel_ms": sum(dq_kms) / len(dq_kms),
+                # executed: S, dP (recomputed) and dQ, 1.5x the forward's matmuls; of these only dQ
+                # (0.5x) counts toward the algorithmic backward
+                "achieved": 1.5 * fwd_flops / (sum(dq_kms) / len(dq_kms) * 1e-3) / 1e12,
+                "frac": 1.5 * fwd_flops / (sum(dq_kms) / len(dq_kms) * 1e-3) / 1e12 / peak,
+                "flops": "executed (S and dP recomputed)"},
             "gpu_launches": launches,
             "clocks": clk.summary(),
             "cpu_baseline": cpu,

@@ -224,8 +224,11 @@ THD_API int thd_attn_fwd_noalloc(const void* q, const void* k, const void* v, vo
  *   including the slack rows [pad[B], rows), is written with 0 (the THD
  *   gradient tail-zero of [P2 "Describe the bug"], done on the device with
  *   no extra launch and no work when there is no slack).
- * dK/dV of each kv head sum over its query-head group.  dQ is accumulated in
- * fp32 with atomic adds, so its rounding may differ between runs.
+ * dK/dV of each kv head sum over its query-head group.  Two passes: a
+ * key-stationary kernel for dK/dV and a query-stationary kernel for dQ (it
+ * recomputes S and dP for its query tile); every output element is summed in
+ * a fixed order, so dQ, dK and dV are bit-reproducible across runs.
+ * Launches: two planner passes, the Delta preprocess, dK/dV, dQ.
  */
 THD_API int thd_attn_bwd(const void* q, const void* k, const void* v, const void* o, const float* lse, const void* dout,
                  void* dq, void* dk, void* dv, int64_t dq_rows, int64_t dkv_rows, const int32_t* cu_seqlens_q,

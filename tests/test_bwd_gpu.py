@@ -107,8 +107,8 @@ def test_non_causal_backward_matches_oracle(case):
 
 
 def test_value_equal_padded_metadata_backward():
-    """dK/dV accumulate in a fixed order (bit-identical); dQ sums with atomics
-    whose order may vary, so it is compared within tolerance."""
+    """[P2]: every way of saying 'no padding' takes the same path, and every
+    gradient is summed in a fixed order, so all of dQ, dK, dV are bit-identical."""
     w = inputs.make_workload("tiny")
     t = inputs.make_tensors(w, with_grad=True)
     d = device_inputs(w, t)
@@ -116,7 +116,7 @@ def test_value_equal_padded_metadata_backward():
     for flag, cp in ((-1, d["cu_pad"]), (0, d["cu_pad"]), (1, d["cu_pad"]), (-1, d["cu"])):
         _, _, dq, dk, dv = _run(w, d, pad_flag=flag, cu_pad=cp)
         assert torch.equal(dk, dk0) and torch.equal(dv, dv0)
-        assert (dq.float() - dq0.float()).abs().max().item() <= 1e-2
+        assert torch.equal(dq, dq0)
 
 
 def test_slack_rows_are_tail_zeroed():
@@ -173,9 +173,11 @@ def test_full_size_backward_sampled(name, heads, n_seq):
         assert torch.isfinite(g.float()).all()
 
 
-def test_backward_dk_dv_bit_reproducible_over_repeats():
-    """dK/dV accumulate in TMEM in a fixed order: repeated calls agree bit for
-    bit (dQ is summed with atomics and may differ in its last bits)."""
+def test_backward_bit_reproducible_over_repeats():
+    """dK/dV accumulate in TMEM over the key tile's query steps and dQ over
+    the query tile's key tiles, each in a fixed order (no atomics): repeated
+    calls agree bit for bit; a pipeline race between the MMA, producer and
+    compute roles shows up here as run-to-run differences."""
     w = inputs.make_workload("packed")
     t = inputs.make_tensors(w, with_grad=True)
     d = device_inputs(w, t)
@@ -186,4 +188,4 @@ def test_backward_dk_dv_bit_reproducible_over_repeats():
         torch.cuda.synchronize()
         assert int(st.item()) == 0
         assert torch.equal(dk, dk0) and torch.equal(dv, dv0)
-        assert (dq.float() - dq0.float()).abs().max().item() <= 1e-2
+        assert torch.equal(dq, dq0)
