@@ -106,6 +106,7 @@ __global__ void __launch_bounds__(320, 1)
   uint64_t* bar_p_ready = bars + 3 + 2 * S;
   uint64_t* bar_dk_done = bars + 4 + 2 * S;
   uint64_t* bar_y_free = bars + 5 + 2 * S;  // the compute warps hold dP^T in registers
+  uint64_t* bar_dp_full = bars + 10 + 2 * S;  // dP^T of the step is in TMEM
   uint64_t* bar_drain = bars + 6 + 2 * S;
   uint64_t* bar_dv_done = bars + 7 + 2 * S;
   uint32_t* s_tmem = reinterpret_cast<uint32_t*>(bars + 8 + 2 * S);
@@ -130,6 +131,7 @@ __global__ void __launch_bounds__(320, 1)
     mbar_init(bar_p_ready, 8);  // one arrival per compute warp
     mbar_init(bar_dk_done, 1);
     mbar_init(bar_y_free, 8);  // one arrival per compute warp
+    mbar_init(bar_dp_full, 1);
     mbar_init(bar_drain, 1);
     mbar_init(bar_dv_done, 1);
     *s_abort = 0;
@@ -217,12 +219,16 @@ __global__ void __launch_bounds__(320, 1)
     __syncwarp();
   } else if (warp == 9) {
     // ------------------------------------------------------------ MMA issuer
-    // Per step s: dP^T(s) -> Y as soon as the compute warps hold dP^T(s-1) in
-    // registers (y_free, early in their step s-1); then, once they have
-    // written P^T(s-1) and dS(s-1), dV(s-1) and dK(s-1); then S^T(s) -> X
-    // once dV(s-1) has read P^T(s-1).  The commit behind S^T(s) covers
-    // dK(s-1), so step s's compute warps see S^T(s) only after dK(s-1) has
-    // read the dS buffer they will overwrite.
+    // The two 128-column TMEM buffers T0, T1 swap roles every step: step s
+    // puts S^T(s) (then P^T(s)) in T[s % 2] and dP^T(s) in T[(s + 1) % 2].
+    // Per step s: S^T(s) as soon as the compute warps hold dP^T(s-1), which
+    // sat in the same buffer, in registers (y_free: while they still work on
+    // step s-1); then, once they have written P^T(s-1) and dS(s-1), dV(s-1)
+    // and dK(s-1); then dP^T(s) into the buffer P^T(s-1) leaves once dV(s-1)
+    // has read it.  The compute warps of step s compute P from S^T(s) while
+    // dV/dK(s-1) run, and dS once dP^T(s) is there; the commit behind dP^T(s)
+    // covers dK(s-1), so they overwrite the dS buffer only after dK(s-1) has
+    // read it.
     if (lane == 0) {
       constexpr uint32_t idesc_kv = idesc_bf16(128, D, false, true);  // dV, dK (B MN-major)
       const uint32_t kb = smem_u32(sK), vb = smem_u32(sV), dsb = smem_u32(sDS);
@@ -233,15 +239,17 @@ __global__ void __launch_bounds__(320, 1)
       int pv_stage = -1, pv_n16 = 0;
       bool pv_first = false;
       auto tail = [&]() -> bool {
-        if (!mbar_wait(bar_p_ready, (su - 1) & 1u, s_abort)) return false;
+        const uint32_t ps = su - 1;  // the pending step
+        if (!mbar_wait(bar_p_ready, ps & 1u, s_abort)) return false;
         tc_fence_after();
         const uint32_t qb = smem_u32(smem + C::kOffQ + pv_stage * 2 * C::kTileBytes);
         const uint32_t dob = qb + C::kTileBytes;
-        // dV += P^T dO  (P^T packed bf16 in X: query columns 16 ks.. of K-step ks
-        // sit at column 64 (ks/4) + 8 (ks%4); K = the valid query rows)
+        const uint32_t pcol = tmem + C::kColX + 128u * (ps & 1u);  // P^T of the pending step
+        // dV += P^T dO  (P^T packed bf16: query columns 16 ks.. of K-step ks sit
+        // at column 64 (ks/4) + 8 (ks%4); K = the valid query rows)
         for (int ks = 0; ks < pv_n16; ++ks)
-          mma_ts(tmem + C::kColDV, tmem + C::kColX + 64 * (ks >> 2) + 8 * (ks & 3),
-                 sdesc_sw128(dob + ks * 2048, 16384, 1024), idesc_kv, (pv_first && ks == 0) ? 0u : 1u);
+          mma_ts(tmem + C::kColDV, pcol + 64 * (ks >> 2) + 8 * (ks & 3), sdesc_sw128(dob + ks * 2048, 16384, 1024),
+                 idesc_kv, (pv_first && ks == 0) ? 0u : 1u);
         tc_commit(bar_dv_done);
         // dK += dS^T Q
         for (int ks = 0; ks < pv_n16; ++ks)
@@ -264,6 +272,8 @@ __global__ void __launch_bounds__(320, 1)
           const int nqv = imin(imin(kTile, it.g.cbq - jq * kTile), it.g.Lq - (qc * it.g.cbq + jq * kTile));
           const int n16 = ceil_div(nqv, 16);  // query rows in MMA units of 16
           const uint32_t idesc_t = idesc_bf16(128, 16 * n16, false, false);  // S^T, dP^T
+          const uint32_t acol = tmem + C::kColX + 128u * (su & 1u);          // S^T(s), then P^T(s)
+          const uint32_t bcol = tmem + C::kColX + 128u * ((su + 1) & 1u);    // dP^T(s)
           if (!mbar_wait(&bar_qdo_full[stage], ph, s_abort) ||
               (su > 0 && !mbar_wait(bar_y_free, (su - 1) & 1u, s_abort))) {
             ok = false;
@@ -272,19 +282,20 @@ __global__ void __launch_bounds__(320, 1)
           tc_fence_after();
           const uint32_t qb = smem_u32(smem + C::kOffQ + stage * 2 * C::kTileBytes);
           const uint32_t dob = qb + C::kTileBytes;
-          // dP^T = V dO^T -> Y
+          // S^T = K Q^T -> the buffer dP^T(s-1) has left
 #pragma unroll
           for (int ks = 0; ks < D / 16; ++ks) {
             const uint32_t off = (ks >> 2) * 16384 + (ks & 3) * 32;
-            mma_ss(tmem + C::kColY, sdesc_sw128(vb + off, 16, 1024), sdesc_sw128(dob + off, 16, 1024), idesc_t,
-                   ks > 0);
+            mma_ss(acol, sdesc_sw128(kb + off, 16, 1024), sdesc_sw128(qb + off, 16, 1024), idesc_t, ks > 0);
           }
-          // dV, dK of the previous step of this item
+          tc_commit(bar_st_full);
+          // dV, dK of the previous step (of this item; an item's last step is
+          // finished at the item's end)
           if (pv_stage >= 0 && !tail()) {
             ok = false;
             return;
           }
-          // S^T = K Q^T -> X, once dV of the previous step has read P^T there
+          // dP^T = V dO^T -> the buffer P^T(s-1) leaves once dV(s-1) has read it
           if (su > 0 && !mbar_wait(bar_dv_done, (su - 1) & 1u, s_abort)) {
             ok = false;
             return;
@@ -293,10 +304,9 @@ __global__ void __launch_bounds__(320, 1)
 #pragma unroll
           for (int ks = 0; ks < D / 16; ++ks) {
             const uint32_t off = (ks >> 2) * 16384 + (ks & 3) * 32;
-            mma_ss(tmem + C::kColX, sdesc_sw128(kb + off, 16, 1024), sdesc_sw128(qb + off, 16, 1024), idesc_t,
-                   ks > 0);
+            mma_ss(bcol, sdesc_sw128(vb + off, 16, 1024), sdesc_sw128(dob + off, 16, 1024), idesc_t, ks > 0);
           }
-          tc_commit(bar_st_full);
+          tc_commit(bar_dp_full);
           pv_stage = stage;
           pv_n16 = n16;
           pv_first = first;
@@ -352,61 +362,86 @@ __global__ void __launch_bounds__(320, 1)
         // lse arrives pre-scaled to log2 units by the preprocess kernel
         const uint32_t lse_s = smem_u32(sLse + (su % S) * 256), dl_s = lse_s + 512;
         const int nch = ceil_div(nqv, 32);
-        // dP^T of this thread's chunks first, so Y can take the next step's
-        // dP^T while P and dS are computed
-        uint32_t dq2[2][32];
-#pragma unroll
-        for (int i = 0; i < 2; ++i)
-          if (2 * half + i < nch) tmem_ld32(tmem + lane_base + C::kColY + 32 * (2 * half + i), dq2[i]);
-#pragma unroll
-        for (int i = 0; i < 2; ++i)
-          if (2 * half + i < nch) tmem_ld_wait(dq2[i]);
-        tc_fence_before();
-        __syncwarp();
-        if (lane == 0) mbar_arrive(bar_y_free);
+        const uint32_t acol = tmem + lane_base + C::kColX + 128u * (su & 1u);        // S^T, then P^T
+        const uint32_t bcol = tmem + lane_base + C::kColX + 128u * ((su + 1) & 1u);  // dP^T
+        // ---- P = 2^(S^T scale log2(e) - lse) for this thread's chunks (query
+        // columns outside [n_lo, n_hi) -- causal, or past the valid rows -- get
+        // S = -inf, hence P = 0 and dS = 0); packed P^T goes back over S^T
+        float pv[2][32];
 #pragma unroll
         for (int i = 0; i < 2; ++i) {
           const int kk = 2 * half + i;
-          if (kk >= nch) break;
-          uint32_t sr[32];
-          const uint32_t* dr = dq2[i];
-          tmem_ld32(tmem + lane_base + C::kColX + 32 * kk, sr);
-          tmem_ld_wait(sr);
-          // query columns outside [n_lo, n_hi) (causal, or past the valid rows)
-          // get S = -inf, hence P = 0 and dS = 0; warps whose rows see the
-          // whole chunk (every step off the causal diagonal) skip the selects
-          if (__any_sync(0xffffffffu, n_lo > 32 * kk || n_hi < 32 * kk + 32)) {
+          if (kk < nch) {
+            uint32_t sr[32];
+            tmem_ld32(acol + 32 * kk, sr);
+            tmem_ld_wait(sr);
+            if (__any_sync(0xffffffffu, n_lo > 32 * kk || n_hi < 32 * kk + 32)) {
 #pragma unroll
-            for (int e = 0; e < 32; ++e) {
-              const int n = 32 * kk + e;
-              if (n < n_lo || n >= n_hi) sr[e] = __float_as_uint(-INFINITY);
+              for (int e = 0; e < 32; ++e) {
+                const int n = 32 * kk + e;
+                if (n < n_lo || n >= n_hi) sr[e] = __float_as_uint(-INFINITY);
+              }
             }
-          }
-          uint32_t pk[16], dk[16];
+            uint32_t pk[16];
 #pragma unroll
-          for (int q4 = 0; q4 < 8; ++q4) {  // four query columns at a time, as packed pairs
-            const float4 l4 = lds128f(lse_s + 4 * (32 * kk + 4 * q4));
-            const float4 d4 = lds128f(dl_s + 4 * (32 * kk + 4 * q4));
-            float x0, x1, x2, x3, t0, t1, t2, t3, g0, g1, g2, g3;
-            ffma2(x0, x1, __uint_as_float(sr[4 * q4]), __uint_as_float(sr[4 * q4 + 1]), sl2, sl2, -l4.x, -l4.y);
-            ffma2(x2, x3, __uint_as_float(sr[4 * q4 + 2]), __uint_as_float(sr[4 * q4 + 3]), sl2, sl2, -l4.z, -l4.w);
-            const float p0 = ex2(x0), p1 = ex2(x1), p2 = ex2(x2), p3 = ex2(x3);
-            fadd2(t0, t1, __uint_as_float(dr[4 * q4]), __uint_as_float(dr[4 * q4 + 1]), -d4.x, -d4.y);
-            fadd2(t2, t3, __uint_as_float(dr[4 * q4 + 2]), __uint_as_float(dr[4 * q4 + 3]), -d4.z, -d4.w);
-            fmul2(g0, g1, p0, p1, t0, t1);
-            fmul2(g2, g3, p2, p3, t2, t3);
-            pk[2 * q4] = pack_bf16x2(p0, p1);
-            pk[2 * q4 + 1] = pack_bf16x2(p2, p3);
-            dk[2 * q4] = pack_bf16x2(g0, g1);
-            dk[2 * q4 + 1] = pack_bf16x2(g2, g3);
+            for (int q4 = 0; q4 < 8; ++q4) {
+              const float4 l4 = lds128f(lse_s + 4 * (32 * kk + 4 * q4));
+              float x0, x1, x2, x3;
+              ffma2(x0, x1, __uint_as_float(sr[4 * q4]), __uint_as_float(sr[4 * q4 + 1]), sl2, sl2, -l4.x, -l4.y);
+              ffma2(x2, x3, __uint_as_float(sr[4 * q4 + 2]), __uint_as_float(sr[4 * q4 + 3]), sl2, sl2, -l4.z, -l4.w);
+              pv[i][4 * q4] = ex2(x0);
+              pv[i][4 * q4 + 1] = ex2(x1);
+              pv[i][4 * q4 + 2] = ex2(x2);
+              pv[i][4 * q4 + 3] = ex2(x3);
+              pk[2 * q4] = pack_bf16x2(pv[i][4 * q4], pv[i][4 * q4 + 1]);
+              pk[2 * q4 + 1] = pack_bf16x2(pv[i][4 * q4 + 2], pv[i][4 * q4 + 3]);
+            }
+            // packed P^T stays inside this warpgroup's own S^T columns (the other
+            // warpgroup may still be reading its half): chunk kk -> 64 (kk/2) + 16 (kk%2)
+            tmem_st16(acol + 64 * (kk >> 1) + 16 * (kk & 1), pk);
           }
-          // packed P^T stays inside this warpgroup's own S^T columns (the other
-          // warpgroup may still be reading its half): chunk kk -> 64 (kk/2) + 16 (kk%2)
-          tmem_st16(tmem + lane_base + C::kColX + 64 * (kk >> 1) + 16 * (kk & 1), pk);
+        }
+        // ---- dS = P (dP^T - Delta), once dP^T is in TMEM; the buffer is
+        // released (y_free) as soon as this warp's last chunk of it is loaded
+        if (!mbar_wait(bar_dp_full, su & 1u, s_abort)) {
+          ok = false;
+          return;
+        }
+        tc_fence_after();
+        if (2 * half >= nch) {
+          tc_fence_before();
+          __syncwarp();
+          if (lane == 0) mbar_arrive(bar_y_free);
+        }
 #pragma unroll
-          for (int i = 0; i < 4; ++i)
-            sts128(ds_s + sw128_offset(row, 32 * kk + 8 * i, kTile), dk[4 * i], dk[4 * i + 1], dk[4 * i + 2],
-                   dk[4 * i + 3]);
+        for (int i = 0; i < 2; ++i) {
+          const int kk = 2 * half + i;
+          if (kk < nch) {
+            uint32_t dr[32];
+            tmem_ld32(bcol + 32 * kk, dr);
+            tmem_ld_wait(dr);
+            if (kk + 1 >= imin(nch, 2 * half + 2)) {  // this warp's last dP^T chunk is in registers
+              tc_fence_before();
+              __syncwarp();
+              if (lane == 0) mbar_arrive(bar_y_free);
+            }
+            uint32_t dk[16];
+#pragma unroll
+            for (int q4 = 0; q4 < 8; ++q4) {
+              const float4 d4 = lds128f(dl_s + 4 * (32 * kk + 4 * q4));
+              float t0, t1, t2, t3, g0, g1, g2, g3;
+              fadd2(t0, t1, __uint_as_float(dr[4 * q4]), __uint_as_float(dr[4 * q4 + 1]), -d4.x, -d4.y);
+              fadd2(t2, t3, __uint_as_float(dr[4 * q4 + 2]), __uint_as_float(dr[4 * q4 + 3]), -d4.z, -d4.w);
+              fmul2(g0, g1, pv[i][4 * q4], pv[i][4 * q4 + 1], t0, t1);
+              fmul2(g2, g3, pv[i][4 * q4 + 2], pv[i][4 * q4 + 3], t2, t3);
+              dk[2 * q4] = pack_bf16x2(g0, g1);
+              dk[2 * q4 + 1] = pack_bf16x2(g2, g3);
+            }
+#pragma unroll
+            for (int j = 0; j < 4; ++j)
+              sts128(ds_s + sw128_offset(row, 32 * kk + 8 * j, kTile), dk[4 * j], dk[4 * j + 1], dk[4 * j + 2],
+                     dk[4 * j + 3]);
+          }
         }
         tmem_st_wait();
         fence_proxy_async_smem();
