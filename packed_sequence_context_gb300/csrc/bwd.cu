@@ -17,10 +17,10 @@
 //   S^T  = K Q^T            (TMEM X)     dP^T = V dO^T         (TMEM Y)
 //   P^T  = exp(S^T scale - lse)          dS^T = P^T (dP^T - Delta)
 //   dV  += P^T dO   (A = P^T from TMEM)  dK  += dS^T Q   (A = dS^T, smem)
-// CTA (320 threads): warps 0-7 compute in two warpgroups -- a thread owns one
+// CTA (352 threads): warps 0-7 compute in two warpgroups -- a thread owns one
 // key row (its TMEM lane) and half of the query columns for P/dS, and half of
 // the head dimension when writing dK/dV; warp 8 TMA producer (+ lse/Delta
-// staging); warp 9 TMEM allocator and single-thread MMA issuer.
+// staging); warp 9 TMEM allocator and S^T issuer; warp 10 dV/dK/dP^T issuer.
 #include "common.cuh"
 #include "ptx.cuh"
 
@@ -87,7 +87,7 @@ __device__ inline void drain_wait_b(uint64_t* bar, uint32_t parity) {
 }
 
 template <int D>
-__global__ void __launch_bounds__(320, 1)
+__global__ void __launch_bounds__(352, 1)
     bwd_kernel(const BwdParams p, const __grid_constant__ CUtensorMap tmQ, const __grid_constant__ CUtensorMap tmDO,
                const __grid_constant__ CUtensorMap tmK, const __grid_constant__ CUtensorMap tmV) {
   using C = BwdCfg<D>;
@@ -108,6 +108,7 @@ __global__ void __launch_bounds__(320, 1)
   uint64_t* bar_y_free = bars + 5 + 2 * S;  // the compute warps hold dP^T in registers
   uint64_t* bar_dp_full = bars + 10 + 2 * S;  // dP^T of the step is in TMEM
   uint64_t* bar_drain = bars + 6 + 2 * S;
+  uint64_t* bar_drain2 = bars + 11 + 2 * S;
   uint64_t* bar_dv_done = bars + 7 + 2 * S;
   uint32_t* s_tmem = reinterpret_cast<uint32_t*>(bars + 8 + 2 * S);
   int* s_abort = reinterpret_cast<int*>(bars + 9 + 2 * S);
@@ -132,6 +133,7 @@ __global__ void __launch_bounds__(320, 1)
     mbar_init(bar_dk_done, 1);
     mbar_init(bar_y_free, 8);  // one arrival per compute warp
     mbar_init(bar_dp_full, 1);
+    mbar_init(bar_drain2, 1);
     mbar_init(bar_drain, 1);
     mbar_init(bar_dv_done, 1);
     *s_abort = 0;
@@ -218,20 +220,63 @@ __global__ void __launch_bounds__(320, 1)
     }
     __syncwarp();
   } else if (warp == 9) {
-    // ------------------------------------------------------------ MMA issuer
+    // ------------------------------------------------------------ S^T issuer
     // The two 128-column TMEM buffers T0, T1 swap roles every step: step s
     // puts S^T(s) (then P^T(s)) in T[s % 2] and dP^T(s) in T[(s + 1) % 2].
-    // Per step s: S^T(s) as soon as the compute warps hold dP^T(s-1), which
-    // sat in the same buffer, in registers (y_free: while they still work on
-    // step s-1); then, once they have written P^T(s-1) and dS(s-1), dV(s-1)
-    // and dK(s-1); then dP^T(s) into the buffer P^T(s-1) leaves once dV(s-1)
-    // has read it.  The compute warps of step s compute P from S^T(s) while
-    // dV/dK(s-1) run, and dS once dP^T(s) is there; the commit behind dP^T(s)
-    // covers dK(s-1), so they overwrite the dS buffer only after dK(s-1) has
-    // read it.
+    // Two issuing threads, as in the forward (a barrier wait in one does not
+    // idle the tensor pipe while the other has products to issue):
+    //   warp 9:  S^T(s), as soon as the compute warps hold dP^T(s-1), which sat
+    //            in the same buffer, in registers (y_free)
+    //   warp 10: once the compute warps have written P^T(s-1) and dS(s-1),
+    //            dV(s-1) and dK(s-1); then dP^T(s) into the buffer P^T(s-1)
+    //            leaves once dV(s-1) has read it.
+    // The compute warps of step s compute P from S^T(s) while dV/dK(s-1) run
+    // and dS once dP^T(s) is there; warp 10's commit behind dP^T(s) covers
+    // its dK(s-1), so they overwrite the dS buffer only after dK(s-1) read it.
+    if (lane == 0) {
+      const uint32_t kb = smem_u32(sK);
+      int stage = 0;
+      uint32_t ph = 0, su = 0, kv_iter = 0;
+      bool ok = true;
+      for (int w = blockIdx.x; w < n_items && ok; w += gridDim.x) {
+        const BwdItem it = bwd_item(p, w);
+        if (it.kv_first > it.kv_last) continue;
+        if (!mbar_wait(bar_kv_full, kv_iter & 1u, s_abort)) break;
+        ++kv_iter;
+        for_each_q_step(it, p, [&](int qc, int jq, int) {
+          if (!ok) return;
+          const int nqv = imin(imin(kTile, it.g.cbq - jq * kTile), it.g.Lq - (qc * it.g.cbq + jq * kTile));
+          const uint32_t idesc_t = idesc_bf16(128, 16 * ceil_div(nqv, 16), false, false);
+          const uint32_t acol = tmem + C::kColX + 128u * (su & 1u);  // S^T(s), then P^T(s)
+          if (!mbar_wait(&bar_qdo_full[stage], ph, s_abort) ||
+              (su > 0 && !mbar_wait(bar_y_free, (su - 1) & 1u, s_abort))) {
+            ok = false;
+            return;
+          }
+          tc_fence_after();
+          const uint32_t qb = smem_u32(smem + C::kOffQ + stage * 2 * C::kTileBytes);
+#pragma unroll
+          for (int ks = 0; ks < D / 16; ++ks) {
+            const uint32_t off = (ks >> 2) * 16384 + (ks & 3) * 32;
+            mma_ss(acol, sdesc_sw128(kb + off, 16, 1024), sdesc_sw128(qb + off, 16, 1024), idesc_t, ks > 0);
+          }
+          tc_commit(bar_st_full);
+          ++su;
+          if (++stage == S) {
+            stage = 0;
+            ph ^= 1u;
+          }
+        });
+      }
+      tc_commit(bar_drain);
+      drain_wait_b(bar_drain, 0);
+    }
+    __syncwarp();
+  } else if (warp == 10) {
+    // ------------------------------------------------------------ dV, dK and dP^T issuer
     if (lane == 0) {
       constexpr uint32_t idesc_kv = idesc_bf16(128, D, false, true);  // dV, dK (B MN-major)
-      const uint32_t kb = smem_u32(sK), vb = smem_u32(sV), dsb = smem_u32(sDS);
+      const uint32_t vb = smem_u32(sV), dsb = smem_u32(sDS);
       int stage = 0;
       uint32_t ph = 0, su = 0, kv_iter = 0;
       bool ok = true;
@@ -270,25 +315,13 @@ __global__ void __launch_bounds__(320, 1)
         for_each_q_step(it, p, [&](int qc, int jq, int) {
           if (!ok) return;
           const int nqv = imin(imin(kTile, it.g.cbq - jq * kTile), it.g.Lq - (qc * it.g.cbq + jq * kTile));
-          const int n16 = ceil_div(nqv, 16);  // query rows in MMA units of 16
-          const uint32_t idesc_t = idesc_bf16(128, 16 * n16, false, false);  // S^T, dP^T
-          const uint32_t acol = tmem + C::kColX + 128u * (su & 1u);          // S^T(s), then P^T(s)
-          const uint32_t bcol = tmem + C::kColX + 128u * ((su + 1) & 1u);    // dP^T(s)
-          if (!mbar_wait(&bar_qdo_full[stage], ph, s_abort) ||
-              (su > 0 && !mbar_wait(bar_y_free, (su - 1) & 1u, s_abort))) {
+          const int n16 = ceil_div(nqv, 16);
+          const uint32_t idesc_t = idesc_bf16(128, 16 * n16, false, false);
+          const uint32_t bcol = tmem + C::kColX + 128u * ((su + 1) & 1u);  // dP^T(s)
+          if (!mbar_wait(&bar_qdo_full[stage], ph, s_abort)) {
             ok = false;
             return;
           }
-          tc_fence_after();
-          const uint32_t qb = smem_u32(smem + C::kOffQ + stage * 2 * C::kTileBytes);
-          const uint32_t dob = qb + C::kTileBytes;
-          // S^T = K Q^T -> the buffer dP^T(s-1) has left
-#pragma unroll
-          for (int ks = 0; ks < D / 16; ++ks) {
-            const uint32_t off = (ks >> 2) * 16384 + (ks & 3) * 32;
-            mma_ss(acol, sdesc_sw128(kb + off, 16, 1024), sdesc_sw128(qb + off, 16, 1024), idesc_t, ks > 0);
-          }
-          tc_commit(bar_st_full);
           // dV, dK of the previous step (of this item; an item's last step is
           // finished at the item's end)
           if (pv_stage >= 0 && !tail()) {
@@ -301,6 +334,7 @@ __global__ void __launch_bounds__(320, 1)
             return;
           }
           tc_fence_after();
+          const uint32_t dob = smem_u32(smem + C::kOffQ + stage * 2 * C::kTileBytes) + C::kTileBytes;
 #pragma unroll
           for (int ks = 0; ks < D / 16; ++ks) {
             const uint32_t off = (ks >> 2) * 16384 + (ks & 3) * 32;
@@ -321,8 +355,8 @@ __global__ void __launch_bounds__(320, 1)
         if (pv_stage >= 0 && !tail()) break;  // the item's last step; dk_done then covers all its products
         tc_commit(bar_kv_empty);
       }
-      tc_commit(bar_drain);
-      drain_wait_b(bar_drain, 0);
+      tc_commit(bar_drain2);
+      drain_wait_b(bar_drain2, 0);
     }
     __syncwarp();
   } else {
@@ -525,7 +559,7 @@ static cudaError_t launch_bwd_t(const BwdParams& p, const CUtensorMap& tq, const
   cudaError_t e = cudaFuncSetAttribute(bwd_kernel<D>, cudaFuncAttributeMaxDynamicSharedMemorySize, C::kSmem);
   if (e != cudaSuccess) return e;
   prof_before(THD_KERNEL_BWD, st);
-  bwd_kernel<D><<<grid, 320, C::kSmem, st>>>(p, tq, tdo, tk, tv);
+  bwd_kernel<D><<<grid, 352, C::kSmem, st>>>(p, tq, tdo, tk, tv);
   count_launch();
   e = cudaGetLastError();
   prof_after(THD_KERNEL_BWD, st);
