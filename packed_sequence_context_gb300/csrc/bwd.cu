@@ -14,9 +14,10 @@
 // One work item = (sequence b, key chunk c, key tile jk within the chunk, kv
 // head hk).  For each query tile (chunk qc, tile jq) that sees it and each
 // query head h of the GQA group:
-//   S^T  = K Q^T            (TMEM X)     dP^T = V dO^T         (TMEM Y)
+//   S^T  = K Q^T      dP^T = V dO^T     (two TMEM buffers, roles swapped every step)
 //   P^T  = exp(S^T scale - lse)          dS^T = P^T (dP^T - Delta)
-//   dV  += P^T dO   (A = P^T from TMEM)  dK  += dS^T Q   (A = dS^T, smem)
+//   dV  += P^T dO     dK  += dS^T Q       (A = P^T / dS^T from TMEM, packed bf16
+//                                          over the S^T they were computed from)
 // CTA (352 threads): warps 0-7 compute in two warpgroups -- a thread owns one
 // key row (its TMEM lane) and half of the query columns for P/dS, and half of
 // the head dimension when writing dK/dV; warp 8 TMA producer (+ lse/Delta
@@ -33,8 +34,7 @@ struct BwdCfg {
   static constexpr int kOffK = 0;
   static constexpr int kOffV = kTileBytes;
   static constexpr int kOffQ = 2 * kTileBytes;                 // stage s: Q at kOffQ + s * 2 * kTileBytes
-  static constexpr int kOffDS = kOffQ + kStages * 2 * kTileBytes;
-  static constexpr int kOffLse = kOffDS + kTile * kTile * 2;   // stage s: lse2[128], delta[128]
+  static constexpr int kOffLse = kOffQ + kStages * 2 * kTileBytes;  // stage s: lse2[128], delta[128]
   static constexpr int kOffBar = kOffLse + kStages * 2 * kTile * 4;
   static constexpr int kSmem = kOffBar + 256;
   static constexpr uint32_t kTmemCols = 512;
@@ -95,7 +95,6 @@ __global__ void __launch_bounds__(352, 1)
   extern __shared__ __align__(1024) uint8_t smem[];
   uint8_t* sK = smem + C::kOffK;
   uint8_t* sV = smem + C::kOffV;
-  uint8_t* sDS = smem + C::kOffDS;
   float* sLse = reinterpret_cast<float*>(smem + C::kOffLse);  // stage s: [s*256, s*256+128) lse2, then delta
   uint64_t* bars = reinterpret_cast<uint64_t*>(smem + C::kOffBar);
   uint64_t* bar_kv_full = bars + 0;
@@ -231,8 +230,10 @@ __global__ void __launch_bounds__(352, 1)
     //            dV(s-1) and dK(s-1); then dP^T(s) into the buffer P^T(s-1)
     //            leaves once dV(s-1) has read it.
     // The compute warps of step s compute P from S^T(s) while dV/dK(s-1) run
-    // and dS once dP^T(s) is there; warp 10's commit behind dP^T(s) covers
-    // its dK(s-1), so they overwrite the dS buffer only after dK(s-1) read it.
+    // and dS once dP^T(s) is there.  P^T(s) and dS^T(s) both go back over
+    // S^T(s) as packed bf16 (each thread into the S^T columns it has read) and
+    // are the TMEM A operands of dV(s) and dK(s): dS never touches shared
+    // memory, which the SS products already keep busy.
     if (lane == 0) {
       const uint32_t kb = smem_u32(sK);
       int stage = 0;
@@ -276,7 +277,7 @@ __global__ void __launch_bounds__(352, 1)
     // ------------------------------------------------------------ dV, dK and dP^T issuer
     if (lane == 0) {
       constexpr uint32_t idesc_kv = idesc_bf16(128, D, false, true);  // dV, dK (B MN-major)
-      const uint32_t vb = smem_u32(sV), dsb = smem_u32(sDS);
+      const uint32_t vb = smem_u32(sV);
       int stage = 0;
       uint32_t ph = 0, su = 0, kv_iter = 0;
       bool ok = true;
@@ -296,10 +297,11 @@ __global__ void __launch_bounds__(352, 1)
           mma_ts(tmem + C::kColDV, pcol + 64 * (ks >> 2) + 8 * (ks & 3), sdesc_sw128(dob + ks * 2048, 16384, 1024),
                  idesc_kv, (pv_first && ks == 0) ? 0u : 1u);
         tc_commit(bar_dv_done);
-        // dK += dS^T Q
+        // dK += dS^T Q  (dS^T packed bf16 beside P^T: K-step ks at column
+        // 64 (ks/4) + 32 + 8 (ks%4))
         for (int ks = 0; ks < pv_n16; ++ks)
-          mma_ss(tmem + C::kColDK, sdesc_sw128(dsb + (ks >> 2) * 16384 + (ks & 3) * 32, 16, 1024),
-                 sdesc_sw128(qb + ks * 2048, 16384, 1024), idesc_kv, (pv_first && ks == 0) ? 0u : 1u);
+          mma_ts(tmem + C::kColDK, pcol + 64 * (ks >> 2) + 32 + 8 * (ks & 3), sdesc_sw128(qb + ks * 2048, 16384, 1024),
+                 idesc_kv, (pv_first && ks == 0) ? 0u : 1u);
         tc_commit(bar_dk_done);
         tc_commit(&bar_qdo_empty[pv_stage]);
         pv_stage = -1;
@@ -328,8 +330,9 @@ __global__ void __launch_bounds__(352, 1)
             ok = false;
             return;
           }
-          // dP^T = V dO^T -> the buffer P^T(s-1) leaves once dV(s-1) has read it
-          if (su > 0 && !mbar_wait(bar_dv_done, (su - 1) & 1u, s_abort)) {
+          // dP^T = V dO^T -> the buffer P^T(s-1) and dS^T(s-1) leave once dV(s-1)
+          // and dK(s-1) have read them
+          if (su > 0 && !mbar_wait(bar_dk_done, (su - 1) & 1u, s_abort)) {
             ok = false;
             return;
           }
@@ -365,7 +368,6 @@ __global__ void __launch_bounds__(352, 1)
     const int row = tid & 127;      // its key row (TMEM lane) / query row when draining dQ
     const uint32_t lane_base = (uint32_t)((warp & 3) * 32) << 16;
     const float sl2 = p.scale_log2;
-    const uint32_t ds_s = smem_u32(sDS);
     uint32_t su = 0;
     bool ok = true;
     for (int w = blockIdx.x; w < n_items && ok; w += gridDim.x) {
@@ -471,16 +473,14 @@ __global__ void __launch_bounds__(352, 1)
               dk[2 * q4] = pack_bf16x2(g0, g1);
               dk[2 * q4 + 1] = pack_bf16x2(g2, g3);
             }
-#pragma unroll
-            for (int j = 0; j < 4; ++j)
-              sts128(ds_s + sw128_offset(row, 32 * kk + 8 * j, kTile), dk[4 * j], dk[4 * j + 1], dk[4 * j + 2],
-                     dk[4 * j + 3]);
+            // packed dS^T beside P^T, in the S^T columns this thread has read:
+            // chunk kk -> 64 (kk/2) + 32 + 16 (kk%2)
+            tmem_st16(acol + 64 * (kk >> 1) + 32 + 16 * (kk & 1), dk);
           }
         }
         tmem_st_wait();
-        fence_proxy_async_smem();
         tc_fence_before();
-        __syncwarp();  // every lane's P^T and dS are written: one arrival speaks for the warp
+        __syncwarp();  // every lane's P^T and dS^T are in TMEM: one arrival speaks for the warp
         if (lane == 0) mbar_arrive(bar_p_ready);
         ++su;
         ++nsteps;
