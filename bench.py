@@ -4,8 +4,8 @@
 One step = one pass of the whole hot path over one synthetic packed batch:
 metadata validation + pad detection + per-rank partition + schedule (one
 planner launch), the fused ring-decomposed forward (thd_attn_fwd), and the
-backward (thd_attn_bwd: two planner passes, Delta preprocess, the
-key-stationary dK/dV kernel, the query-stationary dQ kernel).  Inputs are resident in HBM before the timed
+backward (thd_attn_bwd: the planner, the Delta preprocess, the
+query-stationary dQ kernel, the key-stationary dK/dV kernel).  Inputs are resident in HBM before the timed
 region; L2 is flushed (256 MiB write) between timed steps, outside the
 events.  Each step is timed with CUDA events on the launching stream.
 

@@ -228,7 +228,8 @@ THD_API int thd_attn_fwd_noalloc(const void* q, const void* k, const void* v, vo
  * key-stationary kernel for dK/dV and a query-stationary kernel for dQ (it
  * recomputes S and dP for its query tile); every output element is summed in
  * a fixed order, so dQ, dK and dV are bit-reproducible across runs.
- * Launches: two planner passes, the Delta preprocess, dK/dV, dQ.
+ * Launches: the planner (both schedules in one launch), the Delta
+ * preprocess, dQ, dK/dV.
  */
 THD_API int thd_attn_bwd(const void* q, const void* k, const void* v, const void* o, const float* lse, const void* dout,
                  void* dq, void* dk, void* dv, int64_t dq_rows, int64_t dkv_rows, const int32_t* cu_seqlens_q,

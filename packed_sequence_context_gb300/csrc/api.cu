@@ -281,18 +281,15 @@ int thd_attn_bwd(const void* q, const void* k, const void* v, const void* o, con
   rc = check_ws(workspace, workspace_bytes, L.total);
   if (rc) return rc;
   char* w = static_cast<char*>(workspace);
-  // two schedules: key tiles for the dK/dV pass, query tiles for the dQ pass
+  // one planner launch, two schedules: key tiles for the dK/dV pass, query
+  // tiles for the dQ pass
   PlanParams pp = plan_params(cu_seqlens_q, cu_seqlens_kv, cu_seqlens_q_padded, cu_seqlens_kv_padded, B, cp_size,
-                              causal, pad_between_seqs, T_q, T_kv, 2, w, L, dev_status);
+                              causal, pad_between_seqs, T_q, T_kv, 3, w, L, dev_status);
+  pp.tile_off_q = reinterpret_cast<int32_t*>(w + L.tile_off_q);
+  pp.counters_q = reinterpret_cast<int32_t*>(w + L.counters_q);
+  pp.items_q = reinterpret_cast<int4*>(w + L.items_q);
+  pp.item_cap_q = L.item_cap_q;
   rc = cuda_status(launch_plan(pp, st));
-  if (rc) return rc;
-  PlanParams pq = pp;
-  pq.mode = 1;
-  pq.tile_off = reinterpret_cast<int32_t*>(w + L.tile_off_q);
-  pq.counters = reinterpret_cast<int32_t*>(w + L.counters_q);
-  pq.items = reinterpret_cast<int4*>(w + L.items_q);
-  pq.item_cap = L.item_cap_q;
-  rc = cuda_status(launch_plan(pq, st));
   if (rc) return rc;
   float* delta = reinterpret_cast<float*>(w + L.delta);
   float* lse2 = reinterpret_cast<float*>(w + L.lse2);
@@ -303,6 +300,32 @@ int thd_attn_bwd(const void* q, const void* k, const void* v, const void* o, con
   if (!make_thd_map(&tq, q, T_q, Hq, D) || !make_thd_map(&tdo, dout, T_q, Hq, D) ||
       !make_thd_map(&tk, k, T_kv, Hkv, D) || !make_thd_map(&tv, v, T_kv, Hkv, D))
     return THD_ERR_CUDA;
+  DqParams dp;
+  std::memset(&dp, 0, sizeof(dp));
+  dp.q = static_cast<const uint16_t*>(q);
+  dp.dout = static_cast<const uint16_t*>(dout);
+  dp.lse2 = lse2;
+  dp.delta = delta;
+  dp.dq = static_cast<uint16_t*>(dq);
+  dp.eff = pp.eff;
+  dp.items = pp.items_q;
+  dp.counters = pp.counters_q;
+  dp.dev_status = dev_status;
+  dp.B = B;
+  dp.Hq = Hq;
+  dp.Hkv = Hkv;
+  dp.cp = cp_size;
+  dp.causal = causal;
+  dp.T_q = T_q;
+  dp.dq_rows = dq_rows;
+  dp.scale = softmax_scale;
+  dp.scale_log2 = softmax_scale * 1.4426950408889634f;
+  dp.step_lo = 0;
+  dp.step_hi = cp_size;
+  const int64_t bound_q = (int64_t)L.item_cap_q * Hq;
+  const int grid_q = (int)(bound_q < num_sms() ? (bound_q > 0 ? bound_q : 1) : num_sms());
+  rc = cuda_status(launch_dq(dp, tk, tv, D, grid_q, st));
+  if (rc) return rc;
   BwdParams bp;
   std::memset(&bp, 0, sizeof(bp));
   bp.q = static_cast<const uint16_t*>(q);
@@ -326,33 +349,7 @@ int thd_attn_bwd(const void* q, const void* k, const void* v, const void* o, con
   bp.scale_log2 = softmax_scale * 1.4426950408889634f;
   const int64_t bound = (int64_t)L.item_cap * Hkv;
   const int grid = (int)(bound < num_sms() ? (bound > 0 ? bound : 1) : num_sms());
-  rc = cuda_status(launch_bwd(bp, tq, tdo, tk, tv, D, grid, st));
-  if (rc) return rc;
-  DqParams dp;
-  std::memset(&dp, 0, sizeof(dp));
-  dp.q = static_cast<const uint16_t*>(q);
-  dp.dout = static_cast<const uint16_t*>(dout);
-  dp.lse2 = lse2;
-  dp.delta = delta;
-  dp.dq = static_cast<uint16_t*>(dq);
-  dp.eff = pq.eff;
-  dp.items = pq.items;
-  dp.counters = pq.counters;
-  dp.dev_status = dev_status;
-  dp.B = B;
-  dp.Hq = Hq;
-  dp.Hkv = Hkv;
-  dp.cp = cp_size;
-  dp.causal = causal;
-  dp.T_q = T_q;
-  dp.dq_rows = dq_rows;
-  dp.scale = softmax_scale;
-  dp.scale_log2 = softmax_scale * 1.4426950408889634f;
-  dp.step_lo = 0;
-  dp.step_hi = cp_size;
-  const int64_t bound_q = (int64_t)L.item_cap_q * Hq;
-  const int grid_q = (int)(bound_q < num_sms() ? (bound_q > 0 ? bound_q : 1) : num_sms());
-  return cuda_status(launch_dq(dp, tk, tv, D, grid_q, st));
+  return cuda_status(launch_bwd(bp, tq, tdo, tk, tv, D, grid, st));
 }
 
 int thd_lse_merge(float* o_acc, float* lse_acc, const float* o_part, const float* lse_part, int64_t T, int H, int D,

@@ -181,19 +181,24 @@ __global__ void __launch_bounds__(352, 1)
         const int q0 = qc * it.g.cbq + jq * kTile;
         const int nqv = imin(imin(kTile, it.g.cbq - jq * kTile), it.g.Lq - q0);
         const int q_row = it.g.q_off + q0;
-        const uint32_t lse2 = smem_u32(sLse + stage * 256);
-        // lse and Delta of the valid query rows, copied asynchronously (entries
-        // past nqv are left stale: the compute warps never read them unmasked)
+        const uint32_t lse_st = smem_u32(sLse + stage * 256);
+        // lse and Delta of the valid query rows, copied asynchronously; the
+        // entries past nqv are zeroed so that masked columns stay finite
+        // (S = -inf gives P = 0 and dS = 0 only against finite lse and Delta)
 #pragma unroll
         for (int k = 0; k < 4; ++k) {
           const int n = lane + 32 * k;
           if (n < nqv) {
             const int64_t idx = (int64_t)h * p.T_q + q_row + n;
-            cp_async_4(lse2 + 4 * n, p.lse2 + idx);
-            cp_async_4(lse2 + 512 + 4 * n, p.delta + idx);
+            cp_async_4(lse_st + 4 * n, p.lse2 + idx);
+            cp_async_4(lse_st + 512 + 4 * n, p.delta + idx);
+          } else {
+            sLse[stage * 256 + n] = 0.f;
+            sLse[stage * 256 + 128 + n] = 0.f;
           }
         }
         cp_async_arrive_noinc(&bar_qdo_full[stage]);
+        __syncwarp();  // the zeroed entries are ordered before lane 0's arrival
         if (lane == 0) {
           mbar_arrive_expect_tx(&bar_qdo_full[stage], 2 * C::kTileBytes);
           uint8_t* sQ = smem + C::kOffQ + stage * 2 * C::kTileBytes;
@@ -395,7 +400,6 @@ __global__ void __launch_bounds__(352, 1)
           ok = false;
           return;
         }
-        // lse arrives pre-scaled to log2 units by the preprocess kernel
         const uint32_t lse_s = smem_u32(sLse + (su % S) * 256), dl_s = lse_s + 512;
         const int nch = ceil_div(nqv, 32);
         const uint32_t acol = tmem + lane_base + C::kColX + 128u * (su & 1u);        // S^T, then P^T
@@ -421,7 +425,7 @@ __global__ void __launch_bounds__(352, 1)
             uint32_t pk[16];
 #pragma unroll
             for (int q4 = 0; q4 < 8; ++q4) {
-              const float4 l4 = lds128f(lse_s + 4 * (32 * kk + 4 * q4));
+              const float4 l4 = lds128f(lse_s + 4 * (32 * kk + 4 * q4));  // lse in log2 units
               float x0, x1, x2, x3;
               ffma2(x0, x1, __uint_as_float(sr[4 * q4]), __uint_as_float(sr[4 * q4 + 1]), sl2, sl2, -l4.x, -l4.y);
               ffma2(x2, x3, __uint_as_float(sr[4 * q4 + 2]), __uint_as_float(sr[4 * q4 + 3]), sl2, sl2, -l4.z, -l4.w);

@@ -29,7 +29,7 @@ struct WsLayout {
   size_t counters = 0;  // int32 [64]: [0] number of schedule entries
   size_t items = 0;     // int4 [item_cap]
   // backward only: the query-tile schedule of the dQ pass (its own planner
-  // outputs), Delta and lse in log2 units
+  // outputs), Delta = rowsum(dO * O) and lse in log2 units
   size_t tile_off_q = 0;  // int32 [B+1]
   size_t counters_q = 0;  // int32 [64]
   size_t items_q = 0;     // int4 [item_cap_q]
@@ -241,7 +241,8 @@ struct PlanParams {
   const int32_t* pad_kv;  // may be null
   int B, cp, causal, pad_mode;
   int64_t rows_q, rows_kv;  // buffer rows
-  int mode;                 // 0: partition only, 1: forward schedule, 2: backward schedule
+  int mode;                 // 0: partition only, 1: query-tile schedule, 2: key-tile schedule,
+                            // 3: both (key tiles into items, query tiles into items_q)
   int step_lo, step_hi;     // ring steps the forward items cover (for the cost)
   int32_t* eff;             // [4][B+1]
   int32_t* cu_rank;         // optional partition outputs (q side)
@@ -253,6 +254,10 @@ struct PlanParams {
   int32_t* counters;  // [64]
   int4* items;
   int item_cap;
+  int32_t* tile_off_q;  // mode 3: the query-tile schedule's outputs
+  int32_t* counters_q;
+  int4* items_q;
+  int item_cap_q;
   int32_t* dev_status;
 };
 
@@ -274,8 +279,8 @@ struct FwdParams {
 struct BwdParams {
   const uint16_t* q;
   const uint16_t* dout;
-  const float* lse2;  // lse * log2(e), [Hq][T_q]
-  const float* delta;
+  const float* lse2;   // [Hq][T_q], lse * log2(e)
+  const float* delta;  // [Hq][T_q]: Delta = rowsum(dO * O)
   uint16_t* dk;
   uint16_t* dv;
   const int32_t* eff;
@@ -290,8 +295,8 @@ struct BwdParams {
 struct DqParams {
   const uint16_t* q;
   const uint16_t* dout;
-  const float* lse2;  // lse * log2(e), [Hq][T_q]
-  const float* delta;
+  const float* lse2;   // [Hq][T_q], lse * log2(e)
+  const float* delta;  // [Hq][T_q]: Delta = rowsum(dO * O)
   uint16_t* dq;       // bf16 [dq_rows][Hq][D]
   const int32_t* eff;
   const int4* items;  // the query-tile schedule

@@ -361,8 +361,8 @@ __global__ void __launch_bounds__(384, 1)
       const int64_t grow = (int64_t)it.g.q_off + pos;
       // this row's lse (log2 units) and Delta; rows without a valid query mask
       // every key, so their values never matter
-      const float lse2 = valid ? p.lse2[(int64_t)it.h * p.T_q + grow] : 0.f;
       const float dlt = valid ? p.delta[(int64_t)it.h * p.T_q + grow] : 0.f;
+      const float lse2 = valid ? p.lse2[(int64_t)it.h * p.T_q + grow] : 0.f;
       int jl = 0;
       for_each_kv_tile(it, p, [&](int c, int j) {
         if (!ok) return;

@@ -58,6 +58,89 @@ __device__ inline int upper_index(const int32_t* a, int n, int x) {
 __device__ inline void set_err(int* s_err, int code) { atomicMin(s_err, code); }
 
 // ------------------------------------------------------------------ planner
+// a3: one schedule.  Query-tile entries are rank-local query tiles (b, r, t);
+// key-tile entries are chunk-aligned key tiles (b, c, jk).  Both are ordered
+// longest-first (counting sort on the number of tiles visited).  Returns
+// false when the schedule exceeds its capacity.
+__device__ bool plan_schedule(const PlanParams& p, const int32_t* eff, int mode, int32_t* tile_off,
+                              int32_t* counters, int4* items, int item_cap, int* s_warp, int* s_hist) {
+  const int tid = threadIdx.x, nt = blockDim.x;
+  const int B = p.B, cp = p.cp;
+
+  int carry = 0;
+  for (int base = 0; base < B; base += nt) {
+    const int b = base + tid;
+    int n = 0;
+    if (b < B) {
+      SeqGeom g = seq_geom(eff, B, b, cp);
+      n = mode == 1 ? cp * ceil_div(2 * g.cbq, kTile) : 2 * cp * ceil_div(g.cbkv, kTile);
+    }
+    int tot;
+    const int ex = block_exclusive_scan(n, s_warp, tot);
+    if (b < B) tile_off[b] = carry + ex;
+    carry += tot;
+  }
+  if (tid == 0) tile_off[B] = carry;
+  const int total = carry;
+  if (total > item_cap) {
+    if (tid == 0) *p.dev_status = THD_DEV_ERR_CAPACITY;
+    return false;
+  }
+  for (int i = tid; i < kCostBins; i += nt) s_hist[i] = 0;
+  __syncthreads();
+  auto entry = [&](int w, int& b, int& x, int& y, int& cost) {
+    b = upper_index(tile_off, B, w);
+    // skip empty sequences that share the same offset
+    while (b < B && tile_off[b + 1] <= w) ++b;
+    SeqGeom g = seq_geom(eff, B, b, cp);
+    const int rem = w - tile_off[b];
+    if (mode == 1) {
+      const int per_r = ceil_div(2 * g.cbq, kTile);
+      x = rem / per_r;
+      y = rem % per_r;
+      cost = fwd_item_tiles(g, x, y, cp, p.causal != 0, p.step_lo, p.step_hi);
+    } else {
+      const int per_c = ceil_div(g.cbkv, kTile);
+      x = rem / per_c;
+      y = rem % per_c;
+      cost = bwd_item_qtiles(g, x, y, cp, p.causal != 0);
+    }
+  };
+  for (int w = tid; w < total; w += nt) {
+    int b, x, y, cost;
+    entry(w, b, x, y, cost);
+    atomicAdd(&s_hist[kCostBins - 1 - imin(cost, kCostBins - 1)], 1);
+  }
+  __syncthreads();
+  // exclusive scan of the histogram: 4 bins per thread
+  {
+    constexpr int per = kCostBins / kPlanThreads;
+    int loc[per];
+    int sum = 0;
+#pragma unroll
+    for (int j = 0; j < per; ++j) {
+      loc[j] = s_hist[tid * per + j];
+      sum += loc[j];
+    }
+    int tot;
+    int ex = block_exclusive_scan(sum, s_warp, tot);
+#pragma unroll
+    for (int j = 0; j < per; ++j) {
+      s_hist[tid * per + j] = ex;
+      ex += loc[j];
+    }
+  }
+  __syncthreads();
+  for (int w = tid; w < total; w += nt) {
+    int b, x, y, cost;
+    entry(w, b, x, y, cost);
+    const int pos = atomicAdd(&s_hist[kCostBins - 1 - imin(cost, kCostBins - 1)], 1);
+    items[pos] = make_int4(b, x, y, cost);
+  }
+  if (tid == 0) counters[0] = total;
+  return true;
+}
+
 __global__ void __launch_bounds__(kPlanThreads) plan_kernel(PlanParams p) {
   __shared__ int s_err;
   __shared__ int s_pad[2];
@@ -154,81 +237,12 @@ __global__ void __launch_bounds__(kPlanThreads) plan_kernel(PlanParams p) {
     }
   }
   if (p.mode == 0) return;
-
-  // a3: the schedule.  Forward entries are rank-local query tiles (b, r, t);
-  // backward entries are chunk-aligned key tiles (b, c, jk).  Both are
-  // ordered longest-first (counting sort on the number of tiles visited).
-  int carry = 0;
-  for (int base = 0; base < B; base += nt) {
-    const int b = base + tid;
-    int n = 0;
-    if (b < B) {
-      SeqGeom g = seq_geom(eff, B, b, cp);
-      n = p.mode == 1 ? cp * ceil_div(2 * g.cbq, kTile) : 2 * cp * ceil_div(g.cbkv, kTile);
-    }
-    int tot;
-    const int ex = block_exclusive_scan(n, s_warp, tot);
-    if (b < B) p.tile_off[b] = carry + ex;
-    carry += tot;
-  }
-  if (tid == 0) p.tile_off[B] = carry;
-  const int total = carry;
-  if (total > p.item_cap) {
-    if (tid == 0) *p.dev_status = THD_DEV_ERR_CAPACITY;
+  if (!plan_schedule(p, eff, p.mode == 3 ? 2 : p.mode, p.tile_off, p.counters, p.items, p.item_cap, s_warp, s_hist))
     return;
+  if (p.mode == 3) {
+    __syncthreads();  // s_hist is reused
+    plan_schedule(p, eff, 1, p.tile_off_q, p.counters_q, p.items_q, p.item_cap_q, s_warp, s_hist);
   }
-  for (int i = tid; i < kCostBins; i += nt) s_hist[i] = 0;
-  __syncthreads();
-  auto entry = [&](int w, int& b, int& x, int& y, int& cost) {
-    b = upper_index(p.tile_off, B, w);
-    // skip empty sequences that share the same offset
-    while (b < B && p.tile_off[b + 1] <= w) ++b;
-    SeqGeom g = seq_geom(eff, B, b, cp);
-    const int rem = w - p.tile_off[b];
-    if (p.mode == 1) {
-      const int per_r = ceil_div(2 * g.cbq, kTile);
-      x = rem / per_r;
-      y = rem % per_r;
-      cost = fwd_item_tiles(g, x, y, cp, p.causal != 0, p.step_lo, p.step_hi);
-    } else {
-      const int per_c = ceil_div(g.cbkv, kTile);
-      x = rem / per_c;
-      y = rem % per_c;
-      cost = bwd_item_qtiles(g, x, y, cp, p.causal != 0);
-    }
-  };
-  for (int w = tid; w < total; w += nt) {
-    int b, x, y, cost;
-    entry(w, b, x, y, cost);
-    atomicAdd(&s_hist[kCostBins - 1 - imin(cost, kCostBins - 1)], 1);
-  }
-  __syncthreads();
-  // exclusive scan of the histogram: 4 bins per thread
-  {
-    constexpr int per = kCostBins / kPlanThreads;
-    int loc[per];
-    int sum = 0;
-#pragma unroll
-    for (int j = 0; j < per; ++j) {
-      loc[j] = s_hist[tid * per + j];
-      sum += loc[j];
-    }
-    int tot;
-    int ex = block_exclusive_scan(sum, s_warp, tot);
-#pragma unroll
-    for (int j = 0; j < per; ++j) {
-      s_hist[tid * per + j] = ex;
-      ex += loc[j];
-    }
-  }
-  __syncthreads();
-  for (int w = tid; w < total; w += nt) {
-    int b, x, y, cost;
-    entry(w, b, x, y, cost);
-    const int pos = atomicAdd(&s_hist[kCostBins - 1 - imin(cost, kCostBins - 1)], 1);
-    p.items[pos] = make_int4(b, x, y, cost);
-  }
-  if (tid == 0) p.counters[0] = total;
 }
 
 cudaError_t launch_plan(const PlanParams& p, cudaStream_t st) {
@@ -330,7 +344,8 @@ cudaError_t launch_tail_zero(uint16_t* dq, uint16_t* dk, uint16_t* dv, int64_t d
 
 // ------------------------------------------------------------------ backward preprocess
 // Delta[h][t] = sum_d dO[t,h,d] * O[t,h,d] and lse2[h][t] = lse * log2(e) on
-// valid rows (0 elsewhere).  One warp per (t, h) row.
+// valid rows (0 elsewhere), read by both backward passes.  One warp per (t, h)
+// row.
 __device__ inline bool row_valid(const int32_t* eff, int B, int t) {
   const int32_t* cu = eff;
   const int32_t* pad = eff + (B + 1);
