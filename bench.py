@@ -234,6 +234,24 @@ def run_reference(a):
     return 0
 
 
+# ----------------------------------------------------------------- replicas
+def slowest_rank_ms(ms: float, world: int, device) -> float:
+    """The step time of the slowest replica: an all-reduce MAX of each rank's
+    mean step time (the only collective of a run; none on the data path)."""
+    import torch
+    import torch.distributed as dist
+    t = torch.tensor([ms], dtype=torch.float64, device=device)
+    if world > 1:
+        dist.all_reduce(t, op=dist.ReduceOp.MAX)
+    return float(t.item())
+
+
+def weak_scaling_tflops(step_flops: float, world: int, ms_max: float) -> float:
+    """Whole-job throughput: every rank runs its own replica of the step, so
+    the job does world x step_flops in the slowest rank's step time."""
+    return step_flops * world / (ms_max * 1e-3) / 1e12
+
+
 # ----------------------------------------------------------------- GPU arm
 def run_ours(a):
     import torch
@@ -330,11 +348,8 @@ def run_ours(a):
     assert int(st.item()) == 0, T.thd_status_string(int(st.item()))
 
     ms = sum(times) / len(times)
-    ms_t = torch.tensor([ms], device=dev)
-    if world > 1:
-        dist.all_reduce(ms_t, op=dist.ReduceOp.MAX)
-    ms_max = float(ms_t.item())
-    value = step_flops * world / (ms_max * 1e-3) / 1e12
+    ms_max = slowest_rank_ms(ms, world, dev)
+    value = weak_scaling_tflops(step_flops, world, ms_max)
     fwd_ms = sum(fwd_times) / len(fwd_times)
     fwd_tflops = fwd_flops / (fwd_ms * 1e-3) / 1e12
 
