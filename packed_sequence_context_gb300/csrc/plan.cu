@@ -1,7 +1,7 @@
 // Metadata validation + pad detection (from values), the per-rank partition,
 // the longest-first tile schedule, and the small HBM-bound kernels: LSE
-// merge, gradient tail-zero, backward preprocess (Delta, dQ accumulator
-// reset) and dQ conversion.
+// merge, gradient tail-zero and the backward preprocess (Delta, lse in log2
+// units).
 //
 // Pages: [P2] TransformerEngine issue #3487 ("Describe the bug": the
 // padding detector decides by object identity and get_cu_seqlens_on_cp_rank
@@ -58,11 +58,17 @@ __device__ inline int upper_index(const int32_t* a, int n, int x) {
 __device__ inline void set_err(int* s_err, int code) { atomicMin(s_err, code); }
 
 // ------------------------------------------------------------------ planner
+// The planner stages the effective metadata and tile offsets in shared memory
+// when B + 1 <= kPlanSmemSeqs.
+constexpr int kPlanSmemSeqs = 1024;
+
 // a3: one schedule.  Query-tile entries are rank-local query tiles (b, r, t);
 // key-tile entries are chunk-aligned key tiles (b, c, jk).  Both are ordered
-// longest-first (counting sort on the number of tiles visited).  Returns
-// false when the schedule exceeds its capacity.
-__device__ bool plan_schedule(const PlanParams& p, const int32_t* eff, int mode, int32_t* tile_off,
+// longest-first (counting sort on the number of tiles visited).  `eff` and
+// `toff` are where the planner reads the effective metadata and the tile
+// offsets (shared memory when they fit); `tile_off` receives the offsets in
+// the workspace.  Returns false when the schedule exceeds its capacity.
+__device__ bool plan_schedule(const PlanParams& p, const int32_t* eff, int32_t* toff, int mode, int32_t* tile_off,
                               int32_t* counters, int4* items, int item_cap, int* s_warp, int* s_hist) {
   const int tid = threadIdx.x, nt = blockDim.x;
   const int B = p.B, cp = p.cp;
@@ -77,10 +83,16 @@ __device__ bool plan_schedule(const PlanParams& p, const int32_t* eff, int mode,
     }
     int tot;
     const int ex = block_exclusive_scan(n, s_warp, tot);
-    if (b < B) tile_off[b] = carry + ex;
+    if (b < B) {
+      tile_off[b] = carry + ex;
+      toff[b] = carry + ex;
+    }
     carry += tot;
   }
-  if (tid == 0) tile_off[B] = carry;
+  if (tid == 0) {
+    tile_off[B] = carry;
+    toff[B] = carry;
+  }
   const int total = carry;
   if (total > item_cap) {
     if (tid == 0) *p.dev_status = THD_DEV_ERR_CAPACITY;
@@ -89,11 +101,11 @@ __device__ bool plan_schedule(const PlanParams& p, const int32_t* eff, int mode,
   for (int i = tid; i < kCostBins; i += nt) s_hist[i] = 0;
   __syncthreads();
   auto entry = [&](int w, int& b, int& x, int& y, int& cost) {
-    b = upper_index(tile_off, B, w);
+    b = upper_index(toff, B, w);
     // skip empty sequences that share the same offset
-    while (b < B && tile_off[b + 1] <= w) ++b;
+    while (b < B && toff[b + 1] <= w) ++b;
     SeqGeom g = seq_geom(eff, B, b, cp);
-    const int rem = w - tile_off[b];
+    const int rem = w - toff[b];
     if (mode == 1) {
       const int per_r = ceil_div(2 * g.cbq, kTile);
       x = rem / per_r;
@@ -146,8 +158,11 @@ __global__ void __launch_bounds__(kPlanThreads) plan_kernel(PlanParams p) {
   __shared__ int s_pad[2];
   __shared__ int s_warp[32];
   __shared__ int s_hist[kCostBins];
+  // effective metadata [4][B+1] and tile offsets [B+1], when B + 1 <= kPlanSmemSeqs
+  __shared__ int32_t s_meta[5 * kPlanSmemSeqs];
   const int tid = threadIdx.x, nt = blockDim.x;
   const int B = p.B, cp = p.cp;
+  const bool meta_in_smem = B + 1 <= kPlanSmemSeqs;
   if (tid == 0) {
     s_err = INT_MAX;
     s_pad[0] = 0;
@@ -174,6 +189,12 @@ __global__ void __launch_bounds__(kPlanThreads) plan_kernel(PlanParams p) {
       eff[(B + 1) + b] = pq;
       eff[2 * (B + 1) + b] = ck;
       eff[3 * (B + 1) + b] = pk;
+    }
+    if (meta_in_smem) {
+      s_meta[b] = cq;
+      s_meta[(B + 1) + b] = pq;
+      s_meta[2 * (B + 1) + b] = ck;
+      s_meta[3 * (B + 1) + b] = pk;
     }
     if (b == 0 && (cq != 0 || pq != 0 || ck != 0 || pk != 0)) set_err(&s_err, THD_DEV_ERR_NONZERO_START);
     if (b < B) {
@@ -237,11 +258,14 @@ __global__ void __launch_bounds__(kPlanThreads) plan_kernel(PlanParams p) {
     }
   }
   if (p.mode == 0) return;
-  if (!plan_schedule(p, eff, p.mode == 3 ? 2 : p.mode, p.tile_off, p.counters, p.items, p.item_cap, s_warp, s_hist))
+  const int32_t* effr = meta_in_smem ? s_meta : eff;
+  if (!plan_schedule(p, effr, meta_in_smem ? s_meta + 4 * (B + 1) : p.tile_off, p.mode == 3 ? 2 : p.mode,
+                     p.tile_off, p.counters, p.items, p.item_cap, s_warp, s_hist))
     return;
   if (p.mode == 3) {
-    __syncthreads();  // s_hist is reused
-    plan_schedule(p, eff, 1, p.tile_off_q, p.counters_q, p.items_q, p.item_cap_q, s_warp, s_hist);
+    __syncthreads();  // s_hist and the staged tile offsets are reused
+    plan_schedule(p, effr, meta_in_smem ? s_meta + 4 * (B + 1) : p.tile_off_q, 1, p.tile_off_q, p.counters_q,
+                  p.items_q, p.item_cap_q, s_warp, s_hist);
   }
 }
 
@@ -344,8 +368,7 @@ cudaError_t launch_tail_zero(uint16_t* dq, uint16_t* dk, uint16_t* dv, int64_t d
 
 // ------------------------------------------------------------------ backward preprocess
 // Delta[h][t] = sum_d dO[t,h,d] * O[t,h,d] and lse2[h][t] = lse * log2(e) on
-// valid rows (0 elsewhere), read by both backward passes.  One warp per (t, h)
-// row.
+// valid rows (0 elsewhere), read by both backward passes.
 __device__ inline bool row_valid(const int32_t* eff, int B, int t) {
   const int32_t* cu = eff;
   const int32_t* pad = eff + (B + 1);
@@ -354,61 +377,105 @@ __device__ inline bool row_valid(const int32_t* eff, int B, int t) {
   return b < B && t - pad[b] < cu[b + 1] - cu[b];
 }
 
+// Sum of the eight bf16 x bf16 products of two 16-byte vectors, in fp32.
+__device__ inline float dot8_bf16(const uint4& a, const uint4& b) {
+  const uint32_t aw[4] = {a.x, a.y, a.z, a.w}, bw[4] = {b.x, b.y, b.z, b.w};
+  float acc = 0.f;
+#pragma unroll
+  for (int k = 0; k < 4; ++k) {
+    const float2 fa = __bfloat1622float2(*reinterpret_cast<const __nv_bfloat162*>(&aw[k]));
+    const float2 fb = __bfloat1622float2(*reinterpret_cast<const __nv_bfloat162*>(&bw[k]));
+    acc = fmaf(fa.x, fb.x, acc);
+    acc = fmaf(fa.y, fb.y, acc);
+  }
+  return acc;
+}
+
+// A CTA takes a tile of `tt` consecutive tokens with all Hq heads: those
+// rows are one contiguous block of O and of dO, read with 16-byte loads, D/8
+// lanes per row and kPrepBatch rows per thread in flight.  Delta is staged
+// in shared memory as [Hq][tt], so Delta, lse and lse2 move as tt contiguous
+// floats per head.
+constexpr int kPrepThreads = 256;
+constexpr int kPrepBatch = 4;
+constexpr int kPrepMaxTok = 16;
+
 template <int D>
-__global__ void __launch_bounds__(256) bwd_prep_kernel(const uint16_t* __restrict__ o,
-                                                       const uint16_t* __restrict__ dout,
-                                                       const float* __restrict__ lse, float* __restrict__ delta,
-                                                       float* __restrict__ lse2,
-                                                       const int32_t* __restrict__ eff, int B, int64_t T, int Hq,
-                                                       const int32_t* dev_status) {
+__global__ void __launch_bounds__(kPrepThreads) bwd_prep_kernel(const uint16_t* __restrict__ o,
+                                                                const uint16_t* __restrict__ dout,
+                                                                const float* __restrict__ lse,
+                                                                float* __restrict__ delta, float* __restrict__ lse2,
+                                                                const int32_t* __restrict__ eff, int B, int64_t T,
+                                                                int Hq, int tt, const int32_t* dev_status) {
+  extern __shared__ float s_delta[];  // [Hq][tt]
+  __shared__ int s_valid[kPrepMaxTok];
   if (*dev_status != 0) return;
-  constexpr int PER = D / 32;  // elements per lane (4 or 2)
-  const int lane = threadIdx.x & 31;
-  const int64_t nrows = T * Hq;
-  for (int64_t row = (blockIdx.x * (int64_t)blockDim.x + threadIdx.x) >> 5; row < nrows;
-       row += ((int64_t)gridDim.x * blockDim.x) >> 5) {
-    const int64_t t = row / Hq;
-    const int h = (int)(row - t * Hq);
-    float acc = 0.f;
-    const bool valid = row_valid(eff, B, (int)t);
-    if (valid) {
-      const uint16_t* po = o + row * D + lane * PER;
-      const uint16_t* pd = dout + row * D + lane * PER;
-      if (PER == 4) {
-        uint2 a = *reinterpret_cast<const uint2*>(po), b = *reinterpret_cast<const uint2*>(pd);
-        __nv_bfloat162 a0 = *reinterpret_cast<__nv_bfloat162*>(&a.x), a1 = *reinterpret_cast<__nv_bfloat162*>(&a.y);
-        __nv_bfloat162 b0 = *reinterpret_cast<__nv_bfloat162*>(&b.x), b1 = *reinterpret_cast<__nv_bfloat162*>(&b.y);
-        float2 fa0 = __bfloat1622float2(a0), fa1 = __bfloat1622float2(a1);
-        float2 fb0 = __bfloat1622float2(b0), fb1 = __bfloat1622float2(b1);
-        acc = fa0.x * fb0.x + fa0.y * fb0.y + fa1.x * fb1.x + fa1.y * fb1.y;
-      } else {
-        uint32_t a = *reinterpret_cast<const uint32_t*>(po), b = *reinterpret_cast<const uint32_t*>(pd);
-        float2 fa = __bfloat1622float2(*reinterpret_cast<__nv_bfloat162*>(&a));
-        float2 fb = __bfloat1622float2(*reinterpret_cast<__nv_bfloat162*>(&b));
-        acc = fa.x * fb.x + fa.y * fb.y;
+  constexpr int LPR = D / 8;                 // lanes per row
+  constexpr int G = kPrepThreads / LPR;      // rows per pass
+  const int tid = threadIdx.x, g = tid / LPR, j = tid % LPR;
+  const int64_t ntiles = (T + tt - 1) / tt;
+  for (int64_t tile = blockIdx.x; tile < ntiles; tile += gridDim.x) {
+    const int64_t t0 = tile * tt;
+    const int nt = (int)(T - t0 < tt ? T - t0 : tt);
+    if (tid < tt) s_valid[tid] = tid < nt && row_valid(eff, B, (int)(t0 + tid));
+    __syncthreads();
+    const int rows = nt * Hq;
+    const uint4* po = reinterpret_cast<const uint4*>(o + t0 * Hq * D) + j;
+    const uint4* pd = reinterpret_cast<const uint4*>(dout + t0 * Hq * D) + j;
+    for (int r0 = 0; r0 < rows; r0 += G * kPrepBatch) {
+      uint4 a[kPrepBatch], b[kPrepBatch];
+#pragma unroll
+      for (int u = 0; u < kPrepBatch; ++u) {
+        const int r = r0 + u * G + g;
+        a[u] = make_uint4(0, 0, 0, 0);
+        b[u] = a[u];
+        if (r < rows && s_valid[r / Hq]) {
+          a[u] = __ldg(po + (int64_t)r * LPR);
+          b[u] = __ldg(pd + (int64_t)r * LPR);
+        }
+      }
+#pragma unroll
+      for (int u = 0; u < kPrepBatch; ++u) {
+        float acc = dot8_bf16(a[u], b[u]);
+#pragma unroll
+        for (int off = LPR / 2; off > 0; off >>= 1) acc += __shfl_xor_sync(0xffffffffu, acc, off);
+        const int r = r0 + u * G + g;
+        if (j == 0 && r < rows) {
+          const int tl = r / Hq;
+          s_delta[(r - tl * Hq) * tt + tl] = acc;
+        }
       }
     }
-#pragma unroll
-    for (int off = 16; off > 0; off >>= 1) acc += __shfl_xor_sync(0xffffffffu, acc, off);
-    if (lane == 0) {
-      delta[(int64_t)h * T + t] = acc;
-      lse2[(int64_t)h * T + t] = valid ? lse[(int64_t)h * T + t] * 1.4426950408889634f : 0.f;
+    __syncthreads();
+    for (int i = tid; i < tt * Hq; i += kPrepThreads) {
+      const int h = i / tt, tl = i - h * tt;
+      if (tl < nt) {
+        const int64_t gi = (int64_t)h * T + t0 + tl;
+        delta[gi] = s_delta[i];
+        lse2[gi] = s_valid[tl] ? lse[gi] * 1.4426950408889634f : 0.f;
+      }
     }
+    __syncthreads();
   }
 }
 
 cudaError_t launch_bwd_prep(const uint16_t* o, const uint16_t* dout, const float* lse, float* delta, float* lse2,
                             const int32_t* eff, int B, int64_t T_q, int Hq, int D, const int32_t* dev_status,
                             cudaStream_t st) {
-  const int64_t warps = T_q * Hq;
-  if (warps == 0) return cudaSuccess;
-  const int64_t want = (warps + 7) / 8;
-  const int grid = (int)(want < 8LL * num_sms() ? want : 8LL * num_sms());
+  if (T_q == 0) return cudaSuccess;
+  // tokens per tile: at most kPrepMaxTok, and the [Hq][tt] stage within 48 KB
+  int tt = 12288 / Hq;
+  tt = tt < 1 ? 1 : (tt > kPrepMaxTok ? kPrepMaxTok : tt);
+  const size_t smem = sizeof(float) * (size_t)Hq * tt;
+  const int64_t ntiles = (T_q + tt - 1) / tt;
+  const int grid = (int)(ntiles < 8LL * num_sms() ? ntiles : 8LL * num_sms());
+  auto kern = D == 128 ? bwd_prep_kernel<128> : bwd_prep_kernel<64>;
+  if (smem > 48 * 1024) {
+    cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
+    if (e != cudaSuccess) return e;
+  }
   prof_before(THD_KERNEL_BWD_PREP, st);
-  if (D == 128)
-    bwd_prep_kernel<128><<<grid, 256, 0, st>>>(o, dout, lse, delta, lse2, eff, B, T_q, Hq, dev_status);
-  else
-    bwd_prep_kernel<64><<<grid, 256, 0, st>>>(o, dout, lse, delta, lse2, eff, B, T_q, Hq, dev_status);
+  kern<<<grid, kPrepThreads, smem, st>>>(o, dout, lse, delta, lse2, eff, B, T_q, Hq, tt, dev_status);
   count_launch();
   cudaError_t e = cudaGetLastError();
   prof_after(THD_KERNEL_BWD_PREP, st);
