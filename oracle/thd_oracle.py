@@ -38,6 +38,7 @@ this module takes the plainest reading (each one is listed in the design doc):
   ``s = (r - i) mod CP``.
 
 Parity pins: every function here is checked in ``tests/test_oracle_pins.py``
+(the Ulysses/A2A and hierarchical functions in ``tests/test_oracle_a2a_pins.py``)
 against brute force, closed forms, library special cases (torch SDPA in
 fp64 on the CPU) and invariants.  No function is "parity unpinned".
 """
@@ -492,6 +493,143 @@ def cp_ring_fwd(q, k, v, cu_seqlens, cu_seqlens_padded, cp_size: int, causal: bo
     if return_partials:
         return O, lse, partials
     return O, lse
+
+
+# ---------------------------------------------------------------------------
+# next: Ulysses (A2A) and hierarchical a2a+p2p decompositions, emulated
+# ---------------------------------------------------------------------------
+
+def hierarchical_cp_sizes(sizes, cp_size: int) -> tuple[int, int]:
+    """The two levels of a hierarchical CP layer, (a2a group size, p2p group size).
+
+    [P3, the ``hierarchical_context_parallel_sizes`` docstring: the first value
+    is the a2a group size, the second the p2p group size] and [P3
+    "Contraintes requises" / "Pitfalls" item 6: their product must equal the
+    CP size, else an assertion].
+    """
+    s = [int(x) for x in sizes]
+    if len(s) != 2 or min(s) < 1:
+        raise ValueError("hierarchical CP takes two sizes, a2a then p2p")
+    if s[0] * s[1] != int(cp_size):
+        raise ValueError("prod(hierarchical sizes) != cp_size")
+    return s[0], s[1]
+
+
+def _a2a_shape_check(H: int, cp: int, a2a: int) -> int:
+    if cp < 1 or a2a < 1 or cp % a2a != 0:
+        raise ValueError("the a2a group size must divide cp_size")
+    if H % a2a != 0:
+        raise ValueError("heads must divide evenly over the a2a group")
+    return H // a2a
+
+
+def a2a_seq_to_head(x_shards, cu_seqlens_padded, cp_size: int, a2a_size: int) -> np.ndarray:
+    """The all-to-all in front of attention: scatter heads, gather the sequence.
+
+    [P1, the maintainer's reply]: A2A (Ulysses) context parallelism, which
+    THD lacked; [P3]: hierarchical CP runs that A2A inside groups of
+    ``a2a_size`` ranks and the P2P ring across the groups.  Readings (the
+    pages print no layout):
+
+    * Before the A2A, CP rank r holds its THD shard ``x_shards[r]``
+      (``[T/cp, H, ...]``): rank-local rows in ``cp_partition``'s token_map
+      order, chunk r then chunk ``2cp-1-r`` of every sequence.
+    * Groups are runs of consecutive ranks: rank ``j*a2a + i`` is member i of
+      group j.  Member i receives query/key/value heads
+      ``[i*H/a2a, (i+1)*H/a2a)`` of every token its group holds, placed at the
+      token's global padded row.  With ``a2a_size == cp_size`` (pure Ulysses)
+      there is one group that holds every token.
+    * Emulated on one host, member i's buffers of all groups form one tensor in
+      global order, so the result is ``y[i, g] = x[r, l, i*Hg:(i+1)*Hg]`` for
+      every (r, l) with ``token_map[r, l] == g``; ``y`` is
+      ``[a2a, T, H/a2a, ...]``.
+    """
+    x = np.asarray(x_shards)
+    cp, rows_r, H = x.shape[0], x.shape[1], x.shape[2]
+    a = int(a2a_size)
+    if cp != int(cp_size):
+        raise ValueError("x_shards must hold cp_size shards")
+    Hg = _a2a_shape_check(H, cp, a)
+    pad = _as_int_list(cu_seqlens_padded)
+    T = pad[-1]
+    if rows_r * cp != T:
+        raise ValueError("each shard holds T/cp rows")
+    tmap = cp_partition(pad, pad, cp)["token_map"]
+    y = np.zeros((a, T, Hg) + x.shape[3:], x.dtype)
+    for r in range(cp):
+        for l in range(rows_r):
+            g = int(tmap[r, l])
+            for i in range(a):
+                y[i, g] = x[r, l, i * Hg:(i + 1) * Hg]
+    return y
+
+
+def a2a_head_to_seq(y, cu_seqlens_padded, cp_size: int, a2a_size: int) -> np.ndarray:
+    """The all-to-all behind attention, the inverse of ``a2a_seq_to_head``:
+    ``x[r, l, i*Hg:(i+1)*Hg] = y[i, token_map[r, l]]``; ``x`` is
+    ``[cp, T/cp, H, ...]``."""
+    y = np.asarray(y)
+    a, T, Hg = y.shape[0], y.shape[1], y.shape[2]
+    cp = int(cp_size)
+    if a != int(a2a_size):
+        raise ValueError("y must hold a2a_size head groups")
+    _a2a_shape_check(a * Hg, cp, a)
+    pad = _as_int_list(cu_seqlens_padded)
+    if pad[-1] != T or T % cp != 0:
+        raise ValueError("y must hold the T padded rows")
+    tmap = cp_partition(pad, pad, cp)["token_map"]
+    x = np.zeros((cp, T // cp, a * Hg) + y.shape[3:], y.dtype)
+    for r in range(cp):
+        for l in range(T // cp):
+            g = int(tmap[r, l])
+            for i in range(a):
+                x[r, l, i * Hg:(i + 1) * Hg] = y[i, g]
+    return x
+
+
+def cp_a2a_attn_fwd(q_shards, k_shards, v_shards, cu_seqlens, cu_seqlens_padded, cp_size: int, a2a_size: int,
+                    softmax_scale: float | None = None):
+    """Causal attention through the emulated A2A (``a2a_size == cp_size``) or
+    hierarchical a2a+p2p (``p2p = cp_size / a2a_size``) decomposition.
+
+    1. ``a2a_seq_to_head`` of q, k and v (GQA: the KV heads split the same way);
+    2. member i of every group runs the P2P ring of ``p2p`` ranks over its
+       heads (``cp_ring_fwd``, which for ``p2p == 1`` is plain causal
+       attention on the whole sequence);
+    3. ``a2a_head_to_seq`` of the output.
+
+    Returns the output shards ``[cp, T/cp, Hq, D]`` and lse ``[Hq, T]`` in
+    global row order (the members' heads stacked are the global heads).
+    """
+    cp, a = int(cp_size), int(a2a_size)
+    p2p = cp // a
+    qh = a2a_seq_to_head(_f64(q_shards), cu_seqlens_padded, cp, a)
+    kh = a2a_seq_to_head(_f64(k_shards), cu_seqlens_padded, cp, a)
+    vh = a2a_seq_to_head(_f64(v_shards), cu_seqlens_padded, cp, a)
+    Hg, T = qh.shape[2], qh.shape[1]
+    oh = np.zeros_like(qh)
+    lse = np.full((a * Hg, T), NEG_INF)
+    for i in range(a):
+        oh[i], lse[i * Hg:(i + 1) * Hg] = cp_ring_fwd(qh[i], kh[i], vh[i], cu_seqlens, cu_seqlens_padded, p2p,
+                                                      softmax_scale=softmax_scale)
+    return a2a_head_to_seq(oh, cu_seqlens_padded, cp, a), lse
+
+
+def cp_a2a_attn_bwd(q_shards, k_shards, v_shards, do_shards, cu_seqlens, cu_seqlens_padded, cp_size: int,
+                    a2a_size: int, causal: bool = True, softmax_scale: float | None = None):
+    """Gradients through the same decomposition: dO goes through
+    ``a2a_seq_to_head`` with q, k, v; member i's gradients are those of its
+    heads' attention (``attn_bwd``); dQ, dK, dV come back through
+    ``a2a_head_to_seq``.  Returns the three gradient shard arrays."""
+    cp, a = int(cp_size), int(a2a_size)
+    pad = cu_seqlens_padded
+    qh, kh, vh, doh = (a2a_seq_to_head(_f64(x), pad, cp, a) for x in (q_shards, k_shards, v_shards, do_shards))
+    dqh, dkh, dvh = np.zeros_like(qh), np.zeros_like(kh), np.zeros_like(vh)
+    T = qh.shape[1]
+    for i in range(a):
+        dqh[i], dkh[i], dvh[i] = attn_bwd(qh[i], kh[i], vh[i], doh[i], cu_seqlens, cu_seqlens, pad, pad,
+                                          causal=causal, softmax_scale=softmax_scale, dq_rows=T, dkv_rows=T)
+    return tuple(a2a_head_to_seq(g, pad, cp, a) for g in (dqh, dkh, dvh))
 
 
 # ---------------------------------------------------------------------------
