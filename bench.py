@@ -11,6 +11,8 @@ events.  Each step is timed with CUDA events on the launching stream.
 
     python bench.py [--gpus N] [--steps K] [--warmup W] [--config packed]
     python bench.py --impl reference ...   # the CPU fp64 oracle on host cores
+    python bench.py --a2a 4 ...            # the same step through the emulated Ulysses layer (cp 4);
+                                           # --a2a 2: hierarchical a2a+p2p sizes [2, 2]
 
 Under torchrun each rank runs its own replica of the workload (weak scaling,
 no collective on the data path); rank 0 prints one JSON line.
@@ -44,6 +46,9 @@ def _args():
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--no-e2e", action="store_true")
     ap.add_argument("--fwd-only", action="store_true", help="time the forward alone as the step")
+    ap.add_argument("--a2a", type=int, default=0,
+                    help="a2a group size: time the step through the emulated Ulysses (a2a = cp) or hierarchical "
+                         "a2a+p2p layer (thd_attn_fwd_a2a / thd_attn_bwd_a2a on per-rank shards)")
     return ap.parse_args()
 
 
@@ -402,6 +407,107 @@ def run_ours(a):
     return 0
 
 
+def run_a2a(a):
+    """The fwd+bwd step through the emulated A2A / hierarchical layer: inputs
+    and outputs are per-rank shards; the layout moves (a2a_kernel) run inside
+    the step.  One GPU; prints one JSON line with the step's TFLOPS and the
+    moves' HBM roofline."""
+    import torch
+
+    from packed_sequence_context_gb300 import inputs
+    from packed_sequence_context_gb300 import thd_attn as T
+
+    if int(os.environ.get("WORLD_SIZE", "1")) > 1:
+        raise SystemExit("--a2a runs on one GPU")
+    if not torch.cuda.is_available():
+        raise SystemExit("bench.py needs a CUDA GPU")
+    T.lib()
+    peak, _, hbm, _ = _peaks()
+    w = inputs.make_workload(a.config)
+    t = inputs.make_tensors(w, with_grad=True)
+    dev = torch.device("cuda", 0)
+    cp, A = w.cp_size, a.a2a
+    B, Tn, Hq, Hkv, D = w.B, w.T, w.Hq, w.Hkv, w.D
+    cu = torch.from_numpy(w.cu_seqlens).to(dev)
+    cup = torch.from_numpy(w.cu_seqlens_padded).to(dev)
+    # per-rank shards of the synthetic tensors, made with the library's own move
+    # (with a2a 1 the single member's layout is the global tensor)
+    sh = {}
+    for x in ("q", "k", "v", "do"):
+        sh[x], st0 = T.cp_a2a(t[x].to(dev)[None], cup, cp_size=cp, a2a_size=1, direction=T.THD_A2A_TO_SHARDS)
+        T.check_status(st0)
+    o = torch.empty_like(sh["q"])
+    lse = torch.empty((Hq, Tn), dtype=torch.float32, device=dev)
+    dq, dk, dv = torch.empty_like(sh["q"]), torch.empty_like(sh["k"]), torch.empty_like(sh["v"])
+    st = torch.zeros(1, dtype=torch.int32, device=dev)
+    wsf = torch.empty(T.thd_a2a_workspace_size(B, Tn, Hq, Hkv, D, cp, A, 0), dtype=torch.uint8, device=dev)
+    wsb = torch.empty(T.thd_a2a_workspace_size(B, Tn, Hq, Hkv, D, cp, A, 1), dtype=torch.uint8, device=dev)
+    flush_buf = torch.empty(256 << 20, dtype=torch.uint8, device=dev)
+    stream = torch.cuda.current_stream()
+    sptr = stream.cuda_stream
+
+    def fwd():
+        assert T.thd_attn_fwd_a2a(sh["q"], sh["k"], sh["v"], o, lse, cu, cup, B, Tn, Hq, Hkv, D, 1, w.softmax_scale,
+                                  cp, A, wsf, wsf.numel(), st, sptr) == 0
+
+    def step():
+        fwd()
+        assert T.thd_attn_bwd_a2a(sh["q"], sh["k"], sh["v"], o, lse, sh["do"], dq, dk, dv, cu, cup, B, Tn, Hq, Hkv,
+                                  D, 1, w.softmax_scale, cp, A, wsb, wsb.numel(), st, sptr) == 0
+
+    def timed(fn, n, kernel_id=0, per_step=0):
+        evs = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)) for _ in range(n)]
+        T.thd_profile_enable(kernel_id, n * per_step)
+        n0 = T.thd_launch_count()
+        torch.cuda.synchronize()
+        for e0, e1 in evs:
+            flush_buf.zero_()
+            e0.record(stream)
+            fn()
+            e1.record(stream)
+        torch.cuda.synchronize()
+        launches = T.thd_launch_count() - n0
+        kms = T.thd_profile_read(n * per_step) if kernel_id else []
+        T.thd_profile_enable(0, 0)
+        return [e0.elapsed_time(e1) for e0, e1 in evs], kms, launches
+
+    fwd_flops, both_flops = inputs.algorithmic_flops(w.lengths, Hq, D)
+    for _ in range(max(a.warmup, 3)):
+        flush_buf.zero_()
+        step()
+    torch.cuda.synchronize()
+    T.check_status(st)
+    with ClockSampler(0) as clk:
+        times, kms, launches = timed(step, a.steps, T.THD_KERNEL_A2A, 4)
+        fwd_times, _, _ = timed(fwd, a.steps)
+    T.check_status(st)
+    ms = sum(times) / len(times)
+    fwd_ms = sum(fwd_times) / len(fwd_times)
+    # every element of the moved tensors is read once and written once: forward q, k, v in and O out;
+    # backward q, k, v, O, dO in and dQ, dK, dV out
+    elems = Tn * D * (6 * Hq + 6 * Hkv)
+    move_bytes = 2 * 2 * elems
+    move_ms = sum(kms) / a.steps
+    gbs = move_bytes / (move_ms * 1e-3) / 1e9
+    mode = "a2a" if A == cp else ("p2p" if A == 1 else "a2a+p2p")
+    line = {
+        "metric": METRIC, "value": both_flops / (ms * 1e-3) / 1e12, "unit": UNIT, "n_gpus": 1, "steps": a.steps,
+        "warmup": a.warmup, "ms_per_step": ms, "higher_is_better": True, "scaling": "weak", "vs_baseline": None,
+        "dtype": "bf16", "data": "synthetic",
+        "config": {"workload": w.name, "sequences": B, "tokens": Tn, "Hq": Hq, "Hkv": Hkv, "D": D, "cp_size": cp,
+                   "cp_comm": mode, "hierarchical_sizes": [A, cp // A], "causal": True, "step": "fwd+bwd",
+                   "inputs": "per-rank shards", "l2": "flushed between timed steps (256 MiB write)"},
+        "fwd_tflops": fwd_flops / (fwd_ms * 1e-3) / 1e12, "fwd_ms": fwd_ms,
+        "a2a_roofline": {"bound": "hbm", "kernel": "a2a_kernel", "achieved": gbs, "peak": hbm, "unit": "GB/s",
+                         "frac": gbs / hbm, "ms_per_step": move_ms, "share_of_step": move_ms / ms,
+                         "bytes_per_step": move_bytes, "launches_per_step": 4, "traffic": None},
+        "gpu_launches": launches,
+        "clocks": clk.summary(),
+    }
+    print(json.dumps(line), flush=True)
+    return 0
+
+
 def e2e_measure(a, w, t, dev, stream, step_flops):
     """Same metric through the public API with host buffers: pinned H2D of the
     step's inputs and metadata, the calls, and D2H of O, lse, dQ, dK, dV."""
@@ -455,6 +561,8 @@ def main():
     a.config = CONFIG_ALIASES.get(a.config, a.config)
     if a.impl == "reference":
         return run_reference(a)
+    if a.a2a:
+        return run_a2a(a)
     return run_ours(a)
 
 

@@ -90,6 +90,11 @@ typedef struct CUstream_st* thd_stream_t; /* identical to cudaStream_t */
 #define THD_KERNEL_LSE_MERGE 6
 #define THD_KERNEL_TAIL_ZERO 7
 #define THD_KERNEL_PARTITION 8
+#define THD_KERNEL_A2A 9
+
+/* thd_cp_a2a directions */
+#define THD_A2A_TO_GROUPS 0 /* shards -> per-member head groups (the all-to-all in front of attention) */
+#define THD_A2A_TO_SHARDS 1 /* per-member head groups -> shards (the all-to-all behind it) */
 
 /* Human-readable text for any status above (host or device). Never NULL. */
 THD_API const char* thd_status_string(int status);
@@ -263,6 +268,83 @@ THD_API int thd_lse_merge(float* o_acc, float* lse_acc, const float* o_part, con
 THD_API int thd_grad_tail_zero(void* dq, void* dk, void* dv, int64_t dq_rows, int64_t dkv_rows, int Hq, int Hkv, int D,
                        const int32_t* cu_seqlens_q_padded, const int32_t* cu_seqlens_kv_padded, int B,
                        int host_knows_no_tail, thd_stream_t stream);
+
+/*
+ * ---- Ulysses (A2A) and hierarchical a2a+p2p context parallelism, emulated ----
+ *
+ * [P1, the maintainer's reply]: A2A (Ulysses) exchanges heads for sequence
+ * and THD had no A2A path; [P3]: hierarchical CP runs A2A inside groups of
+ * a2a_size ranks and the P2P ring across cp_size / a2a_size groups, with
+ * prod(sizes) == cp_size.  Layouts (the pages print none; plainest reading):
+ *   shards [cp_size][T/cp_size, H, D] bf16: CP rank r's THD shard, its rows
+ *     in load-balanced order -- chunk r then chunk 2cp-1-r of every sequence,
+ *     chunk = P_b / (2 cp_size) rows -- the rows thd_cp_partition's token map
+ *     lists for rank r;
+ *   groups [a2a_size][T, H/a2a_size, D] bf16: member i of the A2A groups
+ *     holds heads [i H/a2a, (i+1) H/a2a) of every token at its global padded
+ *     row.  Groups are runs of a2a_size consecutive ranks, so group j holds
+ *     exactly p2p rank j's rows of the 2 * (cp/a2a) split.
+ * a2a_size == cp_size is pure Ulysses; a2a_size == 1 is the plain P2P ring.
+ * T is the global row count (shard stride T/cp_size rows, T % cp_size == 0);
+ * rows past cu_seqlens_padded[B] are not moved.
+ */
+
+/*
+ * thd_cp_a2a -- move one tensor between the two layouts, every rank and
+ * group in one launch.  direction THD_A2A_TO_GROUPS reads shards from src
+ * and writes groups to dst; THD_A2A_TO_SHARDS the reverse.
+ *   src, dst: device bf16, 16-byte aligned, not overlapping.
+ *   cu_seqlens_padded: device int32 [B+1]; checked on the device (starts at
+ *     0, monotone, every P_b divisible by 2*cp_size, pad[B] <= T), else a
+ *     THD_DEV_ERR_* code in *dev_status and nothing written.
+ *   H % a2a_size == 0, cp_size % a2a_size == 0, D a multiple of 8.
+ * Bit-exact (a permutation of rows).  Launches: the planner (checks only)
+ * and the copy kernel.
+ */
+THD_API int thd_cp_a2a(const void* src, void* dst, const int32_t* cu_seqlens_padded, int B, int64_t T, int H, int D,
+                       int cp_size, int a2a_size, int direction, int32_t* dev_status, thd_stream_t stream);
+
+/*
+ * Bytes of workspace thd_attn_fwd_a2a (for_bwd = 0) or thd_attn_bwd_a2a
+ * (for_bwd = 1) needs: the group-layout copies of the tensors plus the
+ * attention workspace of one member.  Returns 0 for unsupported sizes.
+ */
+THD_API size_t thd_a2a_workspace_size(int B, int64_t T, int Hq, int Hkv, int D, int cp_size, int a2a_size,
+                                      int for_bwd);
+
+/*
+ * thd_attn_fwd_a2a -- attention through the emulated A2A / hierarchical
+ * decomposition: q, k, v shards -> groups (one launch); member i runs the
+ * fused P2P ring of p2p = cp_size / a2a_size ranks over its heads (the
+ * thd_attn_fwd path with cp_size = p2p); O groups -> shards.  Equal to
+ * unsplit attention (tested).
+ *   q [cp][T/cp, Hq, D], k, v [cp][T/cp, Hkv, D], o [cp][T/cp, Hq, D]: shards.
+ *   lse: fp32 [Hq, T] in global row order (members' heads stacked).
+ *   cu_seqlens, cu_seqlens_padded: device int32 [B+1], self-attention (the
+ *     same for q and kv); the padded offsets define the shards.
+ *   Hq, Hkv divisible by a2a_size; D 64 or 128.
+ * Launches: 3 + 2 * a2a_size.  Workspace: thd_a2a_workspace_size(.., 0).
+ */
+THD_API int thd_attn_fwd_a2a(const void* q, const void* k, const void* v, void* o, float* lse,
+                             const int32_t* cu_seqlens, const int32_t* cu_seqlens_padded, int B, int64_t T, int Hq,
+                             int Hkv, int D, int causal, float softmax_scale, int cp_size, int a2a_size,
+                             void* workspace, size_t workspace_bytes, int32_t* dev_status, thd_stream_t stream);
+
+/*
+ * thd_attn_bwd_a2a -- gradients through the same decomposition: q, k, v, o,
+ * dO shards -> groups (one launch); member i runs the thd_attn_bwd path with
+ * cp_size = p2p over its heads; dQ, dK, dV groups -> shards (one launch).
+ *   Shards as in thd_attn_fwd_a2a; lse [Hq, T] as it returns it; dq
+ *   [cp][T/cp, Hq, D], dk, dv [cp][T/cp, Hkv, D].  Rows of each shard past
+ *   cu_seqlens_padded[B] / cp_size are not written.
+ * Launches: 3 + 4 * a2a_size.  Workspace: thd_a2a_workspace_size(.., 1).
+ * Bit-reproducible.
+ */
+THD_API int thd_attn_bwd_a2a(const void* q, const void* k, const void* v, const void* o, const float* lse,
+                             const void* dout, void* dq, void* dk, void* dv, const int32_t* cu_seqlens,
+                             const int32_t* cu_seqlens_padded, int B, int64_t T, int Hq, int Hkv, int D, int causal,
+                             float softmax_scale, int cp_size, int a2a_size, void* workspace, size_t workspace_bytes,
+                             int32_t* dev_status, thd_stream_t stream);
 
 /*
  * Profiling hook (not needed for normal use): while enabled for `kernel_id`

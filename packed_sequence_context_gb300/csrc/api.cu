@@ -9,6 +9,7 @@
 
 #include <cudaTypedefs.h>
 
+#include "a2a.cuh"
 #include "common.cuh"
 
 namespace thd {
@@ -81,8 +82,6 @@ static bool make_thd_map(CUtensorMap* m, const void* base, int64_t rows, int H, 
              CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
 }
 
-// 3-D map over the fp32 dQ accumulator [rows, H, D]; box = 32 rows x 1 head
-// x 32 columns (128 bytes, the 128B-swizzle width), used for reduce-add.
 static bool aligned(const void* p, uintptr_t a) { return (reinterpret_cast<uintptr_t>(p) & (a - 1)) == 0; }
 
 static int check_sizes(int B, int64_t T_q, int64_t T_kv, int Hq, int Hkv, int D, int cp, int pad_mode) {
@@ -174,6 +173,81 @@ static int fwd_common(const void* q, const void* k, const void* v, void* o, floa
   const int64_t bound = (int64_t)L.item_cap * Hq;
   const int grid = (int)(bound < num_sms() ? (bound > 0 ? bound : 1) : num_sms());
   return cuda_status(launch_fwd(fp, tk, tv, D, step >= 0, grid, st));
+}
+
+// ------------------------------------------------------------------ A2A / hierarchical
+// Sizes the emulated A2A layer accepts (see thd_cp_a2a in the header).
+static int check_a2a_sizes(int B, int64_t T, int H, int D, int cp, int a2a) {
+  if (B < 1 || B >= (1 << 24) || T < 0 || T >= ((int64_t)1 << 31) || H < 1 || D < 8 || D % 8 != 0)
+    return THD_ERR_INVALID_ARG;
+  if (cp < 1 || cp > 1024 || a2a < 1 || cp % a2a != 0 || H % a2a != 0 || T % cp != 0) return THD_ERR_INVALID_ARG;
+  return THD_OK;
+}
+
+// Device-side checks of the padded offsets (the planner's validation alone):
+// starts at 0, monotone, every P_b divisible by 2 cp, pad[B] <= T.  `cu` may
+// be the valid-length offsets (also checked against the padded ones) or the
+// padded offsets themselves.
+static cudaError_t launch_a2a_checks(const int32_t* cu, const int32_t* pad, int B, int64_t T, int cp,
+                                     int32_t* dev_status, cudaStream_t st) {
+  PlanParams p;
+  std::memset(&p, 0, sizeof(p));
+  p.cu_q = cu;
+  p.cu_kv = cu;
+  p.pad_q = pad;
+  p.pad_kv = pad;
+  p.B = B;
+  p.cp = cp;
+  p.pad_mode = 1;
+  p.rows_q = T;
+  p.rows_kv = T;
+  p.mode = 0;
+  p.dev_status = dev_status;
+  return launch_plan(p, st);
+}
+
+// Workspace of the composites: group-layout copies of the tensors, then one
+// member's attention workspace.
+struct A2aWs {
+  size_t buf[8];  // q k v o (forward) + dO dQ dK dV (backward)
+  size_t attn = 0;
+  size_t total = 0;
+};
+
+static A2aWs a2a_ws_layout(int B, int64_t T, int Hq, int Hkv, int D, int cp, int a2a, bool bwd) {
+  A2aWs w;
+  size_t off = 0;
+  const size_t bq = sizeof(uint16_t) * (size_t)T * Hq * D, bkv = sizeof(uint16_t) * (size_t)T * Hkv * D;
+  const size_t sizes[8] = {bq, bkv, bkv, bq, bq, bq, bkv, bkv};
+  const int n = bwd ? 8 : 4;
+  for (int i = 0; i < 8; ++i) {
+    w.buf[i] = off;
+    if (i < n) off = align_up(off + sizes[i], 256);
+  }
+  w.attn = off;
+  w.total = off + ws_layout(B, T, T, Hq / a2a, D, cp / a2a, bwd).total;
+  return w;
+}
+
+static A2aJob a2a_job(const void* shard, void* groups, int H, int a2a) {
+  A2aJob j;
+  j.shard = const_cast<void*>(shard);
+  j.groups = groups;
+  j.Hg = H / a2a;
+  return j;
+}
+
+static A2aParams a2a_params(const int32_t* pad, int B, int64_t T, int D, int cp, int a2a, const int32_t* dev_status) {
+  A2aParams p;
+  std::memset(&p, 0, sizeof(p));
+  p.pad = pad;
+  p.dev_status = dev_status;
+  p.B = B;
+  p.cp = cp;
+  p.a2a = a2a;
+  p.D = D;
+  p.T = T;
+  return p;
 }
 
 }  // namespace thd
@@ -373,6 +447,124 @@ int thd_grad_tail_zero(void* dq, void* dk, void* dv, int64_t dq_rows, int64_t dk
                                       cu_seqlens_q_padded ? cu_seqlens_q_padded + B : nullptr,
                                       cu_seqlens_kv_padded ? cu_seqlens_kv_padded + B : nullptr, nullptr,
                                       reinterpret_cast<cudaStream_t>(stream)));
+}
+
+int thd_cp_a2a(const void* src, void* dst, const int32_t* cu_seqlens_padded, int B, int64_t T, int H, int D,
+               int cp_size, int a2a_size, int direction, int32_t* dev_status, thd_stream_t stream) {
+  cudaStream_t st = reinterpret_cast<cudaStream_t>(stream);
+  int rc = check_a2a_sizes(B, T, H, D, cp_size, a2a_size);
+  if (rc) return rc;
+  if (!src || !dst || !cu_seqlens_padded || !dev_status || !aligned(src, 16) || !aligned(dst, 16))
+    return THD_ERR_INVALID_ARG;
+  if (direction != THD_A2A_TO_GROUPS && direction != THD_A2A_TO_SHARDS) return THD_ERR_INVALID_ARG;
+  rc = cuda_status(launch_a2a_checks(cu_seqlens_padded, cu_seqlens_padded, B, T, cp_size, dev_status, st));
+  if (rc) return rc;
+  A2aParams p = a2a_params(cu_seqlens_padded, B, T, D, cp_size, a2a_size, dev_status);
+  const bool to_groups = direction == THD_A2A_TO_GROUPS;
+  p.job[0] = to_groups ? a2a_job(src, dst, H, a2a_size) : a2a_job(dst, const_cast<void*>(src), H, a2a_size);
+  p.njobs = 1;
+  return cuda_status(launch_a2a(p, to_groups, st));
+}
+
+size_t thd_a2a_workspace_size(int B, int64_t T, int Hq, int Hkv, int D, int cp_size, int a2a_size, int for_bwd) {
+  if (check_a2a_sizes(B, T, Hq, D, cp_size, a2a_size) != THD_OK || Hkv < 1 || Hkv % a2a_size != 0) return 0;
+  if (check_sizes(B, T, T, Hq / a2a_size, Hkv / a2a_size, D, cp_size / a2a_size, -1) != THD_OK) return 0;
+  return a2a_ws_layout(B, T, Hq, Hkv, D, cp_size, a2a_size, for_bwd != 0).total;
+}
+
+// Shared checks of the two composites; returns the layout through `L`.
+static int a2a_composite_checks(const int32_t* cu, const int32_t* pad, int B, int64_t T, int Hq, int Hkv, int D,
+                                int causal, float scale, int cp, int a2a, void* ws, size_t ws_bytes,
+                                const int32_t* dev_status, bool bwd, A2aWs& L) {
+  int rc = check_a2a_sizes(B, T, Hq, D, cp, a2a);
+  if (rc) return rc;
+  if (Hkv < 1 || Hkv % a2a != 0) return THD_ERR_INVALID_ARG;
+  rc = check_sizes(B, T, T, Hq / a2a, Hkv / a2a, D, cp / a2a, -1);
+  if (rc) return rc;
+  if (!cu || !pad || !dev_status) return THD_ERR_INVALID_ARG;
+  if (!(scale > 0.f) || !std::isfinite(scale) || (causal != 0 && causal != 1)) return THD_ERR_INVALID_ARG;
+  L = a2a_ws_layout(B, T, Hq, Hkv, D, cp, a2a, bwd);
+  return check_ws(ws, ws_bytes, L.total);
+}
+
+int thd_attn_fwd_a2a(const void* q, const void* k, const void* v, void* o, float* lse, const int32_t* cu_seqlens,
+                     const int32_t* cu_seqlens_padded, int B, int64_t T, int Hq, int Hkv, int D, int causal,
+                     float softmax_scale, int cp_size, int a2a_size, void* workspace, size_t workspace_bytes,
+                     int32_t* dev_status, thd_stream_t stream) {
+  cudaStream_t st = reinterpret_cast<cudaStream_t>(stream);
+  A2aWs L;
+  int rc = a2a_composite_checks(cu_seqlens, cu_seqlens_padded, B, T, Hq, Hkv, D, causal, softmax_scale, cp_size,
+                                a2a_size, workspace, workspace_bytes, dev_status, false, L);
+  if (rc) return rc;
+  if (!q || !k || !v || !o || !lse || !aligned(q, 16) || !aligned(k, 16) || !aligned(v, 16) || !aligned(o, 16) ||
+      !aligned(lse, 4))
+    return THD_ERR_INVALID_ARG;
+  char* w = static_cast<char*>(workspace);
+  const int a = a2a_size, p2p = cp_size / a2a_size, Hgq = Hq / a, Hgkv = Hkv / a;
+  rc = cuda_status(launch_a2a_checks(cu_seqlens, cu_seqlens_padded, B, T, cp_size, dev_status, st));
+  if (rc) return rc;
+  A2aParams in = a2a_params(cu_seqlens_padded, B, T, D, cp_size, a, dev_status);
+  in.job[0] = a2a_job(q, w + L.buf[0], Hq, a);
+  in.job[1] = a2a_job(k, w + L.buf[1], Hkv, a);
+  in.job[2] = a2a_job(v, w + L.buf[2], Hkv, a);
+  in.njobs = 3;
+  rc = cuda_status(launch_a2a(in, true, st));
+  if (rc) return rc;
+  const size_t gq = sizeof(uint16_t) * (size_t)T * Hgq * D, gkv = sizeof(uint16_t) * (size_t)T * Hgkv * D;
+  for (int i = 0; i < a; ++i) {
+    rc = fwd_common(w + L.buf[0] + i * gq, w + L.buf[1] + i * gkv, w + L.buf[2] + i * gkv, w + L.buf[3] + i * gq,
+                    lse + (size_t)i * Hgq * T, cu_seqlens, cu_seqlens, cu_seqlens_padded, cu_seqlens_padded, B, T, T,
+                    Hgq, Hgkv, D, causal, softmax_scale, p2p, -1, -1, w + L.attn, workspace_bytes - L.attn,
+                    dev_status, st);
+    if (rc) return rc;
+  }
+  A2aParams out = a2a_params(cu_seqlens_padded, B, T, D, cp_size, a, dev_status);
+  out.job[0] = a2a_job(o, w + L.buf[3], Hq, a);
+  out.njobs = 1;
+  return cuda_status(launch_a2a(out, false, st));
+}
+
+int thd_attn_bwd_a2a(const void* q, const void* k, const void* v, const void* o, const float* lse, const void* dout,
+                     void* dq, void* dk, void* dv, const int32_t* cu_seqlens, const int32_t* cu_seqlens_padded, int B,
+                     int64_t T, int Hq, int Hkv, int D, int causal, float softmax_scale, int cp_size, int a2a_size,
+                     void* workspace, size_t workspace_bytes, int32_t* dev_status, thd_stream_t stream) {
+  cudaStream_t st = reinterpret_cast<cudaStream_t>(stream);
+  A2aWs L;
+  int rc = a2a_composite_checks(cu_seqlens, cu_seqlens_padded, B, T, Hq, Hkv, D, causal, softmax_scale, cp_size,
+                                a2a_size, workspace, workspace_bytes, dev_status, true, L);
+  if (rc) return rc;
+  if (!q || !k || !v || !o || !lse || !dout || !dq || !dk || !dv) return THD_ERR_INVALID_ARG;
+  if (!aligned(q, 16) || !aligned(k, 16) || !aligned(v, 16) || !aligned(o, 16) || !aligned(dout, 16) ||
+      !aligned(dq, 16) || !aligned(dk, 16) || !aligned(dv, 16) || !aligned(lse, 4))
+    return THD_ERR_INVALID_ARG;
+  char* w = static_cast<char*>(workspace);
+  const int a = a2a_size, p2p = cp_size / a2a_size, Hgq = Hq / a, Hgkv = Hkv / a;
+  rc = cuda_status(launch_a2a_checks(cu_seqlens, cu_seqlens_padded, B, T, cp_size, dev_status, st));
+  if (rc) return rc;
+  A2aParams in = a2a_params(cu_seqlens_padded, B, T, D, cp_size, a, dev_status);
+  in.job[0] = a2a_job(q, w + L.buf[0], Hq, a);
+  in.job[1] = a2a_job(k, w + L.buf[1], Hkv, a);
+  in.job[2] = a2a_job(v, w + L.buf[2], Hkv, a);
+  in.job[3] = a2a_job(o, w + L.buf[3], Hq, a);
+  in.job[4] = a2a_job(dout, w + L.buf[4], Hq, a);
+  in.njobs = 5;
+  rc = cuda_status(launch_a2a(in, true, st));
+  if (rc) return rc;
+  const size_t gq = sizeof(uint16_t) * (size_t)T * Hgq * D, gkv = sizeof(uint16_t) * (size_t)T * Hgkv * D;
+  for (int i = 0; i < a; ++i) {
+    rc = thd_attn_bwd(w + L.buf[0] + i * gq, w + L.buf[1] + i * gkv, w + L.buf[2] + i * gkv, w + L.buf[3] + i * gq,
+                      lse + (size_t)i * Hgq * T, w + L.buf[4] + i * gq, w + L.buf[5] + i * gq, w + L.buf[6] + i * gkv,
+                      w + L.buf[7] + i * gkv, T, T, cu_seqlens, cu_seqlens, cu_seqlens_padded, cu_seqlens_padded, B,
+                      T, T, Hgq, Hgkv, D, causal, softmax_scale, p2p, -1, w + L.attn, workspace_bytes - L.attn,
+                      dev_status, stream);
+    if (rc) return rc;
+  }
+  A2aParams out = a2a_params(cu_seqlens_padded, B, T, D, cp_size, a, dev_status);
+  out.job[0] = a2a_job(dq, w + L.buf[5], Hq, a);
+  out.job[1] = a2a_job(dk, w + L.buf[6], Hkv, a);
+  out.job[2] = a2a_job(dv, w + L.buf[7], Hkv, a);
+  out.njobs = 3;
+  return cuda_status(launch_a2a(out, false, st));
 }
 
 int thd_profile_enable(int kernel_id, int max_records) {

@@ -42,6 +42,10 @@ THD_KERNEL_BWD_DQ = 5
 THD_KERNEL_LSE_MERGE = 6
 THD_KERNEL_TAIL_ZERO = 7
 THD_KERNEL_PARTITION = 8
+THD_KERNEL_A2A = 9
+
+THD_A2A_TO_GROUPS = 0
+THD_A2A_TO_SHARDS = 1
 
 _vp = ctypes.c_void_p
 _i32 = ctypes.c_int
@@ -65,6 +69,12 @@ SIGNATURES = {
                             _i64, _i64, _i32, _i32, _i32, _i32, _f32, _i32, _i32, _vp, _sz, _vp, _vp]),
     "thd_lse_merge": (_i32, [_vp, _vp, _vp, _vp, _i64, _i32, _i32, _vp]),
     "thd_grad_tail_zero": (_i32, [_vp, _vp, _vp, _i64, _i64, _i32, _i32, _i32, _vp, _vp, _i32, _i32, _vp]),
+    "thd_cp_a2a": (_i32, [_vp, _vp, _vp, _i32, _i64, _i32, _i32, _i32, _i32, _i32, _vp, _vp]),
+    "thd_a2a_workspace_size": (_sz, [_i32, _i64, _i32, _i32, _i32, _i32, _i32, _i32]),
+    "thd_attn_fwd_a2a": (_i32, [_vp, _vp, _vp, _vp, _vp, _vp, _vp, _i32, _i64, _i32, _i32, _i32, _i32, _f32, _i32,
+                                _i32, _vp, _sz, _vp, _vp]),
+    "thd_attn_bwd_a2a": (_i32, [_vp, _vp, _vp, _vp, _vp, _vp, _vp, _vp, _vp, _vp, _vp, _i32, _i64, _i32, _i32, _i32,
+                                _i32, _f32, _i32, _i32, _vp, _sz, _vp, _vp]),
     "thd_profile_enable": (_i32, [_i32, _i32]),
     "thd_profile_read": (_i32, [_vp, _i32, _vp]),
     "thd_launch_count": (ctypes.c_uint64, []),
@@ -169,6 +179,30 @@ def thd_grad_tail_zero(dq, dk, dv, dq_rows, dkv_rows, Hq, Hkv, D, cu_seqlens_q_p
                        host_knows_no_tail, stream=None) -> int:
     return lib().thd_grad_tail_zero(_p(dq), _p(dk), _p(dv), dq_rows, dkv_rows, Hq, Hkv, D, _p(cu_seqlens_q_padded),
                                     _p(cu_seqlens_kv_padded), B, host_knows_no_tail, _s(stream))
+
+
+def thd_cp_a2a(src, dst, cu_seqlens_padded, B, T, H, D, cp_size, a2a_size, direction, dev_status,
+               stream=None) -> int:
+    return lib().thd_cp_a2a(_p(src), _p(dst), _p(cu_seqlens_padded), B, T, H, D, cp_size, a2a_size, direction,
+                            _p(dev_status), _s(stream))
+
+
+def thd_a2a_workspace_size(B, T, Hq, Hkv, D, cp_size, a2a_size, for_bwd) -> int:
+    return lib().thd_a2a_workspace_size(B, T, Hq, Hkv, D, cp_size, a2a_size, for_bwd)
+
+
+def thd_attn_fwd_a2a(q, k, v, o, lse, cu_seqlens, cu_seqlens_padded, B, T, Hq, Hkv, D, causal, softmax_scale,
+                     cp_size, a2a_size, workspace, workspace_bytes, dev_status, stream=None) -> int:
+    return lib().thd_attn_fwd_a2a(_p(q), _p(k), _p(v), _p(o), _p(lse), _p(cu_seqlens), _p(cu_seqlens_padded), B, T,
+                                  Hq, Hkv, D, causal, softmax_scale, cp_size, a2a_size, _p(workspace),
+                                  workspace_bytes, _p(dev_status), _s(stream))
+
+
+def thd_attn_bwd_a2a(q, k, v, o, lse, dout, dq, dk, dv, cu_seqlens, cu_seqlens_padded, B, T, Hq, Hkv, D, causal,
+                     softmax_scale, cp_size, a2a_size, workspace, workspace_bytes, dev_status, stream=None) -> int:
+    return lib().thd_attn_bwd_a2a(_p(q), _p(k), _p(v), _p(o), _p(lse), _p(dout), _p(dq), _p(dk), _p(dv),
+                                  _p(cu_seqlens), _p(cu_seqlens_padded), B, T, Hq, Hkv, D, causal, softmax_scale,
+                                  cp_size, a2a_size, _p(workspace), workspace_bytes, _p(dev_status), _s(stream))
 
 
 def thd_profile_enable(kernel_id: int, max_records: int) -> int:
@@ -313,3 +347,67 @@ def grad_tail_zero(dq, dk, dv, cu_seqlens_q_padded, cu_seqlens_kv_padded, host_k
     _check("thd_grad_tail_zero", thd_grad_tail_zero(dq, dk, dv, dq.shape[0], dk.shape[0], Hq, Hkv, D,
                                                     cu_seqlens_q_padded, cu_seqlens_kv_padded, B,
                                                     int(host_knows_no_tail), stream))
+
+
+def cp_a2a(src, cu_seqlens_padded, *, cp_size, a2a_size, direction, out=None, dev_status=None, stream=None):
+    """Allocate the other layout and call thd_cp_a2a.  THD_A2A_TO_GROUPS:
+    src shards [cp, T/cp, H, D] -> [a2a, T, H/a2a, D]; THD_A2A_TO_SHARDS: the
+    reverse.  Returns (dst, dev_status)."""
+    import torch
+    if direction == THD_A2A_TO_GROUPS:
+        cp, rows_r, H, D = src.shape
+        T = cp * rows_r
+        shape = (a2a_size, T, H // a2a_size, D)
+    else:
+        a, T, Hg, D = src.shape
+        H = a * Hg
+        shape = (cp_size, T // cp_size, H, D)
+    B = cu_seqlens_padded.numel() - 1
+    dst = torch.empty(shape, dtype=src.dtype, device=src.device) if out is None else out
+    st = torch.zeros(1, dtype=torch.int32, device=src.device) if dev_status is None else dev_status
+    _check("thd_cp_a2a", thd_cp_a2a(src, dst, cu_seqlens_padded, B, T, H, D, cp_size, a2a_size, direction, st,
+                                    stream))
+    return dst, st
+
+
+def attn_fwd_a2a(q, k, v, cu_seqlens, cu_seqlens_padded, *, cp_size, a2a_size, causal=True, softmax_scale=None,
+                 out=None, lse=None, dev_status=None, workspace=None, stream=None):
+    """Attention through the emulated A2A / hierarchical layer on shards
+    q [cp, T/cp, Hq, D], k, v [cp, T/cp, Hkv, D].  Returns (o shards,
+    lse [Hq, T] in global row order, dev_status)."""
+    import torch
+    cp, rows_r, Hq, D = q.shape
+    Hkv = k.shape[2]
+    T = cp * rows_r
+    B = cu_seqlens.numel() - 1
+    scale = 1.0 / math.sqrt(D) if softmax_scale is None else float(softmax_scale)
+    o = torch.empty_like(q) if out is None else out
+    l = torch.empty((Hq, T), dtype=torch.float32, device=q.device) if lse is None else lse
+    st = torch.zeros(1, dtype=torch.int32, device=q.device) if dev_status is None else dev_status
+    nbytes = thd_a2a_workspace_size(B, T, Hq, Hkv, D, cp_size, a2a_size, 0)
+    ws = _workspace(nbytes, q.device) if workspace is None else workspace
+    _check("thd_attn_fwd_a2a", thd_attn_fwd_a2a(q, k, v, o, l, cu_seqlens, cu_seqlens_padded, B, T, Hq, Hkv, D,
+                                                int(causal), scale, cp_size, a2a_size, ws, ws.numel(), st, stream))
+    return o, l, st
+
+
+def attn_bwd_a2a(q, k, v, o, lse, dout, cu_seqlens, cu_seqlens_padded, *, cp_size, a2a_size, causal=True,
+                 softmax_scale=None, dq=None, dk=None, dv=None, dev_status=None, workspace=None, stream=None):
+    """Gradients through the emulated A2A / hierarchical layer; shards in and
+    out.  Returns (dq, dk, dv, dev_status)."""
+    import torch
+    cp, rows_r, Hq, D = q.shape
+    Hkv = k.shape[2]
+    T = cp * rows_r
+    B = cu_seqlens.numel() - 1
+    scale = 1.0 / math.sqrt(D) if softmax_scale is None else float(softmax_scale)
+    dq = torch.empty_like(q) if dq is None else dq
+    dk = torch.empty_like(k) if dk is None else dk
+    dv = torch.empty_like(v) if dv is None else dv
+    st = torch.zeros(1, dtype=torch.int32, device=q.device) if dev_status is None else dev_status
+    nbytes = thd_a2a_workspace_size(B, T, Hq, Hkv, D, cp_size, a2a_size, 1)
+    ws = _workspace(nbytes, q.device) if workspace is None else workspace
+    _check("thd_attn_bwd_a2a", thd_attn_bwd_a2a(q, k, v, o, lse, dout, dq, dk, dv, cu_seqlens, cu_seqlens_padded, B,
+                                                T, Hq, Hkv, D, int(causal), scale, cp_size, a2a_size, ws, ws.numel(),
+                                                st, stream))
+    return dq, dk, dv, st

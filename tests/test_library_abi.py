@@ -108,3 +108,30 @@ def test_library_refuses_to_load_when_missing(monkeypatch, tmp_path):
     with pytest.raises(RuntimeError):
         mod.lib()
     importlib.reload(T)
+
+
+def test_a2a_host_side_checks(thd_lib):
+    A = T.THD_A2A_TO_GROUPS
+    # heads not divisible by the a2a group, a2a not dividing cp, T not divisible by cp, bad direction,
+    # misaligned pointer, missing metadata: rejected before any CUDA call
+    for args in ((16, 16, 16, 2, 192, 3, 64, 2, 2, A), (16, 16, 16, 2, 192, 4, 64, 4, 3, A),
+                 (16, 16, 16, 2, 190, 4, 64, 4, 2, A), (16, 16, 16, 2, 192, 4, 64, 4, 2, 2),
+                 (18, 16, 16, 2, 192, 4, 64, 4, 2, A), (16, 16, None, 2, 192, 4, 64, 4, 2, A),
+                 (16, 16, 16, 2, 192, 4, 12, 4, 2, A)):
+        assert T.thd_cp_a2a(*args, 16, stream=0) == T.THD_ERR_INVALID_ARG, args
+    f = T.thd_a2a_workspace_size(8, 14632, 16, 16, 128, 4, 2, 0)
+    b = T.thd_a2a_workspace_size(8, 14632, 16, 16, 128, 4, 2, 1)
+    # the forward holds q, k, v, O in the group layout, the backward also dO, dQ, dK, dV
+    assert f >= 4 * 14632 * 16 * 128 * 2 and b >= 8 * 14632 * 16 * 128 * 2 and b > f
+    assert T.thd_a2a_workspace_size(8, 14632, 16, 16, 96, 4, 2, 0) == 0     # head dim of the attention
+    assert T.thd_a2a_workspace_size(8, 14632, 16, 16, 128, 4, 3, 0) == 0    # 3 does not divide cp
+    assert T.thd_a2a_workspace_size(8, 14632, 16, 6, 128, 4, 4, 0) == 0     # kv heads over 4 members
+    # composites: workspace too small, bad scale
+    rc = T.thd_attn_fwd_a2a(16, 16, 16, 16, 16, 16, 16, 2, 192, 4, 4, 64, 1, 0.125, 4, 2, 256, 8, 16, stream=0)
+    assert rc == T.THD_ERR_WORKSPACE
+    rc = T.thd_attn_fwd_a2a(16, 16, 16, 16, 16, 16, 16, 2, 192, 4, 4, 64, 1, -1.0, 4, 2, 256, 1 << 30, 16,
+                            stream=0)
+    assert rc == T.THD_ERR_INVALID_ARG
+    rc = T.thd_attn_bwd_a2a(16, 16, 16, 16, 16, 16, 16, 16, 16, 16, 16, 2, 192, 4, 4, 64, 1, 0.125, 4, 2, 256, 8,
+                            16, stream=0)
+    assert rc == T.THD_ERR_WORKSPACE
