@@ -306,24 +306,28 @@ THD_API int thd_cp_a2a(const void* src, void* dst, const int32_t* cu_seqlens_pad
 
 /*
  * Bytes of workspace thd_attn_fwd_a2a (for_bwd = 0) or thd_attn_bwd_a2a
- * (for_bwd = 1) needs: the group-layout copies of the tensors plus the
- * attention workspace of one member.  Returns 0 for unsupported sizes.
+ * (for_bwd = 1) needs: global-order copies of the moved tensors plus the
+ * attention workspace.  Returns 0 for unsupported sizes.
  */
 THD_API size_t thd_a2a_workspace_size(int B, int64_t T, int Hq, int Hkv, int D, int cp_size, int a2a_size,
                                       int for_bwd);
 
 /*
  * thd_attn_fwd_a2a -- attention through the emulated A2A / hierarchical
- * decomposition: q, k, v shards -> groups (one launch); member i runs the
- * fused P2P ring of p2p = cp_size / a2a_size ranks over its heads (the
- * thd_attn_fwd path with cp_size = p2p); O groups -> shards.  Equal to
- * unsplit attention (tested).
+ * decomposition: q, k, v shards -> the members' buffers (one launch); every
+ * member runs the fused P2P ring of p2p = cp_size / a2a_size ranks over its
+ * heads; O -> shards.  On one GPU the members' buffers are the head slices
+ * of one tensor in global row order (the a2a_size = 1 layout of thd_cp_a2a),
+ * so a single thd_attn_fwd launch with cp_size = p2p serves every member;
+ * its work items are per head, so a member's result depends on its own
+ * slice alone.  Equal to unsplit attention (tested).
  *   q [cp][T/cp, Hq, D], k, v [cp][T/cp, Hkv, D], o [cp][T/cp, Hq, D]: shards.
  *   lse: fp32 [Hq, T] in global row order (members' heads stacked).
  *   cu_seqlens, cu_seqlens_padded: device int32 [B+1], self-attention (the
  *     same for q and kv); the padded offsets define the shards.
  *   Hq, Hkv divisible by a2a_size; D 64 or 128.
- * Launches: 3 + 2 * a2a_size.  Workspace: thd_a2a_workspace_size(.., 0).
+ * Launches: 5 (checks, move in, planner, forward, move out).  Workspace:
+ * thd_a2a_workspace_size(.., 0).
  */
 THD_API int thd_attn_fwd_a2a(const void* q, const void* k, const void* v, void* o, float* lse,
                              const int32_t* cu_seqlens, const int32_t* cu_seqlens_padded, int B, int64_t T, int Hq,
@@ -332,12 +336,13 @@ THD_API int thd_attn_fwd_a2a(const void* q, const void* k, const void* v, void* 
 
 /*
  * thd_attn_bwd_a2a -- gradients through the same decomposition: q, k, v, o,
- * dO shards -> groups (one launch); member i runs the thd_attn_bwd path with
- * cp_size = p2p over its heads; dQ, dK, dV groups -> shards (one launch).
+ * dO shards -> the members' buffers (one launch); the thd_attn_bwd path with
+ * cp_size = p2p for every member at once; dQ, dK, dV -> shards (one launch).
  *   Shards as in thd_attn_fwd_a2a; lse [Hq, T] as it returns it; dq
  *   [cp][T/cp, Hq, D], dk, dv [cp][T/cp, Hkv, D].  Rows of each shard past
  *   cu_seqlens_padded[B] / cp_size are not written.
- * Launches: 3 + 4 * a2a_size.  Workspace: thd_a2a_workspace_size(.., 1).
+ * Launches: 7 (checks, move in, the four of thd_attn_bwd, move out).
+ * Workspace: thd_a2a_workspace_size(.., 1).
  * Bit-reproducible.
  */
 THD_API int thd_attn_bwd_a2a(const void* q, const void* k, const void* v, const void* o, const float* lse,

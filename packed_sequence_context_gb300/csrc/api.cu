@@ -206,8 +206,13 @@ static cudaError_t launch_a2a_checks(const int32_t* cu, const int32_t* pad, int 
   return launch_plan(p, st);
 }
 
-// Workspace of the composites: group-layout copies of the tensors, then one
-// member's attention workspace.
+// The composites keep every member's buffer as a head slice of one tensor in
+// global row order (the a2a_size = 1 layout of the move: member i's heads
+// [i H/a2a, (i+1) H/a2a) side by side with the other members'), so ONE
+// attention launch, with the P2P ring of cp/a2a ranks, serves all members; its
+// work items are per head, so a member's outputs depend on its own slice only.
+// Workspace: those global-order copies of the tensors, then the attention
+// workspace.
 struct A2aWs {
   size_t buf[8];  // q k v o (forward) + dO dQ dK dV (backward)
   size_t attn = 0;
@@ -225,7 +230,7 @@ static A2aWs a2a_ws_layout(int B, int64_t T, int Hq, int Hkv, int D, int cp, int
     if (i < n) off = align_up(off + sizes[i], 256);
   }
   w.attn = off;
-  w.total = off + ws_layout(B, T, T, Hq / a2a, D, cp / a2a, bwd).total;
+  w.total = off + ws_layout(B, T, T, Hq, D, cp / a2a, bwd).total;
   return w;
 }
 
@@ -468,7 +473,7 @@ int thd_cp_a2a(const void* src, void* dst, const int32_t* cu_seqlens_padded, int
 
 size_t thd_a2a_workspace_size(int B, int64_t T, int Hq, int Hkv, int D, int cp_size, int a2a_size, int for_bwd) {
   if (check_a2a_sizes(B, T, Hq, D, cp_size, a2a_size) != THD_OK || Hkv < 1 || Hkv % a2a_size != 0) return 0;
-  if (check_sizes(B, T, T, Hq / a2a_size, Hkv / a2a_size, D, cp_size / a2a_size, -1) != THD_OK) return 0;
+  if (check_sizes(B, T, T, Hq, Hkv, D, cp_size / a2a_size, -1) != THD_OK) return 0;
   return a2a_ws_layout(B, T, Hq, Hkv, D, cp_size, a2a_size, for_bwd != 0).total;
 }
 
@@ -479,7 +484,7 @@ static int a2a_composite_checks(const int32_t* cu, const int32_t* pad, int B, in
   int rc = check_a2a_sizes(B, T, Hq, D, cp, a2a);
   if (rc) return rc;
   if (Hkv < 1 || Hkv % a2a != 0) return THD_ERR_INVALID_ARG;
-  rc = check_sizes(B, T, T, Hq / a2a, Hkv / a2a, D, cp / a2a, -1);
+  rc = check_sizes(B, T, T, Hq, Hkv, D, cp / a2a, -1);
   if (rc) return rc;
   if (!cu || !pad || !dev_status) return THD_ERR_INVALID_ARG;
   if (!(scale > 0.f) || !std::isfinite(scale) || (causal != 0 && causal != 1)) return THD_ERR_INVALID_ARG;
@@ -500,26 +505,22 @@ int thd_attn_fwd_a2a(const void* q, const void* k, const void* v, void* o, float
       !aligned(lse, 4))
     return THD_ERR_INVALID_ARG;
   char* w = static_cast<char*>(workspace);
-  const int a = a2a_size, p2p = cp_size / a2a_size, Hgq = Hq / a, Hgkv = Hkv / a;
+  const int p2p = cp_size / a2a_size;
   rc = cuda_status(launch_a2a_checks(cu_seqlens, cu_seqlens_padded, B, T, cp_size, dev_status, st));
   if (rc) return rc;
-  A2aParams in = a2a_params(cu_seqlens_padded, B, T, D, cp_size, a, dev_status);
-  in.job[0] = a2a_job(q, w + L.buf[0], Hq, a);
-  in.job[1] = a2a_job(k, w + L.buf[1], Hkv, a);
-  in.job[2] = a2a_job(v, w + L.buf[2], Hkv, a);
+  A2aParams in = a2a_params(cu_seqlens_padded, B, T, D, cp_size, 1, dev_status);
+  in.job[0] = a2a_job(q, w + L.buf[0], Hq, 1);
+  in.job[1] = a2a_job(k, w + L.buf[1], Hkv, 1);
+  in.job[2] = a2a_job(v, w + L.buf[2], Hkv, 1);
   in.njobs = 3;
   rc = cuda_status(launch_a2a(in, true, st));
   if (rc) return rc;
-  const size_t gq = sizeof(uint16_t) * (size_t)T * Hgq * D, gkv = sizeof(uint16_t) * (size_t)T * Hgkv * D;
-  for (int i = 0; i < a; ++i) {
-    rc = fwd_common(w + L.buf[0] + i * gq, w + L.buf[1] + i * gkv, w + L.buf[2] + i * gkv, w + L.buf[3] + i * gq,
-                    lse + (size_t)i * Hgq * T, cu_seqlens, cu_seqlens, cu_seqlens_padded, cu_seqlens_padded, B, T, T,
-                    Hgq, Hgkv, D, causal, softmax_scale, p2p, -1, -1, w + L.attn, workspace_bytes - L.attn,
-                    dev_status, st);
-    if (rc) return rc;
-  }
-  A2aParams out = a2a_params(cu_seqlens_padded, B, T, D, cp_size, a, dev_status);
-  out.job[0] = a2a_job(o, w + L.buf[3], Hq, a);
+  rc = fwd_common(w + L.buf[0], w + L.buf[1], w + L.buf[2], w + L.buf[3], lse, cu_seqlens, cu_seqlens,
+                  cu_seqlens_padded, cu_seqlens_padded, B, T, T, Hq, Hkv, D, causal, softmax_scale, p2p, -1, -1,
+                  w + L.attn, workspace_bytes - L.attn, dev_status, st);
+  if (rc) return rc;
+  A2aParams out = a2a_params(cu_seqlens_padded, B, T, D, cp_size, 1, dev_status);
+  out.job[0] = a2a_job(o, w + L.buf[3], Hq, 1);
   out.njobs = 1;
   return cuda_status(launch_a2a(out, false, st));
 }
@@ -538,31 +539,27 @@ int thd_attn_bwd_a2a(const void* q, const void* k, const void* v, const void* o,
       !aligned(dq, 16) || !aligned(dk, 16) || !aligned(dv, 16) || !aligned(lse, 4))
     return THD_ERR_INVALID_ARG;
   char* w = static_cast<char*>(workspace);
-  const int a = a2a_size, p2p = cp_size / a2a_size, Hgq = Hq / a, Hgkv = Hkv / a;
+  const int p2p = cp_size / a2a_size;
   rc = cuda_status(launch_a2a_checks(cu_seqlens, cu_seqlens_padded, B, T, cp_size, dev_status, st));
   if (rc) return rc;
-  A2aParams in = a2a_params(cu_seqlens_padded, B, T, D, cp_size, a, dev_status);
-  in.job[0] = a2a_job(q, w + L.buf[0], Hq, a);
-  in.job[1] = a2a_job(k, w + L.buf[1], Hkv, a);
-  in.job[2] = a2a_job(v, w + L.buf[2], Hkv, a);
-  in.job[3] = a2a_job(o, w + L.buf[3], Hq, a);
-  in.job[4] = a2a_job(dout, w + L.buf[4], Hq, a);
+  A2aParams in = a2a_params(cu_seqlens_padded, B, T, D, cp_size, 1, dev_status);
+  in.job[0] = a2a_job(q, w + L.buf[0], Hq, 1);
+  in.job[1] = a2a_job(k, w + L.buf[1], Hkv, 1);
+  in.job[2] = a2a_job(v, w + L.buf[2], Hkv, 1);
+  in.job[3] = a2a_job(o, w + L.buf[3], Hq, 1);
+  in.job[4] = a2a_job(dout, w + L.buf[4], Hq, 1);
   in.njobs = 5;
   rc = cuda_status(launch_a2a(in, true, st));
   if (rc) return rc;
-  const size_t gq = sizeof(uint16_t) * (size_t)T * Hgq * D, gkv = sizeof(uint16_t) * (size_t)T * Hgkv * D;
-  for (int i = 0; i < a; ++i) {
-    rc = thd_attn_bwd(w + L.buf[0] + i * gq, w + L.buf[1] + i * gkv, w + L.buf[2] + i * gkv, w + L.buf[3] + i * gq,
-                      lse + (size_t)i * Hgq * T, w + L.buf[4] + i * gq, w + L.buf[5] + i * gq, w + L.buf[6] + i * gkv,
-                      w + L.buf[7] + i * gkv, T, T, cu_seqlens, cu_seqlens, cu_seqlens_padded, cu_seqlens_padded, B,
-                      T, T, Hgq, Hgkv, D, causal, softmax_scale, p2p, -1, w + L.attn, workspace_bytes - L.attn,
-                      dev_status, stream);
-    if (rc) return rc;
-  }
-  A2aParams out = a2a_params(cu_seqlens_padded, B, T, D, cp_size, a, dev_status);
-  out.job[0] = a2a_job(dq, w + L.buf[5], Hq, a);
-  out.job[1] = a2a_job(dk, w + L.buf[6], Hkv, a);
-  out.job[2] = a2a_job(dv, w + L.buf[7], Hkv, a);
+  rc = thd_attn_bwd(w + L.buf[0], w + L.buf[1], w + L.buf[2], w + L.buf[3], lse, w + L.buf[4], w + L.buf[5],
+                    w + L.buf[6], w + L.buf[7], T, T, cu_seqlens, cu_seqlens, cu_seqlens_padded, cu_seqlens_padded,
+                    B, T, T, Hq, Hkv, D, causal, softmax_scale, p2p, -1, w + L.attn, workspace_bytes - L.attn,
+                    dev_status, stream);
+  if (rc) return rc;
+  A2aParams out = a2a_params(cu_seqlens_padded, B, T, D, cp_size, 1, dev_status);
+  out.job[0] = a2a_job(dq, w + L.buf[5], Hq, 1);
+  out.job[1] = a2a_job(dk, w + L.buf[6], Hkv, 1);
+  out.job[2] = a2a_job(dv, w + L.buf[7], Hkv, 1);
   out.njobs = 3;
   return cuda_status(launch_a2a(out, false, st));
 }

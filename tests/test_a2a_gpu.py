@@ -216,3 +216,21 @@ def test_a2a_matches_fused_ring_bitwise_when_a2a_is_one():
     ref_sh = orc.a2a_head_to_seq(o2.view(torch.int16).cpu().numpy()[None], w.cu_seqlens_padded, w.cp_size, 1)
     assert np.array_equal(_bits(o), ref_sh.view(np.uint16))
     assert torch.equal(lse, lse2)
+
+
+def test_ulysses_matches_unchunked_attention_bitwise():
+    """a2a = cp leaves a ring of one rank: every member attends its heads over
+    whole sequences, the thd_attn_fwd launch with cp_size 1, bit for bit."""
+    w = inputs.make_workload("custom", 7, lengths=[96, 200, 24], pad_to=16, Hq=8, Hkv=4, D=128, cp_size=4)
+    t = inputs.make_tensors(w)
+    sh = _shards(w, t)
+    cu = torch.from_numpy(w.cu_seqlens).cuda()
+    cup = torch.from_numpy(w.cu_seqlens_padded).cuda()
+    o, lse, st = T.attn_fwd_a2a(sh["q"].cuda(), sh["k"].cuda(), sh["v"].cuda(), cu, cup, cp_size=4, a2a_size=4,
+                                softmax_scale=w.softmax_scale)
+    o2, lse2, st2 = T.attn_fwd(t["q"].cuda(), t["k"].cuda(), t["v"].cuda(), cu, cu, cup, cup, cp_size=1,
+                               softmax_scale=w.softmax_scale)
+    assert T.check_status(st) == 0 and T.check_status(st2) == 0
+    ref_sh = orc.a2a_head_to_seq(o2.view(torch.int16).cpu().numpy()[None], w.cu_seqlens_padded, 4, 1)
+    assert np.array_equal(_bits(o), ref_sh.view(np.uint16))
+    assert torch.equal(lse, lse2)
