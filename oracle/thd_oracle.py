@@ -38,7 +38,8 @@ this module takes the plainest reading (each one is listed in the design doc):
   ``s = (r - i) mod CP``.
 
 Parity pins: every function here is checked in ``tests/test_oracle_pins.py``
-(the Ulysses/A2A and hierarchical functions in ``tests/test_oracle_a2a_pins.py``)
+(the Ulysses/A2A and hierarchical functions in ``tests/test_oracle_a2a_pins.py``,
+the bottom-right causal mode in ``tests/test_oracle_bottom_right_pins.py``)
 against brute force, closed forms, library special cases (torch SDPA in
 fp64 on the CPU) and invariants.  No function is "parity unpinned".
 """
@@ -214,11 +215,36 @@ def _logsumexp_rows(S: np.ndarray) -> np.ndarray:
         return np.where(finite, m_safe + np.log(s), NEG_INF)
 
 
-def _mask(i0: int, nq: int, Lkv: int, causal: bool) -> np.ndarray:
-    """Allowed (i, j) for query rows i0..i0+nq-1: j < Lkv, and j <= i if causal."""
+BOTTOM_RIGHT = "bottom_right"
+
+
+def _key_offset(causal, Lq: int, Lkv: int):
+    """None for no mask, else the offset o of the causal mask j <= i + o.
+
+    ``causal`` True is the top-left mask (o = 0), which the pages' training
+    setting uses and which needs equal query and key lengths per sequence.
+    ``BOTTOM_RIGHT`` aligns the last query with the last key, o = Lkv - Lq
+    (the T_q != T_kv case; not on the pages, the usual convention for a
+    query block at the end of its keys): with Lq > Lkv the first Lq - Lkv
+    queries see no key and get O = 0, lse = -inf like pad rows.
+    """
+    if causal == BOTTOM_RIGHT:
+        return Lkv - Lq
+    if causal is True or causal == 1:
+        if Lq != Lkv:
+            raise ValueError("causal attention needs equal q/kv lengths per sequence")
+        return 0
+    if causal is False or causal == 0:
+        return None
+    raise ValueError(f"unknown causal mode {causal!r}")
+
+
+def _mask(i0: int, nq: int, Lkv: int, offset) -> np.ndarray:
+    """Allowed (i, j) for query rows i0..i0+nq-1: j < Lkv, and j <= i + offset
+    unless offset is None (no causal mask)."""
     i = np.arange(i0, i0 + nq)[:, None]
     j = np.arange(Lkv)[None, :]
-    return (j <= i) if causal else np.ones((nq, Lkv), bool)
+    return (j <= i + offset) if offset is not None else np.ones((nq, Lkv), bool)
 
 
 def attn_fwd(q, k, v, cu_seqlens_q, cu_seqlens_kv, cu_seqlens_q_padded=None,
@@ -233,7 +259,7 @@ def attn_fwd(q, k, v, cu_seqlens_q, cu_seqlens_kv, cu_seqlens_q_padded=None,
     (others stay 0 / -inf), for bounded timing samples.
 
     Causal is the top-left mask j <= i, which needs equal query and key
-    lengths per sequence.
+    lengths per sequence; ``causal=BOTTOM_RIGHT`` is j <= i + Lkv - Lq.
     """
     q, k, v = _f64(q), _f64(k), _f64(v)
     Tq, Hq, D = q.shape
@@ -249,8 +275,7 @@ def attn_fwd(q, k, v, cu_seqlens_q, cu_seqlens_kv, cu_seqlens_q_padded=None,
     lse = np.full((Hq, Tq), NEG_INF)
     hs = range(Hq) if heads is None else heads
     for (oq, Lq, ok, Lkv) in _seq_table(cu_q, cu_kv, pq, pkv):
-        if causal and Lq != Lkv:
-            raise ValueError("causal attention needs equal q/kv lengths per sequence")
+        off = _key_offset(causal, Lq, Lkv)
         for h in hs:
             K = k[ok:ok + Lkv, h // G]
             V = v[ok:ok + Lkv, h // G]
@@ -258,7 +283,7 @@ def attn_fwd(q, k, v, cu_seqlens_q, cu_seqlens_kv, cu_seqlens_q_padded=None,
                 nq = min(Q_BLOCK, Lq - i0)
                 Qb = q[oq + i0:oq + i0 + nq, h]
                 S = scale * (Qb @ K.T)
-                S = np.where(_mask(i0, nq, Lkv, causal), S, NEG_INF)
+                S = np.where(_mask(i0, nq, Lkv, off), S, NEG_INF)
                 l = _logsumexp_rows(S)
                 with np.errstate(invalid="ignore", under="ignore"):
                     P = np.where(np.isfinite(l)[:, None], np.exp(S - l[:, None]), 0.0)
@@ -281,7 +306,8 @@ def attn_bwd(q, k, v, do, cu_seqlens_q, cu_seqlens_kv, cu_seqlens_q_padded=None,
     to reproduce bug"] runs forward and backward on this layout; [P2
     "Describe the bug"] has THD dQ/dK/dV rows past the valid endpoint
     zeroed: here every row without a valid token is 0, including the slack
-    rows ``[cu_pad[B], rows)`` of buffers longer than the data.
+    rows ``[cu_pad[B], rows)`` of buffers longer than the data.  ``causal``
+    takes the same modes as ``attn_fwd`` (``BOTTOM_RIGHT`` included).
     """
     q, k, v, do = _f64(q), _f64(k), _f64(v), _f64(do)
     Tq, Hq, D = q.shape
@@ -296,8 +322,7 @@ def attn_bwd(q, k, v, do, cu_seqlens_q, cu_seqlens_kv, cu_seqlens_q_padded=None,
     dv = np.zeros_like(dk)
     hs = range(Hq) if heads is None else heads
     for (oq, Lq, ok, Lkv) in _seq_table(cu_q, cu_kv, pq, pkv):
-        if causal and Lq != Lkv:
-            raise ValueError("causal attention needs equal q/kv lengths per sequence")
+        off = _key_offset(causal, Lq, Lkv)
         for h in hs:
             K = k[ok:ok + Lkv, h // G]
             V = v[ok:ok + Lkv, h // G]
@@ -308,7 +333,7 @@ def attn_bwd(q, k, v, do, cu_seqlens_q, cu_seqlens_kv, cu_seqlens_q_padded=None,
                 Qb = q[oq + i0:oq + i0 + nq, h]
                 dOb = do[oq + i0:oq + i0 + nq, h]
                 S = scale * (Qb @ K.T)
-                S = np.where(_mask(i0, nq, Lkv, causal), S, NEG_INF)
+                S = np.where(_mask(i0, nq, Lkv, off), S, NEG_INF)
                 l = _logsumexp_rows(S)
                 with np.errstate(invalid="ignore", under="ignore"):
                     P = np.where(np.isfinite(l)[:, None], np.exp(S - l[:, None]), 0.0)
@@ -339,6 +364,7 @@ def attn_fwd_rows(q, k, v, cu_seqlens_q, cu_seqlens_kv, cu_seqlens_q_padded, cu_
     pq = effective_padded(cu_q, cu_seqlens_q_padded, pad_between_seqs)
     pkv = effective_padded(cu_kv, cu_seqlens_kv_padded, pad_between_seqs)
     Lq, Lkv = cu_q[b + 1] - cu_q[b], cu_kv[b + 1] - cu_kv[b]
+    off = _key_offset(causal, Lq, Lkv)
     K = _f64(k[pkv[b]:pkv[b] + Lkv, h // G])
     V = _f64(v[pkv[b]:pkv[b] + Lkv, h // G])
     pos = [int(x) for x in positions]
@@ -348,8 +374,8 @@ def attn_fwd_rows(q, k, v, cu_seqlens_q, cu_seqlens_kv, cu_seqlens_q_padded, cu_
         if i >= Lq:
             continue
         S = scale * (K @ _f64(q[pq[b] + i, h]))
-        if causal:
-            S[i + 1:] = NEG_INF
+        if off is not None:
+            S[max(i + off + 1, 0):] = NEG_INF
         l = _logsumexp_rows(S[None, :])[0]
         lse[n] = l
         if np.isfinite(l):
