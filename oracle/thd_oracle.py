@@ -23,7 +23,7 @@ Sources (web pages; cited as [P1], [P2], [P3] with the section on the page):
   and "Pitfalls" item 5 (local-chunk-only attention is fast but wrong).
 
 The pages name the operations but print no formula.  Where they are silent
-this module takes the plainest reading (each one is listed in the design doc):
+this module takes the plainest reading that the rest supports:
 
 * THD layout: tokens of all sequences concatenated, ``[T, H, D]``; sequence b
   occupies buffer rows ``[cu_pad[b], cu_pad[b] + L_b)`` with
