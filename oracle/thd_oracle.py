@@ -658,6 +658,75 @@ def cp_a2a_attn_bwd(q_shards, k_shards, v_shards, do_shards, cu_seqlens, cu_seql
     return tuple(a2a_head_to_seq(g, pad, cp, a) for g in (dqh, dkh, dvh))
 
 
+def _rank_rows(off: int, P: int, cp: int, r: int) -> np.ndarray:
+    """Buffer rows of rank r's share of one sequence (padded length P at row
+    off): chunk r then chunk 2cp-1-r, chunk = P / (2cp) rows."""
+    cb = P // (2 * cp)
+    return np.concatenate([off + r * cb + np.arange(cb), off + (2 * cp - 1 - r) * cb + np.arange(cb)]).astype(int)
+
+
+def cp_ring_fwd_masked(q, k, v, cu_seqlens_q, cu_seqlens_kv, cu_seqlens_q_padded, cu_seqlens_kv_padded,
+                       cp_size: int, causal=True, softmax_scale: float | None = None, pad_between_seqs: int = -1,
+                       return_partials: bool = False):
+    """The P2P ring written with positional masks, for any mask mode.
+
+    At step i rank r attends its query rows (its two q chunks) to the KV rows
+    of rank s = (r - i) mod cp (s's two kv chunks), the mask taken from the
+    rows' positions in the sequence (``_key_offset``: top-left causal,
+    bottom-right causal or none), and the partials are merged with
+    ``lse_merge``.  q and kv are chunked separately (``P_q / 2cp`` and
+    ``P_kv / 2cp`` rows).  For equal-length causal self-attention the
+    step-by-step partials are those of ``cp_ring_fwd``'s three rules; here
+    they follow from positions alone, which also covers non-causal and
+    bottom-right causal attention.  Returns (O, lse) like ``attn_fwd`` and,
+    with ``return_partials``, the per-step partials scattered to global rows.
+    """
+    q, k, v = _f64(q), _f64(k), _f64(v)
+    Tq, Hq, D = q.shape
+    G = Hq // k.shape[1]
+    scale = 1.0 / math.sqrt(D) if softmax_scale is None else float(softmax_scale)
+    cp = int(cp_size)
+    cu_q, cu_kv = _as_int_list(cu_seqlens_q), _as_int_list(cu_seqlens_kv)
+    pq = effective_padded(cu_q, cu_seqlens_q_padded, pad_between_seqs)
+    pkv = effective_padded(cu_kv, cu_seqlens_kv_padded, pad_between_seqs)
+    O = np.zeros((Tq, Hq, D))
+    lse = np.full((Hq, Tq), NEG_INF)
+    partials = [(np.zeros((Tq, Hq, D)), np.full((Hq, Tq), NEG_INF)) for _ in range(cp)]
+    for b in range(len(cu_q) - 1):
+        Lq, Lkv = cu_q[b + 1] - cu_q[b], cu_kv[b + 1] - cu_kv[b]
+        Pq, Pkv = pq[b + 1] - pq[b], pkv[b + 1] - pkv[b]
+        if Pq % (2 * cp) or Pkv % (2 * cp):
+            raise ValueError("padded length not divisible by 2*cp_size")
+        off = _key_offset(causal, Lq, Lkv)
+        for r in range(cp):
+            qrows = _rank_rows(pq[b], Pq, cp, r)
+            qpos = qrows - pq[b]
+            for h in range(Hq):
+                acc_o = np.zeros((len(qrows), D))
+                acc_l = np.full(len(qrows), NEG_INF)
+                for i in range(cp):
+                    s = (r - i) % cp
+                    krows = _rank_rows(pkv[b], Pkv, cp, s)
+                    kpos = krows - pkv[b]
+                    allowed = (qpos[:, None] < Lq) & (kpos[None, :] < Lkv)
+                    if off is not None:
+                        allowed &= kpos[None, :] <= qpos[:, None] + off
+                    S = np.where(allowed, scale * (q[qrows, h] @ k[krows, h // G].T), NEG_INF)
+                    l = _logsumexp_rows(S)
+                    with np.errstate(invalid="ignore", under="ignore"):
+                        P = np.where(np.isfinite(l)[:, None], np.exp(S - l[:, None]), 0.0)
+                    Oi = P @ v[krows, h // G]
+                    partials[i][0][qrows, h] = Oi
+                    partials[i][1][h, qrows] = l
+                    m_o, m_l = lse_merge(acc_o[:, None, :], acc_l[None, :], Oi[:, None, :], l[None, :])
+                    acc_o, acc_l = m_o[:, 0, :], m_l[0]
+                O[qrows, h] = acc_o
+                lse[h, qrows] = acc_l
+    if return_partials:
+        return O, lse, partials
+    return O, lse
+
+
 # ---------------------------------------------------------------------------
 # a9: gradient tail-zero
 # ---------------------------------------------------------------------------

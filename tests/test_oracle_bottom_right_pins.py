@@ -1,7 +1,9 @@
 """Pins for the oracle's bottom-right causal mode (T_q != T_kv per sequence):
 scalar brute force, torch's lower-right causal bias in fp64, the equal-length
 special case, gradients against torch autograd, and a planted offset sign
-mistake.  CPU only."""
+mistake; and for the ring written with positional masks (every mask mode):
+its merge equals unsplit attention and, for equal-length causal
+self-attention, each step equals the hand-ruled ring's step.  CPU only."""
 
 import math
 
@@ -167,3 +169,51 @@ def test_planted_offset_sign_mistake_is_caught(monkeypatch):
     monkeypatch.setattr(orc, "_key_offset", wrong)
     with pytest.raises(AssertionError):
         test_bottom_right_matches_torch_lower_right(0)
+
+
+# ---------------------------------------------------------------- the ring with positional masks
+
+def _padded_case(rng, cp, lq, lkv, Hq=4, Hkv=2, D=8):
+    unit = 2 * cp
+    Pq = [unit * -(-max(L, 1) // unit) for L in lq]
+    Pkv = [unit * -(-max(L, 1) // unit) for L in lkv]
+    cq = np.concatenate([[0], np.cumsum(lq)]).astype(np.int32)
+    ck = np.concatenate([[0], np.cumsum(lkv)]).astype(np.int32)
+    pq = np.concatenate([[0], np.cumsum(Pq)]).astype(np.int32)
+    pk = np.concatenate([[0], np.cumsum(Pkv)]).astype(np.int32)
+    q = rng.standard_normal((int(pq[-1]), Hq, D))
+    k = rng.standard_normal((int(pk[-1]), Hkv, D))
+    v = rng.standard_normal((int(pk[-1]), Hkv, D))
+    return cq, ck, pq, pk, q, k, v
+
+
+@pytest.mark.parametrize("cp", [1, 2, 3, 4])
+@pytest.mark.parametrize("mode", [True, False, BR])
+def test_masked_ring_merges_to_unsplit(cp, mode):
+    rng = np.random.default_rng(100 + 10 * cp + (0 if mode is True else 1 if mode is False else 2))
+    lq = [int(x) for x in rng.integers(1, 40, size=3)]
+    lkv = lq if mode is True else [int(x) for x in rng.integers(1, 50, size=3)]
+    cq, ck, pq, pk, q, k, v = _padded_case(rng, cp, lq, lkv)
+    O, lse = orc.attn_fwd(q, k, v, cq, ck, pq, pk, causal=mode, softmax_scale=0.3)
+    Or, lr = orc.cp_ring_fwd_masked(q, k, v, cq, ck, pq, pk, cp, causal=mode, softmax_scale=0.3)
+    np.testing.assert_allclose(Or, O, rtol=0, atol=1e-12)
+    fin = np.isfinite(lse)
+    assert np.array_equal(fin, np.isfinite(lr))
+    np.testing.assert_allclose(lr[fin], lse[fin], rtol=0, atol=1e-12)
+
+
+@pytest.mark.parametrize("cp", [2, 3, 4])
+def test_masked_ring_steps_equal_the_causal_ring_rules(cp):
+    """Equal-length causal self-attention: step i's partial from positions alone
+    equals the partial of the ring's three hand rules (local causal step;
+    s < r: all rows against chunk s; s > r: second-half rows only)."""
+    rng = np.random.default_rng(200 + cp)
+    lens = [int(x) for x in rng.integers(1, 40, size=3)]
+    cq, ck, pq, pk, q, k, v = _padded_case(rng, cp, lens, lens)
+    _, _, pa = orc.cp_ring_fwd_masked(q, k, v, cq, ck, pq, pk, cp, causal=True, softmax_scale=0.3,
+                                      return_partials=True)
+    _, _, pb = orc.cp_ring_fwd(q, k, v, cq, pq, cp, softmax_scale=0.3, return_partials=True)
+    for (oa, la), (ob, lb) in zip(pa, pb):
+        np.testing.assert_allclose(oa, ob, rtol=0, atol=1e-12)
+        assert np.array_equal(np.isfinite(la), np.isfinite(lb))
+        np.testing.assert_allclose(la[np.isfinite(la)], lb[np.isfinite(lb)], rtol=0, atol=1e-12)
