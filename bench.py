@@ -13,6 +13,7 @@ events.  Each step is timed with CUDA events on the launching stream.
     python bench.py --impl reference ...   # the CPU fp64 oracle on host cores
     python bench.py --a2a 4 ...            # the same step through the emulated Ulysses layer (cp 4);
                                            # --a2a 2: hierarchical a2a+p2p sizes [2, 2]
+    python bench.py --hbm-kernels          # LSE merge, tail-zero and A2A move vs the HBM copy peak
 
 Under torchrun each rank runs its own replica of the workload (weak scaling,
 no collective on the data path); rank 0 prints one JSON line.
@@ -46,6 +47,8 @@ def _args():
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--no-e2e", action="store_true")
     ap.add_argument("--fwd-only", action="store_true", help="time the forward alone as the step")
+    ap.add_argument("--hbm-kernels", action="store_true",
+                    help="time the HBM-bound kernels (LSE merge, gradient tail-zero, A2A move) against the copy peak")
     ap.add_argument("--a2a", type=int, default=0,
                     help="a2a group size: time the step through the emulated Ulysses (a2a = cp) or hierarchical "
                          "a2a+p2p layer (thd_attn_fwd_a2a / thd_attn_bwd_a2a on per-rank shards)")
@@ -483,10 +486,7 @@ def run_a2a(a):
     T.check_status(st)
     ms = sum(times) / len(times)
     fwd_ms = sum(fwd_times) / len(fwd_times)
-    # every element of the moved tensors is read once and written once: forward q, k, v in and O out;
-    # backward q, k, v, O, dO in and dQ, dK, dV out
-    elems = Tn * D * (6 * Hq + 6 * Hkv)
-    move_bytes = 2 * 2 * elems
+    move_bytes = a2a_step_bytes(Tn, Hq, Hkv, D)
     move_ms = sum(kms) / a.steps
     gbs = move_bytes / (move_ms * 1e-3) / 1e9
     mode = "a2a" if A == cp else ("p2p" if A == 1 else "a2a+p2p")
@@ -505,6 +505,106 @@ def run_a2a(a):
         "clocks": clk.summary(),
     }
     print(json.dumps(line), flush=True)
+    return 0
+
+
+# ----------------------------------------------------------------- HBM-bound kernels
+def merge_bytes(T: int, H: int, D: int) -> int:
+    """thd_lse_merge, per launch: reads O and lse of both sides (fp32), writes
+    the merged O and lse."""
+    return 3 * T * H * (4 * D + 4)
+
+
+def tail_zero_bytes(dq_rows: int, dkv_rows: int, end_q: int, end_kv: int, Hq: int, Hkv: int, D: int) -> int:
+    """thd_grad_tail_zero, per launch: bf16 zeros written to the slack rows of
+    dQ, dK and dV (nothing read)."""
+    return 2 * D * ((dq_rows - end_q) * Hq + 2 * (dkv_rows - end_kv) * Hkv)
+
+
+def a2a_move_bytes(T: int, H: int, D: int) -> int:
+    """thd_cp_a2a, per launch and tensor: every bf16 element read once and written once."""
+    return 2 * 2 * T * H * D
+
+
+def a2a_step_bytes(T: int, Hq: int, Hkv: int, D: int) -> int:
+    """The moves of one fwd+bwd step through the emulated A2A layer: forward q,
+    k, v in and O out; backward q, k, v, O, dO in and dQ, dK, dV out."""
+    fwd_in, fwd_out = (Hq, Hkv, Hkv), (Hq,)
+    bwd_in, bwd_out = (Hq, Hkv, Hkv, Hq, Hq), (Hq, Hkv, Hkv)
+    return sum(a2a_move_bytes(T, H, D) for H in fwd_in + fwd_out + bwd_in + bwd_out)
+
+
+def run_hbm_kernels(a):
+    """One JSON line per HBM-bound kernel: algorithmic bytes per launch over the
+    mean duration of `steps` launches (after `warmup`), taken with the
+    library's profiling hook (CUDA events recorded on the launching stream
+    right around the kernel), L2 flushed between launches, against the
+    measured copy peak."""
+    import torch
+
+    from packed_sequence_context_gb300 import inputs
+    from packed_sequence_context_gb300 import thd_attn as T
+
+    if not torch.cuda.is_available():
+        raise SystemExit("bench.py needs a CUDA GPU")
+    T.lib()
+    _, _, hbm, peak_kind = _peaks()
+    dev = torch.device("cuda", 0)
+    flush_buf = torch.empty(256 << 20, dtype=torch.uint8, device=dev)
+
+    def time_it(fn, kernel_id):
+        for _ in range(max(a.warmup, 3)):
+            fn()
+        torch.cuda.synchronize()
+        T.thd_profile_enable(kernel_id, a.steps)
+        for _ in range(a.steps):
+            flush_buf.zero_()
+            fn()
+        torch.cuda.synchronize()
+        kms = T.thd_profile_read(a.steps)
+        T.thd_profile_enable(0, 0)
+        assert len(kms) == a.steps, (kernel_id, len(kms))
+        return sum(kms) / len(kms)
+
+    def line(kernel, workload, nbytes, ms, extra):
+        gbs = nbytes / (ms * 1e-3) / 1e9
+        print(json.dumps({"kernel": kernel, "workload": workload, "bound": "hbm", "achieved": gbs, "peak": hbm,
+                          "unit": "GB/s", "frac": gbs / hbm, "peak_kind": f"copy ({peak_kind})",
+                          "bytes_per_launch": nbytes, "ms": ms, "steps": a.steps, **extra}), flush=True)
+
+    # LSE merge: two fp32 partials of the packed workload's shape (finite lse on every row)
+    w = inputs.make_workload("packed")
+    Tn, H, D = w.T, w.Hq, w.D
+    g = torch.Generator(device=dev).manual_seed(11)
+    o_acc = torch.randn((Tn, H, D), generator=g, device=dev)
+    o_part = torch.randn((Tn, H, D), generator=g, device=dev)
+    l_acc = torch.randn((H, Tn), generator=g, device=dev)
+    l_part = torch.randn((H, Tn), generator=g, device=dev)
+    ms = time_it(lambda: T.lse_merge(o_acc, l_acc, o_part, l_part), T.THD_KERNEL_LSE_MERGE)
+    line("lse_merge_kernel", "packed (fp32 partials)", merge_bytes(Tn, H, D), ms, {})
+
+    # gradient tail-zero: the fwdbwd workload's dQ/dK/dV buffers, 10% slack past the last sequence
+    w = inputs.make_workload("fwdbwd")
+    dq = torch.empty((w.dq_rows, w.Hq, w.D), dtype=torch.bfloat16, device=dev)
+    dk = torch.empty((w.dkv_rows, w.Hkv, w.D), dtype=torch.bfloat16, device=dev)
+    dv = torch.empty_like(dk)
+    cup = torch.from_numpy(w.cu_seqlens_padded).to(dev)
+    ms = time_it(lambda: T.grad_tail_zero(dq, dk, dv, cup, cup), T.THD_KERNEL_TAIL_ZERO)
+    end = int(w.cu_seqlens_padded[-1])
+    line("tail_zero_kernel", "fwdbwd (dQ/dK/dV slack rows)",
+         tail_zero_bytes(w.dq_rows, w.dkv_rows, end, end, w.Hq, w.Hkv, w.D), ms,
+         {"slack_rows": w.dq_rows - end})
+
+    # A2A move of one tensor: the packed workload's q shards -> Ulysses member layout (cp 4, a2a 4)
+    w = inputs.make_workload("packed")
+    x = torch.randn((w.cp_size, w.T // w.cp_size, w.Hq, w.D), generator=g, device=dev).to(torch.bfloat16)
+    y = torch.empty((w.cp_size, w.T, w.Hq // w.cp_size, w.D), dtype=torch.bfloat16, device=dev)
+    cup = torch.from_numpy(w.cu_seqlens_padded).to(dev)
+    st = torch.zeros(1, dtype=torch.int32, device=dev)
+    ms = time_it(lambda: T.cp_a2a(x, cup, cp_size=w.cp_size, a2a_size=w.cp_size, direction=T.THD_A2A_TO_GROUPS,
+                                  out=y, dev_status=st), T.THD_KERNEL_A2A)
+    T.check_status(st)
+    line("a2a_kernel", "packed (q, shards -> Ulysses members)", a2a_move_bytes(w.T, w.Hq, w.D), ms, {})
     return 0
 
 
@@ -561,6 +661,8 @@ def main():
     a.config = CONFIG_ALIASES.get(a.config, a.config)
     if a.impl == "reference":
         return run_reference(a)
+    if a.hbm_kernels:
+        return run_hbm_kernels(a)
     if a.a2a:
         return run_a2a(a)
     return run_ours(a)
