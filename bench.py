@@ -40,9 +40,11 @@ UNIT = "TFLOPS"
 def _args():
     ap = argparse.ArgumentParser()
     ap.add_argument("--gpus", type=int, default=1)
-    ap.add_argument("--steps", type=int, default=100)
-    ap.add_argument("--warmup", type=int, default=10)
-    ap.add_argument("--config", default="packed", help="tiny|packed|padded|long|fwdbwd (or C1..C5)")
+    ap.add_argument("--steps", type=int, default=20)
+    ap.add_argument("--warmup", type=int, default=5)
+    ap.add_argument("--config", default="long", help="tiny|packed|padded|long|fwdbwd (or C1..C5)")
+    ap.add_argument("--no-extras", action="store_true",
+                    help="time only the named workload (no per_config, HBM-kernel, ring or ABBA keys)")
     ap.add_argument("--impl", default="ours", choices=["ours", "reference"])
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--no-e2e", action="store_true")
@@ -153,12 +155,22 @@ def _oracle_item(args):
     return time.perf_counter() - t0
 
 
-def _oracle_items(w, t, heads):
+# The CPU legs time the oracle on whole sequences up to this length; a longer
+# sequence is sampled as the same problem on its first ORACLE_PREFIX tokens
+# (a 131072-token sequence would take the fp64 oracle hours per head).
+ORACLE_PREFIX = 4096
+
+
+def _sample_lengths(w, prefix=ORACLE_PREFIX):
+    return [min(int(L), prefix) for L in w.lengths if L]
+
+
+def _oracle_items(w, t, heads, prefix=ORACLE_PREFIX):
     G = w.Hq // w.Hkv
     items = []
     for b in range(w.B):
         off = int(w.cu_seqlens_padded[b])
-        L = w.lengths[b]
+        L = min(int(w.lengths[b]), prefix)
         if L == 0:
             continue
         for h in heads:
@@ -169,10 +181,18 @@ def _oracle_items(w, t, heads):
     return items
 
 
-def _sample_flops(w, heads):
+def _sample_flops(w, heads, prefix=ORACLE_PREFIX):
     from packed_sequence_context_gb300 import inputs
-    _, both = inputs.algorithmic_flops(w.lengths, 1, w.D)
+    _, both = inputs.algorithmic_flops(_sample_lengths(w, prefix), 1, w.D)
     return both * len(heads)
+
+
+def _sample_scope(w, prefix=ORACLE_PREFIX):
+    cut = [L for L in w.lengths if L > prefix]
+    if not cut:
+        return f"all {w.B} sequences whole"
+    return (f"{w.B} sequences, the {len(cut)} longer than {prefix} tokens cut to their first {prefix} "
+            f"(the same causal problem on fewer tokens)")
 
 
 def _spawn_pool(n):
@@ -184,8 +204,9 @@ def _spawn_pool(n):
 
 def cpu_baseline(w, t, target_s=15.0):
     """Time the oracle (as it stands) on a bounded sample of the workload:
-    fwd+bwd of query heads 0, 1, 2, ... over every sequence, adding batches of
-    heads until about `target_s` seconds of host time (or the whole workload)."""
+    fwd+bwd of query heads 0, 1, 2, ... over every sequence (long sequences
+    cut to ORACLE_PREFIX tokens), adding batches of heads until about
+    `target_s` seconds of host time (or the whole workload)."""
     cores = os.cpu_count() or 1
     n_seq = max(1, sum(1 for L in w.lengths if L))
     per_batch = max(1, cores // n_seq)
@@ -201,8 +222,9 @@ def cpu_baseline(w, t, target_s=15.0):
     flops = _sample_flops(w, list(range(done)))
     scope = "all" if done == w.Hq else f"0..{done - 1} of {w.Hq}"
     return {"value": flops / spent / 1e12, "unit": UNIT, "cores": cores, "kind": "oracle",
-            "sample": f"fp64 oracle fwd+bwd of query heads {scope} over all {w.B} sequences of the "
-                      f"'{w.name}' workload ({spent:.1f} s, process pool of {cores}, one BLAS thread each)",
+            "sample": f"fp64 oracle fwd+bwd of query heads {scope} on the '{w.name}' workload: "
+                      f"{_sample_scope(w)} ({spent:.1f} s, process pool of {cores}, one BLAS thread each); "
+                      f"TFLOPS counted on the sample's own valid pairs",
             "seconds": spent}
 
 
@@ -215,28 +237,29 @@ def run_reference(a):
     w = inputs.make_workload(a.config)
     t = inputs.make_tensors(w, with_grad=True)
     cores = os.cpu_count() or 1
-    fwd_only = a.fwd_only
+    n_seq = max(1, sum(1 for L in w.lengths if L))
+    nh = max(1, min(w.Hq, cores // n_seq))   # query heads per step: one pool's worth of work
     with _spawn_pool(cores) as pool:
         times = []
         for i in range(a.warmup + a.steps):
-            h = i % w.Hq
-            items = _oracle_items(w, t, [h])
+            heads = [(i * nh + j) % w.Hq for j in range(nh)]
+            items = _oracle_items(w, t, heads)
             t0 = time.perf_counter()
             pool.map(_oracle_item, items)
             dt = time.perf_counter() - t0
             if i >= a.warmup:
                 times.append(dt)
-    flops = _sample_flops(w, [0])
+    flops = _sample_flops(w, list(range(nh)))
     mean = sum(times) / len(times)
     value = flops / mean / 1e12
+    sample = (f"fp64 oracle fwd+bwd of {nh} query head(s) per step (rotating) on the '{w.name}' workload: "
+              f"{_sample_scope(w)}")
     line = {"impl": "reference", "metric": METRIC, "value": value, "unit": UNIT, "n_gpus": a.gpus,
             "steps": a.steps, "warmup": a.warmup, "ms_per_step": mean * 1e3, "higher_is_better": True,
             "scaling": "weak", "vs_baseline": None, "dtype": "f64", "data": "synthetic",
             "config": {"workload": w.name, "sequences": w.B, "tokens": w.T, "Hq": w.Hq, "Hkv": w.Hkv, "D": w.D,
-                       "cp_size": w.cp_size, "causal": True, "step": "fwd+bwd" if not fwd_only else "fwd",
-                       "sample": "one query head (rotating) over all sequences per step"},
-            "cpu_baseline": {"value": value, "unit": UNIT, "cores": cores, "kind": "oracle",
-                             "sample": "fp64 oracle fwd+bwd, one query head over all sequences per step"},
+                       "cp_size": w.cp_size, "causal": True, "step": "fwd+bwd", "sample": sample},
+            "cpu_baseline": {"value": value, "unit": UNIT, "cores": cores, "kind": "oracle", "sample": sample},
             "e2e": {"value": value, "unit": UNIT, "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0}}
     print(json.dumps(line), flush=True)
     return 0
@@ -261,6 +284,132 @@ def weak_scaling_tflops(step_flops: float, world: int, ms_max: float) -> float:
 
 
 # ----------------------------------------------------------------- GPU arm
+class Case:
+    """One synthetic workload resident in HBM, with the library calls of one
+    fwd+bwd step bound to its buffers (inputs are never re-created inside a
+    timed region)."""
+
+    def __init__(self, w, t, dev, stream):
+        import torch
+        from packed_sequence_context_gb300 import thd_attn as T
+        self.T, self.w, self.stream = T, w, stream
+        self.q, self.k, self.v, self.do = (t[x].to(dev) for x in ("q", "k", "v", "do"))
+        self.cu = torch.from_numpy(w.cu_seqlens).to(dev)
+        self.cu_pad = torch.from_numpy(w.cu_seqlens_padded).to(dev)   # separately allocated
+        self.o = torch.empty_like(self.q)
+        self.lse = torch.empty((w.Hq, w.T), dtype=torch.float32, device=dev)
+        self.dq = torch.empty((w.dq_rows, w.Hq, w.D), dtype=torch.bfloat16, device=dev)
+        self.dk = torch.empty((w.dkv_rows, w.Hkv, w.D), dtype=torch.bfloat16, device=dev)
+        self.dv = torch.empty_like(self.dk)
+        self.st = torch.zeros(1, dtype=torch.int32, device=dev)
+        ws = lambda b: torch.empty(max(256, T.thd_workspace_size(w.B, w.T, w.T, w.Hq, w.Hkv, w.D, w.cp_size, b)),
+                                   dtype=torch.uint8, device=dev)
+        self.wsf, self.wsb = ws(0), ws(1)
+        self.fwd_flops, self.both_flops = algorithmic_flops(w)
+
+    def fwd(self, pad_flag=-1, cu_pad=None):
+        w, T = self.w, self.T
+        cp = self.cu_pad if cu_pad is None else cu_pad
+        rc = T.thd_attn_fwd(self.q, self.k, self.v, self.o, self.lse, self.cu, self.cu, cp, cp, w.B, w.T, w.T, w.Hq,
+                            w.Hkv, w.D, 1, w.softmax_scale, w.cp_size, pad_flag, self.wsf, self.wsf.numel(), self.st,
+                            self.stream.cuda_stream)
+        assert rc == 0, T.thd_status_string(rc)
+
+    def bwd(self, pad_flag=-1, cu_pad=None):
+        w, T = self.w, self.T
+        cp = self.cu_pad if cu_pad is None else cu_pad
+        rc = T.thd_attn_bwd(self.q, self.k, self.v, self.o, self.lse, self.do, self.dq, self.dk, self.dv, w.dq_rows,
+                            w.dkv_rows, self.cu, self.cu, cp, cp, w.B, w.T, w.T, w.Hq, w.Hkv, w.D, 1, w.softmax_scale,
+                            w.cp_size, pad_flag, self.wsb, self.wsb.numel(), self.st, self.stream.cuda_stream)
+        assert rc == 0, T.thd_status_string(rc)
+
+    def step(self, pad_flag=-1, cu_pad=None):
+        self.fwd(pad_flag, cu_pad)
+        self.bwd(pad_flag, cu_pad)
+
+    def check(self):
+        code = int(self.st.item())
+        assert code == 0, self.T.thd_status_string(code)
+
+
+def algorithmic_flops(w):
+    from packed_sequence_context_gb300 import inputs
+    return inputs.algorithmic_flops(w.lengths, w.Hq, w.D)
+
+
+def timed(fn, n, stream, flush_buf, kernel_id=0, records_per_call=1, world=1):
+    """n calls of fn, L2 flushed (256 MiB write) before each, outside the
+    events; per call the CUDA-event time on `stream`; with kernel_id, the
+    library hook's per-launch times of that kernel.  Returns (ms list,
+    kernel ms list, launches of the library in the timed calls)."""
+    import torch
+    from packed_sequence_context_gb300 import thd_attn as T
+    evs = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)) for _ in range(n)]
+    T.thd_profile_enable(kernel_id, n * records_per_call)
+    n0 = T.thd_launch_count()
+    if world > 1:
+        import torch.distributed as dist
+        dist.barrier()
+    torch.cuda.synchronize()
+    for e0, e1 in evs:
+        flush_buf.zero_()
+        e0.record(stream)
+        fn()
+        e1.record(stream)
+    torch.cuda.synchronize()
+    if world > 1:
+        import torch.distributed as dist
+        dist.barrier()
+    launches = T.thd_launch_count() - n0
+    kms = T.thd_profile_read(n * records_per_call) if kernel_id else []
+    T.thd_profile_enable(0, 0)
+    return [e0.elapsed_time(e1) for e0, e1 in evs], kms, launches
+
+
+def _mean(x):
+    return sum(x) / len(x) if x else float("nan")
+
+
+def tensor_roofline(kernel, flops, kms, peak, peak_sus, peak_kind, workload, executed=False):
+    """The kernel's achieved TFLOP/s: its work per launch over the mean
+    per-launch CUDA-event time (library hook), against the bf16 peak."""
+    k = _mean(kms)
+    ach = flops / (k * 1e-3) / 1e12
+    r = {"bound": "tensor", "kernel": kernel, "achieved": ach, "peak": peak, "unit": "TFLOP/s", "frac": ach / peak,
+         "peak_kind": f"bf16 burst ({peak_kind})", "frac_of_sustained": ach / peak_sus, "kernel_ms": k,
+         "traffic": _kernel_traffic(kernel, workload)}
+    if executed:
+        r["flops"] = "executed (S and dP recomputed: 1.5x the forward's matmuls, 0.5x algorithmic)"
+    return r
+
+
+def measure_case(c, steps, warmup, stream, flush_buf, peaks, world=1):
+    """fwd+bwd steps, forward-only calls and backward-only calls of one
+    workload; TFLOPS on algorithmic work and the three attention kernels'
+    rooflines."""
+    from packed_sequence_context_gb300 import thd_attn as T
+    peak, peak_sus, _, peak_kind = peaks
+    for _ in range(max(warmup, 3)):
+        flush_buf.zero_()
+        c.step()
+    c.check()
+    both, kms, launches = timed(c.step, steps, stream, flush_buf, T.THD_KERNEL_BWD, 1, world)
+    fwd, fkms, _ = timed(c.fwd, steps, stream, flush_buf, T.THD_KERNEL_FWD, 1, world)
+    _, dkms, _ = timed(c.bwd, max(3, min(steps, 20)), stream, flush_buf, T.THD_KERNEL_BWD_DQ, 1, world)
+    c.check()
+    name = c.w.name
+    return {
+        "ms_fwdbwd": _mean(both), "ms_fwd": _mean(fwd), "launches_per_step": launches / steps,
+        "fwdbwd_tflops": c.both_flops / (_mean(both) * 1e-3) / 1e12,
+        "fwd_tflops": c.fwd_flops / (_mean(fwd) * 1e-3) / 1e12,
+        "roofline": tensor_roofline("bwd_kernel", 2.0 * c.fwd_flops, kms, peak, peak_sus, peak_kind, name),
+        "fwd_roofline": tensor_roofline("fwd_kernel", c.fwd_flops, fkms, peak, peak_sus, peak_kind, name),
+        "dq_roofline": tensor_roofline("dq_kernel", 1.5 * c.fwd_flops, dkms, peak, peak_sus, peak_kind, name,
+                                       executed=True),
+        "_times": both,
+    }
+
+
 def run_ours(a):
     import torch
     import torch.distributed as dist
@@ -277,7 +426,8 @@ def run_ours(a):
     if world > 1:
         dist.init_process_group("nccl", device_id=torch.device("cuda", local))
     T.lib()
-    peak, peak_sus, hbm, peak_kind = _peaks()
+    peaks = _peaks()
+    peak, peak_sus, hbm, peak_kind = peaks
 
     w = inputs.make_workload(a.config)
     t = inputs.make_tensors(w, with_grad=True)
@@ -287,91 +437,49 @@ def run_ours(a):
         cpu = cpu_baseline(w, t)
 
     dev = torch.device("cuda", local)
-    q, k, v, do = (t[x].to(dev) for x in ("q", "k", "v", "do"))
-    cu = torch.from_numpy(w.cu_seqlens).to(dev)
-    cu_pad = torch.from_numpy(w.cu_seqlens_padded).to(dev)
-    B, Tq = w.B, w.T
-    o = torch.empty_like(q)
-    lse = torch.empty((w.Hq, Tq), dtype=torch.float32, device=dev)
-    dq = torch.empty((w.dq_rows, w.Hq, w.D), dtype=torch.bfloat16, device=dev)
-    dk = torch.empty((w.dkv_rows, w.Hkv, w.D), dtype=torch.bfloat16, device=dev)
-    dv = torch.empty_like(dk)
-    st = torch.zeros(1, dtype=torch.int32, device=dev)
-    wsf = torch.empty(T.thd_workspace_size(B, Tq, Tq, w.Hq, w.Hkv, w.D, w.cp_size, 0), dtype=torch.uint8, device=dev)
-    wsb = torch.empty(T.thd_workspace_size(B, Tq, Tq, w.Hq, w.Hkv, w.D, w.cp_size, 1), dtype=torch.uint8, device=dev)
-    flush_buf = torch.empty(256 << 20, dtype=torch.uint8, device=dev)
     stream = torch.cuda.current_stream()
-    sptr = stream.cuda_stream
-
-    def fwd():
-        rc = T.thd_attn_fwd(q, k, v, o, lse, cu, cu, cu_pad, cu_pad, B, Tq, Tq, w.Hq, w.Hkv, w.D, 1,
-                            w.softmax_scale, w.cp_size, -1, wsf, wsf.numel(), st, sptr)
-        assert rc == 0, T.thd_status_string(rc)
-
-    def bwd():
-        rc = T.thd_attn_bwd(q, k, v, o, lse, do, dq, dk, dv, w.dq_rows, w.dkv_rows, cu, cu, cu_pad, cu_pad, B, Tq,
-                            Tq, w.Hq, w.Hkv, w.D, 1, w.softmax_scale, w.cp_size, -1, wsb, wsb.numel(), st, sptr)
-        assert rc == 0, T.thd_status_string(rc)
-
-    def step():
-        fwd()
-        if not a.fwd_only:
-            bwd()
-
-    def timed(fn, n, kernel_id):
-        evs = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)) for _ in range(n)]
-        T.thd_profile_enable(kernel_id, n)
-        n0 = T.thd_launch_count()
-        if world > 1:
-            dist.barrier()
-        torch.cuda.synchronize()
-        for e0, e1 in evs:
-            flush_buf.zero_()
-            e0.record(stream)
-            fn()
-            e1.record(stream)
-        torch.cuda.synchronize()
-        if world > 1:
-            dist.barrier()
-        launches = T.thd_launch_count() - n0
-        kms = T.thd_profile_read(n)
-        T.thd_profile_enable(0, 0)
-        return [e0.elapsed_time(e1) for e0, e1 in evs], kms, launches
-
-    fwd_flops, both_flops = inputs.algorithmic_flops(w.lengths, w.Hq, w.D)
-    step_flops = fwd_flops if a.fwd_only else both_flops
+    flush_buf = torch.empty(256 << 20, dtype=torch.uint8, device=dev)
+    c = Case(w, t, dev, stream)
+    step = c.fwd if a.fwd_only else c.step
+    step_flops = c.fwd_flops if a.fwd_only else c.both_flops
     for _ in range(max(a.warmup, 3)):
         flush_buf.zero_()
         step()
     torch.cuda.synchronize()
-    assert int(st.item()) == 0, T.thd_status_string(int(st.item()))
+    c.check()
 
     main_kernel = T.THD_KERNEL_FWD if a.fwd_only else T.THD_KERNEL_BWD
     with ClockSampler(local) as clk:
-        times, kms, launches = timed(step, a.steps, main_kernel)
-        fwd_times, fwd_kms, _ = timed(fwd, a.steps, T.THD_KERNEL_FWD)
-        dq_kms = None
+        times, kms, launches = timed(step, a.steps, stream, flush_buf, main_kernel, 1, world)
+        fwd_times, fwd_kms, _ = timed(c.fwd, a.steps, stream, flush_buf, T.THD_KERNEL_FWD, 1, world)
+        dq_kms = []
         if not a.fwd_only:
-            _, dq_kms, _ = timed(bwd, max(3, min(a.steps, 20)), T.THD_KERNEL_BWD_DQ)
-    assert int(st.item()) == 0, T.thd_status_string(int(st.item()))
+            _, dq_kms, _ = timed(c.bwd, max(3, min(a.steps, 20)), stream, flush_buf, T.THD_KERNEL_BWD_DQ, 1, world)
+    c.check()
 
-    ms = sum(times) / len(times)
+    ms = _mean(times)
     ms_max = slowest_rank_ms(ms, world, dev)
     value = weak_scaling_tflops(step_flops, world, ms_max)
-    fwd_ms = sum(fwd_times) / len(fwd_times)
-    fwd_tflops = fwd_flops / (fwd_ms * 1e-3) / 1e12
-
-    # algorithmic work of the dominant kernel: the forward's two matmuls, or
-    # the dK/dV kernel's four (S^T, dP^T, dV, dK: twice the forward)
-    main_flops = fwd_flops if a.fwd_only else 2.0 * fwd_flops
-    kavg = sum(kms) / len(kms) if kms else float("nan")
-    achieved = main_flops / (kavg * 1e-3) / 1e12
-    fk = sum(fwd_kms) / len(fwd_kms) if fwd_kms else float("nan")
-    fwd_kernel_tflops = fwd_flops / (fk * 1e-3) / 1e12
+    fwd_ms = _mean(fwd_times)
+    fwd_tflops = c.fwd_flops / (fwd_ms * 1e-3) / 1e12
+    fwd_roof = tensor_roofline("fwd_kernel", c.fwd_flops, fwd_kms, peak, peak_sus, peak_kind, w.name)
+    if a.fwd_only:
+        roof = fwd_roof
+    else:
+        # the dominant kernel: dK/dV, four matmuls per tile pair (S^T, dP^T, dV, dK: twice the forward's)
+        roof = tensor_roofline("bwd_kernel", 2.0 * c.fwd_flops, kms, peak, peak_sus, peak_kind, w.name)
+    dq_roof = None if not dq_kms else tensor_roofline("dq_kernel", 1.5 * c.fwd_flops, dq_kms, peak, peak_sus,
+                                                      peak_kind, w.name, executed=True)
 
     e2e = None
     if not a.no_e2e:
         e2e = e2e_measure(a, w, t, dev, stream, step_flops)
+
+    extras = {}
+    if rank == 0 and world == 1 and not a.no_extras and not a.fwd_only:
+        del c
+        torch.cuda.empty_cache()
+        extras = bench_extras(a.config, dev, stream, flush_buf, peaks)
 
     if rank == 0:
         line = {
@@ -382,32 +490,50 @@ def run_ours(a):
                        "cp_size": w.cp_size, "causal": True, "step": "fwd" if a.fwd_only else "fwd+bwd",
                        "grad_rows": w.dq_rows, "l2": "flushed between timed steps (256 MiB write)",
                        "parallelism": f"replicas x{world}"},
+            "frac_of_peak": value / world / peak,
             "fwd_tflops": fwd_tflops, "fwd_ms": fwd_ms, "fwd_frac_of_peak": fwd_tflops / peak,
-            "roofline": {"bound": "tensor", "kernel": "bwd_kernel" if not a.fwd_only else "fwd_kernel",
-                         "achieved": achieved, "peak": peak, "unit": "TFLOP/s", "frac": achieved / peak,
-                         "peak_kind": f"bf16 burst ({peak_kind})", "frac_of_sustained": achieved / peak_sus,
-                         "kernel_ms": kavg,
-                         "traffic": _kernel_traffic("fwd_kernel" if a.fwd_only else "bwd_kernel", w.name)},
-            "fwd_roofline": {"bound": "tensor", "kernel": "fwd_kernel", "achieved": fwd_kernel_tflops, "peak": peak,
-                             "unit": "TFLOP/s", "frac": fwd_kernel_tflops / peak, "kernel_ms": fk,
-                             "traffic": _kernel_traffic("fwd_kernel", w.name)},
-            "dq_roofline": None if not dq_kms else {
-                "bound": "tensor", "kernel": "dq_kernel", "unit": "TFLOP/s", "peak": peak,
-                "kernel_ms": sum(dq_kms) / len(dq_kms),
-                # executed: S, dP (recomputed) and dQ, 1.5x the forward's matmuls; of these only dQ
-                # (0.5x) counts toward the algorithmic backward
-                "achieved": 1.5 * fwd_flops / (sum(dq_kms) / len(dq_kms) * 1e-3) / 1e12,
-                "frac": 1.5 * fwd_flops / (sum(dq_kms) / len(dq_kms) * 1e-3) / 1e12 / peak,
-                "flops": "executed (S and dP recomputed)"},
+            "roofline": roof,
+            "fwd_roofline": fwd_roof,
+            "dq_roofline": dq_roof,
             "gpu_launches": launches,
             "clocks": clk.summary(),
             "cpu_baseline": cpu,
             "e2e": e2e,
+            **extras,
         }
         print(json.dumps(line), flush=True)
     if world > 1:
         dist.destroy_process_group()
     return 0
+
+
+def bench_extras(main_config, dev, stream, flush_buf, peaks, steps=20, warmup=3):
+    """The other measured workloads and kernels, timed after the main line
+    (one GPU, rank 0): per_config (every other named workload's fwd and
+    fwd+bwd TFLOPS with the three kernels' rooflines), the HBM-bound kernels
+    against the copy peak, the materialised ring with bf16 partials, and the
+    four-arm ABBA timing of value-equal padded metadata."""
+    import torch
+    from packed_sequence_context_gb300 import inputs
+
+    out = {"per_config": {}}
+    for name in ("fwdbwd", "padded", "packed"):
+        if name == main_config:
+            continue
+        w = inputs.make_workload(name)
+        c = Case(w, inputs.make_tensors(w, with_grad=True), dev, stream)
+        r = measure_case(c, steps, warmup, stream, flush_buf, peaks)
+        r.pop("_times")
+        r.update({"tokens": w.T, "sequences": w.B, "Hq": w.Hq, "Hkv": w.Hkv, "cp_size": w.cp_size,
+                  "fwd_frac_of_peak": r["fwd_tflops"] / peaks[0], "fwdbwd_frac_of_peak": r["fwdbwd_tflops"] / peaks[0],
+                  "steps": steps})
+        out["per_config"][name] = r
+        del c
+        torch.cuda.empty_cache()
+    out["hbm_kernels"] = hbm_kernel_lines(dev, stream, flush_buf, peaks, steps, warmup)
+    out["ring_bf16"] = ring_bf16_line(dev, stream, flush_buf, peaks, steps, warmup)
+    out["regression_arms"] = abba_arms(dev, stream, flush_buf, steps=5, rounds=3)
+    return out
 
 
 def run_a2a(a):
@@ -509,10 +635,11 @@ def run_a2a(a):
 
 
 # ----------------------------------------------------------------- HBM-bound kernels
-def merge_bytes(T: int, H: int, D: int) -> int:
-    """thd_lse_merge, per launch: reads O and lse of both sides (fp32), writes
-    the merged O and lse."""
-    return 3 * T * H * (4 * D + 4)
+def merge_bytes(T: int, H: int, D: int, part_bytes: int = 4) -> int:
+    """thd_lse_merge (part_bytes 4) / thd_lse_merge_bf16 (2), per launch: reads
+    the fp32 accumulator's O and lse and the partial's O (part_bytes per
+    element) and lse, writes the merged O and lse."""
+    return T * H * (2 * (4 * D + 4) + part_bytes * D + 4)
 
 
 def tail_zero_bytes(dq_rows: int, dkv_rows: int, end_q: int, end_kv: int, Hq: int, Hkv: int, D: int) -> int:
@@ -534,77 +661,165 @@ def a2a_step_bytes(T: int, Hq: int, Hkv: int, D: int) -> int:
     return sum(a2a_move_bytes(T, H, D) for H in fwd_in + fwd_out + bwd_in + bwd_out)
 
 
-def run_hbm_kernels(a):
-    """One JSON line per HBM-bound kernel: algorithmic bytes per launch over the
-    mean duration of `steps` launches (after `warmup`), taken with the
-    library's profiling hook (CUDA events recorded on the launching stream
-    right around the kernel), L2 flushed between launches, against the
-    measured copy peak."""
-    import torch
+def hbm_line(kernel, workload, nbytes, kms, peaks, extra=None):
+    _, _, hbm, peak_kind = peaks
+    ms = _mean(kms)
+    gbs = nbytes / (ms * 1e-3) / 1e9
+    return {"kernel": kernel, "workload": workload, "bound": "hbm", "achieved": gbs, "peak": hbm, "unit": "GB/s",
+            "frac": gbs / hbm, "peak_kind": f"copy ({peak_kind})", "bytes_per_launch": nbytes, "kernel_ms": ms,
+            "launches": len(kms), **(extra or {})}
 
+
+def hbm_kernel_lines(dev, stream, flush_buf, peaks, steps=20, warmup=3):
+    """The HBM-bound kernels, each on its own buffers: algorithmic bytes per
+    launch over the library hook's per-launch CUDA-event time (L2 flushed
+    between launches), against the measured copy peak."""
+    import torch
     from packed_sequence_context_gb300 import inputs
     from packed_sequence_context_gb300 import thd_attn as T
 
-    if not torch.cuda.is_available():
-        raise SystemExit("bench.py needs a CUDA GPU")
-    T.lib()
-    _, _, hbm, peak_kind = _peaks()
-    dev = torch.device("cuda", 0)
-    flush_buf = torch.empty(256 << 20, dtype=torch.uint8, device=dev)
-
-    def time_it(fn, kernel_id):
-        for _ in range(max(a.warmup, 3)):
+    def run(fn, kernel_id):
+        for _ in range(warmup):
             fn()
-        torch.cuda.synchronize()
-        T.thd_profile_enable(kernel_id, a.steps)
-        for _ in range(a.steps):
-            flush_buf.zero_()
-            fn()
-        torch.cuda.synchronize()
-        kms = T.thd_profile_read(a.steps)
-        T.thd_profile_enable(0, 0)
-        assert len(kms) == a.steps, (kernel_id, len(kms))
-        return sum(kms) / len(kms)
+        _, kms, _ = timed(fn, steps, stream, flush_buf, kernel_id)
+        assert len(kms) == steps, (kernel_id, len(kms))
+        return kms
 
-    def line(kernel, workload, nbytes, ms, extra):
-        gbs = nbytes / (ms * 1e-3) / 1e9
-        print(json.dumps({"kernel": kernel, "workload": workload, "bound": "hbm", "achieved": gbs, "peak": hbm,
-                          "unit": "GB/s", "frac": gbs / hbm, "peak_kind": f"copy ({peak_kind})",
-                          "bytes_per_launch": nbytes, "ms": ms, "steps": a.steps, **extra}), flush=True)
-
-    # LSE merge: two fp32 partials of the packed workload's shape (finite lse on every row)
+    lines = {}
+    g = torch.Generator(device=dev).manual_seed(11)
+    # LSE merge: two partials of the packed workload's shape (finite lse on every row)
     w = inputs.make_workload("packed")
     Tn, H, D = w.T, w.Hq, w.D
-    g = torch.Generator(device=dev).manual_seed(11)
     o_acc = torch.randn((Tn, H, D), generator=g, device=dev)
-    o_part = torch.randn((Tn, H, D), generator=g, device=dev)
     l_acc = torch.randn((H, Tn), generator=g, device=dev)
     l_part = torch.randn((H, Tn), generator=g, device=dev)
-    ms = time_it(lambda: T.lse_merge(o_acc, l_acc, o_part, l_part), T.THD_KERNEL_LSE_MERGE)
-    line("lse_merge_kernel", "packed (fp32 partials)", merge_bytes(Tn, H, D), ms, {})
-
+    o_part = torch.randn((Tn, H, D), generator=g, device=dev)
+    kms = run(lambda: T.lse_merge(o_acc, l_acc, o_part, l_part), T.THD_KERNEL_LSE_MERGE)
+    lines["lse_merge"] = hbm_line("lse_merge_kernel<float>", "packed (fp32 partials)", merge_bytes(Tn, H, D), kms,
+                                  peaks)
+    o_part16 = o_part.to(torch.bfloat16)
+    del o_part
+    kms = run(lambda: T.lse_merge_bf16(o_acc, l_acc, o_part16, l_part), T.THD_KERNEL_LSE_MERGE)
+    lines["lse_merge_bf16"] = hbm_line("lse_merge_kernel<bf16>", "packed (bf16 partial into fp32)",
+                                       merge_bytes(Tn, H, D, part_bytes=2), kms, peaks)
+    del o_acc, o_part16
     # gradient tail-zero: the fwdbwd workload's dQ/dK/dV buffers, 10% slack past the last sequence
     w = inputs.make_workload("fwdbwd")
     dq = torch.empty((w.dq_rows, w.Hq, w.D), dtype=torch.bfloat16, device=dev)
     dk = torch.empty((w.dkv_rows, w.Hkv, w.D), dtype=torch.bfloat16, device=dev)
     dv = torch.empty_like(dk)
     cup = torch.from_numpy(w.cu_seqlens_padded).to(dev)
-    ms = time_it(lambda: T.grad_tail_zero(dq, dk, dv, cup, cup), T.THD_KERNEL_TAIL_ZERO)
+    kms = run(lambda: T.grad_tail_zero(dq, dk, dv, cup, cup), T.THD_KERNEL_TAIL_ZERO)
     end = int(w.cu_seqlens_padded[-1])
-    line("tail_zero_kernel", "fwdbwd (dQ/dK/dV slack rows)",
-         tail_zero_bytes(w.dq_rows, w.dkv_rows, end, end, w.Hq, w.Hkv, w.D), ms,
-         {"slack_rows": w.dq_rows - end})
+    lines["tail_zero"] = hbm_line("tail_zero_kernel", "fwdbwd (dQ/dK/dV slack rows)",
+                                  tail_zero_bytes(w.dq_rows, w.dkv_rows, end, end, w.Hq, w.Hkv, w.D), kms, peaks,
+                                  {"slack_rows": w.dq_rows - end})
+    # no tail (the buffer ends at the last sequence): the host flag launches nothing
+    n0 = T.thd_launch_count()
+    T.grad_tail_zero(dq[:end], dk[:end], dv[:end], cup, cup, host_knows_no_tail=True)
+    lines["tail_zero"]["launches_when_host_knows_no_tail"] = T.thd_launch_count() - n0
+    del dq, dk, dv
+    torch.cuda.empty_cache()
+    return lines
 
-    # A2A move of one tensor: the packed workload's q shards -> Ulysses member layout (cp 4, a2a 4)
+
+def ring_bf16_line(dev, stream, flush_buf, peaks, steps=20, warmup=3):
+    """The materialised ring on the packed workload: every ring step's
+    partial written in bf16 (thd_attn_fwd_step_bf16) and merged into an fp32
+    accumulator (thd_lse_merge_bf16), cp_size steps per forward."""
+    import torch
+    from packed_sequence_context_gb300 import inputs
+    from packed_sequence_context_gb300 import thd_attn as T
+
     w = inputs.make_workload("packed")
-    x = torch.randn((w.cp_size, w.T // w.cp_size, w.Hq, w.D), generator=g, device=dev).to(torch.bfloat16)
-    y = torch.empty((w.cp_size, w.T, w.Hq // w.cp_size, w.D), dtype=torch.bfloat16, device=dev)
+    t = inputs.make_tensors(w)
+    q, k, v = (t[x].to(dev) for x in ("q", "k", "v"))
+    cu = torch.from_numpy(w.cu_seqlens).to(dev)
     cup = torch.from_numpy(w.cu_seqlens_padded).to(dev)
+    o_part = torch.empty((w.T, w.Hq, w.D), dtype=torch.bfloat16, device=dev)
+    l_part = torch.empty((w.Hq, w.T), dtype=torch.float32, device=dev)
+    o_acc = torch.empty((w.T, w.Hq, w.D), dtype=torch.float32, device=dev)
+    l_acc = torch.empty((w.Hq, w.T), dtype=torch.float32, device=dev)
     st = torch.zeros(1, dtype=torch.int32, device=dev)
-    ms = time_it(lambda: T.cp_a2a(x, cup, cp_size=w.cp_size, a2a_size=w.cp_size, direction=T.THD_A2A_TO_GROUPS,
-                                  out=y, dev_status=st), T.THD_KERNEL_A2A)
-    T.check_status(st)
-    line("a2a_kernel", "packed (q, shards -> Ulysses members)", a2a_move_bytes(w.T, w.Hq, w.D), ms, {})
+    ws = torch.empty(T.thd_workspace_size(w.B, w.T, w.T, w.Hq, w.Hkv, w.D, w.cp_size, 0), dtype=torch.uint8,
+                     device=dev)
+
+    def ring():
+        o_acc.zero_()
+        l_acc.fill_(float("-inf"))
+        for i in range(w.cp_size):
+            rc = T.thd_attn_fwd_step_bf16(q, k, v, o_part, l_part, cu, cu, cup, cup, w.B, w.T, w.T, w.Hq, w.Hkv,
+                                          w.D, 1, w.softmax_scale, w.cp_size, -1, i, ws, ws.numel(), st,
+                                          stream.cuda_stream)
+            assert rc == 0
+            T.lse_merge_bf16(o_acc, l_acc, o_part, l_part)
+
+    for _ in range(warmup):
+        ring()
+    times, kms, launches = timed(ring, steps, stream, flush_buf, T.THD_KERNEL_LSE_MERGE, w.cp_size)
+    assert int(st.item()) == 0
+    fwd_flops, _ = algorithmic_flops(w)
+    ms = _mean(times)
+    return {"workload": w.name, "cp_size": w.cp_size, "ms_per_forward": ms,
+            "fwd_tflops": fwd_flops / (ms * 1e-3) / 1e12, "launches_per_forward": launches / steps,
+            "merge": hbm_line("lse_merge_kernel<bf16>", "packed ring step (bf16 partial into fp32)",
+                              merge_bytes(w.T, w.Hq, w.D, part_bytes=2), kms, peaks),
+            "note": "each forward also clears the fp32 accumulator (two torch fills, inside the events)"}
+
+
+def abba_arms(dev, stream, flush_buf, steps=5, rounds=3):
+    """The value-equal padded-metadata case of the pages' regression report,
+    timed in ABBA order on the packed workload's fwd+bwd step: arms
+    pad_between_seqs -1 with cu_seqlens_padded the same pointer as
+    cu_seqlens, -1 with a value-equal clone, 0, and 1.  Per arm: mean ms per
+    step, library launches per step, and whether O, dQ, dK, dV equal the first
+    arm's bit for bit."""
+    import torch
+    from packed_sequence_context_gb300 import inputs
+    from packed_sequence_context_gb300 import thd_attn as T
+
+    w = inputs.make_workload("packed")
+    c = Case(w, inputs.make_tensors(w, with_grad=True), dev, stream)
+    arms = {"auto_same_pointer": (-1, c.cu), "auto_value_equal_clone": (-1, c.cu_pad),
+            "flag_0_no_padding": (0, c.cu_pad), "flag_1_padding": (1, c.cu_pad)}
+    names = list(arms)
+    for n in names:
+        c.step(*arms[n])
+    torch.cuda.synchronize()
+    c.check()
+    order = (names + names[::-1]) * rounds
+    acc = {n: [] for n in names}
+    launches = {n: [] for n in names}
+    ref = None
+    same = {n: True for n in names}
+    for n in order:
+        ts, _, nl = timed(lambda: c.step(*arms[n]), steps, stream, flush_buf)
+        acc[n].extend(ts)
+        launches[n].append(nl / steps)
+        outs = [c.o.clone(), c.dq.clone(), c.dk.clone(), c.dv.clone()]
+        if ref is None:
+            ref = outs
+        same[n] = same[n] and all(torch.equal(x, y) for x, y in zip(ref, outs))
+    c.check()
+    return {"workload": w.name, "order": "ABCD DCBA x" + str(rounds), "steps_per_visit": steps,
+            "arms": {n: {"ms_per_step": _mean(acc[n]), "launches_per_step": _mean(launches[n]),
+                         "bit_identical_to_first_arm": same[n]} for n in names}}
+
+
+def run_hbm_kernels(a):
+    """One JSON line per HBM-bound kernel (the same lines the default run
+    adds under hbm_kernels)."""
+    import torch
+    from packed_sequence_context_gb300 import thd_attn as T
+
+    if not torch.cuda.is_available():
+        raise SystemExit("bench.py needs a CUDA GPU")
+    T.lib()
+    dev = torch.device("cuda", 0)
+    stream = torch.cuda.current_stream()
+    flush_buf = torch.empty(256 << 20, dtype=torch.uint8, device=dev)
+    for name, line in hbm_kernel_lines(dev, stream, flush_buf, _peaks(), a.steps, max(a.warmup, 3)).items():
+        print(json.dumps({"name": name, **line}), flush=True)
     return 0
 
 

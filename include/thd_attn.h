@@ -187,6 +187,23 @@ THD_API int thd_attn_fwd_step(const void* q, const void* k, const void* v, float
                       void* workspace, size_t workspace_bytes, int32_t* dev_status, thd_stream_t stream);
 
 /*
+ * thd_attn_fwd_step_bf16 -- thd_attn_fwd_step with the step's partial output
+ * in bf16, the precision the ring keeps its per-step outputs in when they are
+ * materialised [P1 traceback: AttnFuncWithCPAndKVP2P.forward, per-step
+ * outputs corrected into the running output]:
+ *   o_part [T_q, Hq, D] bf16 (16-byte aligned), lse_part [Hq, T_q] fp32.
+ * Same rows, masks and -inf/0 conventions as thd_attn_fwd_step; merge the
+ * steps with thd_lse_merge_bf16 into an fp32 accumulator.
+ */
+THD_API int thd_attn_fwd_step_bf16(const void* q, const void* k, const void* v, void* o_part, float* lse_part,
+                                   const int32_t* cu_seqlens_q, const int32_t* cu_seqlens_kv,
+                                   const int32_t* cu_seqlens_q_padded, const int32_t* cu_seqlens_kv_padded, int B,
+                                   int64_t T_q, int64_t T_kv, int Hq, int Hkv, int D, int causal,
+                                   float softmax_scale, int cp_size, int pad_between_seqs, int step,
+                                   void* workspace, size_t workspace_bytes, int32_t* dev_status,
+                                   thd_stream_t stream);
+
+/*
  * thd_attn_fwd_noalloc -- thd_attn_fwd for callers that cannot allocate device
  * memory where they call the library.  The pages have no counterpart to
  * this entry point; it exists for deployment.  Examples of such callers: a
@@ -257,6 +274,14 @@ THD_API int thd_lse_merge(float* o_acc, float* lse_acc, const float* o_part, con
                   int D, thd_stream_t stream);
 
 /*
+ * thd_lse_merge_bf16 -- thd_lse_merge with the incoming partial o_part in
+ * bf16 ([T, H, D], 8-byte aligned; thd_attn_fwd_step_bf16's output); the
+ * accumulator (o_acc fp32, lse_acc) and lse_part are as in thd_lse_merge.
+ */
+THD_API int thd_lse_merge_bf16(float* o_acc, float* lse_acc, const void* o_part, const float* lse_part, int64_t T,
+                               int H, int D, thd_stream_t stream);
+
+/*
  * thd_grad_tail_zero -- zero gradient rows past the last padded endpoint:
  * rows [cu_seqlens_q_padded[B], dq_rows) of dq and [cu_seqlens_kv_padded[B],
  * dkv_rows) of dk and dv (bf16, [rows, H, D]).  [P2 "Describe the bug"]:
@@ -264,6 +289,8 @@ THD_API int thd_lse_merge(float* o_acc, float* lse_acc, const float* o_part, con
  * endpoint equals the buffer end.  The endpoint is read ON THE DEVICE (no
  * host sync, graph-safe); when the caller already knows there is no tail
  * (host_knows_no_tail = 1) nothing is launched.  Any of dq/dk/dv may be NULL.
+ * An endpoint outside [0, rows] is invalid metadata: that buffer is left
+ * untouched (no write ever falls outside [0, rows) of a buffer).
  */
 THD_API int thd_grad_tail_zero(void* dq, void* dk, void* dv, int64_t dq_rows, int64_t dkv_rows, int Hq, int Hkv, int D,
                        const int32_t* cu_seqlens_q_padded, const int32_t* cu_seqlens_kv_padded, int B,

@@ -24,6 +24,7 @@
 // staging); warp 9 TMEM allocator and S^T issuer; warp 10 dV/dK/dP^T issuer.
 #include "common.cuh"
 #include "ptx.cuh"
+#include "sched.cuh"
 
 namespace thd {
 
@@ -36,7 +37,8 @@ struct BwdCfg {
   static constexpr int kOffQ = 2 * kTileBytes;                 // stage s: Q at kOffQ + s * 2 * kTileBytes
   static constexpr int kOffLse = kOffQ + kStages * 2 * kTileBytes;  // stage s: lse2[128], delta[128]
   static constexpr int kOffBar = kOffLse + kStages * 2 * kTile * 4;
-  static constexpr int kSmem = kOffBar + 256;
+  static constexpr int kOffRing = kOffBar + 256;  // the item hand-out ring
+  static constexpr int kSmem = kOffRing + 256;
   static constexpr uint32_t kTmemCols = 512;
   static constexpr uint32_t kColDV = 0, kColDK = D, kColX = 2 * D, kColY = 2 * D + 128;
 };
@@ -47,10 +49,22 @@ struct BwdItem {
   int kv_first, kv_last;  // valid key positions of the tile (first > last: none)
 };
 
-__device__ inline BwdItem bwd_item(const BwdParams& p, int w) {
+// Work item w -> (schedule entry, kv head).  Items are ordered by groups of
+// p.group_kv kv heads (outermost: while a group runs, the queries and output
+// gradients of its query heads are what the CTAs read, so they stay in L2),
+// then by schedule entry (longest first), then by the group's kv heads.
+__device__ inline BwdItem bwd_item(const BwdParams& p, int n_entries, int w) {
   BwdItem it;
-  const int4 e = p.items[w / p.Hkv];
-  it.hk = w % p.Hkv;
+  int4 e;
+  if (p.group_kv == p.Hkv) {  // one group: entry-major, kv heads innermost
+    e = p.items[w / p.Hkv];
+    it.hk = w % p.Hkv;
+  } else {
+    const int per = n_entries * p.group_kv;  // items per group
+    const int grp = w / per, rem = w - grp * per;
+    e = p.items[rem / p.group_kv];
+    it.hk = grp * p.group_kv + rem % p.group_kv;
+  }
   it.b = e.x;
   it.c = e.y;
   it.jk = e.z;
@@ -111,6 +125,7 @@ __global__ void __launch_bounds__(352, 1)
   uint64_t* bar_dv_done = bars + 7 + 2 * S;
   uint32_t* s_tmem = reinterpret_cast<uint32_t*>(bars + 8 + 2 * S);
   int* s_abort = reinterpret_cast<int*>(bars + 9 + 2 * S);
+  ItemRing* ring = reinterpret_cast<ItemRing*>(smem + C::kOffRing);  // items of this CTA, in claim order
 
   const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
   if (*p.dev_status != 0) return;
@@ -118,7 +133,8 @@ __global__ void __launch_bounds__(352, 1)
     if (tid == 0) atomicCAS(p.dev_status, 0, THD_ERR_UNSUPPORTED);
     return;
   }
-  const int n_items = p.counters[0] * p.Hkv;
+  const int n_entries = p.counters[0];
+  const int n_items = n_entries * p.Hkv;
 
   if (tid == 0) {
     mbar_init(bar_kv_full, 1);
@@ -135,6 +151,7 @@ __global__ void __launch_bounds__(352, 1)
     mbar_init(bar_drain2, 1);
     mbar_init(bar_drain, 1);
     mbar_init(bar_dv_done, 1);
+    item_ring_init(ring, 2 + 8);  // warps 9, 10 (one thread each) and the 8 compute warps
     *s_abort = 0;
     fence_mbar_init();
   }
@@ -158,8 +175,18 @@ __global__ void __launch_bounds__(352, 1)
     int stage = 0;
     uint32_t ph = 0, kv_iter = 0, n_fill = 0;
     bool ok = true;
-    for (int w = blockIdx.x; w < n_items && ok; w += gridDim.x) {
-      const BwdItem it = bwd_item(p, w);
+    int w = item_first();
+    for (uint32_t kit = 0; ok; ++kit, w = __shfl_sync(0xffffffffu, w, 0)) {
+      // publish this item (or the end marker) to the other roles, and claim
+      // the next one (lane 0's w) while this one is loaded
+      int wcur = w;
+      if (lane == 0) {
+        ok = item_publish(ring, kit, wcur, s_abort);
+        if (ok && wcur < n_items) w = item_claim(p.claim);
+      }
+      ok = __shfl_sync(0xffffffffu, ok ? 1 : 0, 0) != 0;
+      if (!ok || wcur >= n_items) break;
+      const BwdItem it = bwd_item(p, n_entries, wcur);
       if (it.kv_first > it.kv_last) continue;  // no valid key: nothing to load
       const int kv_row = it.g.kv_off + it.c * it.g.cbkv + it.jk * kTile;
       if (!mbar_wait(bar_kv_empty, (kv_iter & 1u) ^ 1u, s_abort)) break;
@@ -244,8 +271,10 @@ __global__ void __launch_bounds__(352, 1)
       int stage = 0;
       uint32_t ph = 0, su = 0, kv_iter = 0;
       bool ok = true;
-      for (int w = blockIdx.x; w < n_items && ok; w += gridDim.x) {
-        const BwdItem it = bwd_item(p, w);
+      for (uint32_t kit = 0; ok; ++kit) {
+        int w;
+        if (!item_take_one(ring, kit, w, s_abort) || w >= n_items) break;
+        const BwdItem it = bwd_item(p, n_entries, w);
         if (it.kv_first > it.kv_last) continue;
         if (!mbar_wait(bar_kv_full, kv_iter & 1u, s_abort)) break;
         ++kv_iter;
@@ -312,8 +341,10 @@ __global__ void __launch_bounds__(352, 1)
         pv_stage = -1;
         return true;
       };
-      for (int w = blockIdx.x; w < n_items && ok; w += gridDim.x) {
-        const BwdItem it = bwd_item(p, w);
+      for (uint32_t kit = 0; ok; ++kit) {
+        int w;
+        if (!item_take_one(ring, kit, w, s_abort) || w >= n_items) break;
+        const BwdItem it = bwd_item(p, n_entries, w);
         if (it.kv_first > it.kv_last) continue;
         if (!mbar_wait(bar_kv_full, kv_iter & 1u, s_abort)) break;
         ++kv_iter;
@@ -375,8 +406,14 @@ __global__ void __launch_bounds__(352, 1)
     const float sl2 = p.scale_log2;
     uint32_t su = 0;
     bool ok = true;
-    for (int w = blockIdx.x; w < n_items && ok; w += gridDim.x) {
-      const BwdItem it = bwd_item(p, w);
+    for (uint32_t kit = 0; ok; ++kit) {
+      int w;
+      if (!item_take_warp(ring, kit, w, s_abort)) {
+        ok = false;
+        break;
+      }
+      if (w >= n_items) break;
+      const BwdItem it = bwd_item(p, n_entries, w);
       const int kv_local = it.jk * kTile + row;  // row within the chunk
       const int j_pos = it.c * it.g.cbkv + kv_local;
       const bool in_chunk = kv_local < it.g.cbkv;

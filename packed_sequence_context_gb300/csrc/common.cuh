@@ -156,16 +156,32 @@ struct QItem {
   int b, r, t, h, kvh, qmax;
 };
 
-// Work item w = (schedule entry w / Hq, query head w % Hq).
+// Work item w -> (schedule entry, query head).  Items are ordered by groups
+// of p.group_kv kv heads (outermost: while a group runs, its keys and values
+// are what the CTAs read, so they stay in L2), then by schedule entry
+// (longest first), then by the group's query heads (innermost: query heads
+// that share a kv head run side by side).  With one group (group_kv == Hkv)
+// this is entry-major with every head innermost.  n_entries = schedule length.
 template <class P>
-__device__ inline QItem q_item(const P& p, int w) {
+__device__ inline QItem q_item(const P& p, int n_entries, int w) {
   QItem it;
-  const int4 e = p.items[w / p.Hq];
-  it.h = w % p.Hq;
+  if (p.group_kv == p.Hkv) {  // one group: entry-major, heads innermost
+    const int4 e = p.items[w / p.Hq];
+    it.h = w % p.Hq;
+    it.b = e.x;
+    it.r = e.y;
+    it.t = e.z;
+  } else {
+    const int hg = p.group_kv * (p.Hq / p.Hkv);  // query heads per group
+    const int per = n_entries * hg;               // items per group
+    const int grp = w / per, rem = w - grp * per;
+    const int4 e = p.items[rem / hg];
+    it.h = grp * hg + rem % hg;
+    it.b = e.x;
+    it.r = e.y;
+    it.t = e.z;
+  }
   it.kvh = it.h / (p.Hq / p.Hkv);
-  it.b = e.x;
-  it.r = e.y;
-  it.t = e.z;
   it.g = seq_geom(p.eff, p.B, it.b, p.cp);
   it.qmax = fwd_tile_qmax(it.g, it.r, it.t, p.cp);
   return it;
@@ -269,8 +285,10 @@ struct FwdParams {
   const int32_t* eff;
   const int4* items;
   const int32_t* counters;
+  int32_t* claim;  // dynamic hand-out counter (zeroed by the planner)
   int32_t* dev_status;
   int B, Hq, Hkv, cp, causal;
+  int group_kv;  // kv heads per locality group (divides Hkv)
   int64_t T_q;
   float scale_log2;  // softmax_scale * log2(e)
   int step_lo, step_hi;
@@ -286,8 +304,10 @@ struct BwdParams {
   const int32_t* eff;
   const int4* items;
   const int32_t* counters;
+  int32_t* claim;  // dynamic hand-out counter (zeroed by the planner)
   int32_t* dev_status;
   int B, Hq, Hkv, cp, causal;
+  int group_kv;  // kv heads per locality group (divides Hkv)
   int64_t T_q, dkv_rows;
   float scale, scale_log2;
 };
@@ -301,8 +321,10 @@ struct DqParams {
   const int32_t* eff;
   const int4* items;  // the query-tile schedule
   const int32_t* counters;
+  int32_t* claim;  // dynamic hand-out counter (zeroed by the planner)
   int32_t* dev_status;
   int B, Hq, Hkv, cp, causal;
+  int group_kv;  // kv heads per locality group (divides Hkv)
   int64_t T_q, dq_rows;
   float scale, scale_log2;
   int step_lo, step_hi;  // always the whole ring
@@ -311,13 +333,15 @@ struct DqParams {
 // host launchers (each returns a cudaError_t)
 cudaError_t launch_plan(const PlanParams& p, cudaStream_t st);
 cudaError_t launch_fwd(const FwdParams& p, const CUtensorMap& tk, const CUtensorMap& tv, int D, bool step_mode,
-                       int grid, cudaStream_t st);
+                       bool dyn, int grid, cudaStream_t st);
 cudaError_t launch_bwd(const BwdParams& p, const CUtensorMap& tq, const CUtensorMap& tdo, const CUtensorMap& tk,
                        const CUtensorMap& tv, int D, int grid, cudaStream_t st);
 cudaError_t launch_dq(const DqParams& p, const CUtensorMap& tk, const CUtensorMap& tv, int D, int grid,
                       cudaStream_t st);
 cudaError_t launch_lse_merge(float* o_acc, float* lse_acc, const float* o_part, const float* lse_part, int64_t T,
                              int H, int D, cudaStream_t st);
+cudaError_t launch_lse_merge_bf16(float* o_acc, float* lse_acc, const uint16_t* o_part, const float* lse_part,
+                                  int64_t T, int H, int D, cudaStream_t st);
 cudaError_t launch_tail_zero(uint16_t* dq, uint16_t* dk, uint16_t* dv, int64_t dq_rows, int64_t dkv_rows, int Hq,
                              int Hkv, int D, const int32_t* pad_q_end, const int32_t* pad_kv_end,
                              const int32_t* dev_status, cudaStream_t st);

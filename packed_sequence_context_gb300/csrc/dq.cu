@@ -34,6 +34,7 @@
 // has completed (s_free).
 #include "common.cuh"
 #include "ptx.cuh"
+#include "sched.cuh"
 
 namespace thd {
 
@@ -76,10 +77,12 @@ __global__ void __launch_bounds__(384, 1)
   __shared__ __align__(8) uint64_t bar_drain2;
   __shared__ uint32_t s_tmem;
   __shared__ int s_abort;
+  __shared__ ItemRing ring;  // items handed out to this CTA, in claim order
 
   const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
   if (*p.dev_status != 0) return;  // metadata rejected: outputs untouched
-  const int n_items = p.counters[0] * p.Hq;
+  const int n_entries = p.counters[0];
+  const int n_items = n_entries * p.Hq;
 
   if (tid == 0) {
     for (int s = 0; s < KS; ++s) {
@@ -102,6 +105,7 @@ __global__ void __launch_bounds__(384, 1)
     mbar_init(&bar_dq_done, 1);
     mbar_init(&bar_drain, 1);
     mbar_init(&bar_drain2, 1);
+    item_ring_init(&ring, 3 + 8);  // warps 9, 10, 11 (one thread each) and the 8 dS warps
     s_abort = 0;
     fence_mbar_init();
   }
@@ -123,8 +127,18 @@ __global__ void __launch_bounds__(384, 1)
     int ks = 0;
     uint32_t kph = 0, n_fill = 0, q_iter = 0;
     bool ok = true;
-    for (int w = blockIdx.x; w < n_items && ok; w += gridDim.x) {
-      const QItem it = q_item(p, w);
+    int w = item_first();
+    for (uint32_t kit = 0; ok; ++kit) {
+      // publish this item (or the end marker) to the other roles, and claim
+      // the next one while this one is loaded
+      int wnext = 0;
+      if (lane == 0) {
+        ok = item_publish(&ring, kit, w, &s_abort);
+        if (ok && w < n_items) wnext = item_claim(p.claim);
+      }
+      ok = __shfl_sync(0xffffffffu, ok ? 1 : 0, 0) != 0;
+      if (!ok || w >= n_items) break;
+      const QItem it = q_item(p, n_entries, w);
       // the item's rank-local query rows of Q and dO, once the previous
       // item's last products that read them have completed; rows without a
       // valid query are zero
@@ -167,6 +181,7 @@ __global__ void __launch_bounds__(384, 1)
           kph ^= 1u;
         }
       });
+      w = __shfl_sync(0xffffffffu, wnext, 0);
     }
     if (lane == 0) {
       for (int s = 0; s < KS; ++s) {
@@ -181,8 +196,10 @@ __global__ void __launch_bounds__(384, 1)
       int vs = 0;
       uint32_t vph = 0, n_fill = 0;
       bool ok = true;
-      for (int w = blockIdx.x; w < n_items && ok; w += gridDim.x) {
-        const QItem it = q_item(p, w);
+      for (uint32_t kit = 0; ok; ++kit) {
+        int w;
+        if (!item_take_one(&ring, kit, w, &s_abort) || w >= n_items) break;
+        const QItem it = q_item(p, n_entries, w);
         for_each_kv_tile(it, p, [&](int c, int j) {
           if (!ok) return;
           if (!mbar_wait(&bar_v_empty[vs], vph ^ 1u, &s_abort)) {
@@ -217,8 +234,10 @@ __global__ void __launch_bounds__(384, 1)
       int ks = 0;
       uint32_t kph = 0, g = 0, q_iter = 0;
       bool ok = true;
-      for (int w = blockIdx.x; w < n_items && ok; w += gridDim.x) {
-        const QItem it = q_item(p, w);
+      for (uint32_t kit = 0; ok; ++kit) {
+        int w;
+        if (!item_take_one(&ring, kit, w, &s_abort) || w >= n_items) break;
+        const QItem it = q_item(p, n_entries, w);
         int n = 0;
         for_each_kv_tile(it, p, [&](int, int) { ++n; });
         if (!mbar_wait(&bar_q_full, q_iter & 1u, &s_abort)) break;
@@ -285,8 +304,10 @@ __global__ void __launch_bounds__(384, 1)
         tc_commit(&bar_k_empty[kslot]);
         return true;
       };
-      for (int w = blockIdx.x; w < n_items && ok; w += gridDim.x) {
-        const QItem it = q_item(p, w);
+      for (uint32_t kit = 0; ok; ++kit) {
+        int w;
+        if (!item_take_one(&ring, kit, w, &s_abort) || w >= n_items) break;
+        const QItem it = q_item(p, n_entries, w);
         int n = 0;
         for_each_kv_tile(it, p, [&](int, int) { ++n; });
         if (!mbar_wait(&bar_q_full, q_iter & 1u, &s_abort)) break;
@@ -352,8 +373,14 @@ __global__ void __launch_bounds__(384, 1)
     const float sl2 = p.scale_log2;
     uint32_t g = 0, n_item = 0;
     bool ok = true;
-    for (int w = blockIdx.x; w < n_items && ok; w += gridDim.x) {
-      const QItem it = q_item(p, w);
+    for (uint32_t kit = 0; ok; ++kit) {
+      int w;
+      if (!item_take_warp(&ring, kit, w, &s_abort)) {
+        ok = false;
+        break;
+      }
+      if (w >= n_items) break;
+      const QItem it = q_item(p, n_entries, w);
       const int prow = it.t * kTile + row;
       const bool in_rank = prow < 2 * it.g.cbq;
       const int pos = in_rank ? local_to_pos(prow, it.r, it.g.cbq, p.cp) : 0;

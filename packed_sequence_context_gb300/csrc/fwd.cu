@@ -34,6 +34,7 @@
 // later QK^T only after the PV that read its P has completed (s_free).
 #include "common.cuh"
 #include "ptx.cuh"
+#include "sched.cuh"
 
 namespace thd {
 
@@ -52,7 +53,7 @@ struct FwdCfg {
 
 using FwdItem = QItem;
 
-template <int D, bool kStep>
+template <int D, bool kStep, bool kDyn>
 __global__ void __launch_bounds__(384, 1)
     fwd_kernel(const FwdParams p, const __grid_constant__ CUtensorMap tmK, const __grid_constant__ CUtensorMap tmV) {
   using C = FwdCfg<D>;
@@ -75,12 +76,14 @@ __global__ void __launch_bounds__(384, 1)
   __shared__ __align__(8) uint64_t bar_drain2;
   __shared__ uint32_t s_tmem;
   __shared__ int s_abort;
+  __shared__ ItemRing ring;             // items handed out to this CTA, in claim order
   __shared__ float s_mx[2][2][kTile];   // partial row maxima, [tile parity][half][row]
   __shared__ float s_sum[2][2][kTile];  // partial row sums, [item parity][half][row]
 
   const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
   if (*p.dev_status != 0) return;  // metadata rejected: outputs untouched
-  const int n_items = p.counters[0] * p.Hq;
+  const int n_entries = p.counters[0];
+  const int n_items = n_entries * p.Hq;
 
   if (tid == 0) {
     for (int s = 0; s < KS; ++s) {
@@ -100,6 +103,7 @@ __global__ void __launch_bounds__(384, 1)
     mbar_init(&bar_q_empty, 1);
     mbar_init(&bar_drain, 1);
     mbar_init(&bar_drain2, 1);
+    if constexpr (kDyn) item_ring_init(&ring, 3 + 8);  // warps 9, 10, 11 (one thread each) and the 8 softmax warps
     s_abort = 0;
     fence_mbar_init();
   }
@@ -121,8 +125,21 @@ __global__ void __launch_bounds__(384, 1)
     int ks = 0;
     uint32_t kph = 0, n_fill = 0, q_iter = 0;
     bool ok = true;
-    for (int w = blockIdx.x; w < n_items && ok; w += gridDim.x) {
-      const FwdItem it = q_item(p, w);
+    int w = item_first();
+    for (uint32_t kit = 0; ok; ++kit) {
+      int wnext = w + (int)gridDim.x;  // the fixed-stride walk
+      if constexpr (kDyn) {
+        // publish this item (or the end marker) to the other roles, and
+        // claim the next one while this one is loaded
+        if (lane == 0) {
+          ok = item_publish(&ring, kit, w, &s_abort);
+          if (ok && w < n_items) wnext = item_claim(p.claim);
+        }
+        ok = __shfl_sync(0xffffffffu, ok ? 1 : 0, 0) != 0;
+        if (!ok) break;
+      }
+      if (w >= n_items) break;
+      const FwdItem it = q_item(p, n_entries, w);
       // ---- the query tile: rank-local rows [128 t, 128 t + 128) of rank r,
       // gathered into 128B-swizzled smem once the previous item's last QK^T
       // has completed; rows without a valid query are zero
@@ -166,6 +183,7 @@ __global__ void __launch_bounds__(384, 1)
           kph ^= 1u;
         }
       });
+      w = kDyn ? __shfl_sync(0xffffffffu, wnext, 0) : wnext;
     }
     // every issued load must land before the CTA may exit
     if (lane == 0) {
@@ -181,8 +199,12 @@ __global__ void __launch_bounds__(384, 1)
       int vs = 0;
       uint32_t vph = 0, n_fill = 0;
       bool ok = true;
-      for (int w = blockIdx.x; w < n_items && ok; w += gridDim.x) {
-        const FwdItem it = q_item(p, w);
+      for (uint32_t kit = 0; ok; ++kit) {
+        int w = (int)(blockIdx.x + kit * gridDim.x);
+        if constexpr (kDyn)
+          if (!item_take_one(&ring, kit, w, &s_abort)) break;
+        if (w >= n_items) break;
+        const FwdItem it = q_item(p, n_entries, w);
         for_each_kv_tile(it, p, [&](int c, int j) {
           if (!ok) return;
           if (!mbar_wait(&bar_v_empty[vs], vph ^ 1u, &s_abort)) {
@@ -222,8 +244,12 @@ __global__ void __launch_bounds__(384, 1)
       int ks = 0;
       uint32_t kph = 0, g = 0, q_iter = 0;
       bool ok = true;
-      for (int w = blockIdx.x; w < n_items && ok; w += gridDim.x) {
-        const FwdItem it = q_item(p, w);
+      for (uint32_t kit = 0; ok; ++kit) {
+        int w = (int)(blockIdx.x + kit * gridDim.x);
+        if constexpr (kDyn)
+          if (!item_take_one(&ring, kit, w, &s_abort)) break;
+        if (w >= n_items) break;
+        const FwdItem it = q_item(p, n_entries, w);
         int n = 0;
         for_each_kv_tile(it, p, [&](int, int) { ++n; });
         if (!mbar_wait(&bar_q_full, q_iter & 1u, &s_abort)) break;
@@ -271,8 +297,12 @@ __global__ void __launch_bounds__(384, 1)
       int vs = 0;
       uint32_t vph = 0, g = 0;
       bool ok = true;
-      for (int w = blockIdx.x; w < n_items && ok; w += gridDim.x) {
-        const FwdItem it = q_item(p, w);
+      for (uint32_t kit = 0; ok; ++kit) {
+        int w = (int)(blockIdx.x + kit * gridDim.x);
+        if constexpr (kDyn)
+          if (!item_take_one(&ring, kit, w, &s_abort)) break;
+        if (w >= n_items) break;
+        const FwdItem it = q_item(p, n_entries, w);
         int j = 0;
         for_each_kv_tile(it, p, [&](int c, int jt) {
           if (!ok) return;
@@ -318,8 +348,16 @@ __global__ void __launch_bounds__(384, 1)
     const float sl2 = p.scale_log2;
     uint32_t g = 0, n_item = 0;
     bool ok = true;
-    for (int w = blockIdx.x; w < n_items && ok; w += gridDim.x) {
-      const FwdItem it = q_item(p, w);
+    for (uint32_t kit = 0; ok; ++kit) {
+      int w = (int)(blockIdx.x + kit * gridDim.x);
+      if constexpr (kDyn) {
+        if (!item_take_warp(&ring, kit, w, &s_abort)) {
+          ok = false;
+          break;
+        }
+      }
+      if (w >= n_items) break;
+      const FwdItem it = q_item(p, n_entries, w);
       const int prow = it.t * kTile + row;
       const bool in_rank = prow < 2 * it.g.cbq;
       const int pos = in_rank ? local_to_pos(prow, it.r, it.g.cbq, p.cp) : 0;
@@ -529,24 +567,33 @@ __global__ void __launch_bounds__(384, 1)
   if (tid == 0 && s_abort) atomicCAS(p.dev_status, 0, THD_ERR_TIMEOUT);
 }
 
-template <int D, bool kStep>
+template <int D, bool kStep, bool kDyn>
 static cudaError_t launch_fwd_t(const FwdParams& p, const CUtensorMap& tk, const CUtensorMap& tv, int grid,
                                 cudaStream_t st) {
   using C = FwdCfg<D>;
-  cudaError_t ea = cudaFuncSetAttribute(fwd_kernel<D, kStep>, cudaFuncAttributeMaxDynamicSharedMemorySize, C::kSmem);
+  cudaError_t ea =
+      cudaFuncSetAttribute(fwd_kernel<D, kStep, kDyn>, cudaFuncAttributeMaxDynamicSharedMemorySize, C::kSmem);
   if (ea != cudaSuccess) return ea;
   prof_before(THD_KERNEL_FWD, st);
-  fwd_kernel<D, kStep><<<grid, C::kThreads, C::kSmem, st>>>(p, tk, tv);
+  fwd_kernel<D, kStep, kDyn><<<grid, C::kThreads, C::kSmem, st>>>(p, tk, tv);
   count_launch();
   cudaError_t e = cudaGetLastError();
   prof_after(THD_KERNEL_FWD, st);
   return e;
 }
 
+template <int D>
+static cudaError_t launch_fwd_d(const FwdParams& p, const CUtensorMap& tk, const CUtensorMap& tv, bool step_mode,
+                                bool dyn, int grid, cudaStream_t st) {
+  if (step_mode)
+    return dyn ? launch_fwd_t<D, true, true>(p, tk, tv, grid, st) : launch_fwd_t<D, true, false>(p, tk, tv, grid, st);
+  return dyn ? launch_fwd_t<D, false, true>(p, tk, tv, grid, st) : launch_fwd_t<D, false, false>(p, tk, tv, grid, st);
+}
+
 cudaError_t launch_fwd(const FwdParams& p, const CUtensorMap& tk, const CUtensorMap& tv, int D, bool step_mode,
-                       int grid, cudaStream_t st) {
-  if (D == 128) return step_mode ? launch_fwd_t<128, true>(p, tk, tv, grid, st) : launch_fwd_t<128, false>(p, tk, tv, grid, st);
-  return step_mode ? launch_fwd_t<64, true>(p, tk, tv, grid, st) : launch_fwd_t<64, false>(p, tk, tv, grid, st);
+                       bool dyn, int grid, cudaStream_t st) {
+  return D == 128 ? launch_fwd_d<128>(p, tk, tv, step_mode, dyn, grid, st)
+                  : launch_fwd_d<64>(p, tk, tv, step_mode, dyn, grid, st);
 }
 
 }  // namespace thd

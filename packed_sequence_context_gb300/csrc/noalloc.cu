@@ -41,7 +41,11 @@ extern "C" int thd_attn_fwd_noalloc(const void* q, const void* k, const void* v,
                                     float softmax_scale, int cp_size, int pad_between_seqs, int32_t* dev_status,
                                     thd_stream_t stream) {
   const size_t need = thd_workspace_size(B, T_q, T_kv, Hq, Hkv, D, cp_size, 0);
-  if (need == 0) return THD_ERR_INVALID_ARG;
+  // sizes thd_attn_fwd rejects: let it report them (same code, nothing launched)
+  if (need == 0)
+    return thd_attn_fwd(q, k, v, o, lse, cu_seqlens_q, cu_seqlens_kv, cu_seqlens_q_padded, cu_seqlens_kv_padded, B,
+                        T_q, T_kv, Hq, Hkv, D, causal, softmax_scale, cp_size, pad_between_seqs, nullptr, 0,
+                        dev_status, stream);
   if (need > (size_t)THD_NOALLOC_SCRATCH_BYTES) return THD_ERR_WORKSPACE;  // beyond the static maximum
   void* scratch = nullptr;
   const int rc = scratch_address(&scratch);

@@ -149,7 +149,10 @@ __device__ bool plan_schedule(const PlanParams& p, const int32_t* eff, int32_t* 
     const int pos = atomicAdd(&s_hist[kCostBins - 1 - imin(cost, kCostBins - 1)], 1);
     items[pos] = make_int4(b, x, y, cost);
   }
-  if (tid == 0) counters[0] = total;
+  if (tid == 0) {
+    counters[0] = total;
+    counters[1] = 0;  // the attention kernel's dynamic hand-out counter
+  }
   return true;
 }
 
@@ -279,48 +282,92 @@ cudaError_t launch_plan(const PlanParams& p, cudaStream_t st) {
 }
 
 // ------------------------------------------------------------------ LSE merge
-// (o_acc, lse_acc) <- merge with (o_part, lse_part), one float4 per thread.
+// (o_acc, lse_acc) <- merge with (o_part, lse_part).  A group of LPR lanes
+// (a power of two <= 32) owns one (t, h) row: every lane of the group reads
+// the row's two lse values, its float4 slices of O, and computes the merged
+// lse itself; the group's first lane stores the merged lse only after a warp
+// barrier, so no lane can read an lse the merge already replaced.  Rows are
+// walked in [H, T] order (h outer), so the lse reads and writes of
+// consecutive groups are contiguous.  PartT: float (fp32 partials) or
+// uint16_t (bf16 partials, four per 8-byte load).
+__device__ inline float4 load_part4(const float* p, int64_t i) { return reinterpret_cast<const float4*>(p)[i]; }
+__device__ inline float4 load_part4(const uint16_t* p, int64_t i) {
+  const uint2 u = reinterpret_cast<const uint2*>(p)[i];
+  return make_float4(__uint_as_float(u.x << 16), __uint_as_float(u.x & 0xffff0000u), __uint_as_float(u.y << 16),
+                     __uint_as_float(u.y & 0xffff0000u));
+}
+
+template <typename PartT>
 __global__ void __launch_bounds__(256) lse_merge_kernel(float4* __restrict__ o_acc, float* __restrict__ lse_acc,
-                                                        const float4* __restrict__ o_part,
+                                                        const PartT* __restrict__ o_part,
                                                         const float* __restrict__ lse_part, int64_t T, int H,
-                                                        int D4) {
-  const int64_t n = T * H * (int64_t)D4;
-  for (int64_t i = blockIdx.x * (int64_t)blockDim.x + threadIdx.x; i < n; i += (int64_t)gridDim.x * blockDim.x) {
-    const int64_t row = i / D4;  // row = t * H + h
-    const int d4 = (int)(i - row * D4);
-    const int64_t t = row / H;
-    const int h = (int)(row - t * H);
-    const int64_t li = (int64_t)h * T + t;
-    const float a = lse_acc[li], b = lse_part[li];
+                                                        int D4, int lpr) {
+  const int lane = threadIdx.x & 31;
+  const int rpw = 32 / lpr;  // rows per warp and pass
+  const int g = lane / lpr, gl = lane % lpr;
+  const int64_t nrows = T * (int64_t)H;
+  const int64_t npass = (nrows + rpw - 1) / rpw;
+  const int64_t warp0 = (blockIdx.x * (int64_t)blockDim.x + threadIdx.x) >> 5;
+  const int64_t nwarps = ((int64_t)gridDim.x * blockDim.x) >> 5;
+  for (int64_t w = warp0; w < npass; w += nwarps) {  // warp-uniform trip count
+    const int64_t r = w * rpw + g;                     // r = h * T + t
+    const bool live = r < nrows;
+    const int h = live ? (int)(r / T) : 0;
+    const int64_t t = live ? r - (int64_t)h * T : 0;
+    const int64_t li = live ? r : 0;                   // lse index h * T + t
+    float a = -INFINITY, b = -INFINITY;
+    if (live) {
+      a = lse_acc[li];
+      b = lse_part[li];
+    }
     const float hi = fmaxf(a, b), lo = fminf(a, b);
-    float lse, wa, wb;
-    if (hi == -INFINITY) {
-      lse = -INFINITY;
-      wa = 0.f;
-      wb = 0.f;
-    } else {
+    float lse = -INFINITY, wa = 0.f, wb = 0.f;
+    if (hi != -INFINITY) {  // a side at -inf contributes nothing; both -inf give (0, -inf)
       lse = hi + log1pf(expf(lo - hi));
       wa = a == -INFINITY ? 0.f : expf(a - lse);
       wb = b == -INFINITY ? 0.f : expf(b - lse);
     }
-    const float4 x = o_acc[i], y = o_part[i];
-    o_acc[i] = make_float4(wa * x.x + wb * y.x, wa * x.y + wb * y.y, wa * x.z + wb * y.z, wa * x.w + wb * y.w);
-    if (d4 == 0) lse_acc[li] = lse;
+    if (live) {
+      const int64_t base = (t * H + h) * (int64_t)D4;
+      for (int j = gl; j < D4; j += lpr) {
+        const float4 x = o_acc[base + j];
+        const float4 y = load_part4(o_part, base + j);
+        o_acc[base + j] =
+            make_float4(wa * x.x + wb * y.x, wa * x.y + wb * y.y, wa * x.z + wb * y.z, wa * x.w + wb * y.w);
+      }
+    }
+    __syncwarp();  // every lane of the row has read lse_acc[li]
+    if (live && gl == 0) lse_acc[li] = lse;
   }
 }
 
-cudaError_t launch_lse_merge(float* o_acc, float* lse_acc, const float* o_part, const float* lse_part, int64_t T,
-                             int H, int D, cudaStream_t st) {
-  const int64_t n = T * H * (int64_t)(D / 4);
-  if (n == 0) return cudaSuccess;
-  const int64_t want = (n + 255) / 256;
+template <typename PartT>
+static cudaError_t launch_lse_merge_t(float* o_acc, float* lse_acc, const PartT* o_part, const float* lse_part,
+                                      int64_t T, int H, int D, cudaStream_t st) {
+  const int D4 = D / 4;
+  int lpr = 1;
+  while (lpr < D4 && lpr < 32) lpr <<= 1;
+  const int64_t rows = T * (int64_t)H;
+  if (rows == 0) return cudaSuccess;
+  const int64_t warps = (rows + (32 / lpr) - 1) / (32 / lpr);
+  const int64_t want = (warps + 7) / 8;  // 8 warps per block
   const int grid = (int)(want < 8LL * num_sms() ? want : 8LL * num_sms());
   prof_before(THD_KERNEL_LSE_MERGE, st);
-  lse_merge_kernel<<<grid, 256, 0, st>>>((float4*)o_acc, lse_acc, (const float4*)o_part, lse_part, T, H, D / 4);
+  lse_merge_kernel<PartT><<<grid, 256, 0, st>>>((float4*)o_acc, lse_acc, o_part, lse_part, T, H, D4, lpr);
   count_launch();
   cudaError_t e = cudaGetLastError();
   prof_after(THD_KERNEL_LSE_MERGE, st);
   return e;
+}
+
+cudaError_t launch_lse_merge(float* o_acc, float* lse_acc, const float* o_part, const float* lse_part, int64_t T,
+                             int H, int D, cudaStream_t st) {
+  return launch_lse_merge_t<float>(o_acc, lse_acc, o_part, lse_part, T, H, D, st);
+}
+
+cudaError_t launch_lse_merge_bf16(float* o_acc, float* lse_acc, const uint16_t* o_part, const float* lse_part,
+                                  int64_t T, int H, int D, cudaStream_t st) {
+  return launch_lse_merge_t<uint16_t>(o_acc, lse_acc, o_part, lse_part, T, H, D, st);
 }
 
 // ------------------------------------------------------------------ tail-zero
@@ -341,7 +388,12 @@ __global__ void __launch_bounds__(256) tail_zero_kernel(TailJob j0, TailJob j1, 
   for (int k = 0; k < 3; ++k) {
     const TailJob& j = jobs[k];
     if (!j.buf) continue;
-    const int64_t start = (int64_t)(*j.end) * j.hd;
+    // an endpoint outside [0, rows] is invalid metadata: nothing is written
+    // (so a negative or oversized value can never move the writes outside
+    // the buffer)
+    const int64_t end = *j.end;
+    if (end < 0 || end > j.rows) continue;
+    const int64_t start = end * j.hd;
     const int64_t stop = j.rows * (int64_t)j.hd;
     // 16-byte stores (H * D is a multiple of 8)
     for (int64_t i = start + (blockIdx.x * (int64_t)blockDim.x + threadIdx.x) * 8; i < stop;

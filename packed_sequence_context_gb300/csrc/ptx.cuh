@@ -99,26 +99,11 @@ THD_DEV void cp_async_16(uint32_t dst, const void* src, uint32_t src_bytes) {
 }
 THD_DEV void cp_async_wait_all() { asm volatile("cp.async.wait_all;" ::: "memory"); }
 
-// 128-bit shared-memory accesses (one instruction per thread, never split).
-THD_DEV void sts128(uint32_t addr, uint32_t a, uint32_t b, uint32_t c, uint32_t d) {
-  asm volatile("st.shared.v4.b32 [%0], {%1, %2, %3, %4};" ::"r"(addr), "r"(a), "r"(b), "r"(c), "r"(d) : "memory");
-}
-THD_DEV uint4 lds128(uint32_t addr) {
-  uint4 v;
-  asm volatile("ld.shared.v4.b32 {%0, %1, %2, %3}, [%4];" : "=r"(v.x), "=r"(v.y), "=r"(v.z), "=r"(v.w) : "r"(addr) : "memory");
-  return v;
-}
+// 128-bit shared-memory load of four floats (one instruction, never split).
 THD_DEV float4 lds128f(uint32_t addr) {
   float4 v;
   asm volatile("ld.shared.v4.f32 {%0, %1, %2, %3}, [%4];" : "=f"(v.x), "=f"(v.y), "=f"(v.z), "=f"(v.w) : "r"(addr) : "memory");
   return v;
-}
-
-// Fire-and-forget fp32 vector reduction into global memory (no return value,
-// so the issuing thread never waits for it).
-THD_DEV void red_add_v4(float* addr, float a, float b, float c, float d) {
-  asm volatile("red.global.add.v4.f32 [%0], {%1, %2, %3, %4};" ::"l"(addr), "f"(a), "f"(b), "f"(c), "f"(d)
-               : "memory");
 }
 
 // ------------------------------------------------------------------ TMA
@@ -133,21 +118,6 @@ THD_DEV void tma_load_3d(uint32_t dst, const CUtensorMap* map, uint64_t* bar, in
       "l"(reinterpret_cast<uint64_t>(map)), "r"(smem_u32(bar)), "r"(c0), "r"(c1), "r"(c2)
       : "memory");
 }
-
-// 3-D tiled reduce-add from shared memory into global memory (element-wise
-// atomic add), tracked by the issuing thread's bulk group.
-THD_DEV void tma_reduce_add_3d(const CUtensorMap* map, uint32_t src, int c0, int c1, int c2) {
-  asm volatile(
-      "cp.reduce.async.bulk.tensor.3d.global.shared::cta.add.tile.bulk_group"
-      " [%0, {%2, %3, %4}], [%1];" ::"l"(reinterpret_cast<uint64_t>(map)),
-      "r"(src), "r"(c0), "r"(c1), "r"(c2)
-      : "memory");
-}
-THD_DEV void bulk_commit_group() { asm volatile("cp.async.bulk.commit_group;" ::: "memory"); }
-// The shared-memory sources of this thread's bulk copies may be reused.
-THD_DEV void bulk_wait_read_all() { asm volatile("cp.async.bulk.wait_group.read 0;" ::: "memory"); }
-// This thread's bulk copies have completed (their global writes are done).
-THD_DEV void bulk_wait_all() { asm volatile("cp.async.bulk.wait_group 0;" ::: "memory"); }
 
 // ------------------------------------------------------------------ tcgen05
 THD_DEV void tmem_alloc(uint32_t* dst_smem, uint32_t ncols) {

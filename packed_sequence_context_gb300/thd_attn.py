@@ -63,11 +63,14 @@ SIGNATURES = {
                             _i32, _f32, _i32, _i32, _vp, _sz, _vp, _vp]),
     "thd_attn_fwd_step": (_i32, [_vp, _vp, _vp, _vp, _vp, _vp, _vp, _vp, _vp, _i32, _i64, _i64, _i32, _i32, _i32,
                                  _i32, _f32, _i32, _i32, _i32, _vp, _sz, _vp, _vp]),
+    "thd_attn_fwd_step_bf16": (_i32, [_vp, _vp, _vp, _vp, _vp, _vp, _vp, _vp, _vp, _i32, _i64, _i64, _i32, _i32,
+                                      _i32, _i32, _f32, _i32, _i32, _i32, _vp, _sz, _vp, _vp]),
     "thd_attn_fwd_noalloc": (_i32, [_vp, _vp, _vp, _vp, _vp, _vp, _vp, _vp, _vp, _i32, _i64, _i64, _i32, _i32,
                                     _i32, _i32, _f32, _i32, _i32, _vp, _vp]),
     "thd_attn_bwd": (_i32, [_vp, _vp, _vp, _vp, _vp, _vp, _vp, _vp, _vp, _i64, _i64, _vp, _vp, _vp, _vp, _i32,
                             _i64, _i64, _i32, _i32, _i32, _i32, _f32, _i32, _i32, _vp, _sz, _vp, _vp]),
     "thd_lse_merge": (_i32, [_vp, _vp, _vp, _vp, _i64, _i32, _i32, _vp]),
+    "thd_lse_merge_bf16": (_i32, [_vp, _vp, _vp, _vp, _i64, _i32, _i32, _vp]),
     "thd_grad_tail_zero": (_i32, [_vp, _vp, _vp, _i64, _i64, _i32, _i32, _i32, _vp, _vp, _i32, _i32, _vp]),
     "thd_cp_a2a": (_i32, [_vp, _vp, _vp, _i32, _i64, _i32, _i32, _i32, _i32, _i32, _vp, _vp]),
     "thd_a2a_workspace_size": (_sz, [_i32, _i64, _i32, _i32, _i32, _i32, _i32, _i32]),
@@ -154,6 +157,15 @@ def thd_attn_fwd_step(q, k, v, o_part, lse_part, cu_seqlens_q, cu_seqlens_kv, cu
                                    _p(workspace), workspace_bytes, _p(dev_status), _s(stream))
 
 
+def thd_attn_fwd_step_bf16(q, k, v, o_part, lse_part, cu_seqlens_q, cu_seqlens_kv, cu_seqlens_q_padded,
+                           cu_seqlens_kv_padded, B, T_q, T_kv, Hq, Hkv, D, causal, softmax_scale, cp_size,
+                           pad_between_seqs, step, workspace, workspace_bytes, dev_status, stream=None) -> int:
+    return lib().thd_attn_fwd_step_bf16(_p(q), _p(k), _p(v), _p(o_part), _p(lse_part), _p(cu_seqlens_q),
+                                        _p(cu_seqlens_kv), _p(cu_seqlens_q_padded), _p(cu_seqlens_kv_padded), B, T_q,
+                                        T_kv, Hq, Hkv, D, causal, softmax_scale, cp_size, pad_between_seqs, step,
+                                        _p(workspace), workspace_bytes, _p(dev_status), _s(stream))
+
+
 def thd_attn_fwd_noalloc(q, k, v, o, lse, cu_seqlens_q, cu_seqlens_kv, cu_seqlens_q_padded, cu_seqlens_kv_padded,
                          B, T_q, T_kv, Hq, Hkv, D, causal, softmax_scale, cp_size, pad_between_seqs, dev_status,
                          stream=None) -> int:
@@ -173,6 +185,10 @@ def thd_attn_bwd(q, k, v, o, lse, dout, dq, dk, dv, dq_rows, dkv_rows, cu_seqlen
 
 def thd_lse_merge(o_acc, lse_acc, o_part, lse_part, T, H, D, stream=None) -> int:
     return lib().thd_lse_merge(_p(o_acc), _p(lse_acc), _p(o_part), _p(lse_part), T, H, D, _s(stream))
+
+
+def thd_lse_merge_bf16(o_acc, lse_acc, o_part, lse_part, T, H, D, stream=None) -> int:
+    return lib().thd_lse_merge_bf16(_p(o_acc), _p(lse_acc), _p(o_part), _p(lse_part), T, H, D, _s(stream))
 
 
 def thd_grad_tail_zero(dq, dk, dv, dq_rows, dkv_rows, Hq, Hkv, D, cu_seqlens_q_padded, cu_seqlens_kv_padded, B,
@@ -287,6 +303,27 @@ def attn_fwd_step(q, k, v, cu_seqlens_q, cu_seqlens_kv, cu_seqlens_q_padded=None
     return o, l, st
 
 
+def attn_fwd_step_bf16(q, k, v, cu_seqlens_q, cu_seqlens_kv, cu_seqlens_q_padded=None, cu_seqlens_kv_padded=None,
+                       *, step, cp_size=1, causal=True, softmax_scale=None, pad_between_seqs=-1, out=None, lse=None,
+                       dev_status=None, workspace=None, stream=None):
+    """One ring step's partial in bf16: (o_part bf16 [T_q,Hq,D], lse_part fp32 [Hq,T_q], dev_status)."""
+    import torch
+    T_q, Hq, D = q.shape
+    T_kv, Hkv, _ = k.shape
+    B = cu_seqlens_q.numel() - 1
+    scale = 1.0 / math.sqrt(D) if softmax_scale is None else float(softmax_scale)
+    o = torch.empty((T_q, Hq, D), dtype=torch.bfloat16, device=q.device) if out is None else out
+    l = torch.empty((Hq, T_q), dtype=torch.float32, device=q.device) if lse is None else lse
+    st = torch.zeros(1, dtype=torch.int32, device=q.device) if dev_status is None else dev_status
+    ws = _workspace(thd_workspace_size(B, T_q, T_kv, Hq, Hkv, D, cp_size, 0), q.device) if workspace is None \
+        else workspace
+    _check("thd_attn_fwd_step_bf16", thd_attn_fwd_step_bf16(q, k, v, o, l, cu_seqlens_q, cu_seqlens_kv,
+                                                            cu_seqlens_q_padded, cu_seqlens_kv_padded, B, T_q, T_kv,
+                                                            Hq, Hkv, D, int(causal), scale, cp_size,
+                                                            pad_between_seqs, step, ws, ws.numel(), st, stream))
+    return o, l, st
+
+
 def attn_bwd(q, k, v, o, lse, dout, cu_seqlens_q, cu_seqlens_kv, cu_seqlens_q_padded=None,
              cu_seqlens_kv_padded=None, *, cp_size=1, causal=True, softmax_scale=None, pad_between_seqs=-1,
              dq_rows=None, dkv_rows=None, dq=None, dk=None, dv=None, dev_status=None, workspace=None, stream=None):
@@ -338,6 +375,12 @@ def lse_merge(o_acc, lse_acc, o_part, lse_part, stream=None):
     """In-place merge of (o_part, lse_part) into (o_acc, lse_acc)."""
     T, H, D = o_acc.shape
     _check("thd_lse_merge", thd_lse_merge(o_acc, lse_acc, o_part, lse_part, T, H, D, stream))
+
+
+def lse_merge_bf16(o_acc, lse_acc, o_part, lse_part, stream=None):
+    """In-place merge of a bf16 partial (o_part, lse_part) into the fp32 (o_acc, lse_acc)."""
+    T, H, D = o_acc.shape
+    _check("thd_lse_merge_bf16", thd_lse_merge_bf16(o_acc, lse_acc, o_part, lse_part, T, H, D, stream))
 
 
 def grad_tail_zero(dq, dk, dv, cu_seqlens_q_padded, cu_seqlens_kv_padded, host_knows_no_tail=False, stream=None):

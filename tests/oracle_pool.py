@@ -1,0 +1,141 @@
+"""Full-size comparisons of the library's outputs with the CPU fp64 oracle,
+spread over a process pool.
+
+The parent writes every tensor of a workload (inputs and the GPU's results,
+as float32) to memory-mapped .npy files; each worker loads them read-only,
+runs the oracle on one (sequence, kv-head group) or one block of query rows,
+compares element by element and returns only error statistics.  The pool is
+started with the 'spawn' method, so no worker inherits the parent's CUDA
+context.
+
+Bar (the benchmark's tolerances, read as in the design notes): on valid rows,
+O/dQ/dK/dV within 2e-2 and lse within 1e-3 of the oracle.  A bf16 result
+cannot be closer to an exact value than half its own rounding step (0.016
+for |x| in [4, 8), 0.031 in [8, 16)), so the O/dQ/dK/dV bar is applied to
+the error beyond that rounding (``excess``); the raw error is held to 2e-2
+wherever |ref| < 2, where half a bf16 step is at most 0.0039, and reported
+everywhere (max, the |ref| of the worst element, how many elements exceed
+2e-2).  Rows without a valid token must be exactly 0 (and lse -inf).
+"""
+
+from __future__ import annotations
+
+import multiprocessing as mp
+import os
+import tempfile
+
+import numpy as np
+
+TOL = 2e-2
+LSE_TOL = 1e-3
+RAW_BAR_BELOW = 2.0   # |ref| under which the raw error itself must be <= TOL
+
+
+def bf16_half_step(x: np.ndarray) -> np.ndarray:
+    """Half the bf16 spacing at |x| (8 significant bits)."""
+    ax = np.maximum(np.abs(x), np.finfo(np.float32).tiny)
+    return 0.5 * np.exp2(np.floor(np.log2(ax)) - 7)
+
+
+def compare(got: np.ndarray, ref: np.ndarray) -> dict:
+    if got.size == 0:
+        return {"max_abs": 0.0, "ref_at_max": 0.0, "n_over": 0, "excess": -1.0, "raw_small": 0.0, "n": 0}
+    err = np.abs(got - ref)
+    i = int(np.argmax(err))
+    small = np.abs(ref) < RAW_BAR_BELOW
+    return {"max_abs": float(err.flat[i]), "ref_at_max": float(np.abs(ref).flat[i]),
+            "n_over": int((err > TOL).sum()), "excess": float((err - bf16_half_step(ref)).max()),
+            "raw_small": float(err[small].max()) if small.any() else 0.0, "n": int(err.size)}
+
+
+def merge_stats(a: dict | None, b: dict) -> dict:
+    if a is None:
+        return dict(b)
+    out = dict(a)
+    if b["max_abs"] > a["max_abs"]:
+        out["max_abs"], out["ref_at_max"] = b["max_abs"], b["ref_at_max"]
+    out["n_over"] = a["n_over"] + b["n_over"]
+    out["excess"] = max(a["excess"], b["excess"])
+    out["raw_small"] = max(a["raw_small"], b["raw_small"])
+    out["n"] = a["n"] + b["n"]
+    return out
+
+
+def _load(d, name):
+    return np.load(os.path.join(d, name + ".npy"), mmap_mode="r")
+
+
+def _worker_seq(spec):
+    """Oracle fwd (+ bwd) of sequence rows [off, off+L) for the query heads of
+    kv heads `kv_heads`, compared with the GPU's results."""
+    import sys
+    sys.path.insert(0, spec["root"])
+    from oracle import thd_oracle as orc
+    d, off, L, kvh, G, scale, bwd = (spec[k] for k in ("dir", "off", "L", "kv_heads", "G", "scale", "bwd"))
+    qh = [h * G + j for h in kvh for j in range(G)]
+    sl = slice(off, off + L)
+    q = np.asarray(_load(d, "q")[sl][:, qh], np.float64)
+    k = np.asarray(_load(d, "k")[sl][:, kvh], np.float64)
+    v = np.asarray(_load(d, "v")[sl][:, kvh], np.float64)
+    cu = np.array([0, L], np.int32)
+    O, lse = orc.attn_fwd(q, k, v, cu, cu, softmax_scale=scale)
+    out = {"o": compare(np.asarray(_load(d, "o")[sl][:, qh]), O)}
+    lg = np.asarray(_load(d, "lse")[qh][:, sl])
+    out["lse"] = float(np.abs(lg - lse).max()) if L else 0.0
+    if bwd:
+        do = np.asarray(_load(d, "do")[sl][:, qh], np.float64)
+        dq, dk, dv = orc.attn_bwd(q, k, v, do, cu, cu, softmax_scale=scale)
+        out["dq"] = compare(np.asarray(_load(d, "dq")[sl][:, qh]), dq)
+        out["dk"] = compare(np.asarray(_load(d, "dk")[sl][:, kvh]), dk)
+        out["dv"] = compare(np.asarray(_load(d, "dv")[sl][:, kvh]), dv)
+    return out
+
+
+def _worker_rows(spec):
+    """Oracle forward of query rows [i0, i1) of one sequence and query head:
+    the causal rows i0.. see keys 0..i, which is the bottom-right mask of the
+    sub-problem (queries i0..i1-1, keys 0..i1-1)."""
+    import sys
+    sys.path.insert(0, spec["root"])
+    from oracle import thd_oracle as orc
+    d, off, i0, i1, h, G, scale = (spec[k] for k in ("dir", "off", "i0", "i1", "h", "G", "scale"))
+    q = np.asarray(_load(d, "q")[off + i0:off + i1, h:h + 1], np.float64)
+    k = np.asarray(_load(d, "k")[off:off + i1, h // G:h // G + 1], np.float64)
+    v = np.asarray(_load(d, "v")[off:off + i1, h // G:h // G + 1], np.float64)
+    O, lse = orc.attn_fwd(q, k, v, np.array([0, i1 - i0], np.int32), np.array([0, i1], np.int32),
+                          causal=orc.BOTTOM_RIGHT, softmax_scale=scale)
+    og = np.asarray(_load(d, "o")[off + i0:off + i1, h:h + 1])
+    lg = np.asarray(_load(d, "lse")[h:h + 1, off + i0:off + i1])
+    return {"o": compare(og, O), "lse": float(np.abs(lg - lse).max())}
+
+
+class Store:
+    """float32 copies of named arrays in memory-mapped files (a temp dir)."""
+
+    def __init__(self):
+        base = None   # the default temp dir, unless /dev/shm has room to spare
+        try:
+            stv = os.statvfs("/dev/shm")
+            if stv.f_bavail * stv.f_frsize >= (16 << 30):
+                base = "/dev/shm"
+        except OSError:
+            pass
+        self.tmp = tempfile.TemporaryDirectory(dir=base)
+        self.dir = self.tmp.name
+
+    def put(self, name, x):
+        np.save(os.path.join(self.dir, name + ".npy"), np.ascontiguousarray(x, dtype=np.float32))
+
+    def close(self):
+        self.tmp.cleanup()
+
+
+def pool(n=None):
+    for k in ("OMP_NUM_THREADS", "OPENBLAS_NUM_THREADS", "MKL_NUM_THREADS"):
+        os.environ[k] = "1"
+    return mp.get_context("spawn").Pool(n or os.cpu_count() or 1)
+
+
+def run(fn, specs, n=None):
+    with pool(n) as p:
+        return p.map(fn, specs, chunksize=1)

@@ -16,6 +16,15 @@ def test_merge_bytes_from_tensor_shapes():
     assert bench.merge_bytes(T, H, D) == read + write
 
 
+def test_merge_bf16_bytes_from_tensor_shapes():
+    T, H, D = 1000, 6, 128
+    o_acc, o_part = np.zeros((T, H, D), np.float32), np.zeros((T, H, D), np.float16)   # 2-byte partial
+    l_acc, l_part = np.zeros((H, T), np.float32), np.zeros((H, T), np.float32)
+    read = o_acc.nbytes + o_part.nbytes + l_acc.nbytes + l_part.nbytes
+    write = o_acc.nbytes + l_acc.nbytes
+    assert bench.merge_bytes(T, H, D, part_bytes=2) == read + write
+
+
 def test_tail_zero_bytes_from_tensor_shapes():
     rows_q, rows_kv, end, Hq, Hkv, D = 46077, 46077, 41888, 32, 8, 128
     dq = np.zeros((rows_q, Hq, D), np.float16)   # 2-byte elements like bf16

@@ -10,7 +10,7 @@ import torch
 from oracle import thd_oracle as orc
 from packed_sequence_context_gb300 import inputs
 from packed_sequence_context_gb300 import thd_attn as T
-from thd_testutil import O_TOL, device_inputs, f64, rounding_aware_excess
+from thd_testutil import assert_within_bar, device_inputs, f64
 
 pytestmark = pytest.mark.gpu
 
@@ -41,11 +41,9 @@ def _run(w, d, causal=True, canary=7.0, pad_flag=-1, cu_pad="default"):
     return o, lse, dq, dk, dv
 
 
-def _assert_bwd_close(w, t, dq, dk, dv, causal=True, rounding_aware=False):
-    """max-abs <= O_TOL on valid rows.  With rounding_aware, the bar applies to
-    the error beyond the bf16 rounding of the result (half an ulp of the
-    reference value), used for GQA stress cases whose summed dK/dV reach
-    magnitudes where that rounding alone is 0.016-0.031."""
+def _assert_bwd_close(w, t, dq, dk, dv, causal=True):
+    """The bf16 bar (assert_within_bar) on every valid row; rows without a
+    valid token exactly 0."""
     ref = orc.attn_bwd(*(t[x].float().numpy() for x in ("q", "k", "v", "do")), w.cu_seqlens, w.cu_seqlens,
                        w.cu_seqlens_padded, w.cu_seqlens_padded, causal=causal, softmax_scale=w.softmax_scale,
                        dq_rows=w.dq_rows, dkv_rows=w.dkv_rows)
@@ -54,15 +52,9 @@ def _assert_bwd_close(w, t, dq, dk, dv, causal=True, rounding_aware=False):
     errs = []
     for name, got, r in zip(("dq", "dk", "dv"), (dq, dk, dv), ref):
         g = f64(got)
-        e = float(np.abs(g[valid] - r[valid]).max()) if valid.any() else 0.0
-        worst = float(np.abs(r[valid]).max()) if valid.any() else 0.0
-        if rounding_aware:
-            ex = rounding_aware_excess(g[valid], r[valid]) if valid.any() else 0.0
-            assert ex <= O_TOL, f"{name} max-abs {e:.3e}, beyond bf16 rounding {ex:.3e} (largest |ref| {worst:.2f})"
-        else:
-            assert e <= O_TOL, f"{name} max-abs {e:.3e} (largest |ref| {worst:.2f})"
+        if valid.any():
+            errs.append(assert_within_bar(name, g[valid], r[valid])["max_abs"])
         assert np.all(g[~valid] == 0), f"{name}: rows without a valid token must be 0"
-        errs.append(e)
     return errs
 
 
@@ -93,7 +85,7 @@ def test_custom_cases_backward_match_oracle(case):
     t = inputs.make_tensors(w, with_grad=True)
     d = device_inputs(w, t)
     _, _, dq, dk, dv = _run(w, d)
-    _assert_bwd_close(w, t, dq, dk, dv, rounding_aware=Hq > Hkv)
+    _assert_bwd_close(w, t, dq, dk, dv)
 
 
 @pytest.mark.parametrize("case", [1, 3])
@@ -126,51 +118,6 @@ def test_slack_rows_are_tail_zeroed():
     _, _, dq, dk, dv = _run(w, d, canary=5.0)
     for g in (dq, dk, dv):
         assert torch.all(g[w.T:] == 0)
-
-
-def _sub_problem(w, t, b, heads):
-    """Slice sequence b (its valid rows) out of a workload for the oracle."""
-    off = int(w.cu_seqlens_padded[b])
-    L = w.lengths[b]
-    sl = slice(off, off + L)
-    G = w.Hq // w.Hkv
-    kv_heads = sorted({h // G for h in heads})
-    q_heads = [hk * G + j for hk in kv_heads for j in range(G)]
-    qq = t["q"][sl][:, q_heads].float().numpy()
-    dd = t["do"][sl][:, q_heads].float().numpy()
-    kk = t["k"][sl][:, kv_heads].float().numpy()
-    vv = t["v"][sl][:, kv_heads].float().numpy()
-    return sl, q_heads, kv_heads, qq, kk, vv, dd, L
-
-
-@pytest.mark.parametrize("name,heads,n_seq", [("fwdbwd", [3], 4), ("padded", [9], 3), ("packed", [2], 3)])
-def test_full_size_backward_sampled(name, heads, n_seq):
-    """Full-size workloads in the bench's launch configuration; the oracle
-    recomputes whole sequences (the shortest few plus one mid-length) for
-    one query-head group."""
-    w = inputs.make_workload(name)
-    t = inputs.make_tensors(w, with_grad=True)
-    d = device_inputs(w, t)
-    _, _, dq, dk, dv = _run(w, d)
-    order = np.argsort(w.lengths)
-    pick = list(order[:n_seq - 1]) + [order[len(order) // 2]]
-    worst = 0.0
-    for b in pick:
-        sl, q_heads, kv_heads, qq, kk, vv, dd, L = _sub_problem(w, t, int(b), heads)
-        cu = np.array([0, L], np.int32)
-        rq, rk, rv = orc.attn_bwd(qq, kk, vv, dd, cu, cu, softmax_scale=w.softmax_scale)
-        gq = dq[sl][:, q_heads].float().cpu().numpy()
-        gk = dk[sl][:, kv_heads].float().cpu().numpy()
-        gv = dv[sl][:, kv_heads].float().cpu().numpy()
-        for g, r in ((gq, rq), (gk, rk), (gv, rv)):
-            worst = max(worst, float(np.abs(g - r).max()))
-    assert worst <= O_TOL, f"sampled gradient max-abs {worst:.3e}"
-    inv = torch.from_numpy(~inputs.valid_row_mask(w)).cuda()
-    for g in (dq, dk, dv):
-        assert torch.all(g[w.T:] == 0)
-        if inv.any():
-            assert torch.all(g[:w.T][inv] == 0)
-        assert torch.isfinite(g.float()).all()
 
 
 def test_backward_bit_reproducible_over_repeats():

@@ -85,8 +85,11 @@ def test_partition_pad_flag_and_errors():
     assert st == T.THD_DEV_ERR_NONZERO_START
 
 
-@pytest.mark.parametrize("D", [64, 128, 12])
+@pytest.mark.parametrize("D", [64, 128, 12, 160, 4])
 def test_lse_merge_matches_oracle(D):
+    """D = 12 puts several rows in one warp (3 float4 each), D = 160 spreads a
+    row over more float4s than a warp has lanes: the merged lse must come from
+    the two inputs, never from a row's already-merged value."""
     rng = np.random.default_rng(D)
     Tn, H = 333, 3
     oa = rng.standard_normal((Tn, H, D)).astype(np.float32)
@@ -108,6 +111,47 @@ def test_lse_merge_matches_oracle(D):
     assert np.abs(gl[fin] - l_ref[fin]).max() <= 1e-5
     assert np.abs(go - O_ref).max() <= 1e-5
     assert np.all(go[np.isneginf(l_ref).T] == 0)
+
+
+@pytest.mark.parametrize("D", [128, 12])
+def test_lse_merge_bf16_partial_matches_oracle(D):
+    """The bf16-partial merge equals the oracle's merge of the same (bf16-
+    rounded) partial into the fp32 accumulator."""
+    rng = np.random.default_rng(100 + D)
+    Tn, H = 257, 4
+    oa = rng.standard_normal((Tn, H, D)).astype(np.float32)
+    ob16 = torch.tensor(rng.standard_normal((Tn, H, D)).astype(np.float32)).to(torch.bfloat16)
+    ob = ob16.float().numpy()
+    a = (rng.standard_normal((H, Tn)) * 4).astype(np.float32)
+    b = (rng.standard_normal((H, Tn)) * 4).astype(np.float32)
+    a[:, ::7] = -np.inf
+    b[:, ::5] = -np.inf
+    oa[~np.isfinite(a).T] = 0
+    ob16[torch.from_numpy(~np.isfinite(b).T)] = 0
+    ob = ob16.float().numpy()
+    O_ref, l_ref = orc.lse_merge(oa, a, ob, b)
+    acc_o, acc_l = torch.tensor(oa, device="cuda"), torch.tensor(a, device="cuda")
+    T.lse_merge_bf16(acc_o, acc_l, ob16.cuda(), torch.tensor(b, device="cuda"))
+    torch.cuda.synchronize()
+    go, gl = acc_o.cpu().numpy(), acc_l.cpu().numpy()
+    assert np.array_equal(np.isneginf(gl), np.isneginf(l_ref))
+    fin = np.isfinite(l_ref)
+    assert np.abs(gl[fin] - l_ref[fin]).max() <= 1e-5
+    assert np.abs(go - O_ref).max() <= 1e-5
+
+
+@pytest.mark.parametrize("end", [-16, 200])
+def test_grad_tail_zero_ignores_an_endpoint_outside_the_buffer(end):
+    """A corrupt endpoint (negative, or past the buffer's rows) writes nothing:
+    the rows before the buffer (a canary) and the buffer itself stay as they were."""
+    Hq, Hkv, D = 2, 2, 64
+    pad = torch.tensor([0, 32, end], dtype=torch.int32, device="cuda")
+    big = [torch.full((160, H, D), 3.0, dtype=torch.bfloat16, device="cuda") for H in (Hq, Hkv, Hkv)]
+    dq, dk, dv = (x[32:128] for x in big)     # 96-row buffers with 32 canary rows on each side
+    T.grad_tail_zero(dq, dk, dv, pad, pad)
+    torch.cuda.synchronize()
+    for x in big:
+        assert torch.all(x == 3)
 
 
 def test_grad_tail_zero_clears_slack_and_keeps_canary():
