@@ -434,7 +434,8 @@ int thd_attn_bwd(const void* q, const void* k, const void* v, const void* o, con
   dp.items = pp.items_q;
   dp.counters = pp.counters_q;
   dp.claim = pp.counters_q + 1;
-  dp.group_kv = locality_group(Hkv, (size_t)T_kv * D * 2 * 2, long_sequences(B, T_kv));
+  const bool grouped_q = long_sequences(B, T_kv);
+  dp.group_kv = locality_group(Hkv, (size_t)T_kv * D * 2 * 2, grouped_q);
   dp.dev_status = dev_status;
   dp.B = B;
   dp.Hq = Hq;
@@ -449,7 +450,7 @@ int thd_attn_bwd(const void* q, const void* k, const void* v, const void* o, con
   dp.step_hi = cp_size;
   const int64_t bound_q = (int64_t)L.item_cap_q * Hq;
   const int grid_q = (int)(bound_q < num_sms() ? (bound_q > 0 ? bound_q : 1) : num_sms());
-  rc = cuda_status(launch_dq(dp, tk, tv, D, grid_q, st));
+  rc = cuda_status(launch_dq(dp, tk, tv, D, grouped_q, grid_q, st));
   if (rc) return rc;
   BwdParams bp;
   std::memset(&bp, 0, sizeof(bp));
@@ -463,7 +464,8 @@ int thd_attn_bwd(const void* q, const void* k, const void* v, const void* o, con
   bp.items = pp.items;
   bp.counters = pp.counters;
   bp.claim = pp.counters + 1;
-  bp.group_kv = locality_group(Hkv, (size_t)T_q * (Hq / Hkv) * (D * 2 * 2 + 8), long_sequences(B, T_q));
+  const bool grouped_kv = long_sequences(B, T_q);
+  bp.group_kv = locality_group(Hkv, (size_t)T_q * (Hq / Hkv) * (D * 2 * 2 + 8), grouped_kv);
   bp.dev_status = dev_status;
   bp.B = B;
   bp.Hq = Hq;
@@ -476,7 +478,7 @@ int thd_attn_bwd(const void* q, const void* k, const void* v, const void* o, con
   bp.scale_log2 = softmax_scale * 1.4426950408889634f;
   const int64_t bound = (int64_t)L.item_cap * Hkv;
   const int grid = (int)(bound < num_sms() ? (bound > 0 ? bound : 1) : num_sms());
-  return cuda_status(launch_bwd(bp, tq, tdo, tk, tv, D, grid, st));
+  return cuda_status(launch_bwd(bp, tq, tdo, tk, tv, D, grouped_kv, grid, st));
 }
 
 int thd_lse_merge(float* o_acc, float* lse_acc, const float* o_part, const float* lse_part, int64_t T, int H, int D,

@@ -53,17 +53,19 @@ struct BwdItem {
 // p.group_kv kv heads (outermost: while a group runs, the queries and output
 // gradients of its query heads are what the CTAs read, so they stay in L2),
 // then by schedule entry (longest first), then by the group's kv heads.
+template <bool kGrouped>
 __device__ inline BwdItem bwd_item(const BwdParams& p, int n_entries, int w) {
   BwdItem it;
   int4 e;
-  if (p.group_kv == p.Hkv) {  // one group: entry-major, kv heads innermost
-    e = p.items[w / p.Hkv];
-    it.hk = w % p.Hkv;
-  } else {
+  if constexpr (kGrouped) {
     const int per = n_entries * p.group_kv;  // items per group
     const int grp = w / per, rem = w - grp * per;
     e = p.items[rem / p.group_kv];
     it.hk = grp * p.group_kv + rem % p.group_kv;
+  } else {  // one group: entry-major, kv heads innermost
+    (void)n_entries;
+    e = p.items[w / p.Hkv];
+    it.hk = w % p.Hkv;
   }
   it.b = e.x;
   it.c = e.y;
@@ -100,7 +102,7 @@ __device__ inline void drain_wait_b(uint64_t* bar, uint32_t parity) {
   }
 }
 
-template <int D>
+template <int D, bool kGrouped>
 __global__ void __launch_bounds__(352, 1)
     bwd_kernel(const BwdParams p, const __grid_constant__ CUtensorMap tmQ, const __grid_constant__ CUtensorMap tmDO,
                const __grid_constant__ CUtensorMap tmK, const __grid_constant__ CUtensorMap tmV) {
@@ -186,7 +188,7 @@ __global__ void __launch_bounds__(352, 1)
       }
       ok = __shfl_sync(0xffffffffu, ok ? 1 : 0, 0) != 0;
       if (!ok || wcur >= n_items) break;
-      const BwdItem it = bwd_item(p, n_entries, wcur);
+      const BwdItem it = bwd_item<kGrouped>(p, n_entries, wcur);
       if (it.kv_first > it.kv_last) continue;  // no valid key: nothing to load
       const int kv_row = it.g.kv_off + it.c * it.g.cbkv + it.jk * kTile;
       if (!mbar_wait(bar_kv_empty, (kv_iter & 1u) ^ 1u, s_abort)) break;
@@ -274,7 +276,7 @@ __global__ void __launch_bounds__(352, 1)
       for (uint32_t kit = 0; ok; ++kit) {
         int w;
         if (!item_take_one(ring, kit, w, s_abort) || w >= n_items) break;
-        const BwdItem it = bwd_item(p, n_entries, w);
+        const BwdItem it = bwd_item<kGrouped>(p, n_entries, w);
         if (it.kv_first > it.kv_last) continue;
         if (!mbar_wait(bar_kv_full, kv_iter & 1u, s_abort)) break;
         ++kv_iter;
@@ -344,7 +346,7 @@ __global__ void __launch_bounds__(352, 1)
       for (uint32_t kit = 0; ok; ++kit) {
         int w;
         if (!item_take_one(ring, kit, w, s_abort) || w >= n_items) break;
-        const BwdItem it = bwd_item(p, n_entries, w);
+        const BwdItem it = bwd_item<kGrouped>(p, n_entries, w);
         if (it.kv_first > it.kv_last) continue;
         if (!mbar_wait(bar_kv_full, kv_iter & 1u, s_abort)) break;
         ++kv_iter;
@@ -413,7 +415,7 @@ __global__ void __launch_bounds__(352, 1)
         break;
       }
       if (w >= n_items) break;
-      const BwdItem it = bwd_item(p, n_entries, w);
+      const BwdItem it = bwd_item<kGrouped>(p, n_entries, w);
       const int kv_local = it.jk * kTile + row;  // row within the chunk
       const int j_pos = it.c * it.g.cbkv + kv_local;
       const bool in_chunk = kv_local < it.g.cbkv;
@@ -593,14 +595,14 @@ __global__ void __launch_bounds__(352, 1)
   if (tid == 0 && *s_abort) atomicCAS(p.dev_status, 0, THD_ERR_TIMEOUT);
 }
 
-template <int D>
+template <int D, bool kGrouped>
 static cudaError_t launch_bwd_t(const BwdParams& p, const CUtensorMap& tq, const CUtensorMap& tdo,
                                 const CUtensorMap& tk, const CUtensorMap& tv, int grid, cudaStream_t st) {
   using C = BwdCfg<D>;
-  cudaError_t e = cudaFuncSetAttribute(bwd_kernel<D>, cudaFuncAttributeMaxDynamicSharedMemorySize, C::kSmem);
+  cudaError_t e = cudaFuncSetAttribute(bwd_kernel<D, kGrouped>, cudaFuncAttributeMaxDynamicSharedMemorySize, C::kSmem);
   if (e != cudaSuccess) return e;
   prof_before(THD_KERNEL_BWD, st);
-  bwd_kernel<D><<<grid, 352, C::kSmem, st>>>(p, tq, tdo, tk, tv);
+  bwd_kernel<D, kGrouped><<<grid, 352, C::kSmem, st>>>(p, tq, tdo, tk, tv);
   count_launch();
   e = cudaGetLastError();
   prof_after(THD_KERNEL_BWD, st);
@@ -608,8 +610,12 @@ static cudaError_t launch_bwd_t(const BwdParams& p, const CUtensorMap& tq, const
 }
 
 cudaError_t launch_bwd(const BwdParams& p, const CUtensorMap& tq, const CUtensorMap& tdo, const CUtensorMap& tk,
-                       const CUtensorMap& tv, int D, int grid, cudaStream_t st) {
-  return D == 128 ? launch_bwd_t<128>(p, tq, tdo, tk, tv, grid, st) : launch_bwd_t<64>(p, tq, tdo, tk, tv, grid, st);
+                       const CUtensorMap& tv, int D, bool grouped, int grid, cudaStream_t st) {
+  if (D == 128)
+    return grouped ? launch_bwd_t<128, true>(p, tq, tdo, tk, tv, grid, st)
+                   : launch_bwd_t<128, false>(p, tq, tdo, tk, tv, grid, st);
+  return grouped ? launch_bwd_t<64, true>(p, tq, tdo, tk, tv, grid, st)
+                 : launch_bwd_t<64, false>(p, tq, tdo, tk, tv, grid, st);
 }
 
 }  // namespace thd

@@ -50,7 +50,7 @@ struct DqCfg {
   static constexpr int kThreads = 384;
 };
 
-template <int D>
+template <int D, bool kGrouped>
 __global__ void __launch_bounds__(384, 1)
     dq_kernel(const DqParams p, const __grid_constant__ CUtensorMap tmK, const __grid_constant__ CUtensorMap tmV) {
   using C = DqCfg<D>;
@@ -138,7 +138,7 @@ __global__ void __launch_bounds__(384, 1)
       }
       ok = __shfl_sync(0xffffffffu, ok ? 1 : 0, 0) != 0;
       if (!ok || w >= n_items) break;
-      const QItem it = q_item(p, n_entries, w);
+      const QItem it = q_item<kGrouped>(p, n_entries, w);
       // the item's rank-local query rows of Q and dO, once the previous
       // item's last products that read them have completed; rows without a
       // valid query are zero
@@ -199,7 +199,7 @@ __global__ void __launch_bounds__(384, 1)
       for (uint32_t kit = 0; ok; ++kit) {
         int w;
         if (!item_take_one(&ring, kit, w, &s_abort) || w >= n_items) break;
-        const QItem it = q_item(p, n_entries, w);
+        const QItem it = q_item<kGrouped>(p, n_entries, w);
         for_each_kv_tile(it, p, [&](int c, int j) {
           if (!ok) return;
           if (!mbar_wait(&bar_v_empty[vs], vph ^ 1u, &s_abort)) {
@@ -237,7 +237,7 @@ __global__ void __launch_bounds__(384, 1)
       for (uint32_t kit = 0; ok; ++kit) {
         int w;
         if (!item_take_one(&ring, kit, w, &s_abort) || w >= n_items) break;
-        const QItem it = q_item(p, n_entries, w);
+        const QItem it = q_item<kGrouped>(p, n_entries, w);
         int n = 0;
         for_each_kv_tile(it, p, [&](int, int) { ++n; });
         if (!mbar_wait(&bar_q_full, q_iter & 1u, &s_abort)) break;
@@ -307,7 +307,7 @@ __global__ void __launch_bounds__(384, 1)
       for (uint32_t kit = 0; ok; ++kit) {
         int w;
         if (!item_take_one(&ring, kit, w, &s_abort) || w >= n_items) break;
-        const QItem it = q_item(p, n_entries, w);
+        const QItem it = q_item<kGrouped>(p, n_entries, w);
         int n = 0;
         for_each_kv_tile(it, p, [&](int, int) { ++n; });
         if (!mbar_wait(&bar_q_full, q_iter & 1u, &s_abort)) break;
@@ -380,7 +380,7 @@ __global__ void __launch_bounds__(384, 1)
         break;
       }
       if (w >= n_items) break;
-      const QItem it = q_item(p, n_entries, w);
+      const QItem it = q_item<kGrouped>(p, n_entries, w);
       const int prow = it.t * kTile + row;
       const bool in_rank = prow < 2 * it.g.cbq;
       const int pos = in_rank ? local_to_pos(prow, it.r, it.g.cbq, p.cp) : 0;
@@ -509,23 +509,24 @@ __global__ void __launch_bounds__(384, 1)
   if (tid == 0 && s_abort) atomicCAS(p.dev_status, 0, THD_ERR_TIMEOUT);
 }
 
-template <int D>
+template <int D, bool kGrouped>
 static cudaError_t launch_dq_t(const DqParams& p, const CUtensorMap& tk, const CUtensorMap& tv, int grid,
                                cudaStream_t st) {
   using C = DqCfg<D>;
-  cudaError_t ea = cudaFuncSetAttribute(dq_kernel<D>, cudaFuncAttributeMaxDynamicSharedMemorySize, C::kSmem);
+  cudaError_t ea = cudaFuncSetAttribute(dq_kernel<D, kGrouped>, cudaFuncAttributeMaxDynamicSharedMemorySize, C::kSmem);
   if (ea != cudaSuccess) return ea;
   prof_before(THD_KERNEL_BWD_DQ, st);
-  dq_kernel<D><<<grid, C::kThreads, C::kSmem, st>>>(p, tk, tv);
+  dq_kernel<D, kGrouped><<<grid, C::kThreads, C::kSmem, st>>>(p, tk, tv);
   count_launch();
   cudaError_t e = cudaGetLastError();
   prof_after(THD_KERNEL_BWD_DQ, st);
   return e;
 }
 
-cudaError_t launch_dq(const DqParams& p, const CUtensorMap& tk, const CUtensorMap& tv, int D, int grid,
+cudaError_t launch_dq(const DqParams& p, const CUtensorMap& tk, const CUtensorMap& tv, int D, bool grouped, int grid,
                       cudaStream_t st) {
-  return D == 128 ? launch_dq_t<128>(p, tk, tv, grid, st) : launch_dq_t<64>(p, tk, tv, grid, st);
+  if (D == 128) return grouped ? launch_dq_t<128, true>(p, tk, tv, grid, st) : launch_dq_t<128, false>(p, tk, tv, grid, st);
+  return grouped ? launch_dq_t<64, true>(p, tk, tv, grid, st) : launch_dq_t<64, false>(p, tk, tv, grid, st);
 }
 
 }  // namespace thd

@@ -139,7 +139,7 @@ __global__ void __launch_bounds__(384, 1)
         if (!ok) break;
       }
       if (w >= n_items) break;
-      const FwdItem it = q_item(p, n_entries, w);
+      const FwdItem it = q_item<kDyn>(p, n_entries, w);
       // ---- the query tile: rank-local rows [128 t, 128 t + 128) of rank r,
       // gathered into 128B-swizzled smem once the previous item's last QK^T
       // has completed; rows without a valid query are zero
@@ -204,7 +204,7 @@ __global__ void __launch_bounds__(384, 1)
         if constexpr (kDyn)
           if (!item_take_one(&ring, kit, w, &s_abort)) break;
         if (w >= n_items) break;
-        const FwdItem it = q_item(p, n_entries, w);
+        const FwdItem it = q_item<kDyn>(p, n_entries, w);
         for_each_kv_tile(it, p, [&](int c, int j) {
           if (!ok) return;
           if (!mbar_wait(&bar_v_empty[vs], vph ^ 1u, &s_abort)) {
@@ -249,7 +249,7 @@ __global__ void __launch_bounds__(384, 1)
         if constexpr (kDyn)
           if (!item_take_one(&ring, kit, w, &s_abort)) break;
         if (w >= n_items) break;
-        const FwdItem it = q_item(p, n_entries, w);
+        const FwdItem it = q_item<kDyn>(p, n_entries, w);
         int n = 0;
         for_each_kv_tile(it, p, [&](int, int) { ++n; });
         if (!mbar_wait(&bar_q_full, q_iter & 1u, &s_abort)) break;
@@ -302,7 +302,7 @@ __global__ void __launch_bounds__(384, 1)
         if constexpr (kDyn)
           if (!item_take_one(&ring, kit, w, &s_abort)) break;
         if (w >= n_items) break;
-        const FwdItem it = q_item(p, n_entries, w);
+        const FwdItem it = q_item<kDyn>(p, n_entries, w);
         int j = 0;
         for_each_kv_tile(it, p, [&](int c, int jt) {
           if (!ok) return;
@@ -357,7 +357,7 @@ __global__ void __launch_bounds__(384, 1)
         }
       }
       if (w >= n_items) break;
-      const FwdItem it = q_item(p, n_entries, w);
+      const FwdItem it = q_item<kDyn>(p, n_entries, w);
       const int prow = it.t * kTile + row;
       const bool in_rank = prow < 2 * it.g.cbq;
       const int pos = in_rank ? local_to_pos(prow, it.r, it.g.cbq, p.cp) : 0;
