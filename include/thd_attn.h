@@ -268,7 +268,7 @@ THD_API int thd_attn_bwd(const void* q, const void* k, const void* v, const void
  *     o   = exp(a - lse) o_acc + exp(b - lse) o_part
  * A side with lse = -inf contributes nothing; both -inf give (0, -inf).
  *   o_acc, o_part [T, H, D] fp32; lse_acc, lse_part [H, T] fp32; 16-byte
- *   aligned.  D a multiple of 4.
+ *   aligned.  D a multiple of 4.  H at most 16384 (else THD_ERR_UNSUPPORTED).
  */
 THD_API int thd_lse_merge(float* o_acc, float* lse_acc, const float* o_part, const float* lse_part, int64_t T, int H,
                   int D, thd_stream_t stream);
@@ -390,6 +390,17 @@ THD_API int thd_profile_read(float* ms_out, int max_out, int* count_out);
 
 /* Number of kernels this library has launched in this process. */
 THD_API uint64_t thd_launch_count(void);
+
+/*
+ * Test hook for the failure path (not for normal use): the NEXT launch of
+ * kernel_id (THD_KERNEL_FWD, THD_KERNEL_BWD or THD_KERNEL_BWD_DQ) runs no
+ * work: every thread waits on a barrier that nothing completes, the bounded
+ * wait gives up after its limit (2 s), each CTA frees its tensor memory and
+ * the call's *dev_status reads THD_ERR_TIMEOUT.  That call's outputs are not
+ * written.  The device stays usable for the next call.  kernel_id 0 disarms.
+ * One-shot and process-wide.
+ */
+THD_API int thd_test_arm_stall(int kernel_id);
 
 #ifdef __cplusplus
 }

@@ -39,6 +39,14 @@ struct Prof {
 };
 static Prof g_prof;
 
+// One-shot test hook: the next launch of the armed kernel stalls on purpose
+// (see thd_test_arm_stall).
+static std::atomic<int> g_stall_kernel{0};
+bool take_test_stall(int kernel_id) {
+  int expect = kernel_id;
+  return kernel_id != 0 && g_stall_kernel.compare_exchange_strong(expect, 0);
+}
+
 void prof_before(int id, cudaStream_t st) {
   if (g_prof.kernel != id) return;
   std::lock_guard<std::mutex> lk(g_prof.mu);
@@ -128,6 +136,9 @@ static PlanParams plan_params(const int32_t* cu_q, const int32_t* cu_kv, const i
 
 static int cuda_status(cudaError_t e) { return e == cudaSuccess ? THD_OK : THD_ERR_CUDA; }
 
+// The merge keeps two weights per (head, token) of its tile in shared memory.
+constexpr int kMergeMaxHeads = 16384;
+
 // kv heads per locality group of the attention kernels' item order: the
 // largest divisor of Hkv whose group re-reads at most kL2GroupBytes of
 // operands (keys and values in the query-stationary kernels, queries and
@@ -199,6 +210,7 @@ static int fwd_common(const void* q, const void* k, const void* v, void* o, floa
   fp.scale_log2 = scale * 1.4426950408889634f;
   fp.step_lo = pp.step_lo;
   fp.step_hi = pp.step_hi;
+  fp.test_stall = take_test_stall(THD_KERNEL_FWD) ? 1 : 0;
   const int64_t bound = (int64_t)L.item_cap * Hq;
   const int grid = (int)(bound < num_sms() ? (bound > 0 ? bound : 1) : num_sms());
   // O is written in bf16 (the fused forward, or one step's partial in bf16)
@@ -448,6 +460,7 @@ int thd_attn_bwd(const void* q, const void* k, const void* v, const void* o, con
   dp.scale_log2 = softmax_scale * 1.4426950408889634f;
   dp.step_lo = 0;
   dp.step_hi = cp_size;
+  dp.test_stall = take_test_stall(THD_KERNEL_BWD_DQ) ? 1 : 0;
   const int64_t bound_q = (int64_t)L.item_cap_q * Hq;
   const int grid_q = (int)(bound_q < num_sms() ? (bound_q > 0 ? bound_q : 1) : num_sms());
   rc = cuda_status(launch_dq(dp, tk, tv, D, grouped_q, grid_q, st));
@@ -476,6 +489,7 @@ int thd_attn_bwd(const void* q, const void* k, const void* v, const void* o, con
   bp.dkv_rows = dkv_rows;
   bp.scale = softmax_scale;
   bp.scale_log2 = softmax_scale * 1.4426950408889634f;
+  bp.test_stall = take_test_stall(THD_KERNEL_BWD) ? 1 : 0;
   const int64_t bound = (int64_t)L.item_cap * Hkv;
   const int grid = (int)(bound < num_sms() ? (bound > 0 ? bound : 1) : num_sms());
   return cuda_status(launch_bwd(bp, tq, tdo, tk, tv, D, grouped_kv, grid, st));
@@ -485,6 +499,7 @@ int thd_lse_merge(float* o_acc, float* lse_acc, const float* o_part, const float
                   thd_stream_t stream) {
   if (!o_acc || !lse_acc || !o_part || !lse_part || T < 0 || H < 1 || D < 4 || D % 4 != 0) return THD_ERR_INVALID_ARG;
   if (!aligned(o_acc, 16) || !aligned(o_part, 16)) return THD_ERR_INVALID_ARG;
+  if (H > kMergeMaxHeads) return THD_ERR_UNSUPPORTED;
   return cuda_status(launch_lse_merge(o_acc, lse_acc, o_part, lse_part, T, H, D, reinterpret_cast<cudaStream_t>(stream)));
 }
 
@@ -492,6 +507,7 @@ int thd_lse_merge_bf16(float* o_acc, float* lse_acc, const void* o_part, const f
                        int D, thd_stream_t stream) {
   if (!o_acc || !lse_acc || !o_part || !lse_part || T < 0 || H < 1 || D < 4 || D % 4 != 0) return THD_ERR_INVALID_ARG;
   if (!aligned(o_acc, 16) || !aligned(o_part, 8)) return THD_ERR_INVALID_ARG;
+  if (H > kMergeMaxHeads) return THD_ERR_UNSUPPORTED;
   return cuda_status(launch_lse_merge_bf16(o_acc, lse_acc, static_cast<const uint16_t*>(o_part), lse_part, T, H, D,
                                            reinterpret_cast<cudaStream_t>(stream)));
 }
@@ -652,5 +668,12 @@ int thd_profile_read(float* ms_out, int max_out, int* count_out) {
 }
 
 uint64_t thd_launch_count(void) { return g_launches.load(std::memory_order_relaxed); }
+
+int thd_test_arm_stall(int kernel_id) {
+  if (kernel_id != 0 && kernel_id != THD_KERNEL_FWD && kernel_id != THD_KERNEL_BWD && kernel_id != THD_KERNEL_BWD_DQ)
+    return THD_ERR_INVALID_ARG;
+  g_stall_kernel.store(kernel_id);
+  return THD_OK;
+}
 
 }  // extern "C"

@@ -294,6 +294,7 @@ struct FwdParams {
   int64_t T_q;
   float scale_log2;  // softmax_scale * log2(e)
   int step_lo, step_hi;
+  int test_stall;  // test hook: every thread waits for a barrier nothing completes
 };
 
 struct BwdParams {
@@ -312,6 +313,7 @@ struct BwdParams {
   int group_kv;  // kv heads per locality group (divides Hkv)
   int64_t T_q, dkv_rows;
   float scale, scale_log2;
+  int test_stall;  // test hook: every thread waits for a barrier nothing completes
 };
 
 struct DqParams {
@@ -330,6 +332,7 @@ struct DqParams {
   int64_t T_q, dq_rows;
   float scale, scale_log2;
   int step_lo, step_hi;  // always the whole ring
+  int test_stall;  // test hook: every thread waits for a barrier nothing completes
 };
 
 // host launchers (each returns a cudaError_t)
@@ -352,6 +355,7 @@ cudaError_t launch_bwd_prep(const uint16_t* o, const uint16_t* dout, const float
                             cudaStream_t st);
 
 int num_sms();
+bool take_test_stall(int kernel_id);
 void prof_before(int kernel_id, cudaStream_t st);
 void prof_after(int kernel_id, cudaStream_t st);
 void count_launch();

@@ -122,7 +122,14 @@ __global__ void __launch_bounds__(384, 1)
   tc_fence_after();
   const uint32_t tmem = s_tmem;
 
-  if (warp == 8) {
+  // Test hook (thd_test_arm_stall): every thread waits on a barrier nothing
+  // completes, so the bounded wait runs out, the CTA takes the abort path
+  // before any copy or MMA is issued, frees its TMEM and reports
+  // THD_ERR_TIMEOUT.  The drain barrier is free for this: in this mode no
+  // role runs, so nothing ever commits to it.
+  if (p.test_stall) {
+    mbar_wait(&bar_drain, 0, &s_abort);
+  } else if (warp == 8) {
     // ------------------------------------------------------------ Q, dO and K producer (whole warp)
     int ks = 0;
     uint32_t kph = 0, n_fill = 0, q_iter = 0;

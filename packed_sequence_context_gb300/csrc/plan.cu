@@ -282,78 +282,100 @@ cudaError_t launch_plan(const PlanParams& p, cudaStream_t st) {
 }
 
 // ------------------------------------------------------------------ LSE merge
-// (o_acc, lse_acc) <- merge with (o_part, lse_part).  A group of LPR lanes
-// (a power of two <= 32) owns one (t, h) row: every lane of the group reads
-// the row's two lse values, its float4 slices of O, and computes the merged
-// lse itself; the group's first lane stores the merged lse only after a warp
-// barrier, so no lane can read an lse the merge already replaced.  Rows are
-// walked in [H, T] order (h outer), so the lse reads and writes of
-// consecutive groups are contiguous.  PartT: float (fp32 partials) or
-// uint16_t (bf16 partials, four per 8-byte load).
-__device__ inline float4 load_part4(const float* p, int64_t i) { return reinterpret_cast<const float4*>(p)[i]; }
+// (o_acc, lse_acc) <- merge with (o_part, lse_part).  A block owns a tile of
+// tt consecutive tokens with all H heads: that tile's O rows are one
+// contiguous stretch of memory, and for each head its lse values are tt
+// contiguous floats.  Phase 1: each thread reads one (h, t) pair of lse
+// values (coalesced), writes the merged lse back itself -- nothing else reads
+// that entry, so there is no in-place race -- and leaves the two weights in
+// shared memory.  Phase 2: the tile's O rows are streamed, one warp per row
+// and kMergeRows rows per warp in flight, lanes over the row's float4s.
+// PartT: float (fp32 partials) or uint16_t (bf16 partials, four per 8-byte
+// load).
+__device__ inline float4 load_part4(const float* p, int64_t i) { return __ldg(reinterpret_cast<const float4*>(p) + i); }
 __device__ inline float4 load_part4(const uint16_t* p, int64_t i) {
-  const uint2 u = reinterpret_cast<const uint2*>(p)[i];
+  const uint2 u = __ldg(reinterpret_cast<const uint2*>(p) + i);
   return make_float4(__uint_as_float(u.x << 16), __uint_as_float(u.x & 0xffff0000u), __uint_as_float(u.y << 16),
                      __uint_as_float(u.y & 0xffff0000u));
 }
+
+constexpr int kMergeRows = 4;          // O rows per warp in flight
+constexpr int kMergeTileRows = 128;    // about H * tt rows per tile: many small tiles, so the
+                                       // block scheduler balances the last wave
 
 template <typename PartT>
 __global__ void __launch_bounds__(256) lse_merge_kernel(float4* __restrict__ o_acc, float* __restrict__ lse_acc,
                                                         const PartT* __restrict__ o_part,
                                                         const float* __restrict__ lse_part, int64_t T, int H,
-                                                        int D4, int lpr) {
-  const int lane = threadIdx.x & 31;
-  const int rpw = 32 / lpr;  // rows per warp and pass
-  const int g = lane / lpr, gl = lane % lpr;
-  const int64_t nrows = T * (int64_t)H;
-  const int64_t npass = (nrows + rpw - 1) / rpw;
-  const int64_t warp0 = (blockIdx.x * (int64_t)blockDim.x + threadIdx.x) >> 5;
-  const int64_t nwarps = ((int64_t)gridDim.x * blockDim.x) >> 5;
-  for (int64_t w = warp0; w < npass; w += nwarps) {  // warp-uniform trip count
-    const int64_t r = w * rpw + g;                     // r = h * T + t
-    const bool live = r < nrows;
-    const int h = live ? (int)(r / T) : 0;
-    const int64_t t = live ? r - (int64_t)h * T : 0;
-    const int64_t li = live ? r : 0;                   // lse index h * T + t
-    float a = -INFINITY, b = -INFINITY;
-    if (live) {
-      a = lse_acc[li];
-      b = lse_part[li];
+                                                        int D4, int tt) {
+  extern __shared__ float s_w[];  // [2][H][tt]: the weights of the accumulator and of the partial
+  const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5, nwarp = blockDim.x >> 5;
+  const int64_t ntiles = (T + tt - 1) / tt;
+  for (int64_t tile = blockIdx.x; tile < ntiles; tile += gridDim.x) {
+    const int64_t t0 = tile * tt;
+    const int nt = (int)(T - t0 < tt ? T - t0 : tt);
+    for (int i = threadIdx.x; i < H * nt; i += blockDim.x) {
+      const int h = i / nt, tl = i - h * nt;
+      const int64_t li = (int64_t)h * T + t0 + tl;
+      const float a = lse_acc[li], b = __ldg(lse_part + li);
+      const float hi = fmaxf(a, b), lo = fminf(a, b);
+      float lse = -INFINITY, wa = 0.f, wb = 0.f;
+      if (hi != -INFINITY) {  // a side at -inf contributes nothing; both -inf give (0, -inf)
+        lse = hi + log1pf(expf(lo - hi));
+        wa = a == -INFINITY ? 0.f : expf(a - lse);
+        wb = b == -INFINITY ? 0.f : expf(b - lse);
+      }
+      lse_acc[li] = lse;
+      s_w[h * tt + tl] = wa;
+      s_w[(H + h) * tt + tl] = wb;
     }
-    const float hi = fmaxf(a, b), lo = fminf(a, b);
-    float lse = -INFINITY, wa = 0.f, wb = 0.f;
-    if (hi != -INFINITY) {  // a side at -inf contributes nothing; both -inf give (0, -inf)
-      lse = hi + log1pf(expf(lo - hi));
-      wa = a == -INFINITY ? 0.f : expf(a - lse);
-      wb = b == -INFINITY ? 0.f : expf(b - lse);
-    }
-    if (live) {
-      const int64_t base = (t * H + h) * (int64_t)D4;
-      for (int j = gl; j < D4; j += lpr) {
-        const float4 x = o_acc[base + j];
-        const float4 y = load_part4(o_part, base + j);
-        o_acc[base + j] =
-            make_float4(wa * x.x + wb * y.x, wa * x.y + wb * y.y, wa * x.z + wb * y.z, wa * x.w + wb * y.w);
+    __syncthreads();
+    const int nrows = nt * H;  // rows (t0 + tl) * H + h, in memory order
+    const int64_t base = t0 * H * (int64_t)D4;
+    for (int r0 = warp * kMergeRows; r0 < nrows; r0 += nwarp * kMergeRows) {
+      float wa[kMergeRows], wb[kMergeRows];
+#pragma unroll
+      for (int u = 0; u < kMergeRows; ++u) {
+        const int r = r0 + u;
+        const int tl = r / H, h = r - tl * H;
+        wa[u] = r < nrows ? s_w[h * tt + tl] : 0.f;
+        wb[u] = r < nrows ? s_w[(H + h) * tt + tl] : 0.f;
+      }
+      for (int j = lane; j < D4; j += 32) {
+        float4 x[kMergeRows], y[kMergeRows];
+#pragma unroll
+        for (int u = 0; u < kMergeRows; ++u)
+          if (r0 + u < nrows) {
+            x[u] = o_acc[base + (int64_t)(r0 + u) * D4 + j];
+            y[u] = load_part4(o_part, base + (int64_t)(r0 + u) * D4 + j);
+          }
+#pragma unroll
+        for (int u = 0; u < kMergeRows; ++u)
+          if (r0 + u < nrows)
+            o_acc[base + (int64_t)(r0 + u) * D4 + j] =
+                make_float4(wa[u] * x[u].x + wb[u] * y[u].x, wa[u] * x[u].y + wb[u] * y[u].y,
+                            wa[u] * x[u].z + wb[u] * y[u].z, wa[u] * x[u].w + wb[u] * y[u].w);
       }
     }
-    __syncwarp();  // every lane of the row has read lse_acc[li]
-    if (live && gl == 0) lse_acc[li] = lse;
+    __syncthreads();  // the weights are reused by the next tile
   }
 }
 
 template <typename PartT>
 static cudaError_t launch_lse_merge_t(float* o_acc, float* lse_acc, const PartT* o_part, const float* lse_part,
                                       int64_t T, int H, int D, cudaStream_t st) {
-  const int D4 = D / 4;
-  int lpr = 1;
-  while (lpr < D4 && lpr < 32) lpr <<= 1;
-  const int64_t rows = T * (int64_t)H;
-  if (rows == 0) return cudaSuccess;
-  const int64_t warps = (rows + (32 / lpr) - 1) / (32 / lpr);
-  const int64_t want = (warps + 7) / 8;  // 8 warps per block
-  const int grid = (int)(want < 8LL * num_sms() ? want : 8LL * num_sms());
+  if (T == 0) return cudaSuccess;
+  const int tt = H >= kMergeTileRows ? 1 : kMergeTileRows / H;
+  const size_t smem = sizeof(float) * 2 * (size_t)H * tt;
+  if (smem > 48 * 1024) {
+    cudaError_t e = cudaFuncSetAttribute(lse_merge_kernel<PartT>, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                         (int)smem);
+    if (e != cudaSuccess) return e;
+  }
+  const int64_t ntiles = (T + tt - 1) / tt;
+  const int grid = (int)(ntiles < (1LL << 20) ? ntiles : (1LL << 20));  // one tile per block
   prof_before(THD_KERNEL_LSE_MERGE, st);
-  lse_merge_kernel<PartT><<<grid, 256, 0, st>>>((float4*)o_acc, lse_acc, o_part, lse_part, T, H, D4, lpr);
+  lse_merge_kernel<PartT><<<grid, 256, smem, st>>>((float4*)o_acc, lse_acc, o_part, lse_part, T, H, D / 4, tt);
   count_launch();
   cudaError_t e = cudaGetLastError();
   prof_after(THD_KERNEL_LSE_MERGE, st);

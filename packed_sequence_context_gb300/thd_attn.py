@@ -81,6 +81,7 @@ SIGNATURES = {
     "thd_profile_enable": (_i32, [_i32, _i32]),
     "thd_profile_read": (_i32, [_vp, _i32, _vp]),
     "thd_launch_count": (ctypes.c_uint64, []),
+    "thd_test_arm_stall": (_i32, [_i32]),
 }
 
 _LIB = None
@@ -236,6 +237,10 @@ def thd_profile_read(max_out: int = 4096) -> list[float]:
 
 def thd_launch_count() -> int:
     return lib().thd_launch_count()
+
+
+def thd_test_arm_stall(kernel_id: int) -> int:
+    return lib().thd_test_arm_stall(kernel_id)
 
 
 # ----------------------------------------------------------------- helpers

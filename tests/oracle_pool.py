@@ -109,6 +109,24 @@ def _worker_rows(spec):
     return {"o": compare(og, O), "lse": float(np.abs(lg - lse).max())}
 
 
+def _worker_ring(spec):
+    """The oracle's emulated P2P ring (per-step partials merged by the LSE
+    identity) for one sequence (padded rows [off, off+P), L valid) and one
+    query head, compared with the device's merged result on the valid rows."""
+    import sys
+    sys.path.insert(0, spec["root"])
+    from oracle import thd_oracle as orc
+    d, off, L, P, h, G, cp, scale = (spec[k] for k in ("dir", "off", "L", "P", "h", "G", "cp", "scale"))
+    q = np.asarray(_load(d, "q")[off:off + P, h:h + 1], np.float64)
+    k = np.asarray(_load(d, "k")[off:off + P, h // G:h // G + 1], np.float64)
+    v = np.asarray(_load(d, "v")[off:off + P, h // G:h // G + 1], np.float64)
+    O, lse = orc.cp_ring_fwd(q, k, v, np.array([0, L], np.int32), np.array([0, P], np.int32), cp,
+                             softmax_scale=scale)
+    og = np.asarray(_load(d, "o")[off:off + L, h:h + 1])
+    lg = np.asarray(_load(d, "lse")[h:h + 1, off:off + L])
+    return {"o": compare(og, O[:L]), "lse": float(np.abs(lg - lse[:, :L]).max()) if L else 0.0}
+
+
 class Store:
     """float32 copies of named arrays in memory-mapped files (a temp dir)."""
 

@@ -125,3 +125,51 @@ def test_long_forward_every_row_of_two_heads():
         stats["lse"] = max(stats.get("lse", 0.0), r["lse"])
     _report("long, heads 0 and 17", stats)
     _assert(stats)
+
+
+@pytest.mark.parametrize("bf16", [True, False])
+def test_materialised_ring_full_packed_every_row(bf16):
+    """The ring with its per-step partials materialised: cp_size launches of
+    thd_attn_fwd_step_bf16 (or the fp32 thd_attn_fwd_step), each merged into an
+    fp32 accumulator by thd_lse_merge_bf16 (thd_lse_merge), against the
+    oracle's emulated ring on every valid row of every head of the packed
+    workload."""
+    w = inputs.make_workload("packed")
+    t = inputs.make_tensors(w)
+    d = device_inputs(w, t)
+    acc_o = torch.zeros((w.T, w.Hq, w.D), dtype=torch.float32, device="cuda")
+    acc_l = torch.full((w.Hq, w.T), float("-inf"), dtype=torch.float32, device="cuda")
+    for i in range(w.cp_size):
+        kw = dict(step=i, cp_size=w.cp_size, softmax_scale=w.softmax_scale)
+        if bf16:
+            o, l, st = T.attn_fwd_step_bf16(d["q"], d["k"], d["v"], d["cu"], d["cu"], d["cu_pad"], d["cu_pad"], **kw)
+            assert o.dtype == torch.bfloat16
+            T.lse_merge_bf16(acc_o, acc_l, o, l)
+        else:
+            o, l, st = T.attn_fwd_step(d["q"], d["k"], d["v"], d["cu"], d["cu"], d["cu_pad"], d["cu_pad"], **kw)
+            T.lse_merge(acc_o, acc_l, o, l)
+        torch.cuda.synchronize()
+        assert int(st.item()) == 0
+    store = op.Store()
+    try:
+        for k_, x in (("q", t["q"]), ("k", t["k"]), ("v", t["v"])):
+            store.put(k_, x.float().numpy())
+        store.put("o", acc_o.cpu().numpy())
+        store.put("lse", acc_l.cpu().numpy())
+        G = w.Hq // w.Hkv
+        specs = [{"root": ROOT, "dir": store.dir, "off": int(w.cu_seqlens_padded[b]), "L": int(w.lengths[b]),
+                  "P": int(w.cu_seqlens_padded[b + 1] - w.cu_seqlens_padded[b]), "h": h, "G": G,
+                  "cp": w.cp_size, "scale": w.softmax_scale}
+                 for b in range(w.B) if w.lengths[b] > 0 for h in range(w.Hq)]
+        specs.sort(key=lambda s: -s["L"])
+        res = op.run(op._worker_ring, specs)
+    finally:
+        store.close()
+    stats = {"o": None, "lse": 0.0}
+    for r in res:
+        stats["o"] = op.merge_stats(stats["o"], r["o"])
+        stats["lse"] = max(stats["lse"], r["lse"])
+    _report(f"packed ring, {'bf16' if bf16 else 'fp32'} partials", stats)
+    _assert(stats)
+    if not bf16:   # fp32 partials: the raw bar holds on every element
+        assert stats["o"]["n_over"] == 0

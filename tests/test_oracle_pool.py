@@ -73,3 +73,24 @@ def test_bar_counts_rounding_of_large_values():
     assert s["n_over"] == 2 and s["raw_small"] <= op.TOL and s["excess"] <= op.TOL
     s = op.compare(ref + np.array([0.0, 0.0, 0.0, 0.021]), ref)
     assert s["raw_small"] > op.TOL   # |ref| < 2 keeps the raw bar
+
+
+def test_ring_worker_reproduces_unsplit_attention():
+    """The ring worker compares the oracle's emulated ring with the device
+    result; given unsplit attention as the "device" result it reports only
+    rounding (the ring equals plain attention), padded sequences included."""
+    w = inputs.make_workload("custom", 7, lengths=[60, 96], pad_to=16, Hq=2, Hkv=1, D=16, cp_size=2)
+    t = inputs.make_tensors(w)
+    qn, kn, vn = (t[x].float().numpy() for x in ("q", "k", "v"))
+    O, lse = orc.attn_fwd(qn, kn, vn, w.cu_seqlens, w.cu_seqlens, w.cu_seqlens_padded, w.cu_seqlens_padded,
+                          softmax_scale=w.softmax_scale)
+    s = _store(w, t, {"o": O, "lse": lse})
+    try:
+        specs = [{"root": ROOT, "dir": s.dir, "off": int(w.cu_seqlens_padded[b]), "L": w.lengths[b],
+                  "P": int(w.cu_seqlens_padded[b + 1] - w.cu_seqlens_padded[b]), "h": h, "G": 2, "cp": 2,
+                  "scale": w.softmax_scale} for b in range(w.B) for h in range(2)]
+        res = op.run(op._worker_ring, specs, n=2)
+    finally:
+        s.close()
+    assert max(r["o"]["max_abs"] for r in res) < 1e-5
+    assert max(r["lse"] for r in res) < 1e-5
