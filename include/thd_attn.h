@@ -78,7 +78,7 @@ typedef struct CUstream_st* thd_stream_t; /* identical to cudaStream_t */
 #define THD_DEV_ERR_VALID_GT_PAD 103   /* L_b > P_b */
 #define THD_DEV_ERR_NOT_DIVISIBLE 104  /* P_b % (2 cp_size) != 0 */
 #define THD_DEV_ERR_EXCEEDS_BUF 105    /* pad[B] larger than the buffer rows */
-#define THD_DEV_ERR_CAUSAL_LENGTHS 106 /* causal with q and kv lengths differing */
+#define THD_DEV_ERR_CAUSAL_LENGTHS 106 /* top-left causal with q and kv lengths differing */
 #define THD_DEV_ERR_CAPACITY 107       /* internal schedule capacity exceeded */
 
 /* Kernel identifiers for the profiling hook. */
@@ -91,6 +91,11 @@ typedef struct CUstream_st* thd_stream_t; /* identical to cudaStream_t */
 #define THD_KERNEL_TAIL_ZERO 7
 #define THD_KERNEL_PARTITION 8
 #define THD_KERNEL_A2A 9
+
+/* mask modes (the `causal` argument of the attention entry points) */
+#define THD_CAUSAL_NONE 0
+#define THD_CAUSAL_TOP_LEFT 1
+#define THD_CAUSAL_BOTTOM_RIGHT 2
 
 /* thd_cp_a2a directions */
 #define THD_A2A_TO_GROUPS 0 /* shards -> per-member head groups (the all-to-all in front of attention) */
@@ -150,15 +155,26 @@ THD_API int thd_cp_partition(const int32_t* cu_seqlens, const int32_t* cu_seqlen
  * then chunk 2cp-1-r of each sequence) and ring step i, where rank r
  * holds the KV of rank s = (r - i) mod cp_size; per-step partials are merged
  * on chip by online-softmax (log-sum-exp) correction.  The merged result
- * equals plain attention.  Causal uses the top-left mask (key position <=
- * query position) and requires equal q and kv lengths per sequence.
+ * equals plain attention.  Query and key sequences are chunked separately
+ * (P_q / 2cp and P_kv / 2cp rows).
+ *
+ * Masks (`causal`; the pages train causal self-attention, the top-left mask
+ * with equal lengths; the other two are the plainest completions):
+ *   THD_CAUSAL_NONE (0): every valid key.
+ *   THD_CAUSAL_TOP_LEFT (1): query i sees key j iff j <= i; needs equal q
+ *     and kv valid and padded lengths per sequence (else the device status
+ *     THD_DEV_ERR_CAUSAL_LENGTHS).
+ *   THD_CAUSAL_BOTTOM_RIGHT (2): j <= i + L_kv - L_q, the last query aligned
+ *     with the last key (a query block at the end of its keys); equal to
+ *     top-left when the lengths agree.  With L_q > L_kv the first L_q - L_kv
+ *     queries see no key: o = 0, lse = -inf (and zero gradients).
  *
  *   q   [T_q, Hq, D] bf16;  k, v [T_kv, Hkv, D] bf16 (Hq % Hkv == 0; query
  *       head h reads kv head h / (Hq/Hkv)).  16-byte aligned.
  *   o   [T_q, Hq, D] bf16 output; lse [Hq, T_q] fp32 output.  Rows that hold
  *       no valid token (pad rows and rows [pad_q[B], T_q)) get o = 0 and
  *       lse = -inf.
- *   D: 64 or 128.  causal: 1 (causal) or 0 (full).  softmax_scale > 0.
+ *   D: 64 or 128.  causal: 0, 1 or 2 as above.  softmax_scale > 0.
  *   cp_size >= 1: the emulated CP degree.  pad_between_seqs as in
  *   thd_cp_partition (decided per side from values when -1).
  *   Pad rows inside tiles are read: they must hold finite values.

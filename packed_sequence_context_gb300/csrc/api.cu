@@ -172,7 +172,8 @@ static int fwd_common(const void* q, const void* k, const void* v, void* o, floa
   if (!q || !k || !v || !o || !lse || !cu_q || !cu_kv || !dev_status) return THD_ERR_INVALID_ARG;
   if (!aligned(q, 16) || !aligned(k, 16) || !aligned(v, 16) || !aligned(o, 16) || !aligned(lse, 4))
     return THD_ERR_INVALID_ARG;
-  if (!(scale > 0.f) || !std::isfinite(scale) || (causal != 0 && causal != 1)) return THD_ERR_INVALID_ARG;
+  if (!(scale > 0.f) || !std::isfinite(scale) || causal < kCausalNone || causal > kCausalBottomRight)
+    return THD_ERR_INVALID_ARG;
   if (step >= cp) return THD_ERR_INVALID_ARG;
   const WsLayout L = ws_layout(B, T_q, T_kv, Hq, D, cp, false);
   rc = check_ws(ws, ws_bytes, L.total);
@@ -317,7 +318,7 @@ const char* thd_status_string(int s) {
     case THD_DEV_ERR_VALID_GT_PAD: return "valid length exceeds padded length";
     case THD_DEV_ERR_NOT_DIVISIBLE: return "padded length not divisible by 2*cp_size";
     case THD_DEV_ERR_EXCEEDS_BUF: return "sequences exceed the buffer rows";
-    case THD_DEV_ERR_CAUSAL_LENGTHS: return "causal attention needs equal q/kv lengths per sequence";
+    case THD_DEV_ERR_CAUSAL_LENGTHS: return "top-left causal attention needs equal q/kv lengths per sequence";
     case THD_DEV_ERR_CAPACITY: return "internal schedule capacity exceeded";
     default: return "unknown status";
   }
@@ -410,7 +411,7 @@ int thd_attn_bwd(const void* q, const void* k, const void* v, const void* o, con
     return THD_ERR_INVALID_ARG;
   if (dq_rows < T_q || dkv_rows < T_kv || dq_rows >= ((int64_t)1 << 31) || dkv_rows >= ((int64_t)1 << 31))
     return THD_ERR_INVALID_ARG;
-  if (!(softmax_scale > 0.f) || !std::isfinite(softmax_scale) || (causal != 0 && causal != 1))
+  if (!(softmax_scale > 0.f) || !std::isfinite(softmax_scale) || causal < kCausalNone || causal > kCausalBottomRight)
     return THD_ERR_INVALID_ARG;
   const WsLayout L = ws_layout(B, T_q, T_kv, Hq, D, cp_size, true);
   rc = check_ws(workspace, workspace_bytes, L.total);

@@ -70,7 +70,7 @@ __device__ inline BwdItem bwd_item(const BwdParams& p, int n_entries, int w) {
   it.b = e.x;
   it.c = e.y;
   it.jk = e.z;
-  it.g = seq_geom(p.eff, p.B, it.b, p.cp);
+  it.g = seq_geom(p.eff, p.B, it.b, p.cp, p.causal);
   bwd_kv_range(it.g, it.c, it.jk, it.kv_first, it.kv_last);
   return it;
 }
@@ -438,7 +438,7 @@ __global__ void __launch_bounds__(352, 1)
         const int q0 = qc * it.g.cbq + jq * kTile;
         const int nqv = imin(imin(kTile, it.g.cbq - jq * kTile), it.g.Lq - q0);
         int n_lo = 0, n_hi = valid_kv ? nqv : 0;
-        if (p.causal) n_lo = imin(imax(j_pos - q0, 0), kTile);
+        if (p.causal) n_lo = imin(imax(j_pos - it.g.koff - q0, 0), kTile);
         // the cp.async writes of lse/Delta are visible to the threads that
         // observe the stage barrier's phase, so observe it here (it cannot have
         // moved on: the stage is refilled only after this step's p_ready)

@@ -78,9 +78,15 @@ struct SeqGeom {
   int q_off, kv_off;  // buffer row of position 0
   int Lq, Lkv;        // valid lengths
   int cbq, cbkv;      // chunk lengths (padded / (2 cp))
+  int koff;           // causal masks: query i sees key j iff j <= i + koff
 };
 
-__device__ inline SeqGeom seq_geom(const int32_t* eff, int B, int b, int cp) {
+// Causal modes (the `causal` argument of the entry points).
+constexpr int kCausalNone = THD_CAUSAL_NONE;
+constexpr int kCausalTopLeft = THD_CAUSAL_TOP_LEFT;          // j <= i; equal query and key lengths
+constexpr int kCausalBottomRight = THD_CAUSAL_BOTTOM_RIGHT;  // j <= i + Lkv - Lq: last query sees last key
+
+__device__ inline SeqGeom seq_geom(const int32_t* eff, int B, int b, int cp, int causal) {
   const int32_t* cu_q = eff;
   const int32_t* pad_q = eff + (B + 1);
   const int32_t* cu_kv = eff + 2 * (B + 1);
@@ -92,6 +98,7 @@ __device__ inline SeqGeom seq_geom(const int32_t* eff, int B, int b, int cp) {
   g.Lkv = cu_kv[b + 1] - cu_kv[b];
   g.cbq = (pad_q[b + 1] - pad_q[b]) / (2 * cp);
   g.cbkv = (pad_kv[b + 1] - pad_kv[b]) / (2 * cp);
+  g.koff = causal == kCausalBottomRight ? g.Lkv - g.Lq : 0;
   return g;
 }
 
@@ -126,7 +133,8 @@ __host__ __device__ inline int fwd_tile_qmax(const SeqGeom& g, int r, int t, int
 // valid position qmax visits (tiles whose first key is past every query, or
 // past the valid length, are skipped).
 __host__ __device__ inline int fwd_chunk_tiles(const SeqGeom& g, int c, int qmax, bool causal) {
-  const int limit = causal ? imin(g.Lkv, qmax + 1) : (qmax >= 0 ? g.Lkv : 0);
+  if (qmax < 0) return 0;
+  const int limit = causal ? imin(g.Lkv, qmax + g.koff + 1) : g.Lkv;
   const int start = c * g.cbkv;
   if (start >= limit) return 0;
   return imin(ceil_div(g.cbkv, kTile), ceil_div(limit - start, kTile));
@@ -184,7 +192,7 @@ __device__ inline QItem q_item(const P& p, int n_entries, int w) {
   it.r = e.y;
   it.t = e.z;
   it.kvh = it.h / (p.Hq / p.Hkv);
-  it.g = seq_geom(p.eff, p.B, it.b, p.cp);
+  it.g = seq_geom(p.eff, p.B, it.b, p.cp, p.causal);
   it.qmax = fwd_tile_qmax(it.g, it.r, it.t, p.cp);
   return it;
 }
@@ -210,7 +218,7 @@ template <class P>
 __device__ inline int q_tile_ncols(const QItem& it, const P& p, int c, int j) {
   const int j0 = c * it.g.cbkv + j * kTile;
   int n = imin(kTile, imin((c + 1) * it.g.cbkv - j0, it.g.Lkv - j0));
-  if (p.causal) n = imin(n, it.qmax - j0 + 1);
+  if (p.causal) n = imin(n, it.qmax + it.g.koff - j0 + 1);
   return 16 * ceil_div(imax(n, 1), 16);
 }
 
@@ -232,7 +240,7 @@ __host__ __device__ inline bool bwd_q_tile_visits(const SeqGeom& g, int qc, int 
   const int q0 = qc * g.cbq + jq * kTile;
   const int qlast = imin(qc * g.cbq + imin((jq + 1) * kTile, g.cbq), g.Lq) - 1;
   if (q0 > qlast) return false;
-  return causal ? (qlast >= kv_first) : true;
+  return causal ? (qlast + g.koff >= kv_first) : true;
 }
 __host__ __device__ inline int bwd_item_qtiles(const SeqGeom& g, int c, int jk, int cp, bool causal) {
   int kf, kl;

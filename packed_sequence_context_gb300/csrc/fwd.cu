@@ -386,7 +386,7 @@ __global__ void __launch_bounds__(384, 1)
         if (valid) {
           cnt = imin(kTile, (c + 1) * it.g.cbkv - j0);
           cnt = imin(cnt, it.g.Lkv - j0);
-          if (p.causal) cnt = imin(cnt, pos - j0 + 1);
+          if (p.causal) cnt = imin(cnt, pos + it.g.koff - j0 + 1);
           cnt = imax(cnt, 0);
         }
         const int ncols = q_tile_ncols(it, p, c, j);  // the N this tile's QK^T computed

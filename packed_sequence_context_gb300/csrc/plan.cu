@@ -78,7 +78,7 @@ __device__ bool plan_schedule(const PlanParams& p, const int32_t* eff, int32_t* 
     const int b = base + tid;
     int n = 0;
     if (b < B) {
-      SeqGeom g = seq_geom(eff, B, b, cp);
+      SeqGeom g = seq_geom(eff, B, b, cp, p.causal);
       n = mode == 1 ? cp * ceil_div(2 * g.cbq, kTile) : 2 * cp * ceil_div(g.cbkv, kTile);
     }
     int tot;
@@ -104,7 +104,7 @@ __device__ bool plan_schedule(const PlanParams& p, const int32_t* eff, int32_t* 
     b = upper_index(toff, B, w);
     // skip empty sequences that share the same offset
     while (b < B && toff[b + 1] <= w) ++b;
-    SeqGeom g = seq_geom(eff, B, b, cp);
+    SeqGeom g = seq_geom(eff, B, b, cp, p.causal);
     const int rem = w - toff[b];
     if (mode == 1) {
       const int per_r = ceil_div(2 * g.cbq, kTile);
@@ -206,7 +206,7 @@ __global__ void __launch_bounds__(kPlanThreads) plan_kernel(PlanParams p) {
       if (Lq < 0 || Pq < 0 || Lk < 0 || Pk < 0) set_err(&s_err, THD_DEV_ERR_NOT_MONOTONE);
       else if (Lq > Pq || Lk > Pk) set_err(&s_err, THD_DEV_ERR_VALID_GT_PAD);
       else if (Pq % (2 * cp) != 0 || Pk % (2 * cp) != 0) set_err(&s_err, THD_DEV_ERR_NOT_DIVISIBLE);
-      else if (p.causal && (Lq != Lk || Pq != Pk)) set_err(&s_err, THD_DEV_ERR_CAUSAL_LENGTHS);
+      else if (p.causal == kCausalTopLeft && (Lq != Lk || Pq != Pk)) set_err(&s_err, THD_DEV_ERR_CAUSAL_LENGTHS);
     } else {
       if ((int64_t)pq > p.rows_q || (int64_t)pk > p.rows_kv) set_err(&s_err, THD_DEV_ERR_EXCEEDS_BUF);
       if (p.token_map && (int64_t)pq > p.token_map_cap) set_err(&s_err, THD_DEV_ERR_EXCEEDS_BUF);
@@ -526,7 +526,10 @@ __global__ void __launch_bounds__(kPrepThreads) bwd_prep_kernel(const uint16_t* 
       if (tl < nt) {
         const int64_t gi = (int64_t)h * T + t0 + tl;
         delta[gi] = s_delta[i];
-        lse2[gi] = s_valid[tl] ? lse[gi] * 1.4426950408889634f : 0.f;
+        // rows that see no key (bottom-right causal with L_q > L_kv) have
+        // lse = -inf: 0 keeps their masked columns at 2^(-inf - 0) = 0
+        // instead of -inf - (-inf)
+        lse2[gi] = s_valid[tl] && lse[gi] != -INFINITY ? lse[gi] * 1.4426950408889634f : 0.f;
       }
     }
     __syncthreads();

@@ -197,3 +197,39 @@ def algorithmic_flops(lengths, Hq: int, D: int, causal: bool = True) -> tuple[fl
         pairs += L * (L + 1) // 2 if causal else L * L
     fwd = 4.0 * D * Hq * pairs
     return fwd, 3.5 * fwd
+
+
+def make_cross(lengths_q, lengths_kv, *, pad_to: int, Hq: int, Hkv: int, D: int, cp_size: int, seed: int,
+               with_grad: bool = True):
+    """A packed batch whose query and key sequences differ in length (the
+    bottom-right causal case): per sequence b, L_q[b] queries and L_kv[b]
+    keys, each padded up to a multiple of ``pad_to`` (which must itself be a
+    multiple of 2 * cp_size).  Returns a dict of the metadata (int32 numpy:
+    cu_q, cu_kv, cu_q_pad, cu_kv_pad) and bf16 CPU tensors q [T_q, Hq, D],
+    k, v [T_kv, Hkv, D] and, with ``with_grad``, dO [T_q, Hq, D]; pad rows zero.
+    Drawn like make_tensors (fp32 standard normal, RNE to bf16) from
+    ``numpy.random.default_rng(seed + 1000)``."""
+    import torch
+    if pad_to % (2 * cp_size):
+        raise ValueError("pad_to must be a multiple of 2 * cp_size")
+    Lq = [int(x) for x in lengths_q]
+    Lk = [int(x) for x in lengths_kv]
+    Pq = [-(-x // pad_to) * pad_to for x in Lq]
+    Pk = [-(-x // pad_to) * pad_to for x in Lk]
+    meta = {"cu_q": _cumsum0(Lq), "cu_kv": _cumsum0(Lk), "cu_q_pad": _cumsum0(Pq), "cu_kv_pad": _cumsum0(Pk),
+            "L_q": Lq, "L_kv": Lk}
+    rng = np.random.default_rng(seed + 1000)
+    Tq, Tk = int(meta["cu_q_pad"][-1]), int(meta["cu_kv_pad"][-1])
+    t = {"q": _bf16_normal(rng, (Tq, Hq, D)), "k": _bf16_normal(rng, (Tk, Hkv, D)),
+         "v": _bf16_normal(rng, (Tk, Hkv, D))}
+    if with_grad:
+        t["do"] = _bf16_normal(rng, (Tq, Hq, D))
+    for names, L, pad in ((("q", "do"), Lq, meta["cu_q_pad"]), (("k", "v"), Lk, meta["cu_kv_pad"])):
+        m = np.ones(int(pad[-1]), bool)
+        for b, n in enumerate(L):
+            m[int(pad[b]):int(pad[b]) + n] = False
+        for x in names:
+            if x in t:
+                t[x][torch.from_numpy(m)] = 0
+    meta.update(t)
+    return meta

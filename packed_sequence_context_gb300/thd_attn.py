@@ -44,6 +44,10 @@ THD_KERNEL_TAIL_ZERO = 7
 THD_KERNEL_PARTITION = 8
 THD_KERNEL_A2A = 9
 
+THD_CAUSAL_NONE = 0
+THD_CAUSAL_TOP_LEFT = 1
+THD_CAUSAL_BOTTOM_RIGHT = 2
+
 THD_A2A_TO_GROUPS = 0
 THD_A2A_TO_SHARDS = 1
 

@@ -42,6 +42,7 @@ int main() {
       g.Lkv = Lkv;
       g.cbq = Pq / (2 * cp);
       g.cbkv = Pkv / (2 * cp);
+      g.koff = causal == 2 ? Lkv - Lq : 0;   // bottom-right: j <= i + Lkv - Lq
       for (int r = 0; r < cp; ++r)
         for (int t = 0; t < ceil_div(2 * g.cbq, kTile); ++t) {
           const int qmax = fwd_tile_qmax(g, r, t, cp);
@@ -87,14 +88,14 @@ def _cases(seed=0, n=40):
     out = []
     for k in range(n):
         cp = int(rng.choice([1, 2, 3, 4, 8]))
-        causal = int(k % 4 != 3)
+        causal = (1, 1, 2, 0)[k % 4]   # top-left, bottom-right (Lq != Lkv), none
         B = int(rng.integers(1, 5))
         seqs = []
         for _ in range(B):
             unit = 2 * cp
             Pq = unit * int(rng.integers(0, 1200 // unit + 1))
             Lq = int(rng.integers(0, Pq + 1)) if rng.random() < 0.5 else Pq
-            if causal:
+            if causal == 1:
                 Pkv, Lkv = Pq, Lq
             else:
                 Pkv = unit * int(rng.integers(0, 900 // unit + 1))
@@ -106,6 +107,8 @@ def _cases(seed=0, n=40):
     out.append((8, 1, [(16, 16, 16, 16), (0, 32, 0, 32)]))
     out.append((1, 1, [(1000, 1024, 1000, 1024)]))
     out.append((2, 0, [(260, 264, 5, 8)]))
+    # bottom-right: fewer queries than keys, more queries than keys (the first Lq - Lkv see nothing)
+    out.append((4, 2, [(100, 128, 1000, 1024), (1000, 1024, 100, 128), (0, 8, 40, 48)]))
     return out
 
 
@@ -129,8 +132,8 @@ def _pos(p, r, cb, cp):
     return r * cb + p if p < cb else (2 * cp - 1 - r) * cb + (p - cb)
 
 
-def _sees(i, j, Lkv, causal):
-    return j < Lkv and (j <= i if causal else True)
+def _sees(i, j, Lkv, causal, koff=0):
+    return j < Lkv and (j <= i + koff if causal else True)
 
 
 def test_every_allowed_pair_is_visited_exactly_once(walker):
@@ -149,6 +152,7 @@ def test_every_allowed_pair_is_visited_exactly_once(walker):
         bwd = [ln.split() for ln in lines if ln.startswith("K")]
         for b, (Lq, Pq, Lkv, Pkv) in enumerate(seqs):
             cbq, cbkv = Pq // (2 * cp), Pkv // (2 * cp)
+            koff = Lkv - Lq if causal == 2 else 0
 
             def key_range(c, j):
                 lo = c * cbkv + j * TILE
@@ -171,7 +175,7 @@ def test_every_allowed_pair_is_visited_exactly_once(walker):
                     js = [j for cc, j in tiles if cc == c]
                     assert js == list(range(len(js)))
                 # every row's visible keys are a prefix: all of [0, need_hi] must be covered, once
-                need_hi = (min(qmax, Lkv - 1) if causal else Lkv - 1) if valid else -1
+                need_hi = (min(qmax + koff, Lkv - 1) if causal else Lkv - 1) if valid else -1
                 covered = set()
                 for c, j in tiles:
                     lo, hi = key_range(c, j)
@@ -200,8 +204,8 @@ def test_every_allowed_pair_is_visited_exactly_once(walker):
                 s = c if c < cp else 2 * cp - 1 - c
                 order = [qc for i in range(cp) for qc in ((s + i) % cp, 2 * cp - 1 - (s + i) % cp)]
                 assert [qc for qc, _ in qtiles] == sorted((qc for qc, _ in qtiles), key=order.index)
-                # the queries that see some key of [kf, kl]: i >= kf under the causal mask, all otherwise
-                need = set(range(kf if causal else 0, Lq))
+                # the queries that see some key of [kf, kl]: i + koff >= kf under a causal mask, all otherwise
+                need = set(range(max(kf - koff, 0) if causal else 0, Lq))
                 rows_in = set()
                 for qc, jq in qtiles:
                     q_lo, q_hi = qc * cbq + jq * TILE, min(qc * cbq + min((jq + 1) * TILE, cbq), Lq)
