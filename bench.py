@@ -71,7 +71,7 @@ def _kernel_traffic(kernel: str, workload: str):
         return None
     cs = os.path.join(ROOT, "packed_sequence_context_gb300", "csrc")
     h = hashlib.sha256()
-    for name in (kernel.split("_")[0] + ".cu", "common.cuh", "ptx.cuh"):
+    for name in (kernel.split("_")[0] + ".cu", "common.cuh", "ptx.cuh", "sched.cuh"):
         with open(os.path.join(cs, name), "rb") as f:
             h.update(f.read())
     if h.hexdigest()[:16] != rec.get("source_sha"):
