@@ -156,11 +156,14 @@ def test_attn_bwd_a2a_matches_oracle(case):
 
 
 @pytest.mark.parametrize("a", [4, 2])
-def test_attn_a2a_full_size_sampled(a):
-    """The default packed workload (8 sequences, 14,632 tokens, 16 heads,
-    cp 4) through Ulysses (a2a 4) and hierarchical [2, 2]: the shards are
-    un-sharded by the oracle's move and the shortest two sequences plus one
-    mid-length one are recomputed by the oracle for one head group."""
+def test_attn_a2a_full_size_every_row(a):
+    """The packed workload (8 sequences, 14,632 tokens, 16 heads, cp 4)
+    through Ulysses (a2a 4) and hierarchical [2, 2]: the shards are
+    un-sharded by the oracle's move, and O, lse, dQ, dK and dV are compared
+    with the oracle's unsplit attention on every valid row of every head (the
+    oracle in a process pool, the bars of oracle_pool)."""
+    import os
+    import oracle_pool as op
     w = inputs.make_workload("packed")
     t = inputs.make_tensors(w, with_grad=True)
     sh = _shards(w, t)
@@ -175,26 +178,30 @@ def test_attn_a2a_full_size_sampled(a):
     pad = w.cu_seqlens_padded
 
     def unshard(x):
-        return orc.a2a_seq_to_head(x.view(torch.int16).cpu().numpy(), pad, w.cp_size, 1)[0]
+        return torch.from_numpy(orc.a2a_seq_to_head(x.view(torch.int16).cpu().numpy(), pad, w.cp_size, 1)[0]) \
+            .view(torch.bfloat16).float().numpy()
 
-    og, dqg, dkg, dvg = (torch.from_numpy(unshard(x)).view(torch.bfloat16).float().numpy()
-                         for x in (o, dq, dk, dv))
-    lg = f64(lse)
-    h = 5
-    order = np.argsort(w.lengths)
-    worst = 0.0
-    for b in list(order[:2]) + [order[len(order) // 2]]:
-        off, L = int(pad[b]), w.lengths[b]
-        sl = slice(off, off + L)
-        cu1 = np.array([0, L], np.int32)
-        qq, kk, vv, dd = (t[x][sl][:, h:h + 1].float().numpy() for x in ("q", "k", "v", "do"))
-        O_ref, lse_ref = orc.attn_fwd(qq, kk, vv, cu1, cu1, softmax_scale=w.softmax_scale)
-        rq, rk, rv = orc.attn_bwd(qq, kk, vv, dd, cu1, cu1, softmax_scale=w.softmax_scale)
-        for g, r in ((og[sl][:, h:h + 1], O_ref), (dqg[sl][:, h:h + 1], rq), (dkg[sl][:, h:h + 1], rk),
-                     (dvg[sl][:, h:h + 1], rv)):
-            worst = max(worst, float(np.abs(g - r).max()))
-        assert np.abs(lg[h, sl] - lse_ref[0]).max() <= LSE_TOL
-    assert worst <= O_TOL, f"sampled max-abs {worst:.3e}"
+    store = op.Store()
+    try:
+        for k_ in ("q", "k", "v", "do"):
+            store.put(k_, t[k_].float().numpy())
+        for k_, x in (("o", o), ("dq", dq), ("dk", dk), ("dv", dv)):
+            store.put(k_, unshard(x))
+        store.put("lse", lse.cpu().numpy())
+        root = os.path.dirname(os.path.dirname(os.path.abspath(__file__)))
+        specs = [{"root": root, "dir": store.dir, "off": int(pad[b]), "L": int(w.lengths[b]), "kv_heads": [hk],
+                  "G": w.Hq // w.Hkv, "scale": w.softmax_scale, "bwd": True}
+                 for b in range(w.B) if w.lengths[b] > 0 for hk in range(w.Hkv)]
+        specs.sort(key=lambda s_: -s_["L"])
+        res = op.run(op._worker_seq, specs)
+    finally:
+        store.close()
+    for k_ in ("o", "dq", "dk", "dv"):
+        st_ = None
+        for r in res:
+            st_ = op.merge_stats(st_, r[k_])
+        assert st_["excess"] <= op.TOL and st_["raw_small"] <= op.TOL, (k_, st_)
+    assert max(r["lse"] for r in res) <= op.LSE_TOL
     for g in (o, dq, dk, dv):
         assert torch.isfinite(g.float()).all()
 
