@@ -418,6 +418,20 @@ THD_API uint64_t thd_launch_count(void);
  */
 THD_API int thd_test_arm_stall(int kernel_id);
 
+/*
+ * Test hook (not for normal use): the forward has two kernels with the same
+ * results up to rounding order -- one that runs a single work item per CTA
+ * at a time (used when sequences average at least 16384 tokens) and one
+ * with two items in flight per CTA (used otherwise).  which =
+ * THD_FWD_KERNEL_SINGLE or THD_FWD_KERNEL_DUAL makes every later forward
+ * call (fused or one-step) use that kernel, so tests can run both on any
+ * workload; 0 restores the automatic choice.  Process-wide.  Returns
+ * THD_ERR_INVALID_ARG for any other value.
+ */
+#define THD_FWD_KERNEL_SINGLE 1
+#define THD_FWD_KERNEL_DUAL 2
+THD_API int thd_test_select_fwd_kernel(int which);
+
 #ifdef __cplusplus
 }
 #endif

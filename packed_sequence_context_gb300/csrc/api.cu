@@ -47,6 +47,11 @@ bool take_test_stall(int kernel_id) {
   return kernel_id != 0 && g_stall_kernel.compare_exchange_strong(expect, 0);
 }
 
+// Test hook: which forward kernel the next calls use (see
+// thd_test_select_fwd_kernel); 0 = chosen from the workload.
+static std::atomic<int> g_fwd_kernel{0};
+int test_fwd_kernel() { return g_fwd_kernel.load(std::memory_order_relaxed); }
+
 void prof_before(int id, cudaStream_t st) {
   if (g_prof.kernel != id) return;
   std::lock_guard<std::mutex> lk(g_prof.mu);
@@ -197,10 +202,17 @@ static int fwd_common(const void* q, const void* k, const void* v, void* o, floa
   fp.items = pp.items;
   fp.counters = pp.counters;
   fp.claim = pp.counters + 1;
-  // the forward hands its items out dynamically only with the grouped order
-  // (on short sequences the static walk measured 7-8% faster)
+  // Sequences averaging >= kLongSeqTokens: the single-item kernel (three S
+  // buffers keep the tensor pipe busy through the softmax), items grouped by
+  // kv head and handed out dynamically.  Shorter sequences (items of a few
+  // key tiles): the kernel with two items in flight per CTA, entry-major,
+  // dynamic.  Measured on GB300: single-item 1311-1327 vs two-item 1093-1108
+  // TFLOPS on one 131,072-token sequence; two-item 597 / 534 / 841 vs
+  // single-item 519-535 / 515-521 / 835-848 on the 0.1-8K-token batches.
   const bool grouped = long_sequences(B, T_kv);
   fp.group_kv = locality_group(Hkv, (size_t)T_kv * D * 2 * 2, grouped);
+  const int forced = test_fwd_kernel();
+  const bool single = forced ? forced == THD_FWD_KERNEL_SINGLE : grouped;
   fp.dev_status = dev_status;
   fp.B = B;
   fp.Hq = Hq;
@@ -216,7 +228,9 @@ static int fwd_common(const void* q, const void* k, const void* v, void* o, floa
   const int grid = (int)(bound < num_sms() ? (bound > 0 ? bound : 1) : num_sms());
   // O is written in bf16 (the fused forward, or one step's partial in bf16)
   // or, for a step partial requested in fp32, in fp32
-  return cuda_status(launch_fwd(fp, tk, tv, D, step >= 0 && part_fp32, grouped, grid, st));
+  const bool part32 = step >= 0 && part_fp32;
+  return cuda_status(single ? launch_fwd(fp, tk, tv, D, part32, grouped, grid, st)
+                            : launch_fwd_dual(fp, tk, tv, D, part32, grid, st));
 }
 
 // ------------------------------------------------------------------ A2A / hierarchical
@@ -669,6 +683,12 @@ int thd_profile_read(float* ms_out, int max_out, int* count_out) {
 }
 
 uint64_t thd_launch_count(void) { return g_launches.load(std::memory_order_relaxed); }
+
+int thd_test_select_fwd_kernel(int which) {
+  if (which != 0 && which != THD_FWD_KERNEL_SINGLE && which != THD_FWD_KERNEL_DUAL) return THD_ERR_INVALID_ARG;
+  g_fwd_kernel.store(which, std::memory_order_relaxed);
+  return THD_OK;
+}
 
 int thd_test_arm_stall(int kernel_id) {
   if (kernel_id != 0 && kernel_id != THD_KERNEL_FWD && kernel_id != THD_KERNEL_BWD && kernel_id != THD_KERNEL_BWD_DQ)

@@ -347,6 +347,8 @@ struct DqParams {
 cudaError_t launch_plan(const PlanParams& p, cudaStream_t st);
 cudaError_t launch_fwd(const FwdParams& p, const CUtensorMap& tk, const CUtensorMap& tv, int D, bool step_mode,
                        bool dyn, int grid, cudaStream_t st);
+cudaError_t launch_fwd_dual(const FwdParams& p, const CUtensorMap& tk, const CUtensorMap& tv, int D, bool step_mode,
+                            int grid, cudaStream_t st);
 cudaError_t launch_bwd(const BwdParams& p, const CUtensorMap& tq, const CUtensorMap& tdo, const CUtensorMap& tk,
                        const CUtensorMap& tv, int D, bool grouped, int grid, cudaStream_t st);
 cudaError_t launch_dq(const DqParams& p, const CUtensorMap& tk, const CUtensorMap& tv, int D, bool grouped,
@@ -364,6 +366,7 @@ cudaError_t launch_bwd_prep(const uint16_t* o, const uint16_t* dout, const float
 
 int num_sms();
 bool take_test_stall(int kernel_id);
+int test_fwd_kernel();
 void prof_before(int kernel_id, cudaStream_t st);
 void prof_after(int kernel_id, cudaStream_t st);
 void count_launch();

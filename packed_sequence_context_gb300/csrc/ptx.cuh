@@ -48,20 +48,35 @@ THD_DEV bool mbar_try_wait(uint64_t* bar, uint32_t parity) {
   return ok != 0;
 }
 
+// The same test, but the thread may be suspended (it issues nothing) until
+// the phase completes or about `suspend_ns` have passed.
+constexpr uint32_t kWaitSuspendNs = 1000000;
+THD_DEV bool mbar_try_wait_suspend(uint64_t* bar, uint32_t parity) {
+  uint32_t ok;
+  asm volatile(
+      "{\n\t.reg .pred p;\n\t"
+      "mbarrier.try_wait.parity.shared::cta.b64 p, [%1], %2, %3;\n\t"
+      "selp.u32 %0, 1, 0, p;\n\t}"
+      : "=r"(ok)
+      : "r"(smem_u32(bar)), "r"(parity), "n"(kWaitSuspendNs)
+      : "memory");
+  return ok != 0;
+}
+
 // Bounded wait for the phase with the given parity.  Returns false when the
 // CTA-wide abort flag is (or gets) set -- by this wait timing out or by
-// another warp -- so that no thread ever spins without limit.
+// another warp -- so that no thread ever spins without limit.  A waiting
+// thread sleeps in the barrier instead of re-polling it, so waiting warps
+// take no issue slots from the working ones.
 THD_DEV bool mbar_wait(uint64_t* bar, uint32_t parity, volatile int* abort_flag) {
   if (mbar_try_wait(bar, parity)) return true;
   const uint64_t t0 = globaltimer();
-  for (uint32_t it = 1;; ++it) {
-    if (mbar_try_wait(bar, parity)) return true;
-    if ((it & 63u) == 0) {
-      if (*abort_flag) return false;
-      if (globaltimer() - t0 > kWaitTimeoutNs) {
-        *abort_flag = 1;
-        return false;
-      }
+  for (;;) {
+    if (mbar_try_wait_suspend(bar, parity)) return true;
+    if (*abort_flag) return false;
+    if (globaltimer() - t0 > kWaitTimeoutNs) {
+      *abort_flag = 1;
+      return false;
     }
   }
 }
@@ -128,6 +143,18 @@ THD_DEV void tmem_alloc(uint32_t* dst_smem, uint32_t ncols) {
 THD_DEV void tmem_relinquish() { asm volatile("tcgen05.relinquish_alloc_permit.cta_group::1.sync.aligned;" ::: "memory"); }
 THD_DEV void tmem_dealloc(uint32_t taddr, uint32_t ncols) {
   asm volatile("tcgen05.dealloc.cta_group::1.sync.aligned.b32 %0, %1;" ::"r"(taddr), "r"(ncols) : "memory");
+}
+// Per-warpgroup register budget (every warp of the warpgroup executes the
+// same instruction).  A warpgroup that lowers its budget returns registers to
+// the CTA's pool (the count it was launched with); one that raises it waits
+// until the pool holds enough.
+template <uint32_t N>
+THD_DEV void regs_raise() {
+  asm volatile("setmaxnreg.inc.sync.aligned.u32 %0;" ::"n"(N));
+}
+template <uint32_t N>
+THD_DEV void regs_lower() {
+  asm volatile("setmaxnreg.dec.sync.aligned.u32 %0;" ::"n"(N));
 }
 THD_DEV void tc_fence_before() { asm volatile("tcgen05.fence::before_thread_sync;" ::: "memory"); }
 THD_DEV void tc_fence_after() { asm volatile("tcgen05.fence::after_thread_sync;" ::: "memory"); }

@@ -44,6 +44,9 @@ THD_KERNEL_TAIL_ZERO = 7
 THD_KERNEL_PARTITION = 8
 THD_KERNEL_A2A = 9
 
+THD_FWD_KERNEL_SINGLE = 1
+THD_FWD_KERNEL_DUAL = 2
+
 THD_CAUSAL_NONE = 0
 THD_CAUSAL_TOP_LEFT = 1
 THD_CAUSAL_BOTTOM_RIGHT = 2
@@ -86,6 +89,7 @@ SIGNATURES = {
     "thd_profile_read": (_i32, [_vp, _i32, _vp]),
     "thd_launch_count": (ctypes.c_uint64, []),
     "thd_test_arm_stall": (_i32, [_i32]),
+    "thd_test_select_fwd_kernel": (_i32, [_i32]),
 }
 
 _LIB = None
@@ -245,6 +249,10 @@ def thd_launch_count() -> int:
 
 def thd_test_arm_stall(kernel_id: int) -> int:
     return lib().thd_test_arm_stall(kernel_id)
+
+
+def thd_test_select_fwd_kernel(which: int) -> int:
+    return lib().thd_test_select_fwd_kernel(which)
 
 
 # ----------------------------------------------------------------- helpers

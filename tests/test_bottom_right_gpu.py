@@ -26,9 +26,15 @@ CASES = [
 ]
 
 
-@pytest.fixture(scope="module", autouse=True)
-def _lib(thd_lib):
-    return thd_lib
+@pytest.fixture(scope="module", autouse=True, params=[T.THD_FWD_KERNEL_SINGLE, T.THD_FWD_KERNEL_DUAL],
+                ids=["single", "dual"])
+def _lib(thd_lib, request):
+    """Every test of this module runs once per forward kernel (the
+    single-item kernel the library picks for long sequences, and the
+    two-item one it picks for shorter ones)."""
+    assert T.thd_test_select_fwd_kernel(request.param) == T.THD_OK
+    yield thd_lib
+    T.thd_test_select_fwd_kernel(0)
 
 
 def _case(i, grad=True):

@@ -37,7 +37,16 @@ def _tiny():
     return w, t, device_inputs(w, t)
 
 
-def test_forward_wait_runs_out_then_device_recovers():
+@pytest.mark.parametrize("fwd_kernel", [T.THD_FWD_KERNEL_SINGLE, T.THD_FWD_KERNEL_DUAL], ids=["single", "dual"])
+def test_forward_wait_runs_out_then_device_recovers(fwd_kernel):
+    assert T.thd_test_select_fwd_kernel(fwd_kernel) == T.THD_OK
+    try:
+        _forward_stall_case()
+    finally:
+        T.thd_test_select_fwd_kernel(0)
+
+
+def _forward_stall_case():
     w, t, d = _tiny()
     o = torch.full_like(d["q"], CANARY)
     assert T.thd_test_arm_stall(T.THD_KERNEL_FWD) == T.THD_OK
@@ -84,6 +93,7 @@ def test_backward_wait_runs_out_then_device_recovers(kernel):
 
 
 def test_stall_hook_is_one_shot_and_checks_its_argument():
+    assert T.thd_test_select_fwd_kernel(3) == T.THD_ERR_INVALID_ARG
     assert T.thd_test_arm_stall(T.THD_KERNEL_LSE_MERGE) == T.THD_ERR_INVALID_ARG
     assert T.thd_test_arm_stall(T.THD_KERNEL_FWD) == T.THD_OK
     assert T.thd_test_arm_stall(0) == T.THD_OK      # disarmed: the next forward runs normally

@@ -16,9 +16,15 @@ from thd_testutil import LSE_TOL, O_TOL, assert_fwd_close, device_inputs, f64, r
 pytestmark = pytest.mark.gpu
 
 
-@pytest.fixture(scope="module", autouse=True)
-def _lib(thd_lib):
-    return thd_lib
+@pytest.fixture(scope="module", autouse=True, params=[T.THD_FWD_KERNEL_SINGLE, T.THD_FWD_KERNEL_DUAL],
+                ids=["single", "dual"])
+def _lib(thd_lib, request):
+    """Every test of this module runs once per forward kernel (the
+    single-item kernel the library picks for long sequences, and the
+    two-item one it picks for shorter ones)."""
+    assert T.thd_test_select_fwd_kernel(request.param) == T.THD_OK
+    yield thd_lib
+    T.thd_test_select_fwd_kernel(0)
 
 
 def _custom(lengths, cp, Hq=2, Hkv=2, D=64, pad_to=0, seed=0):
