@@ -140,7 +140,7 @@ __global__ void __launch_bounds__(352, 1)
 
   if (tid == 0) {
     mbar_init(bar_kv_full, 1);
-    mbar_init(bar_kv_empty, 1);
+    mbar_init(bar_kv_empty, 2);  // warp 9 saw the tile arrive; warp 10: its last reader completed
     for (int s = 0; s < S; ++s) {
       mbar_init(&bar_qdo_full[s], 33);  // 32 cp.async arrivals + the TMA expect-tx arrival
       mbar_init(&bar_qdo_empty[s], 1);
@@ -287,6 +287,10 @@ __global__ void __launch_bounds__(352, 1)
         if (it.kv_first > it.kv_last) continue;
         if (!mbar_wait(bar_kv_full, kv_iter & 1u, s_abort)) break;
         ++kv_iter;
+        // this thread has seen the tile's phase: the tile may be refilled once
+        // warp 10 also releases it, and never before this wait (which would
+        // leave this wait two phases behind when the item has no step)
+        mbar_arrive(bar_kv_empty);
         for_each_q_step(it, p, [&](int qc, int jq, int) {
           if (!ok) return;
           const int nqv = imin(imin(kTile, it.g.cbq - jq * kTile), it.g.Lq - (qc * it.g.cbq + jq * kTile));
@@ -327,9 +331,14 @@ __global__ void __launch_bounds__(352, 1)
       // the step whose dV / dK are still to be issued
       int pv_stage = -1, pv_n16 = 0;
       bool pv_first = false;
-      auto tail = [&]() -> bool {
+      auto tail = [&](bool last) -> bool {
         const uint32_t ps = su - 1;  // the pending step
         if (!mbar_wait(bar_p_ready, ps & 1u, s_abort)) return false;
+        // The compute warps wrote P^T and dS^T of the item's last step only
+        // after its S^T and dP^T -- the last products that read K and V --
+        // had completed: the K/V tile may be refilled with the next item's
+        // while the last dV and dK run and the epilogue drains them.
+        if (last) mbar_arrive(bar_kv_empty);
         tc_fence_after();
         const uint32_t qb = smem_u32(smem + C::kOffQ + pv_stage * 2 * C::kTileBytes);
         const uint32_t dob = qb + C::kTileBytes;
@@ -371,7 +380,7 @@ __global__ void __launch_bounds__(352, 1)
           }
           // dV, dK of the previous step (of this item; an item's last step is
           // finished at the item's end)
-          if (pv_stage >= 0 && !tail()) {
+          if (pv_stage >= 0 && !tail(false)) {
             ok = false;
             return;
           }
@@ -400,8 +409,11 @@ __global__ void __launch_bounds__(352, 1)
           }
         });
         if (!ok) break;
-        if (pv_stage >= 0 && !tail()) break;  // the item's last step; dk_done then covers all its products
-        tc_commit(bar_kv_empty);
+        if (pv_stage >= 0) {
+          if (!tail(true)) break;  // the item's last step; dk_done then covers all its products
+        } else {
+          mbar_arrive(bar_kv_empty);  // no step read the tile
+        }
       }
       tc_commit(bar_drain2);
       drain_wait_b(bar_drain2, 0);
