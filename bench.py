@@ -71,7 +71,8 @@ def _kernel_traffic(kernel: str, workload: str):
         return None
     cs = os.path.join(ROOT, "packed_sequence_context_gb300", "csrc")
     h = hashlib.sha256()
-    for name in (kernel.split("_")[0] + ".cu", "common.cuh", "ptx.cuh", "sched.cuh"):
+    src = {"fwd_dual_kernel": "fwd_dual.cu"}.get(kernel, kernel.split("_")[0] + ".cu")
+    for name in (src, "common.cuh", "ptx.cuh", "sched.cuh"):
         with open(os.path.join(cs, name), "rb") as f:
             h.update(f.read())
     if h.hexdigest()[:16] != rec.get("source_sha"):
@@ -370,6 +371,13 @@ def _mean(x):
     return sum(x) / len(x) if x else float("nan")
 
 
+def fwd_kernel_name(w) -> str:
+    """The forward kernel the library runs on this workload: the single-item
+    kernel when sequences average >= 16384 rows of K/V buffer, else the
+    two-item one (the rule in csrc/api.cu)."""
+    return "fwd_kernel" if int(w.cu_seqlens_padded[-1]) >= 16384 * len(w.lengths) else "fwd_dual_kernel"
+
+
 def tensor_roofline(kernel, flops, kms, peak, peak_sus, peak_kind, workload, executed=False):
     """The kernel's achieved TFLOP/s: its work per launch over the mean
     per-launch CUDA-event time (library hook), against the bf16 peak."""
@@ -403,7 +411,7 @@ def measure_case(c, steps, warmup, stream, flush_buf, peaks, world=1):
         "fwdbwd_tflops": c.both_flops / (_mean(both) * 1e-3) / 1e12,
         "fwd_tflops": c.fwd_flops / (_mean(fwd) * 1e-3) / 1e12,
         "roofline": tensor_roofline("bwd_kernel", 2.0 * c.fwd_flops, kms, peak, peak_sus, peak_kind, name),
-        "fwd_roofline": tensor_roofline("fwd_kernel", c.fwd_flops, fkms, peak, peak_sus, peak_kind, name),
+        "fwd_roofline": tensor_roofline(fwd_kernel_name(c.w), c.fwd_flops, fkms, peak, peak_sus, peak_kind, name),
         "dq_roofline": tensor_roofline("dq_kernel", 1.5 * c.fwd_flops, dkms, peak, peak_sus, peak_kind, name,
                                        executed=True),
         "_times": both,
@@ -462,7 +470,7 @@ def run_ours(a):
     value = weak_scaling_tflops(step_flops, world, ms_max)
     fwd_ms = _mean(fwd_times)
     fwd_tflops = c.fwd_flops / (fwd_ms * 1e-3) / 1e12
-    fwd_roof = tensor_roofline("fwd_kernel", c.fwd_flops, fwd_kms, peak, peak_sus, peak_kind, w.name)
+    fwd_roof = tensor_roofline(fwd_kernel_name(w), c.fwd_flops, fwd_kms, peak, peak_sus, peak_kind, w.name)
     if a.fwd_only:
         roof = fwd_roof
     else:
