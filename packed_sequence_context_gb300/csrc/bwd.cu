@@ -115,8 +115,8 @@ __global__ void __launch_bounds__(352, 1)
   uint64_t* bars = reinterpret_cast<uint64_t*>(smem + C::kOffBar);
   uint64_t* bar_kv_full = bars + 0;
   uint64_t* bar_kv_empty = bars + 1;
-  uint64_t* bar_qdo_full = bars + 2;       // [S]
-  uint64_t* bar_qdo_empty = bars + 2 + S;  // [S]
+  uint64_t* bar_qdo_full = bars + 2;       // [S] Q (TMA) and lse / Delta (cp.async) of the stage landed
+  uint64_t* bar_qdo_empty = bars + 2 + S;  // [S] the stage's Q may be refilled (its dK completed)
   uint64_t* bar_st_full = bars + 2 + 2 * S;
   uint64_t* bar_p_ready = bars + 3 + 2 * S;
   uint64_t* bar_dk_done = bars + 4 + 2 * S;
@@ -124,7 +124,8 @@ __global__ void __launch_bounds__(352, 1)
   uint64_t* bar_dp_full = bars + 10 + 2 * S;  // dP^T of the step is in TMEM
   uint64_t* bar_drain = bars + 6 + 2 * S;
   uint64_t* bar_drain2 = bars + 11 + 2 * S;
-  uint64_t* bar_dv_done = bars + 7 + 2 * S;
+  uint64_t* bar_do_full = bars + 12 + 2 * S;   // [S] dO of the stage landed (TMA)
+  uint64_t* bar_do_empty = bars + 12 + 3 * S;  // [S] the stage's dO may be refilled (its dV completed)
   uint32_t* s_tmem = reinterpret_cast<uint32_t*>(bars + 8 + 2 * S);
   int* s_abort = reinterpret_cast<int*>(bars + 9 + 2 * S);
   ItemRing* ring = reinterpret_cast<ItemRing*>(smem + C::kOffRing);  // items of this CTA, in claim order
@@ -144,6 +145,8 @@ __global__ void __launch_bounds__(352, 1)
     for (int s = 0; s < S; ++s) {
       mbar_init(&bar_qdo_full[s], 33);  // 32 cp.async arrivals + the TMA expect-tx arrival
       mbar_init(&bar_qdo_empty[s], 1);
+      mbar_init(&bar_do_full[s], 1);
+      mbar_init(&bar_do_empty[s], 1);
     }
     mbar_init(bar_st_full, 1);
     mbar_init(bar_p_ready, 8);  // one arrival per compute warp
@@ -152,7 +155,6 @@ __global__ void __launch_bounds__(352, 1)
     mbar_init(bar_dp_full, 1);
     mbar_init(bar_drain2, 1);
     mbar_init(bar_drain, 1);
-    mbar_init(bar_dv_done, 1);
     item_ring_init(ring, 2 + 8);  // warps 9, 10 (one thread each) and the 8 compute warps
     *s_abort = 0;
     fence_mbar_init();
@@ -235,15 +237,24 @@ __global__ void __launch_bounds__(352, 1)
         }
         cp_async_arrive_noinc(&bar_qdo_full[stage]);
         __syncwarp();  // the zeroed entries are ordered before lane 0's arrival
+        uint8_t* sQ = smem + C::kOffQ + stage * 2 * C::kTileBytes;
+        uint8_t* sDO = sQ + C::kTileBytes;
         if (lane == 0) {
-          mbar_arrive_expect_tx(&bar_qdo_full[stage], 2 * C::kTileBytes);
-          uint8_t* sQ = smem + C::kOffQ + stage * 2 * C::kTileBytes;
-          uint8_t* sDO = sQ + C::kTileBytes;
+          mbar_arrive_expect_tx(&bar_qdo_full[stage], C::kTileBytes);
 #pragma unroll
-          for (int hb = 0; hb < D / 64; ++hb) {
+          for (int hb = 0; hb < D / 64; ++hb)
             tma_load_3d(smem_u32(sQ + hb * 16384), &tmQ, &bar_qdo_full[stage], hb * 64, h, q_row);
-            tma_load_3d(smem_u32(sDO + hb * 16384), &tmDO, &bar_qdo_full[stage], hb * 64, h, q_row);
-          }
+        }
+        // dO has its own release: its last reader (dV) completes after Q's (dK)
+        if (!mbar_wait(&bar_do_empty[stage], ph ^ 1u, s_abort)) {
+          ok = false;
+          return;
+        }
+        if (lane == 0) {
+          mbar_arrive_expect_tx(&bar_do_full[stage], C::kTileBytes);
+#pragma unroll
+          for (int hb = 0; hb < D / 64; ++hb)
+            tma_load_3d(smem_u32(sDO + hb * 16384), &tmDO, &bar_do_full[stage], hb * 64, h, q_row);
         }
         ++n_fill;
         if (++stage == S) {
@@ -256,7 +267,10 @@ __global__ void __launch_bounds__(352, 1)
     if (kv_iter > 0) drain_wait_b(bar_kv_full, (kv_iter - 1) & 1u);
     for (int s = 0; s < S; ++s) {
       const uint32_t fills = n_fill > (uint32_t)s ? (n_fill - 1 - s) / S + 1 : 0;
-      if (fills > 0) drain_wait_b(&bar_qdo_full[s], (fills - 1) & 1u);
+      if (fills > 0) {
+        drain_wait_b(&bar_qdo_full[s], (fills - 1) & 1u);
+        drain_wait_b(&bar_do_full[s], (fills - 1) & 1u);
+      }
     }
     __syncwarp();
   } else if (warp == 9) {
@@ -343,19 +357,21 @@ __global__ void __launch_bounds__(352, 1)
         const uint32_t qb = smem_u32(smem + C::kOffQ + pv_stage * 2 * C::kTileBytes);
         const uint32_t dob = qb + C::kTileBytes;
         const uint32_t pcol = tmem + C::kColX + 128u * (ps & 1u);  // P^T of the pending step
-        // dV += P^T dO  (P^T packed bf16: query columns 16 ks.. of K-step ks sit
-        // at column 64 (ks/4) + 8 (ks%4); K = the valid query rows)
-        for (int ks = 0; ks < pv_n16; ++ks)
-          mma_ts(tmem + C::kColDV, pcol + 64 * (ks >> 2) + 8 * (ks & 3), sdesc_sw128(dob + ks * 2048, 16384, 1024),
-                 idesc_kv, (pv_first && ks == 0) ? 0u : 1u);
-        tc_commit(bar_dv_done);
+        // dK first: its completion frees the stage's Q, which the S^T two
+        // steps on waits for, one product earlier than dO.
         // dK += dS^T Q  (dS^T packed bf16 beside P^T: K-step ks at column
-        // 64 (ks/4) + 32 + 8 (ks%4))
+        // 64 (ks/4) + 32 + 8 (ks%4); K = the valid query rows)
         for (int ks = 0; ks < pv_n16; ++ks)
           mma_ts(tmem + C::kColDK, pcol + 64 * (ks >> 2) + 32 + 8 * (ks & 3), sdesc_sw128(qb + ks * 2048, 16384, 1024),
                  idesc_kv, (pv_first && ks == 0) ? 0u : 1u);
-        tc_commit(bar_dk_done);
         tc_commit(&bar_qdo_empty[pv_stage]);
+        // dV += P^T dO  (P^T packed bf16: query columns 16 ks.. of K-step ks sit
+        // at column 64 (ks/4) + 8 (ks%4))
+        for (int ks = 0; ks < pv_n16; ++ks)
+          mma_ts(tmem + C::kColDV, pcol + 64 * (ks >> 2) + 8 * (ks & 3), sdesc_sw128(dob + ks * 2048, 16384, 1024),
+                 idesc_kv, (pv_first && ks == 0) ? 0u : 1u);
+        tc_commit(&bar_do_empty[pv_stage]);
+        tc_commit(bar_dk_done);  // both of the step's products (this thread's MMAs complete in order)
         pv_stage = -1;
         return true;
       };
@@ -386,7 +402,8 @@ __global__ void __launch_bounds__(352, 1)
           }
           // dP^T = V dO^T -> the buffer P^T(s-1) and dS^T(s-1) leave once dV(s-1)
           // and dK(s-1) have read them
-          if (su > 0 && !mbar_wait(bar_dk_done, (su - 1) & 1u, s_abort)) {
+          if ((su > 0 && !mbar_wait(bar_dk_done, (su - 1) & 1u, s_abort)) ||
+              !mbar_wait(&bar_do_full[stage], ph, s_abort)) {
             ok = false;
             return;
           }
