@@ -18,10 +18,12 @@
 //   P^T  = exp(S^T scale - lse)          dS^T = P^T (dP^T - Delta)
 //   dV  += P^T dO     dK  += dS^T Q       (A = P^T / dS^T from TMEM, packed bf16
 //                                          over the S^T they were computed from)
-// CTA (352 threads): warps 0-7 compute in two warpgroups -- a thread owns one
+// CTA (384 threads): warps 0-7 compute in two warpgroups -- a thread owns one
 // key row (its TMEM lane) and half of the query columns for P/dS, and half of
 // the head dimension when writing dK/dV; warp 8 TMA producer (+ lse/Delta
-// staging); warp 9 TMEM allocator and S^T issuer; warp 10 dV/dK/dP^T issuer.
+// staging); warp 9 TMEM allocator and S^T issuer; warp 10 dV/dK/dP^T issuer;
+// warp 11 idle (it completes the fourth warpgroup, so that the warpgroups can
+// move registers to the compute warps with setmaxnreg).
 #include "common.cuh"
 #include "ptx.cuh"
 #include "sched.cuh"
@@ -41,6 +43,9 @@ struct BwdCfg {
   static constexpr int kSmem = kOffRing + 256;
   static constexpr uint32_t kTmemCols = 512;
   static constexpr uint32_t kColDV = 0, kColDK = D, kColX = 2 * D, kColY = 2 * D + 128;
+  static constexpr uint32_t kComputeRegs = 200;  // per thread, warps 0-7
+  static constexpr uint32_t kOtherRegs = 96;     // per thread, warps 8-11
+  static_assert(256 * kComputeRegs + 128 * kOtherRegs <= 384 * 168, "register split above the launch budget");
 };
 
 struct BwdItem {
@@ -103,7 +108,7 @@ __device__ inline void drain_wait_b(uint64_t* bar, uint32_t parity) {
 }
 
 template <int D, bool kGrouped>
-__global__ void __launch_bounds__(352, 1)
+__global__ void __launch_bounds__(384, 1)
     bwd_kernel(const BwdParams p, const __grid_constant__ CUtensorMap tmQ, const __grid_constant__ CUtensorMap tmDO,
                const __grid_constant__ CUtensorMap tmK, const __grid_constant__ CUtensorMap tmV) {
   using C = BwdCfg<D>;
@@ -181,7 +186,12 @@ __global__ void __launch_bounds__(352, 1)
   // role runs, so nothing ever commits to it.
   if (p.test_stall) {
     mbar_wait(bar_drain, 0, s_abort);
-  } else if (warp == 8) {
+  } else if (warp >= 8) {
+    // The compute warps hold a step's P (64 values) and S^T / dP^T chunks per
+    // thread: they get 200 registers, warps 8-11 (producer, issuers, idle) 96;
+    // 256 x 200 + 128 x 96 fits the 384 x 168 the CTA is launched with.
+    regs_lower<C::kOtherRegs>();
+    if (warp == 8) {
     // ------------------------------------------------------------ producer (whole warp)
     int stage = 0;
     uint32_t ph = 0, kv_iter = 0, n_fill = 0;
@@ -436,7 +446,9 @@ __global__ void __launch_bounds__(352, 1)
       drain_wait_b(bar_drain2, 0);
     }
     __syncwarp();
+  }
   } else {
+    regs_raise<C::kComputeRegs>();
     // ------------------------------------------------------------ compute warps
     const int half = warp >> 2;     // which half of the columns this thread owns
     const int row = tid & 127;      // its key row (TMEM lane) / query row when draining dQ
@@ -638,7 +650,7 @@ static cudaError_t launch_bwd_t(const BwdParams& p, const CUtensorMap& tq, const
   cudaError_t e = cudaFuncSetAttribute(bwd_kernel<D, kGrouped>, cudaFuncAttributeMaxDynamicSharedMemorySize, C::kSmem);
   if (e != cudaSuccess) return e;
   prof_before(THD_KERNEL_BWD, st);
-  bwd_kernel<D, kGrouped><<<grid, 352, C::kSmem, st>>>(p, tq, tdo, tk, tv);
+  bwd_kernel<D, kGrouped><<<grid, 384, C::kSmem, st>>>(p, tq, tdo, tk, tv);
   count_launch();
   e = cudaGetLastError();
   prof_after(THD_KERNEL_BWD, st);
