@@ -312,7 +312,7 @@ __global__ void __launch_bounds__(384, 1)
             ks = 0;
             kph ^= 1u;
           }
-          if (!mbar_wait(&sb.p_ready, g & 1u, &s_abort) || !mbar_wait(&sb.v_full[vs], vph, &s_abort)) {
+          if (!mbar_wait_poll(&sb.p_ready, g & 1u, &s_abort) || !mbar_wait(&sb.v_full[vs], vph, &s_abort)) {
             ok = false;
             return;
           }

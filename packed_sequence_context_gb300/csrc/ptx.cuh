@@ -81,6 +81,24 @@ THD_DEV bool mbar_wait(uint64_t* bar, uint32_t parity, volatile int* abort_flag)
   }
 }
 
+// The same bounded wait re-polling the barrier instead of sleeping in it: for
+// a thread whose wake-up latency is on the critical path and which has no
+// warp-mates to take issue slots from.
+THD_DEV bool mbar_wait_poll(uint64_t* bar, uint32_t parity, volatile int* abort_flag) {
+  if (mbar_try_wait(bar, parity)) return true;
+  const uint64_t t0 = globaltimer();
+  for (uint32_t it = 1;; ++it) {
+    if (mbar_try_wait(bar, parity)) return true;
+    if ((it & 63u) == 0) {
+      if (*abort_flag) return false;
+      if (globaltimer() - t0 > kWaitTimeoutNs) {
+        *abort_flag = 1;
+        return false;
+      }
+    }
+  }
+}
+
 // Bounded wait that ignores the abort flag (used to drain in-flight async
 // work before a CTA exits).
 THD_DEV void drain_wait(uint64_t* bar, uint32_t parity) {
