@@ -192,261 +192,261 @@ __global__ void __launch_bounds__(384, 1)
     // 256 x 200 + 128 x 96 fits the 384 x 168 the CTA is launched with.
     regs_lower<C::kOtherRegs>();
     if (warp == 8) {
-    // ------------------------------------------------------------ producer (whole warp)
-    int stage = 0;
-    uint32_t ph = 0, kv_iter = 0, n_fill = 0;
-    bool ok = true;
-    int w = item_first();
-    for (uint32_t kit = 0; ok; ++kit, w = __shfl_sync(0xffffffffu, w, 0)) {
-      // publish this item (or the end marker) to the other roles, and claim
-      // the next one (lane 0's w) while this one is loaded
-      int wcur = w;
-      if (lane == 0) {
-        ok = item_publish(ring, kit, wcur, s_abort);
-        if (ok && wcur < n_items) w = item_claim(p.claim);
-      }
-      ok = __shfl_sync(0xffffffffu, ok ? 1 : 0, 0) != 0;
-      if (!ok || wcur >= n_items) break;
-      const BwdItem it = bwd_item<kGrouped>(p, n_entries, wcur);
-      if (it.kv_first > it.kv_last) continue;  // no valid key: nothing to load
-      const int kv_row = it.g.kv_off + it.c * it.g.cbkv + it.jk * kTile;
-      if (!mbar_wait(bar_kv_empty, (kv_iter & 1u) ^ 1u, s_abort)) break;
-      if (lane == 0) {
-        mbar_arrive_expect_tx(bar_kv_full, 2 * C::kTileBytes);
+      // ------------------------------------------------------------ producer (whole warp)
+      int stage = 0;
+      uint32_t ph = 0, kv_iter = 0, n_fill = 0;
+      bool ok = true;
+      int w = item_first();
+      for (uint32_t kit = 0; ok; ++kit, w = __shfl_sync(0xffffffffu, w, 0)) {
+        // publish this item (or the end marker) to the other roles, and claim
+        // the next one (lane 0's w) while this one is loaded
+        int wcur = w;
+        if (lane == 0) {
+          ok = item_publish(ring, kit, wcur, s_abort);
+          if (ok && wcur < n_items) w = item_claim(p.claim);
+        }
+        ok = __shfl_sync(0xffffffffu, ok ? 1 : 0, 0) != 0;
+        if (!ok || wcur >= n_items) break;
+        const BwdItem it = bwd_item<kGrouped>(p, n_entries, wcur);
+        if (it.kv_first > it.kv_last) continue;  // no valid key: nothing to load
+        const int kv_row = it.g.kv_off + it.c * it.g.cbkv + it.jk * kTile;
+        if (!mbar_wait(bar_kv_empty, (kv_iter & 1u) ^ 1u, s_abort)) break;
+        if (lane == 0) {
+          mbar_arrive_expect_tx(bar_kv_full, 2 * C::kTileBytes);
 #pragma unroll
-        for (int hb = 0; hb < D / 64; ++hb) {
-          tma_load_3d(smem_u32(sK + hb * 16384), &tmK, bar_kv_full, hb * 64, it.hk, kv_row);
-          tma_load_3d(smem_u32(sV + hb * 16384), &tmV, bar_kv_full, hb * 64, it.hk, kv_row);
+          for (int hb = 0; hb < D / 64; ++hb) {
+            tma_load_3d(smem_u32(sK + hb * 16384), &tmK, bar_kv_full, hb * 64, it.hk, kv_row);
+            tma_load_3d(smem_u32(sV + hb * 16384), &tmV, bar_kv_full, hb * 64, it.hk, kv_row);
+          }
+        }
+        ++kv_iter;
+        for_each_q_step(it, p, [&](int qc, int jq, int h) {
+          if (!ok) return;
+          if (!mbar_wait(&bar_qdo_empty[stage], ph ^ 1u, s_abort)) {
+            ok = false;
+            return;
+          }
+          const int q0 = qc * it.g.cbq + jq * kTile;
+          const int nqv = imin(imin(kTile, it.g.cbq - jq * kTile), it.g.Lq - q0);
+          const int q_row = it.g.q_off + q0;
+          const uint32_t lse_st = smem_u32(sLse + stage * 256);
+          // lse and Delta of the valid query rows, copied asynchronously; the
+          // entries past nqv are zeroed so that masked columns stay finite
+          // (S = -inf gives P = 0 and dS = 0 only against finite lse and Delta)
+#pragma unroll
+          for (int k = 0; k < 4; ++k) {
+            const int n = lane + 32 * k;
+            if (n < nqv) {
+              const int64_t idx = (int64_t)h * p.T_q + q_row + n;
+              cp_async_4(lse_st + 4 * n, p.lse2 + idx);
+              cp_async_4(lse_st + 512 + 4 * n, p.delta + idx);
+            } else {
+              sLse[stage * 256 + n] = 0.f;
+              sLse[stage * 256 + 128 + n] = 0.f;
+            }
+          }
+          cp_async_arrive_noinc(&bar_qdo_full[stage]);
+          __syncwarp();  // the zeroed entries are ordered before lane 0's arrival
+          uint8_t* sQ = smem + C::kOffQ + stage * 2 * C::kTileBytes;
+          uint8_t* sDO = sQ + C::kTileBytes;
+          if (lane == 0) {
+            mbar_arrive_expect_tx(&bar_qdo_full[stage], C::kTileBytes);
+#pragma unroll
+            for (int hb = 0; hb < D / 64; ++hb)
+              tma_load_3d(smem_u32(sQ + hb * 16384), &tmQ, &bar_qdo_full[stage], hb * 64, h, q_row);
+          }
+          // dO has its own release: its last reader (dV) completes after Q's (dK)
+          if (!mbar_wait(&bar_do_empty[stage], ph ^ 1u, s_abort)) {
+            ok = false;
+            return;
+          }
+          if (lane == 0) {
+            mbar_arrive_expect_tx(&bar_do_full[stage], C::kTileBytes);
+#pragma unroll
+            for (int hb = 0; hb < D / 64; ++hb)
+              tma_load_3d(smem_u32(sDO + hb * 16384), &tmDO, &bar_do_full[stage], hb * 64, h, q_row);
+          }
+          ++n_fill;
+          if (++stage == S) {
+            stage = 0;
+            ph ^= 1u;
+          }
+        });
+      }
+      // every issued copy must land before the CTA may exit
+      if (kv_iter > 0) drain_wait_b(bar_kv_full, (kv_iter - 1) & 1u);
+      for (int s = 0; s < S; ++s) {
+        const uint32_t fills = n_fill > (uint32_t)s ? (n_fill - 1 - s) / S + 1 : 0;
+        if (fills > 0) {
+          drain_wait_b(&bar_qdo_full[s], (fills - 1) & 1u);
+          drain_wait_b(&bar_do_full[s], (fills - 1) & 1u);
         }
       }
-      ++kv_iter;
-      for_each_q_step(it, p, [&](int qc, int jq, int h) {
-        if (!ok) return;
-        if (!mbar_wait(&bar_qdo_empty[stage], ph ^ 1u, s_abort)) {
-          ok = false;
-          return;
-        }
-        const int q0 = qc * it.g.cbq + jq * kTile;
-        const int nqv = imin(imin(kTile, it.g.cbq - jq * kTile), it.g.Lq - q0);
-        const int q_row = it.g.q_off + q0;
-        const uint32_t lse_st = smem_u32(sLse + stage * 256);
-        // lse and Delta of the valid query rows, copied asynchronously; the
-        // entries past nqv are zeroed so that masked columns stay finite
-        // (S = -inf gives P = 0 and dS = 0 only against finite lse and Delta)
+      __syncwarp();
+    } else if (warp == 9) {
+      // ------------------------------------------------------------ S^T issuer
+      // The two 128-column TMEM buffers T0, T1 swap roles every step: step s
+      // puts S^T(s) (then P^T(s)) in T[s % 2] and dP^T(s) in T[(s + 1) % 2].
+      // Two issuing threads, as in the forward (a barrier wait in one does not
+      // idle the tensor pipe while the other has products to issue):
+      //   warp 9:  S^T(s), as soon as the compute warps hold dP^T(s-1), which sat
+      //            in the same buffer, in registers (y_free)
+      //   warp 10: once the compute warps have written P^T(s-1) and dS(s-1),
+      //            dV(s-1) and dK(s-1); then dP^T(s) into the buffer P^T(s-1)
+      //            leaves once dV(s-1) has read it.
+      // The compute warps of step s compute P from S^T(s) while dV/dK(s-1) run
+      // and dS once dP^T(s) is there.  P^T(s) and dS^T(s) both go back over
+      // S^T(s) as packed bf16 (each thread into the S^T columns it has read) and
+      // are the TMEM A operands of dV(s) and dK(s): dS never touches shared
+      // memory, which the SS products already keep busy.
+      if (lane == 0) {
+        const uint32_t kb = smem_u32(sK);
+        int stage = 0;
+        uint32_t ph = 0, su = 0, kv_iter = 0;
+        bool ok = true;
+        for (uint32_t kit = 0; ok; ++kit) {
+          int w;
+          if (!item_take_one(ring, kit, w, s_abort) || w >= n_items) break;
+          const BwdItem it = bwd_item<kGrouped>(p, n_entries, w);
+          if (it.kv_first > it.kv_last) continue;
+          if (!mbar_wait(bar_kv_full, kv_iter & 1u, s_abort)) break;
+          ++kv_iter;
+          // this thread has seen the tile's phase: the tile may be refilled once
+          // warp 10 also releases it, and never before this wait (which would
+          // leave this wait two phases behind when the item has no step)
+          mbar_arrive(bar_kv_empty);
+          for_each_q_step(it, p, [&](int qc, int jq, int) {
+            if (!ok) return;
+            const int nqv = imin(imin(kTile, it.g.cbq - jq * kTile), it.g.Lq - (qc * it.g.cbq + jq * kTile));
+            const uint32_t idesc_t = idesc_bf16(128, 16 * ceil_div(nqv, 16), false, false);
+            const uint32_t acol = tmem + C::kColX + 128u * (su & 1u);  // S^T(s), then P^T(s)
+            if (!mbar_wait(&bar_qdo_full[stage], ph, s_abort) ||
+                (su > 0 && !mbar_wait(bar_y_free, (su - 1) & 1u, s_abort))) {
+              ok = false;
+              return;
+            }
+            tc_fence_after();
+            const uint32_t qb = smem_u32(smem + C::kOffQ + stage * 2 * C::kTileBytes);
 #pragma unroll
-        for (int k = 0; k < 4; ++k) {
-          const int n = lane + 32 * k;
-          if (n < nqv) {
-            const int64_t idx = (int64_t)h * p.T_q + q_row + n;
-            cp_async_4(lse_st + 4 * n, p.lse2 + idx);
-            cp_async_4(lse_st + 512 + 4 * n, p.delta + idx);
+            for (int ks = 0; ks < D / 16; ++ks) {
+              const uint32_t off = (ks >> 2) * 16384 + (ks & 3) * 32;
+              mma_ss(acol, sdesc_sw128(kb + off, 16, 1024), sdesc_sw128(qb + off, 16, 1024), idesc_t, ks > 0);
+            }
+            tc_commit(bar_st_full);
+            ++su;
+            if (++stage == S) {
+              stage = 0;
+              ph ^= 1u;
+            }
+          });
+        }
+        tc_commit(bar_drain);
+        drain_wait_b(bar_drain, 0);
+      }
+      __syncwarp();
+    } else if (warp == 10) {
+      // ------------------------------------------------------------ dV, dK and dP^T issuer
+      if (lane == 0) {
+        constexpr uint32_t idesc_kv = idesc_bf16(128, D, false, true);  // dV, dK (B MN-major)
+        const uint32_t vb = smem_u32(sV);
+        int stage = 0;
+        uint32_t ph = 0, su = 0, kv_iter = 0;
+        bool ok = true;
+        // the step whose dV / dK are still to be issued
+        int pv_stage = -1, pv_n16 = 0;
+        bool pv_first = false;
+        auto tail = [&](bool last) -> bool {
+          const uint32_t ps = su - 1;  // the pending step
+          if (!mbar_wait(bar_p_ready, ps & 1u, s_abort)) return false;
+          // The compute warps wrote P^T and dS^T of the item's last step only
+          // after its S^T and dP^T -- the last products that read K and V --
+          // had completed: the K/V tile may be refilled with the next item's
+          // while the last dV and dK run and the epilogue drains them.
+          if (last) mbar_arrive(bar_kv_empty);
+          tc_fence_after();
+          const uint32_t qb = smem_u32(smem + C::kOffQ + pv_stage * 2 * C::kTileBytes);
+          const uint32_t dob = qb + C::kTileBytes;
+          const uint32_t pcol = tmem + C::kColX + 128u * (ps & 1u);  // P^T of the pending step
+          // dK first: its completion frees the stage's Q, which the S^T two
+          // steps on waits for, one product earlier than dO.
+          // dK += dS^T Q  (dS^T packed bf16 beside P^T: K-step ks at column
+          // 64 (ks/4) + 32 + 8 (ks%4); K = the valid query rows)
+          for (int ks = 0; ks < pv_n16; ++ks)
+            mma_ts(tmem + C::kColDK, pcol + 64 * (ks >> 2) + 32 + 8 * (ks & 3), sdesc_sw128(qb + ks * 2048, 16384, 1024),
+                   idesc_kv, (pv_first && ks == 0) ? 0u : 1u);
+          tc_commit(&bar_qdo_empty[pv_stage]);
+          // dV += P^T dO  (P^T packed bf16: query columns 16 ks.. of K-step ks sit
+          // at column 64 (ks/4) + 8 (ks%4))
+          for (int ks = 0; ks < pv_n16; ++ks)
+            mma_ts(tmem + C::kColDV, pcol + 64 * (ks >> 2) + 8 * (ks & 3), sdesc_sw128(dob + ks * 2048, 16384, 1024),
+                   idesc_kv, (pv_first && ks == 0) ? 0u : 1u);
+          tc_commit(&bar_do_empty[pv_stage]);
+          tc_commit(bar_dk_done);  // both of the step's products (this thread's MMAs complete in order)
+          pv_stage = -1;
+          return true;
+        };
+        for (uint32_t kit = 0; ok; ++kit) {
+          int w;
+          if (!item_take_one(ring, kit, w, s_abort) || w >= n_items) break;
+          const BwdItem it = bwd_item<kGrouped>(p, n_entries, w);
+          if (it.kv_first > it.kv_last) continue;
+          if (!mbar_wait(bar_kv_full, kv_iter & 1u, s_abort)) break;
+          ++kv_iter;
+          tc_fence_after();
+          bool first = true;
+          for_each_q_step(it, p, [&](int qc, int jq, int) {
+            if (!ok) return;
+            const int nqv = imin(imin(kTile, it.g.cbq - jq * kTile), it.g.Lq - (qc * it.g.cbq + jq * kTile));
+            const int n16 = ceil_div(nqv, 16);
+            const uint32_t idesc_t = idesc_bf16(128, 16 * n16, false, false);
+            const uint32_t bcol = tmem + C::kColX + 128u * ((su + 1) & 1u);  // dP^T(s)
+            if (!mbar_wait(&bar_qdo_full[stage], ph, s_abort)) {
+              ok = false;
+              return;
+            }
+            // dV, dK of the previous step (of this item; an item's last step is
+            // finished at the item's end)
+            if (pv_stage >= 0 && !tail(false)) {
+              ok = false;
+              return;
+            }
+            // dP^T = V dO^T -> the buffer P^T(s-1) and dS^T(s-1) leave once dV(s-1)
+            // and dK(s-1) have read them
+            if ((su > 0 && !mbar_wait(bar_dk_done, (su - 1) & 1u, s_abort)) ||
+                !mbar_wait(&bar_do_full[stage], ph, s_abort)) {
+              ok = false;
+              return;
+            }
+            tc_fence_after();
+            const uint32_t dob = smem_u32(smem + C::kOffQ + stage * 2 * C::kTileBytes) + C::kTileBytes;
+#pragma unroll
+            for (int ks = 0; ks < D / 16; ++ks) {
+              const uint32_t off = (ks >> 2) * 16384 + (ks & 3) * 32;
+              mma_ss(bcol, sdesc_sw128(vb + off, 16, 1024), sdesc_sw128(dob + off, 16, 1024), idesc_t, ks > 0);
+            }
+            tc_commit(bar_dp_full);
+            pv_stage = stage;
+            pv_n16 = n16;
+            pv_first = first;
+            first = false;
+            ++su;
+            if (++stage == S) {
+              stage = 0;
+              ph ^= 1u;
+            }
+          });
+          if (!ok) break;
+          if (pv_stage >= 0) {
+            if (!tail(true)) break;  // the item's last step; dk_done then covers all its products
           } else {
-            sLse[stage * 256 + n] = 0.f;
-            sLse[stage * 256 + 128 + n] = 0.f;
+            mbar_arrive(bar_kv_empty);  // no step read the tile
           }
         }
-        cp_async_arrive_noinc(&bar_qdo_full[stage]);
-        __syncwarp();  // the zeroed entries are ordered before lane 0's arrival
-        uint8_t* sQ = smem + C::kOffQ + stage * 2 * C::kTileBytes;
-        uint8_t* sDO = sQ + C::kTileBytes;
-        if (lane == 0) {
-          mbar_arrive_expect_tx(&bar_qdo_full[stage], C::kTileBytes);
-#pragma unroll
-          for (int hb = 0; hb < D / 64; ++hb)
-            tma_load_3d(smem_u32(sQ + hb * 16384), &tmQ, &bar_qdo_full[stage], hb * 64, h, q_row);
-        }
-        // dO has its own release: its last reader (dV) completes after Q's (dK)
-        if (!mbar_wait(&bar_do_empty[stage], ph ^ 1u, s_abort)) {
-          ok = false;
-          return;
-        }
-        if (lane == 0) {
-          mbar_arrive_expect_tx(&bar_do_full[stage], C::kTileBytes);
-#pragma unroll
-          for (int hb = 0; hb < D / 64; ++hb)
-            tma_load_3d(smem_u32(sDO + hb * 16384), &tmDO, &bar_do_full[stage], hb * 64, h, q_row);
-        }
-        ++n_fill;
-        if (++stage == S) {
-          stage = 0;
-          ph ^= 1u;
-        }
-      });
-    }
-    // every issued copy must land before the CTA may exit
-    if (kv_iter > 0) drain_wait_b(bar_kv_full, (kv_iter - 1) & 1u);
-    for (int s = 0; s < S; ++s) {
-      const uint32_t fills = n_fill > (uint32_t)s ? (n_fill - 1 - s) / S + 1 : 0;
-      if (fills > 0) {
-        drain_wait_b(&bar_qdo_full[s], (fills - 1) & 1u);
-        drain_wait_b(&bar_do_full[s], (fills - 1) & 1u);
+        tc_commit(bar_drain2);
+        drain_wait_b(bar_drain2, 0);
       }
+      __syncwarp();
     }
-    __syncwarp();
-  } else if (warp == 9) {
-    // ------------------------------------------------------------ S^T issuer
-    // The two 128-column TMEM buffers T0, T1 swap roles every step: step s
-    // puts S^T(s) (then P^T(s)) in T[s % 2] and dP^T(s) in T[(s + 1) % 2].
-    // Two issuing threads, as in the forward (a barrier wait in one does not
-    // idle the tensor pipe while the other has products to issue):
-    //   warp 9:  S^T(s), as soon as the compute warps hold dP^T(s-1), which sat
-    //            in the same buffer, in registers (y_free)
-    //   warp 10: once the compute warps have written P^T(s-1) and dS(s-1),
-    //            dV(s-1) and dK(s-1); then dP^T(s) into the buffer P^T(s-1)
-    //            leaves once dV(s-1) has read it.
-    // The compute warps of step s compute P from S^T(s) while dV/dK(s-1) run
-    // and dS once dP^T(s) is there.  P^T(s) and dS^T(s) both go back over
-    // S^T(s) as packed bf16 (each thread into the S^T columns it has read) and
-    // are the TMEM A operands of dV(s) and dK(s): dS never touches shared
-    // memory, which the SS products already keep busy.
-    if (lane == 0) {
-      const uint32_t kb = smem_u32(sK);
-      int stage = 0;
-      uint32_t ph = 0, su = 0, kv_iter = 0;
-      bool ok = true;
-      for (uint32_t kit = 0; ok; ++kit) {
-        int w;
-        if (!item_take_one(ring, kit, w, s_abort) || w >= n_items) break;
-        const BwdItem it = bwd_item<kGrouped>(p, n_entries, w);
-        if (it.kv_first > it.kv_last) continue;
-        if (!mbar_wait(bar_kv_full, kv_iter & 1u, s_abort)) break;
-        ++kv_iter;
-        // this thread has seen the tile's phase: the tile may be refilled once
-        // warp 10 also releases it, and never before this wait (which would
-        // leave this wait two phases behind when the item has no step)
-        mbar_arrive(bar_kv_empty);
-        for_each_q_step(it, p, [&](int qc, int jq, int) {
-          if (!ok) return;
-          const int nqv = imin(imin(kTile, it.g.cbq - jq * kTile), it.g.Lq - (qc * it.g.cbq + jq * kTile));
-          const uint32_t idesc_t = idesc_bf16(128, 16 * ceil_div(nqv, 16), false, false);
-          const uint32_t acol = tmem + C::kColX + 128u * (su & 1u);  // S^T(s), then P^T(s)
-          if (!mbar_wait(&bar_qdo_full[stage], ph, s_abort) ||
-              (su > 0 && !mbar_wait(bar_y_free, (su - 1) & 1u, s_abort))) {
-            ok = false;
-            return;
-          }
-          tc_fence_after();
-          const uint32_t qb = smem_u32(smem + C::kOffQ + stage * 2 * C::kTileBytes);
-#pragma unroll
-          for (int ks = 0; ks < D / 16; ++ks) {
-            const uint32_t off = (ks >> 2) * 16384 + (ks & 3) * 32;
-            mma_ss(acol, sdesc_sw128(kb + off, 16, 1024), sdesc_sw128(qb + off, 16, 1024), idesc_t, ks > 0);
-          }
-          tc_commit(bar_st_full);
-          ++su;
-          if (++stage == S) {
-            stage = 0;
-            ph ^= 1u;
-          }
-        });
-      }
-      tc_commit(bar_drain);
-      drain_wait_b(bar_drain, 0);
-    }
-    __syncwarp();
-  } else if (warp == 10) {
-    // ------------------------------------------------------------ dV, dK and dP^T issuer
-    if (lane == 0) {
-      constexpr uint32_t idesc_kv = idesc_bf16(128, D, false, true);  // dV, dK (B MN-major)
-      const uint32_t vb = smem_u32(sV);
-      int stage = 0;
-      uint32_t ph = 0, su = 0, kv_iter = 0;
-      bool ok = true;
-      // the step whose dV / dK are still to be issued
-      int pv_stage = -1, pv_n16 = 0;
-      bool pv_first = false;
-      auto tail = [&](bool last) -> bool {
-        const uint32_t ps = su - 1;  // the pending step
-        if (!mbar_wait(bar_p_ready, ps & 1u, s_abort)) return false;
-        // The compute warps wrote P^T and dS^T of the item's last step only
-        // after its S^T and dP^T -- the last products that read K and V --
-        // had completed: the K/V tile may be refilled with the next item's
-        // while the last dV and dK run and the epilogue drains them.
-        if (last) mbar_arrive(bar_kv_empty);
-        tc_fence_after();
-        const uint32_t qb = smem_u32(smem + C::kOffQ + pv_stage * 2 * C::kTileBytes);
-        const uint32_t dob = qb + C::kTileBytes;
-        const uint32_t pcol = tmem + C::kColX + 128u * (ps & 1u);  // P^T of the pending step
-        // dK first: its completion frees the stage's Q, which the S^T two
-        // steps on waits for, one product earlier than dO.
-        // dK += dS^T Q  (dS^T packed bf16 beside P^T: K-step ks at column
-        // 64 (ks/4) + 32 + 8 (ks%4); K = the valid query rows)
-        for (int ks = 0; ks < pv_n16; ++ks)
-          mma_ts(tmem + C::kColDK, pcol + 64 * (ks >> 2) + 32 + 8 * (ks & 3), sdesc_sw128(qb + ks * 2048, 16384, 1024),
-                 idesc_kv, (pv_first && ks == 0) ? 0u : 1u);
-        tc_commit(&bar_qdo_empty[pv_stage]);
-        // dV += P^T dO  (P^T packed bf16: query columns 16 ks.. of K-step ks sit
-        // at column 64 (ks/4) + 8 (ks%4))
-        for (int ks = 0; ks < pv_n16; ++ks)
-          mma_ts(tmem + C::kColDV, pcol + 64 * (ks >> 2) + 8 * (ks & 3), sdesc_sw128(dob + ks * 2048, 16384, 1024),
-                 idesc_kv, (pv_first && ks == 0) ? 0u : 1u);
-        tc_commit(&bar_do_empty[pv_stage]);
-        tc_commit(bar_dk_done);  // both of the step's products (this thread's MMAs complete in order)
-        pv_stage = -1;
-        return true;
-      };
-      for (uint32_t kit = 0; ok; ++kit) {
-        int w;
-        if (!item_take_one(ring, kit, w, s_abort) || w >= n_items) break;
-        const BwdItem it = bwd_item<kGrouped>(p, n_entries, w);
-        if (it.kv_first > it.kv_last) continue;
-        if (!mbar_wait(bar_kv_full, kv_iter & 1u, s_abort)) break;
-        ++kv_iter;
-        tc_fence_after();
-        bool first = true;
-        for_each_q_step(it, p, [&](int qc, int jq, int) {
-          if (!ok) return;
-          const int nqv = imin(imin(kTile, it.g.cbq - jq * kTile), it.g.Lq - (qc * it.g.cbq + jq * kTile));
-          const int n16 = ceil_div(nqv, 16);
-          const uint32_t idesc_t = idesc_bf16(128, 16 * n16, false, false);
-          const uint32_t bcol = tmem + C::kColX + 128u * ((su + 1) & 1u);  // dP^T(s)
-          if (!mbar_wait(&bar_qdo_full[stage], ph, s_abort)) {
-            ok = false;
-            return;
-          }
-          // dV, dK of the previous step (of this item; an item's last step is
-          // finished at the item's end)
-          if (pv_stage >= 0 && !tail(false)) {
-            ok = false;
-            return;
-          }
-          // dP^T = V dO^T -> the buffer P^T(s-1) and dS^T(s-1) leave once dV(s-1)
-          // and dK(s-1) have read them
-          if ((su > 0 && !mbar_wait(bar_dk_done, (su - 1) & 1u, s_abort)) ||
-              !mbar_wait(&bar_do_full[stage], ph, s_abort)) {
-            ok = false;
-            return;
-          }
-          tc_fence_after();
-          const uint32_t dob = smem_u32(smem + C::kOffQ + stage * 2 * C::kTileBytes) + C::kTileBytes;
-#pragma unroll
-          for (int ks = 0; ks < D / 16; ++ks) {
-            const uint32_t off = (ks >> 2) * 16384 + (ks & 3) * 32;
-            mma_ss(bcol, sdesc_sw128(vb + off, 16, 1024), sdesc_sw128(dob + off, 16, 1024), idesc_t, ks > 0);
-          }
-          tc_commit(bar_dp_full);
-          pv_stage = stage;
-          pv_n16 = n16;
-          pv_first = first;
-          first = false;
-          ++su;
-          if (++stage == S) {
-            stage = 0;
-            ph ^= 1u;
-          }
-        });
-        if (!ok) break;
-        if (pv_stage >= 0) {
-          if (!tail(true)) break;  // the item's last step; dk_done then covers all its products
-        } else {
-          mbar_arrive(bar_kv_empty);  // no step read the tile
-        }
-      }
-      tc_commit(bar_drain2);
-      drain_wait_b(bar_drain2, 0);
-    }
-    __syncwarp();
-  }
   } else {
     regs_raise<C::kComputeRegs>();
     // ------------------------------------------------------------ compute warps

@@ -77,7 +77,6 @@ struct FwdStreamBars {
   uint64_t drain;                  // the issuer's MMAs all completed
 };
 
-
 // Work items are handed out dynamically: every stream starts with item
 // blockIdx.x + x gridDim.x, then its producer claims the next free item from
 // the per-launch counter (items 2 gridDim.x and up) and publishes it to the
@@ -152,191 +151,191 @@ __global__ void __launch_bounds__(384, 1)
     // CTA is launched with.
     regs_lower<C::kOtherRegs>();
     if (warp < 10) {
-    // ------------------------------------------------------------ producer of stream x (whole warp)
-    const int x = warp - 8;
-    FwdStreamBars& sb = bars[x];
-    uint8_t* sQ = smem + x * C::kStreamBytes;
-    uint8_t* sK = sQ + C::kQBytes;
-    uint8_t* sV = sK + KS * C::kKVBytes;
-    int ks = 0, vs = 0;
-    uint32_t kph = 0, vph = 0, nk = 0, nv = 0, q_iter = 0;
-    bool ok = true;
-    int w = fwd_dual_first_item(x);
-    for (uint32_t kit = 0; ok; ++kit) {
-      // publish this item (or the end marker) to the stream's other roles,
-      // and claim the next one while this one is loaded
-      int wnext = 0;
-      if (lane == 0) {
-        ok = item_publish(&ring[x], kit, w, &s_abort);
-        if (ok && w < n_items) wnext = 2 * (int)gridDim.x + atomicAdd(p.claim, 1);
-      }
-      ok = __shfl_sync(0xffffffffu, ok ? 1 : 0, 0) != 0;
-      if (!ok) break;
-      if (w >= n_items) break;
-      const QItem it = q_item<true>(p, n_entries, w);
-      // ---- the query tile: rank-local rows [128 t, 128 t + 128) of rank r,
-      // gathered once the previous item's last QK^T has completed; rows
-      // without a valid query are zero.  The copies are waited for after the
-      // item's first K load has been issued, so the two latencies overlap.
-      if (!mbar_wait(&sb.q_empty, (q_iter & 1u) ^ 1u, &s_abort)) break;
-      const uint32_t qdst = smem_u32(sQ);
-#pragma unroll
-      for (int rr = 0; rr < 4; ++rr) {
-        const int row = lane + 32 * rr;
-        const int prow = it.t * kTile + row;
-        const bool in_rank = prow < 2 * it.g.cbq;
-        const int pos = in_rank ? local_to_pos(prow, it.r, it.g.cbq, p.cp) : 0;
-        const bool valid = in_rank && pos < it.g.Lq;
-        const uint16_t* src = valid ? p.q + (((int64_t)it.g.q_off + pos) * p.Hq + it.h) * D : p.q;
-#pragma unroll
-        for (int c = 0; c < D / 8; ++c)
-          cp_async_16(qdst + sw128_offset(row, 8 * c, kTile), src + (valid ? 8 * c : 0), valid ? 16u : 0u);
-      }
-      bool q_pending = true;
-      // the copies must have landed and be visible to the tensor core's
-      // (async) proxy before the MMA thread may read them
-      auto finish_q = [&]() {
-        cp_async_wait_all();
-        fence_proxy_async_smem();
-        mbar_arrive(&sb.q_full);
-        q_pending = false;
-      };
-      // ---- the key and value tiles of the item, in ring order
-      for_each_kv_tile(it, p, [&](int c, int j) {
-        if (!ok) return;
-        const int row = it.g.kv_off + c * it.g.cbkv + j * kTile;
-        if (!mbar_wait(&sb.k_empty[ks], kph ^ 1u, &s_abort)) {
-          ok = false;
-          return;
-        }
-        if (lane == 0) {
-          mbar_arrive_expect_tx(&sb.k_full[ks], C::kKVBytes);
-#pragma unroll
-          for (int hb = 0; hb < D / 64; ++hb)
-            tma_load_3d(smem_u32(sK + ks * C::kKVBytes + hb * 16384), &tmK, &sb.k_full[ks], hb * 64, it.kvh, row);
-        }
-        ++nk;
-        if (++ks == KS) {
-          ks = 0;
-          kph ^= 1u;
-        }
-        if (q_pending) finish_q();
-        if (!mbar_wait(&sb.v_empty[vs], vph ^ 1u, &s_abort)) {
-          ok = false;
-          return;
-        }
-        if (lane == 0) {
-          mbar_arrive_expect_tx(&sb.v_full[vs], C::kKVBytes);
-#pragma unroll
-          for (int hb = 0; hb < D / 64; ++hb)
-            tma_load_3d(smem_u32(sV + vs * C::kKVBytes + hb * 16384), &tmV, &sb.v_full[vs], hb * 64, it.kvh, row);
-        }
-        ++nv;
-        if (++vs == VS) {
-          vs = 0;
-          vph ^= 1u;
-        }
-      });
-      if (!ok) break;
-      if (q_pending) finish_q();  // an item without key tiles
-      ++q_iter;
-      w = __shfl_sync(0xffffffffu, wnext, 0);
-    }
-    // every issued copy must land before the CTA may exit
-    cp_async_wait_all();
-    if (lane == 0) {
-      for (int s = 0; s < KS; ++s) {
-        const uint32_t fills = nk > (uint32_t)s ? (nk - 1 - s) / KS + 1 : 0;
-        if (fills > 0) drain_wait(&sb.k_full[s], (fills - 1) & 1u);
-      }
-      for (int s = 0; s < VS; ++s) {
-        const uint32_t fills = nv > (uint32_t)s ? (nv - 1 - s) / VS + 1 : 0;
-        if (fills > 0) drain_wait(&sb.v_full[s], (fills - 1) & 1u);
-      }
-    }
-    __syncwarp();
-    } else {
-    // ------------------------------------------------------------ MMA issuer of stream x
-    // Per key tile: S = QK^T once the tile's K has landed, then O += PV once
-    // the softmax has written P and the tile's V has landed.  While this
-    // thread waits, the other stream's issuer keeps the pipe fed.
-    const int x = warp - 10;
-    FwdStreamBars& sb = bars[x];
-    uint8_t* sQ = smem + x * C::kStreamBytes;
-    uint8_t* sK = sQ + C::kQBytes;
-    uint8_t* sV = sK + KS * C::kKVBytes;
-    if (lane == 0) {
-      const uint64_t qdesc = sdesc_sw128(smem_u32(sQ), 16, 1024);
-      const uint64_t kdesc = sdesc_sw128(smem_u32(sK), 16, 1024);
-      const uint64_t vdesc = sdesc_sw128(smem_u32(sV), 16384, 1024);
-      const uint32_t s_col = tmem + 128u * (uint32_t)x;
-      const uint32_t o_col = tmem + C::kColO + 128u * (uint32_t)x;
-      constexpr uint32_t idesc_pv = idesc_bf16(128, D, false, true);
+      // ------------------------------------------------------------ producer of stream x (whole warp)
+      const int x = warp - 8;
+      FwdStreamBars& sb = bars[x];
+      uint8_t* sQ = smem + x * C::kStreamBytes;
+      uint8_t* sK = sQ + C::kQBytes;
+      uint8_t* sV = sK + KS * C::kKVBytes;
       int ks = 0, vs = 0;
-      uint32_t kph = 0, vph = 0, g = 0, q_iter = 0;
+      uint32_t kph = 0, vph = 0, nk = 0, nv = 0, q_iter = 0;
       bool ok = true;
+      int w = fwd_dual_first_item(x);
       for (uint32_t kit = 0; ok; ++kit) {
-        int w = 0;
-        if (!item_take_one(&ring[x], kit, w, &s_abort)) break;
+        // publish this item (or the end marker) to the stream's other roles,
+        // and claim the next one while this one is loaded
+        int wnext = 0;
+        if (lane == 0) {
+          ok = item_publish(&ring[x], kit, w, &s_abort);
+          if (ok && w < n_items) wnext = 2 * (int)gridDim.x + atomicAdd(p.claim, 1);
+        }
+        ok = __shfl_sync(0xffffffffu, ok ? 1 : 0, 0) != 0;
+        if (!ok) break;
         if (w >= n_items) break;
         const QItem it = q_item<true>(p, n_entries, w);
-        int n = 0;
-        for_each_kv_tile(it, p, [&](int, int) { ++n; });
-        if (!mbar_wait(&sb.q_full, q_iter & 1u, &s_abort)) break;
-        ++q_iter;
-        tc_fence_after();
-        if (n == 0) tc_commit(&sb.q_empty);
-        int j = 0;
-        for_each_kv_tile(it, p, [&](int c, int jt) {
+        // ---- the query tile: rank-local rows [128 t, 128 t + 128) of rank r,
+        // gathered once the previous item's last QK^T has completed; rows
+        // without a valid query are zero.  The copies are waited for after the
+        // item's first K load has been issued, so the two latencies overlap.
+        if (!mbar_wait(&sb.q_empty, (q_iter & 1u) ^ 1u, &s_abort)) break;
+        const uint32_t qdst = smem_u32(sQ);
+#pragma unroll
+        for (int rr = 0; rr < 4; ++rr) {
+          const int row = lane + 32 * rr;
+          const int prow = it.t * kTile + row;
+          const bool in_rank = prow < 2 * it.g.cbq;
+          const int pos = in_rank ? local_to_pos(prow, it.r, it.g.cbq, p.cp) : 0;
+          const bool valid = in_rank && pos < it.g.Lq;
+          const uint16_t* src = valid ? p.q + (((int64_t)it.g.q_off + pos) * p.Hq + it.h) * D : p.q;
+#pragma unroll
+          for (int c = 0; c < D / 8; ++c)
+            cp_async_16(qdst + sw128_offset(row, 8 * c, kTile), src + (valid ? 8 * c : 0), valid ? 16u : 0u);
+        }
+        bool q_pending = true;
+        // the copies must have landed and be visible to the tensor core's
+        // (async) proxy before the MMA thread may read them
+        auto finish_q = [&]() {
+          cp_async_wait_all();
+          fence_proxy_async_smem();
+          mbar_arrive(&sb.q_full);
+          q_pending = false;
+        };
+        // ---- the key and value tiles of the item, in ring order
+        for_each_kv_tile(it, p, [&](int c, int j) {
           if (!ok) return;
-          const int ncols = q_tile_ncols(it, p, c, jt);
-          // S of this tile overwrites the P the previous PV reads: both are
-          // issued by this thread, and the tensor pipe executes one thread's
-          // MMAs in issue order, so no wait for that PV is needed here
-          if (!mbar_wait(&sb.k_full[ks], kph, &s_abort)) {
+          const int row = it.g.kv_off + c * it.g.cbkv + j * kTile;
+          if (!mbar_wait(&sb.k_empty[ks], kph ^ 1u, &s_abort)) {
             ok = false;
             return;
           }
-          tc_fence_after();
-          const uint32_t idesc_qk = idesc_bf16(128, ncols, false, false);
-          const uint64_t kd = kdesc + (uint64_t)((ks * C::kKVBytes) >> 4);
+          if (lane == 0) {
+            mbar_arrive_expect_tx(&sb.k_full[ks], C::kKVBytes);
 #pragma unroll
-          for (int kk = 0; kk < D / 16; ++kk) {
-            const uint64_t off = (uint64_t)(((kk >> 2) * 16384 + (kk & 3) * 32) >> 4);
-            mma_ss(s_col, qdesc + off, kd + off, idesc_qk, kk > 0 ? 1u : 0u);
+            for (int hb = 0; hb < D / 64; ++hb)
+              tma_load_3d(smem_u32(sK + ks * C::kKVBytes + hb * 16384), &tmK, &sb.k_full[ks], hb * 64, it.kvh, row);
           }
-          tc_commit(&sb.s_full);
-          tc_commit(&sb.k_empty[ks]);                // the K slot frees once this QK^T completes
-          if (j + 1 == n) tc_commit(&sb.q_empty);    // and the query tile after the item's last QK^T
+          ++nk;
           if (++ks == KS) {
             ks = 0;
             kph ^= 1u;
           }
-          if (!mbar_wait_poll(&sb.p_ready, g & 1u, &s_abort) || !mbar_wait(&sb.v_full[vs], vph, &s_abort)) {
+          if (q_pending) finish_q();
+          if (!mbar_wait(&sb.v_empty[vs], vph ^ 1u, &s_abort)) {
             ok = false;
             return;
           }
-          tc_fence_after();
-          const uint64_t vd = vdesc + (uint64_t)((vs * C::kKVBytes) >> 4);
-          // packed P of key columns [16 kk, 16 kk + 16) sits in TMEM columns [8 kk, 8 kk + 8)
-          for (int kk = 0; kk < ncols / 16; ++kk)
-            mma_ts(o_col, s_col + 8u * (uint32_t)kk, vd + (uint64_t)(kk * (2048 >> 4)), idesc_pv,
-                   (j == 0 && kk == 0) ? 0u : 1u);
-          tc_commit(&sb.v_empty[vs]);
-          tc_commit(&sb.s_free);  // P consumed, O holds this tile
+          if (lane == 0) {
+            mbar_arrive_expect_tx(&sb.v_full[vs], C::kKVBytes);
+#pragma unroll
+            for (int hb = 0; hb < D / 64; ++hb)
+              tma_load_3d(smem_u32(sV + vs * C::kKVBytes + hb * 16384), &tmV, &sb.v_full[vs], hb * 64, it.kvh, row);
+          }
+          ++nv;
           if (++vs == VS) {
             vs = 0;
             vph ^= 1u;
           }
-          ++g;
-          ++j;
         });
+        if (!ok) break;
+        if (q_pending) finish_q();  // an item without key tiles
+        ++q_iter;
+        w = __shfl_sync(0xffffffffu, wnext, 0);
       }
-      // all issued MMAs must complete before TMEM is released
-      tc_commit(&sb.drain);
-      drain_wait(&sb.drain, 0);
-    }
-    __syncwarp();
+      // every issued copy must land before the CTA may exit
+      cp_async_wait_all();
+      if (lane == 0) {
+        for (int s = 0; s < KS; ++s) {
+          const uint32_t fills = nk > (uint32_t)s ? (nk - 1 - s) / KS + 1 : 0;
+          if (fills > 0) drain_wait(&sb.k_full[s], (fills - 1) & 1u);
+        }
+        for (int s = 0; s < VS; ++s) {
+          const uint32_t fills = nv > (uint32_t)s ? (nv - 1 - s) / VS + 1 : 0;
+          if (fills > 0) drain_wait(&sb.v_full[s], (fills - 1) & 1u);
+        }
+      }
+      __syncwarp();
+    } else {
+      // ------------------------------------------------------------ MMA issuer of stream x
+      // Per key tile: S = QK^T once the tile's K has landed, then O += PV once
+      // the softmax has written P and the tile's V has landed.  While this
+      // thread waits, the other stream's issuer keeps the pipe fed.
+      const int x = warp - 10;
+      FwdStreamBars& sb = bars[x];
+      uint8_t* sQ = smem + x * C::kStreamBytes;
+      uint8_t* sK = sQ + C::kQBytes;
+      uint8_t* sV = sK + KS * C::kKVBytes;
+      if (lane == 0) {
+        const uint64_t qdesc = sdesc_sw128(smem_u32(sQ), 16, 1024);
+        const uint64_t kdesc = sdesc_sw128(smem_u32(sK), 16, 1024);
+        const uint64_t vdesc = sdesc_sw128(smem_u32(sV), 16384, 1024);
+        const uint32_t s_col = tmem + 128u * (uint32_t)x;
+        const uint32_t o_col = tmem + C::kColO + 128u * (uint32_t)x;
+        constexpr uint32_t idesc_pv = idesc_bf16(128, D, false, true);
+        int ks = 0, vs = 0;
+        uint32_t kph = 0, vph = 0, g = 0, q_iter = 0;
+        bool ok = true;
+        for (uint32_t kit = 0; ok; ++kit) {
+          int w = 0;
+          if (!item_take_one(&ring[x], kit, w, &s_abort)) break;
+          if (w >= n_items) break;
+          const QItem it = q_item<true>(p, n_entries, w);
+          int n = 0;
+          for_each_kv_tile(it, p, [&](int, int) { ++n; });
+          if (!mbar_wait(&sb.q_full, q_iter & 1u, &s_abort)) break;
+          ++q_iter;
+          tc_fence_after();
+          if (n == 0) tc_commit(&sb.q_empty);
+          int j = 0;
+          for_each_kv_tile(it, p, [&](int c, int jt) {
+            if (!ok) return;
+            const int ncols = q_tile_ncols(it, p, c, jt);
+            // S of this tile overwrites the P the previous PV reads: both are
+            // issued by this thread, and the tensor pipe executes one thread's
+            // MMAs in issue order, so no wait for that PV is needed here
+            if (!mbar_wait(&sb.k_full[ks], kph, &s_abort)) {
+              ok = false;
+              return;
+            }
+            tc_fence_after();
+            const uint32_t idesc_qk = idesc_bf16(128, ncols, false, false);
+            const uint64_t kd = kdesc + (uint64_t)((ks * C::kKVBytes) >> 4);
+#pragma unroll
+            for (int kk = 0; kk < D / 16; ++kk) {
+              const uint64_t off = (uint64_t)(((kk >> 2) * 16384 + (kk & 3) * 32) >> 4);
+              mma_ss(s_col, qdesc + off, kd + off, idesc_qk, kk > 0 ? 1u : 0u);
+            }
+            tc_commit(&sb.s_full);
+            tc_commit(&sb.k_empty[ks]);                // the K slot frees once this QK^T completes
+            if (j + 1 == n) tc_commit(&sb.q_empty);    // and the query tile after the item's last QK^T
+            if (++ks == KS) {
+              ks = 0;
+              kph ^= 1u;
+            }
+            if (!mbar_wait_poll(&sb.p_ready, g & 1u, &s_abort) || !mbar_wait(&sb.v_full[vs], vph, &s_abort)) {
+              ok = false;
+              return;
+            }
+            tc_fence_after();
+            const uint64_t vd = vdesc + (uint64_t)((vs * C::kKVBytes) >> 4);
+            // packed P of key columns [16 kk, 16 kk + 16) sits in TMEM columns [8 kk, 8 kk + 8)
+            for (int kk = 0; kk < ncols / 16; ++kk)
+              mma_ts(o_col, s_col + 8u * (uint32_t)kk, vd + (uint64_t)(kk * (2048 >> 4)), idesc_pv,
+                     (j == 0 && kk == 0) ? 0u : 1u);
+            tc_commit(&sb.v_empty[vs]);
+            tc_commit(&sb.s_free);  // P consumed, O holds this tile
+            if (++vs == VS) {
+              vs = 0;
+              vph ^= 1u;
+            }
+            ++g;
+            ++j;
+          });
+        }
+        // all issued MMAs must complete before TMEM is released
+        tc_commit(&sb.drain);
+        drain_wait(&sb.drain, 0);
+      }
+      __syncwarp();
     }
   } else {
     regs_raise<C::kSoftmaxRegs>();
