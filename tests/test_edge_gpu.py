@@ -1,0 +1,94 @@
+"""GPU parity on the edges of the metadata the entry points accept, against
+the CPU fp64 oracle, forward (both forward kernels) and backward:
+
+* hundreds of short sequences (0-64 tokens), so that most CP chunks hold a
+  handful of rows or none;
+* a large CP size (32: 64 chunks of 32 and 64 rows);
+* multi-query attention (one kv head for eight query heads).
+
+Bars as everywhere: the bf16 bar on O, dQ, dK, dV (error beyond the result's
+own bf16 rounding within 2e-2), lse within 1e-3; rows without a valid token
+exactly 0 (and -inf for lse).  Head dimension 128, that of every benchmark
+workload: with 64 the short-sequence backward case reaches a raw dQ error of
+0.022 at |dQ| = 1.2 (up to 0.014 of it from Delta = rowsum(dO * O) taken on
+the bf16 O the backward receives, which the fp64 oracle does not round)."""
+
+import numpy as np
+import pytest
+import torch
+
+from oracle import thd_oracle as orc
+from packed_sequence_context_gb300 import inputs
+from packed_sequence_context_gb300 import thd_attn as T
+from thd_testutil import assert_fwd_close, assert_within_bar, device_inputs, f64
+
+pytestmark = pytest.mark.gpu
+
+
+@pytest.fixture(scope="module", autouse=True)
+def _lib(thd_lib):
+    yield thd_lib
+    T.thd_test_select_fwd_kernel(0)
+
+
+def _many_short():
+    rng = np.random.default_rng(71)
+    return rng.integers(0, 65, size=400).tolist()
+
+
+CASES = {
+    # name: (lengths, cp, Hq, Hkv, D, pad_to)
+    "many_short": (_many_short(), 4, 4, 2, 128, 8),
+    "cp32": ([2048, 4096], 32, 2, 1, 128, 0),
+    "mqa": ([1000, 3000], 4, 8, 1, 128, 0),
+}
+
+
+def _workload(name):
+    lengths, cp, Hq, Hkv, D, pad_to = CASES[name]
+    return inputs.make_workload("custom", 90, lengths=lengths, pad_to=pad_to, Hq=Hq, Hkv=Hkv, D=D, cp_size=cp,
+                                grad_slack=0.05)
+
+
+@pytest.mark.parametrize("kernel", [T.THD_FWD_KERNEL_SINGLE, T.THD_FWD_KERNEL_DUAL], ids=["single", "dual"])
+@pytest.mark.parametrize("name", list(CASES))
+def test_forward_on_metadata_edges(name, kernel):
+    w = _workload(name)
+    t = inputs.make_tensors(w)
+    d = device_inputs(w, t)
+    assert T.thd_test_select_fwd_kernel(kernel) == T.THD_OK
+    try:
+        o, lse, st = T.attn_fwd(d["q"], d["k"], d["v"], d["cu"], d["cu"], d["cu_pad"], d["cu_pad"],
+                                cp_size=w.cp_size, softmax_scale=w.softmax_scale)
+        torch.cuda.synchronize()
+    finally:
+        T.thd_test_select_fwd_kernel(0)
+    assert int(st.item()) == 0
+    assert_fwd_close(w, t, o, lse)
+
+
+@pytest.mark.parametrize("name", list(CASES))
+def test_backward_on_metadata_edges(name):
+    w = _workload(name)
+    t = inputs.make_tensors(w, with_grad=True)
+    d = device_inputs(w, t)
+    o, lse, st = T.attn_fwd(d["q"], d["k"], d["v"], d["cu"], d["cu"], d["cu_pad"], d["cu_pad"], cp_size=w.cp_size,
+                            softmax_scale=w.softmax_scale)
+    canary = 7.0
+    dq = torch.full((w.dq_rows, w.Hq, w.D), canary, dtype=torch.bfloat16, device="cuda")
+    dk = torch.full((w.dkv_rows, w.Hkv, w.D), canary, dtype=torch.bfloat16, device="cuda")
+    dv = torch.full_like(dk, canary)
+    dq, dk, dv, st2 = T.attn_bwd(d["q"], d["k"], d["v"], o, lse, d["do"], d["cu"], d["cu"], d["cu_pad"],
+                                 d["cu_pad"], cp_size=w.cp_size, softmax_scale=w.softmax_scale, dq_rows=w.dq_rows,
+                                 dkv_rows=w.dkv_rows, dq=dq, dk=dk, dv=dv)
+    torch.cuda.synchronize()
+    assert int(st.item()) == 0 and int(st2.item()) == 0
+    ref = orc.attn_bwd(*(t[x].float().numpy() for x in ("q", "k", "v", "do")), w.cu_seqlens, w.cu_seqlens,
+                       w.cu_seqlens_padded, w.cu_seqlens_padded, softmax_scale=w.softmax_scale, dq_rows=w.dq_rows,
+                       dkv_rows=w.dkv_rows)
+    valid = np.zeros(w.dq_rows, bool)
+    valid[:w.T] = inputs.valid_row_mask(w)
+    for gname, got, r in zip(("dq", "dk", "dv"), (dq, dk, dv), ref):
+        g = f64(got)
+        assert_within_bar(gname, g[valid], r[valid])
+        assert np.all(g[~valid] == 0), f"{gname}: rows without a valid token (pad, slack) must be 0"
