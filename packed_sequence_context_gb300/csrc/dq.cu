@@ -48,6 +48,11 @@ struct DqCfg {
   static constexpr uint32_t kTmemCols = 512;
   static constexpr uint32_t kColDP = 256, kColDQ = 384;
   static constexpr int kThreads = 384;
+  // register split (setmaxnreg) for the instantiation shorter sequences take:
+  // dQ +2-3% on batches of 0.1-8K-token sequences, -0.9% on one long sequence
+  static constexpr uint32_t kComputeRegs = 192;  // per thread, warps 0-7
+  static constexpr uint32_t kOtherRegs = 112;    // per thread, warps 8-11
+  static_assert(256 * kComputeRegs + 128 * kOtherRegs <= 384 * 168, "register split above the launch budget");
 };
 
 template <int D, bool kGrouped>
@@ -129,246 +134,250 @@ __global__ void __launch_bounds__(384, 1)
   // role runs, so nothing ever commits to it.
   if (p.test_stall) {
     mbar_wait(&bar_drain, 0, &s_abort);
-  } else if (warp == 8) {
-    // ------------------------------------------------------------ Q, dO and K producer (whole warp)
-    int ks = 0;
-    uint32_t kph = 0, n_fill = 0, q_iter = 0;
-    bool ok = true;
-    int w = item_first();
-    for (uint32_t kit = 0; ok; ++kit) {
-      // publish this item (or the end marker) to the other roles, and claim
-      // the next one while this one is loaded
-      int wnext = 0;
-      if (lane == 0) {
-        ok = item_publish(&ring, kit, w, &s_abort);
-        if (ok && w < n_items) wnext = item_claim(p.claim);
-      }
-      ok = __shfl_sync(0xffffffffu, ok ? 1 : 0, 0) != 0;
-      if (!ok || w >= n_items) break;
-      const QItem it = q_item<kGrouped>(p, n_entries, w);
-      // the item's rank-local query rows of Q and dO, once the previous
-      // item's last products that read them have completed; rows without a
-      // valid query are zero
-      if (!mbar_wait(&bar_q_empty, (q_iter & 1u) ^ 1u, &s_abort)) break;
-      const uint32_t qdst = smem_u32(sQ), ddst = smem_u32(sDO);
-#pragma unroll
-      for (int rr = 0; rr < 4; ++rr) {
-        const int row = lane + 32 * rr;
-        const int prow = it.t * kTile + row;
-        const bool in_rank = prow < 2 * it.g.cbq;
-        const int pos = in_rank ? local_to_pos(prow, it.r, it.g.cbq, p.cp) : 0;
-        const bool valid = in_rank && pos < it.g.Lq;
-        const int64_t off = valid ? (((int64_t)it.g.q_off + pos) * p.Hq + it.h) * D : 0;
-#pragma unroll
-        for (int c = 0; c < D / 8; ++c) {
-          cp_async_16(qdst + sw128_offset(row, 8 * c, kTile), p.q + off + (valid ? 8 * c : 0), valid ? 16u : 0u);
-          cp_async_16(ddst + sw128_offset(row, 8 * c, kTile), p.dout + off + (valid ? 8 * c : 0), valid ? 16u : 0u);
-        }
-      }
-      cp_async_wait_all();
-      fence_proxy_async_smem();
-      mbar_arrive(&bar_q_full);
-      ++q_iter;
-      for_each_kv_tile(it, p, [&](int c, int j) {
-        if (!ok) return;
-        if (!mbar_wait(&bar_k_empty[ks], kph ^ 1u, &s_abort)) {
-          ok = false;
-          return;
-        }
-        if (lane == 0) {
-          const int row = it.g.kv_off + c * it.g.cbkv + j * kTile;
-          mbar_arrive_expect_tx(&bar_k_full[ks], C::kKVBytes);
-#pragma unroll
-          for (int hb = 0; hb < D / 64; ++hb)
-            tma_load_3d(smem_u32(sK + ks * C::kKVBytes + hb * 16384), &tmK, &bar_k_full[ks], hb * 64, it.kvh, row);
-        }
-        ++n_fill;
-        if (++ks == KS) {
-          ks = 0;
-          kph ^= 1u;
-        }
-      });
-      w = __shfl_sync(0xffffffffu, wnext, 0);
-    }
-    if (lane == 0) {
-      for (int s = 0; s < KS; ++s) {
-        const uint32_t fills = n_fill > (uint32_t)s ? (n_fill - 1 - s) / KS + 1 : 0;
-        if (fills > 0) drain_wait(&bar_k_full[s], (fills - 1) & 1u);
-      }
-    }
-    __syncwarp();
-  } else if (warp == 10) {
-    // ------------------------------------------------------------ value producer
-    if (lane == 0) {
-      int vs = 0;
-      uint32_t vph = 0, n_fill = 0;
+  } else if (warp >= 8) {
+    if constexpr (!kGrouped) regs_lower<C::kOtherRegs>();
+    if (warp == 8) {
+      // ------------------------------------------------------------ Q, dO and K producer (whole warp)
+      int ks = 0;
+      uint32_t kph = 0, n_fill = 0, q_iter = 0;
       bool ok = true;
+      int w = item_first();
       for (uint32_t kit = 0; ok; ++kit) {
-        int w;
-        if (!item_take_one(&ring, kit, w, &s_abort) || w >= n_items) break;
+        // publish this item (or the end marker) to the other roles, and claim
+        // the next one while this one is loaded
+        int wnext = 0;
+        if (lane == 0) {
+          ok = item_publish(&ring, kit, w, &s_abort);
+          if (ok && w < n_items) wnext = item_claim(p.claim);
+        }
+        ok = __shfl_sync(0xffffffffu, ok ? 1 : 0, 0) != 0;
+        if (!ok || w >= n_items) break;
         const QItem it = q_item<kGrouped>(p, n_entries, w);
+        // the item's rank-local query rows of Q and dO, once the previous
+        // item's last products that read them have completed; rows without a
+        // valid query are zero
+        if (!mbar_wait(&bar_q_empty, (q_iter & 1u) ^ 1u, &s_abort)) break;
+        const uint32_t qdst = smem_u32(sQ), ddst = smem_u32(sDO);
+#pragma unroll
+        for (int rr = 0; rr < 4; ++rr) {
+          const int row = lane + 32 * rr;
+          const int prow = it.t * kTile + row;
+          const bool in_rank = prow < 2 * it.g.cbq;
+          const int pos = in_rank ? local_to_pos(prow, it.r, it.g.cbq, p.cp) : 0;
+          const bool valid = in_rank && pos < it.g.Lq;
+          const int64_t off = valid ? (((int64_t)it.g.q_off + pos) * p.Hq + it.h) * D : 0;
+#pragma unroll
+          for (int c = 0; c < D / 8; ++c) {
+            cp_async_16(qdst + sw128_offset(row, 8 * c, kTile), p.q + off + (valid ? 8 * c : 0), valid ? 16u : 0u);
+            cp_async_16(ddst + sw128_offset(row, 8 * c, kTile), p.dout + off + (valid ? 8 * c : 0), valid ? 16u : 0u);
+          }
+        }
+        cp_async_wait_all();
+        fence_proxy_async_smem();
+        mbar_arrive(&bar_q_full);
+        ++q_iter;
         for_each_kv_tile(it, p, [&](int c, int j) {
           if (!ok) return;
-          if (!mbar_wait(&bar_v_empty[vs], vph ^ 1u, &s_abort)) {
+          if (!mbar_wait(&bar_k_empty[ks], kph ^ 1u, &s_abort)) {
             ok = false;
             return;
           }
-          const int row = it.g.kv_off + c * it.g.cbkv + j * kTile;
-          mbar_arrive_expect_tx(&bar_v_full[vs], C::kKVBytes);
+          if (lane == 0) {
+            const int row = it.g.kv_off + c * it.g.cbkv + j * kTile;
+            mbar_arrive_expect_tx(&bar_k_full[ks], C::kKVBytes);
 #pragma unroll
-          for (int hb = 0; hb < D / 64; ++hb)
-            tma_load_3d(smem_u32(sV + vs * C::kKVBytes + hb * 16384), &tmV, &bar_v_full[vs], hb * 64, it.kvh, row);
+            for (int hb = 0; hb < D / 64; ++hb)
+              tma_load_3d(smem_u32(sK + ks * C::kKVBytes + hb * 16384), &tmK, &bar_k_full[ks], hb * 64, it.kvh, row);
+          }
           ++n_fill;
-          if (++vs == VS) {
-            vs = 0;
-            vph ^= 1u;
-          }
-        });
-      }
-      for (int s = 0; s < VS; ++s) {
-        const uint32_t fills = n_fill > (uint32_t)s ? (n_fill - 1 - s) / VS + 1 : 0;
-        if (fills > 0) drain_wait(&bar_v_full[s], (fills - 1) & 1u);
-      }
-    }
-    __syncwarp();
-  } else if (warp == 9) {
-    // ------------------------------------------------------------ S = Q K^T issuer
-    // Two issuing threads, as in the forward: a barrier wait in one does not
-    // leave the tensor pipe idle while the other has products to issue.
-    if (lane == 0) {
-      const uint64_t qdesc = sdesc_sw128(smem_u32(sQ), 16, 1024);
-      const uint64_t kdesc = sdesc_sw128(smem_u32(sK), 16, 1024);
-      int ks = 0;
-      uint32_t kph = 0, g = 0, q_iter = 0;
-      bool ok = true;
-      for (uint32_t kit = 0; ok; ++kit) {
-        int w;
-        if (!item_take_one(&ring, kit, w, &s_abort) || w >= n_items) break;
-        const QItem it = q_item<kGrouped>(p, n_entries, w);
-        int n = 0;
-        for_each_kv_tile(it, p, [&](int, int) { ++n; });
-        if (!mbar_wait(&bar_q_full, q_iter & 1u, &s_abort)) break;
-        ++q_iter;
-        tc_fence_after();
-        if (n == 0) tc_commit(&bar_q_empty);
-        int j = 0;
-        for_each_kv_tile(it, p, [&](int c, int jt) {
-          if (!ok) return;
-          const int ncols = q_tile_ncols(it, p, c, jt);
-          const uint32_t b = g & 1u;
-          if (!mbar_wait(&bar_k_full[ks], kph, &s_abort) ||
-              (g >= 2 && !mbar_wait(&bar_s_free[b], ((g >> 1) - 1) & 1u, &s_abort))) {
-            ok = false;
-            return;
-          }
-          tc_fence_after();
-          const uint32_t idesc_s = idesc_bf16(128, ncols, false, false);
-          const uint64_t kd = kdesc + (uint64_t)((ks * C::kKVBytes) >> 4);
-#pragma unroll
-          for (int kk = 0; kk < D / 16; ++kk) {
-            const uint64_t off = (uint64_t)(((kk >> 2) * 16384 + (kk & 3) * 32) >> 4);
-            mma_ss(tmem + b * 128u, qdesc + off, kd + off, idesc_s, kk > 0 ? 1u : 0u);
-          }
-          tc_commit(&bar_s_full[b]);
-          if (++j == n) tc_commit(&bar_q_empty);  // the item's last read of Q
           if (++ks == KS) {
             ks = 0;
             kph ^= 1u;
           }
-          ++g;
         });
+        w = __shfl_sync(0xffffffffu, wnext, 0);
       }
-      tc_commit(&bar_drain);
-      drain_wait(&bar_drain, 0);
-    }
-    __syncwarp();
-  } else if (warp == 11) {
-    // ------------------------------------------------------------ dP = dO V^T and dQ += dS K issuer
-    // Per tile g: once the dS warps have read dP of tile g-1 into registers
-    // (dp_free: early in their work on g-1), dP of tile g -- so it is ready
-    // when they come to g -- then, once their dS of g-1 is in TMEM, dQ of
-    // tile g-1.  The item's last dQ follows its last dS.
-    if (lane == 0) {
-      constexpr uint32_t idesc_dq = idesc_bf16(128, D, false, true);
-      const uint64_t dodesc = sdesc_sw128(smem_u32(sDO), 16, 1024);
-      const uint64_t vdesc = sdesc_sw128(smem_u32(sV), 16, 1024);
-      const uint64_t kmn = sdesc_sw128(smem_u32(sK), 16384, 1024);  // K read MN-major
-      int vs = 0;
-      uint32_t vph = 0, g = 0, q_iter = 0;
-      bool ok = true;
-      // issue dQ += dS K for tile gg (its dS in S buffer gg % 2, its K in ring slot gg % KS)
-      auto issue_dq = [&](uint32_t gg, int ncols, bool first) -> bool {
-        const uint32_t b = gg & 1u;
-        if (!mbar_wait(&bar_ds_ready[b], (gg >> 1) & 1u, &s_abort)) return false;
-        tc_fence_after();
-        const int kslot = (int)(gg % KS);
-        const uint64_t kd = kmn + (uint64_t)((kslot * C::kKVBytes) >> 4);
-        // packed dS of key columns 16 kk.. sits at column 64 (kk/4) + 8 (kk%4)
-        for (int kk = 0; kk < ncols / 16; ++kk)
-          mma_ts(tmem + C::kColDQ, tmem + b * 128u + 64 * (kk >> 2) + 8 * (kk & 3),
-                 kd + (uint64_t)(kk * (2048 >> 4)), idesc_dq, (first && kk == 0) ? 0u : 1u);
-        tc_commit(&bar_s_free[b]);
-        tc_commit(&bar_k_empty[kslot]);
-        return true;
-      };
-      for (uint32_t kit = 0; ok; ++kit) {
-        int w;
-        if (!item_take_one(&ring, kit, w, &s_abort) || w >= n_items) break;
-        const QItem it = q_item<kGrouped>(p, n_entries, w);
-        int n = 0;
-        for_each_kv_tile(it, p, [&](int, int) { ++n; });
-        if (!mbar_wait(&bar_q_full, q_iter & 1u, &s_abort)) break;
-        ++q_iter;
-        tc_fence_after();
-        if (n == 0) {
-          tc_commit(&bar_q_empty);
-          continue;
+      if (lane == 0) {
+        for (int s = 0; s < KS; ++s) {
+          const uint32_t fills = n_fill > (uint32_t)s ? (n_fill - 1 - s) / KS + 1 : 0;
+          if (fills > 0) drain_wait(&bar_k_full[s], (fills - 1) & 1u);
         }
-        int j = 0, prev_cols = 0;
-        for_each_kv_tile(it, p, [&](int c, int jt) {
-          if (!ok) return;
-          const int ncols = q_tile_ncols(it, p, c, jt);
-          // the dP buffer is free once the dS warps have read tile g-1's dP
-          if (g > 0 && !mbar_wait(&bar_dp_free, (g - 1) & 1u, &s_abort)) {
-            ok = false;
-            return;
-          }
-          if (!mbar_wait(&bar_v_full[vs], vph, &s_abort)) {
-            ok = false;
-            return;
-          }
-          tc_fence_after();
-          const uint32_t idesc_p = idesc_bf16(128, ncols, false, false);
-          const uint64_t vd = vdesc + (uint64_t)((vs * C::kKVBytes) >> 4);
-#pragma unroll
-          for (int kk = 0; kk < D / 16; ++kk) {
-            const uint64_t off = (uint64_t)(((kk >> 2) * 16384 + (kk & 3) * 32) >> 4);
-            mma_ss(tmem + C::kColDP, dodesc + off, vd + off, idesc_p, kk > 0 ? 1u : 0u);
-          }
-          tc_commit(&bar_dp_full);
-          tc_commit(&bar_v_empty[vs]);
-          if (j == n - 1) tc_commit(&bar_q_empty);  // the item's last read of dO
-          if (++vs == VS) {
-            vs = 0;
-            vph ^= 1u;
-          }
-          if (j > 0 && !issue_dq(g - 1, prev_cols, j == 1)) {
-            ok = false;
-            return;
-          }
-          prev_cols = ncols;
-          ++g;
-          ++j;
-        });
-        if (!ok) break;
-        if (!issue_dq(g - 1, prev_cols, n == 1)) break;
-        tc_commit(&bar_dq_done);
       }
-      tc_commit(&bar_drain2);
-      drain_wait(&bar_drain2, 0);
+      __syncwarp();
+    } else if (warp == 10) {
+      // ------------------------------------------------------------ value producer
+      if (lane == 0) {
+        int vs = 0;
+        uint32_t vph = 0, n_fill = 0;
+        bool ok = true;
+        for (uint32_t kit = 0; ok; ++kit) {
+          int w;
+          if (!item_take_one(&ring, kit, w, &s_abort) || w >= n_items) break;
+          const QItem it = q_item<kGrouped>(p, n_entries, w);
+          for_each_kv_tile(it, p, [&](int c, int j) {
+            if (!ok) return;
+            if (!mbar_wait(&bar_v_empty[vs], vph ^ 1u, &s_abort)) {
+              ok = false;
+              return;
+            }
+            const int row = it.g.kv_off + c * it.g.cbkv + j * kTile;
+            mbar_arrive_expect_tx(&bar_v_full[vs], C::kKVBytes);
+#pragma unroll
+            for (int hb = 0; hb < D / 64; ++hb)
+              tma_load_3d(smem_u32(sV + vs * C::kKVBytes + hb * 16384), &tmV, &bar_v_full[vs], hb * 64, it.kvh, row);
+            ++n_fill;
+            if (++vs == VS) {
+              vs = 0;
+              vph ^= 1u;
+            }
+          });
+        }
+        for (int s = 0; s < VS; ++s) {
+          const uint32_t fills = n_fill > (uint32_t)s ? (n_fill - 1 - s) / VS + 1 : 0;
+          if (fills > 0) drain_wait(&bar_v_full[s], (fills - 1) & 1u);
+        }
+      }
+      __syncwarp();
+    } else if (warp == 9) {
+      // ------------------------------------------------------------ S = Q K^T issuer
+      // Two issuing threads, as in the forward: a barrier wait in one does not
+      // leave the tensor pipe idle while the other has products to issue.
+      if (lane == 0) {
+        const uint64_t qdesc = sdesc_sw128(smem_u32(sQ), 16, 1024);
+        const uint64_t kdesc = sdesc_sw128(smem_u32(sK), 16, 1024);
+        int ks = 0;
+        uint32_t kph = 0, g = 0, q_iter = 0;
+        bool ok = true;
+        for (uint32_t kit = 0; ok; ++kit) {
+          int w;
+          if (!item_take_one(&ring, kit, w, &s_abort) || w >= n_items) break;
+          const QItem it = q_item<kGrouped>(p, n_entries, w);
+          int n = 0;
+          for_each_kv_tile(it, p, [&](int, int) { ++n; });
+          if (!mbar_wait(&bar_q_full, q_iter & 1u, &s_abort)) break;
+          ++q_iter;
+          tc_fence_after();
+          if (n == 0) tc_commit(&bar_q_empty);
+          int j = 0;
+          for_each_kv_tile(it, p, [&](int c, int jt) {
+            if (!ok) return;
+            const int ncols = q_tile_ncols(it, p, c, jt);
+            const uint32_t b = g & 1u;
+            if (!mbar_wait(&bar_k_full[ks], kph, &s_abort) ||
+                (g >= 2 && !mbar_wait(&bar_s_free[b], ((g >> 1) - 1) & 1u, &s_abort))) {
+              ok = false;
+              return;
+            }
+            tc_fence_after();
+            const uint32_t idesc_s = idesc_bf16(128, ncols, false, false);
+            const uint64_t kd = kdesc + (uint64_t)((ks * C::kKVBytes) >> 4);
+#pragma unroll
+            for (int kk = 0; kk < D / 16; ++kk) {
+              const uint64_t off = (uint64_t)(((kk >> 2) * 16384 + (kk & 3) * 32) >> 4);
+              mma_ss(tmem + b * 128u, qdesc + off, kd + off, idesc_s, kk > 0 ? 1u : 0u);
+            }
+            tc_commit(&bar_s_full[b]);
+            if (++j == n) tc_commit(&bar_q_empty);  // the item's last read of Q
+            if (++ks == KS) {
+              ks = 0;
+              kph ^= 1u;
+            }
+            ++g;
+          });
+        }
+        tc_commit(&bar_drain);
+        drain_wait(&bar_drain, 0);
+      }
+      __syncwarp();
+    } else if (warp == 11) {
+      // ------------------------------------------------------------ dP = dO V^T and dQ += dS K issuer
+      // Per tile g: once the dS warps have read dP of tile g-1 into registers
+      // (dp_free: early in their work on g-1), dP of tile g -- so it is ready
+      // when they come to g -- then, once their dS of g-1 is in TMEM, dQ of
+      // tile g-1.  The item's last dQ follows its last dS.
+      if (lane == 0) {
+        constexpr uint32_t idesc_dq = idesc_bf16(128, D, false, true);
+        const uint64_t dodesc = sdesc_sw128(smem_u32(sDO), 16, 1024);
+        const uint64_t vdesc = sdesc_sw128(smem_u32(sV), 16, 1024);
+        const uint64_t kmn = sdesc_sw128(smem_u32(sK), 16384, 1024);  // K read MN-major
+        int vs = 0;
+        uint32_t vph = 0, g = 0, q_iter = 0;
+        bool ok = true;
+        // issue dQ += dS K for tile gg (its dS in S buffer gg % 2, its K in ring slot gg % KS)
+        auto issue_dq = [&](uint32_t gg, int ncols, bool first) -> bool {
+          const uint32_t b = gg & 1u;
+          if (!mbar_wait(&bar_ds_ready[b], (gg >> 1) & 1u, &s_abort)) return false;
+          tc_fence_after();
+          const int kslot = (int)(gg % KS);
+          const uint64_t kd = kmn + (uint64_t)((kslot * C::kKVBytes) >> 4);
+          // packed dS of key columns 16 kk.. sits at column 64 (kk/4) + 8 (kk%4)
+          for (int kk = 0; kk < ncols / 16; ++kk)
+            mma_ts(tmem + C::kColDQ, tmem + b * 128u + 64 * (kk >> 2) + 8 * (kk & 3),
+                   kd + (uint64_t)(kk * (2048 >> 4)), idesc_dq, (first && kk == 0) ? 0u : 1u);
+          tc_commit(&bar_s_free[b]);
+          tc_commit(&bar_k_empty[kslot]);
+          return true;
+        };
+        for (uint32_t kit = 0; ok; ++kit) {
+          int w;
+          if (!item_take_one(&ring, kit, w, &s_abort) || w >= n_items) break;
+          const QItem it = q_item<kGrouped>(p, n_entries, w);
+          int n = 0;
+          for_each_kv_tile(it, p, [&](int, int) { ++n; });
+          if (!mbar_wait(&bar_q_full, q_iter & 1u, &s_abort)) break;
+          ++q_iter;
+          tc_fence_after();
+          if (n == 0) {
+            tc_commit(&bar_q_empty);
+            continue;
+          }
+          int j = 0, prev_cols = 0;
+          for_each_kv_tile(it, p, [&](int c, int jt) {
+            if (!ok) return;
+            const int ncols = q_tile_ncols(it, p, c, jt);
+            // the dP buffer is free once the dS warps have read tile g-1's dP
+            if (g > 0 && !mbar_wait(&bar_dp_free, (g - 1) & 1u, &s_abort)) {
+              ok = false;
+              return;
+            }
+            if (!mbar_wait(&bar_v_full[vs], vph, &s_abort)) {
+              ok = false;
+              return;
+            }
+            tc_fence_after();
+            const uint32_t idesc_p = idesc_bf16(128, ncols, false, false);
+            const uint64_t vd = vdesc + (uint64_t)((vs * C::kKVBytes) >> 4);
+#pragma unroll
+            for (int kk = 0; kk < D / 16; ++kk) {
+              const uint64_t off = (uint64_t)(((kk >> 2) * 16384 + (kk & 3) * 32) >> 4);
+              mma_ss(tmem + C::kColDP, dodesc + off, vd + off, idesc_p, kk > 0 ? 1u : 0u);
+            }
+            tc_commit(&bar_dp_full);
+            tc_commit(&bar_v_empty[vs]);
+            if (j == n - 1) tc_commit(&bar_q_empty);  // the item's last read of dO
+            if (++vs == VS) {
+              vs = 0;
+              vph ^= 1u;
+            }
+            if (j > 0 && !issue_dq(g - 1, prev_cols, j == 1)) {
+              ok = false;
+              return;
+            }
+            prev_cols = ncols;
+            ++g;
+            ++j;
+          });
+          if (!ok) break;
+          if (!issue_dq(g - 1, prev_cols, n == 1)) break;
+          tc_commit(&bar_dq_done);
+        }
+        tc_commit(&bar_drain2);
+        drain_wait(&bar_drain2, 0);
+      }
+      __syncwarp();
     }
-    __syncwarp();
   } else {
+    if constexpr (!kGrouped) regs_raise<C::kComputeRegs>();
     // ------------------------------------------------------------ dS + epilogue
     // Thread (half, row) owns query row `row` (its TMEM lane) and key columns
     // [64 half, 64 half + 64) of every tile, plus head-dim columns
