@@ -18,12 +18,14 @@
 //   P^T  = exp(S^T scale - lse)          dS^T = P^T (dP^T - Delta)
 //   dV  += P^T dO     dK  += dS^T Q       (A = P^T / dS^T from TMEM, packed bf16
 //                                          over the S^T they were computed from)
-// CTA (384 threads): warps 0-7 compute in two warpgroups -- a thread owns one
-// key row (its TMEM lane) and half of the query columns for P/dS, and half of
-// the head dimension when writing dK/dV; warp 8 TMA producer (+ lse/Delta
-// staging); warp 9 TMEM allocator and S^T issuer; warp 10 dV/dK/dP^T issuer;
-// warp 11 idle (it completes the fourth warpgroup, so that the warpgroups can
-// move registers to the compute warps with setmaxnreg).
+// CTA: warps 0-7 compute in two warpgroups -- a thread owns one key row (its
+// TMEM lane) and half of the query columns for P/dS, and half of the head
+// dimension when writing dK/dV; warp 8 TMA producer (+ lse/Delta staging);
+// warp 9 TMEM allocator and S^T issuer; warp 10 dV/dK/dP^T issuer.  The
+// entry-major instantiation (shorter sequences) runs 384 threads: warp 11,
+// idle, completes the fourth warpgroup so that setmaxnreg can move registers
+// to the compute warps (dK/dV +5% on batches of 0.1-8K-token sequences); the
+// grouped one (long sequences, where that measured -1%) runs 352.
 #include "common.cuh"
 #include "ptx.cuh"
 #include "sched.cuh"
@@ -108,7 +110,7 @@ __device__ inline void drain_wait_b(uint64_t* bar, uint32_t parity) {
 }
 
 template <int D, bool kGrouped>
-__global__ void __launch_bounds__(384, 1)
+__global__ void __launch_bounds__(kGrouped ? 352 : 384, 1)
     bwd_kernel(const BwdParams p, const __grid_constant__ CUtensorMap tmQ, const __grid_constant__ CUtensorMap tmDO,
                const __grid_constant__ CUtensorMap tmK, const __grid_constant__ CUtensorMap tmV) {
   using C = BwdCfg<D>;
@@ -190,7 +192,7 @@ __global__ void __launch_bounds__(384, 1)
     // The compute warps hold a step's P (64 values) and S^T / dP^T chunks per
     // thread: they get 200 registers, warps 8-11 (producer, issuers, idle) 96;
     // 256 x 200 + 128 x 96 fits the 384 x 168 the CTA is launched with.
-    regs_lower<C::kOtherRegs>();
+    if constexpr (!kGrouped) regs_lower<C::kOtherRegs>();
     if (warp == 8) {
       // ------------------------------------------------------------ producer (whole warp)
       int stage = 0;
@@ -448,7 +450,7 @@ __global__ void __launch_bounds__(384, 1)
       __syncwarp();
     }
   } else {
-    regs_raise<C::kComputeRegs>();
+    if constexpr (!kGrouped) regs_raise<C::kComputeRegs>();
     // ------------------------------------------------------------ compute warps
     const int half = warp >> 2;     // which half of the columns this thread owns
     const int row = tid & 127;      // its key row (TMEM lane) / query row when draining dQ
@@ -650,7 +652,7 @@ static cudaError_t launch_bwd_t(const BwdParams& p, const CUtensorMap& tq, const
   cudaError_t e = cudaFuncSetAttribute(bwd_kernel<D, kGrouped>, cudaFuncAttributeMaxDynamicSharedMemorySize, C::kSmem);
   if (e != cudaSuccess) return e;
   prof_before(THD_KERNEL_BWD, st);
-  bwd_kernel<D, kGrouped><<<grid, 384, C::kSmem, st>>>(p, tq, tdo, tk, tv);
+  bwd_kernel<D, kGrouped><<<grid, kGrouped ? 352 : 384, C::kSmem, st>>>(p, tq, tdo, tk, tv);
   count_launch();
   e = cudaGetLastError();
   prof_after(THD_KERNEL_BWD, st);
