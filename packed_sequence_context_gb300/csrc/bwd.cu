@@ -456,6 +456,9 @@ __global__ void __launch_bounds__(kGrouped ? 352 : 384, 1)
     const int row = tid & 127;      // its key row (TMEM lane) / query row when draining dQ
     const uint32_t lane_base = (uint32_t)((warp & 3) * 32) << 16;
     const float sl2 = p.scale_log2;
+    // dK/dV rows start at multiples of 128 bytes: with 32-byte aligned buffers
+    // the epilogue stores whole 32-byte sectors (the API asks for 16)
+    const bool v8_ok = ((reinterpret_cast<uintptr_t>(p.dk) | reinterpret_cast<uintptr_t>(p.dv)) & 31u) == 0;
     uint32_t su = 0;
     bool ok = true;
     for (uint32_t kit = 0; ok; ++kit) {
@@ -604,21 +607,27 @@ __global__ void __launch_bounds__(kGrouped ? 352 : 384, 1)
           const float fk = valid_kv ? p.scale : 0.f;
           const float fv = valid_kv ? 1.f : 0.f;
           const int64_t grow = (int64_t)it.g.kv_off + j_pos;
-          uint4* dkp = reinterpret_cast<uint4*>(p.dk + (grow * p.Hkv + it.hk) * D + 32 * kk);
-          uint4* dvp = reinterpret_cast<uint4*>(p.dv + (grow * p.Hkv + it.hk) * D + 32 * kk);
+          uint16_t* dkp = p.dk + (grow * p.Hkv + it.hk) * D + 32 * kk;
+          uint16_t* dvp = p.dv + (grow * p.Hkv + it.hk) * D + 32 * kk;
+          uint32_t x[16], y[16];  // the 32 columns of dK and of dV, packed bf16
 #pragma unroll
-          for (int n = 0; n < 4; ++n) {
-            uint4 x, y;
-            x.x = pack_bf16x2(__uint_as_float(a[8 * n + 0]) * fk, __uint_as_float(a[8 * n + 1]) * fk);
-            x.y = pack_bf16x2(__uint_as_float(a[8 * n + 2]) * fk, __uint_as_float(a[8 * n + 3]) * fk);
-            x.z = pack_bf16x2(__uint_as_float(a[8 * n + 4]) * fk, __uint_as_float(a[8 * n + 5]) * fk);
-            x.w = pack_bf16x2(__uint_as_float(a[8 * n + 6]) * fk, __uint_as_float(a[8 * n + 7]) * fk);
-            y.x = pack_bf16x2(__uint_as_float(bq[8 * n + 0]) * fv, __uint_as_float(bq[8 * n + 1]) * fv);
-            y.y = pack_bf16x2(__uint_as_float(bq[8 * n + 2]) * fv, __uint_as_float(bq[8 * n + 3]) * fv);
-            y.z = pack_bf16x2(__uint_as_float(bq[8 * n + 4]) * fv, __uint_as_float(bq[8 * n + 5]) * fv);
-            y.w = pack_bf16x2(__uint_as_float(bq[8 * n + 6]) * fv, __uint_as_float(bq[8 * n + 7]) * fv);
-            dkp[n] = x;
-            dvp[n] = y;
+          for (int n = 0; n < 16; ++n) {
+            x[n] = pack_bf16x2(__uint_as_float(a[2 * n]) * fk, __uint_as_float(a[2 * n + 1]) * fk);
+            y[n] = pack_bf16x2(__uint_as_float(bq[2 * n]) * fv, __uint_as_float(bq[2 * n + 1]) * fv);
+          }
+          if (v8_ok) {
+            // two 32-byte stores per tensor: each writes one whole sector of the row
+#pragma unroll
+            for (int h2 = 0; h2 < 2; ++h2) {
+              st_global_v8(dkp + 16 * h2, *reinterpret_cast<const uint32_t(*)[8]>(x + 8 * h2));
+              st_global_v8(dvp + 16 * h2, *reinterpret_cast<const uint32_t(*)[8]>(y + 8 * h2));
+            }
+          } else {
+#pragma unroll
+            for (int n = 0; n < 4; ++n) {
+              reinterpret_cast<uint4*>(dkp)[n] = make_uint4(x[4 * n], x[4 * n + 1], x[4 * n + 2], x[4 * n + 3]);
+              reinterpret_cast<uint4*>(dvp)[n] = make_uint4(y[4 * n], y[4 * n + 1], y[4 * n + 2], y[4 * n + 3]);
+            }
           }
         }
       }

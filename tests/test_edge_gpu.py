@@ -92,3 +92,33 @@ def test_backward_on_metadata_edges(name):
         g = f64(got)
         assert_within_bar(gname, g[valid], r[valid])
         assert np.all(g[~valid] == 0), f"{gname}: rows without a valid token (pad, slack) must be 0"
+
+
+def test_backward_into_16_byte_aligned_buffers_is_bit_identical():
+    """dQ/dK/dV buffers aligned to 16 bytes but not 32 (the API's minimum):
+    the kernels then write rows with 16-byte stores instead of 32-byte ones;
+    the results must be the same bits."""
+    w = _workload("mqa")
+    t = inputs.make_tensors(w, with_grad=True)
+    d = device_inputs(w, t)
+    o, lse, st = T.attn_fwd(d["q"], d["k"], d["v"], d["cu"], d["cu"], d["cu_pad"], d["cu_pad"], cp_size=w.cp_size,
+                            softmax_scale=w.softmax_scale)
+
+    def run(offset):
+        out = []
+        for rows, H in ((w.dq_rows, w.Hq), (w.dkv_rows, w.Hkv), (w.dkv_rows, w.Hkv)):
+            n = rows * H * w.D
+            big = torch.full((n + offset,), 7.0, dtype=torch.bfloat16, device="cuda")
+            out.append(big[offset:].view(rows, H, w.D))
+        dq, dk, dv, st2 = T.attn_bwd(d["q"], d["k"], d["v"], o, lse, d["do"], d["cu"], d["cu"], d["cu_pad"],
+                                     d["cu_pad"], cp_size=w.cp_size, softmax_scale=w.softmax_scale,
+                                     dq_rows=w.dq_rows, dkv_rows=w.dkv_rows, dq=out[0], dk=out[1], dv=out[2])
+        torch.cuda.synchronize()
+        assert int(st2.item()) == 0
+        return dq, dk, dv
+
+    a = run(0)
+    b = run(8)  # 8 bf16 = 16 bytes past a 256-byte aligned allocation
+    assert b[1].data_ptr() % 32 == 16
+    for x, y in zip(a, b):
+        assert torch.equal(x, y)
