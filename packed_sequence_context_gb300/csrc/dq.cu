@@ -387,6 +387,8 @@ __global__ void __launch_bounds__(384, 1)
     const uint32_t lane_base = (uint32_t)((warp & 3) * 32) << 16;
     constexpr int DH = D / 2;
     const float sl2 = p.scale_log2;
+    // dQ rows start at multiples of 128 bytes: 32-byte stores when dQ is 32-byte aligned
+    const bool dq_v8 = (reinterpret_cast<uintptr_t>(p.dq) & 31u) == 0;
     uint32_t g = 0, n_item = 0;
     bool ok = true;
     for (uint32_t kit = 0; ok; ++kit) {
@@ -490,19 +492,8 @@ __global__ void __launch_bounds__(384, 1)
 #pragma unroll
           for (int n = 0; n < 32; ++n) o[n] = 0u;
         }
-        if (in_rank) {
-          const float f = valid ? p.scale : 0.f;
-          uint4* dst = reinterpret_cast<uint4*>(p.dq + (grow * p.Hq + it.h) * D + half * DH + 32 * k);
-#pragma unroll
-          for (int n = 0; n < 4; ++n) {
-            uint4 v;
-            v.x = pack_bf16x2(__uint_as_float(o[8 * n + 0]) * f, __uint_as_float(o[8 * n + 1]) * f);
-            v.y = pack_bf16x2(__uint_as_float(o[8 * n + 2]) * f, __uint_as_float(o[8 * n + 3]) * f);
-            v.z = pack_bf16x2(__uint_as_float(o[8 * n + 4]) * f, __uint_as_float(o[8 * n + 5]) * f);
-            v.w = pack_bf16x2(__uint_as_float(o[8 * n + 6]) * f, __uint_as_float(o[8 * n + 7]) * f);
-            dst[n] = v;
-          }
-        }
+        if (in_rank)
+          store32_bf16(p.dq + (grow * p.Hq + it.h) * D + half * DH + 32 * k, o, valid ? p.scale : 0.f, dq_v8);
       }
       tc_fence_before();
     }

@@ -353,6 +353,8 @@ __global__ void __launch_bounds__(384, 1)
     const uint32_t lane_base = (uint32_t)((warp & 3) * 32) << 16;
     constexpr int DH = D / 2;
     const float sl2 = p.scale_log2;
+    // O rows start at multiples of 128 bytes: 32-byte stores when O is 32-byte aligned
+    const bool o_v8 = (reinterpret_cast<uintptr_t>(p.o) & 31u) == 0;
     uint32_t g = 0, n_item = 0;
     bool ok = true;
     for (uint32_t kit = 0; ok; ++kit) {
@@ -524,24 +526,10 @@ __global__ void __launch_bounds__(384, 1)
         }
         if (in_rank) {
           const int64_t col = (grow * p.Hq + it.h) * D + half * DH + 32 * k;
-          if constexpr (kStep) {
-            float4* dst = reinterpret_cast<float4*>(static_cast<float*>(p.o) + col);
-#pragma unroll
-            for (int n = 0; n < 8; ++n)
-              dst[n] = make_float4(__uint_as_float(o[4 * n]) * inv_l, __uint_as_float(o[4 * n + 1]) * inv_l,
-                                   __uint_as_float(o[4 * n + 2]) * inv_l, __uint_as_float(o[4 * n + 3]) * inv_l);
-          } else {
-            uint4* dst = reinterpret_cast<uint4*>(static_cast<uint16_t*>(p.o) + col);
-#pragma unroll
-            for (int n = 0; n < 4; ++n) {
-              uint4 v;
-              v.x = pack_bf16x2(__uint_as_float(o[8 * n + 0]) * inv_l, __uint_as_float(o[8 * n + 1]) * inv_l);
-              v.y = pack_bf16x2(__uint_as_float(o[8 * n + 2]) * inv_l, __uint_as_float(o[8 * n + 3]) * inv_l);
-              v.z = pack_bf16x2(__uint_as_float(o[8 * n + 4]) * inv_l, __uint_as_float(o[8 * n + 5]) * inv_l);
-              v.w = pack_bf16x2(__uint_as_float(o[8 * n + 6]) * inv_l, __uint_as_float(o[8 * n + 7]) * inv_l);
-              dst[n] = v;
-            }
-          }
+          if constexpr (kStep)
+            store32_f32(static_cast<float*>(p.o) + col, o, inv_l, o_v8);
+          else
+            store32_bf16(static_cast<uint16_t*>(p.o) + col, o, inv_l, o_v8);
         }
       }
       tc_fence_before();

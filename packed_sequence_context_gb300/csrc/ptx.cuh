@@ -314,6 +314,36 @@ THD_DEV uint32_t pack_bf16x2(float lo, float hi) {
   return r;
 }
 
+// 32 consecutive fp32 values times f, stored as bf16 (64 bytes) or fp32 (128
+// bytes): 32-byte stores when `v8` (the destination 32-byte aligned), else
+// 16-byte ones.
+THD_DEV void store32_bf16(uint16_t* dst, const uint32_t (&o)[32], float f, bool v8) {
+  uint32_t x[16];
+#pragma unroll
+  for (int n = 0; n < 16; ++n) x[n] = pack_bf16x2(__uint_as_float(o[2 * n]) * f, __uint_as_float(o[2 * n + 1]) * f);
+  if (v8) {
+    st_global_v8(dst, *reinterpret_cast<const uint32_t(*)[8]>(x));
+    st_global_v8(dst + 16, *reinterpret_cast<const uint32_t(*)[8]>(x + 8));
+  } else {
+#pragma unroll
+    for (int n = 0; n < 4; ++n)
+      reinterpret_cast<uint4*>(dst)[n] = make_uint4(x[4 * n], x[4 * n + 1], x[4 * n + 2], x[4 * n + 3]);
+  }
+}
+THD_DEV void store32_f32(float* dst, const uint32_t (&o)[32], float f, bool v8) {
+  uint32_t x[32];
+#pragma unroll
+  for (int n = 0; n < 32; ++n) x[n] = __float_as_uint(__uint_as_float(o[n]) * f);
+  if (v8) {
+#pragma unroll
+    for (int n = 0; n < 4; ++n) st_global_v8(dst + 8 * n, *reinterpret_cast<const uint32_t(*)[8]>(x + 8 * n));
+  } else {
+#pragma unroll
+    for (int n = 0; n < 8; ++n)
+      reinterpret_cast<uint4*>(dst)[n] = make_uint4(x[4 * n], x[4 * n + 1], x[4 * n + 2], x[4 * n + 3]);
+  }
+}
+
 // Byte offset of element (row, col) inside a 128B-swizzled tile made of
 // 64-column blocks of `rows` rows each (col in bf16 elements).
 __host__ __device__ inline uint32_t sw128_offset(uint32_t row, uint32_t col, uint32_t rows) {

@@ -302,15 +302,16 @@ def attn_fwd(q, k, v, cu_seqlens_q, cu_seqlens_kv, cu_seqlens_q_padded=None, cu_
 
 
 def attn_fwd_step(q, k, v, cu_seqlens_q, cu_seqlens_kv, cu_seqlens_q_padded=None, cu_seqlens_kv_padded=None, *,
-                  step, cp_size=1, causal=True, softmax_scale=None, pad_between_seqs=-1, stream=None):
+                  step, cp_size=1, causal=True, softmax_scale=None, pad_between_seqs=-1, out=None, lse=None,
+                  stream=None):
     """One ring step's materialised partial: (o_part fp32 [T_q,Hq,D], lse_part [Hq,T_q], dev_status)."""
     import torch
     T_q, Hq, D = q.shape
     T_kv, Hkv, _ = k.shape
     B = cu_seqlens_q.numel() - 1
     scale = 1.0 / math.sqrt(D) if softmax_scale is None else float(softmax_scale)
-    o = torch.empty((T_q, Hq, D), dtype=torch.float32, device=q.device)
-    l = torch.empty((Hq, T_q), dtype=torch.float32, device=q.device)
+    o = torch.empty((T_q, Hq, D), dtype=torch.float32, device=q.device) if out is None else out
+    l = torch.empty((Hq, T_q), dtype=torch.float32, device=q.device) if lse is None else lse
     st = torch.zeros(1, dtype=torch.int32, device=q.device)
     ws = _workspace(thd_workspace_size(B, T_q, T_kv, Hq, Hkv, D, cp_size, 0), q.device)
     _check("thd_attn_fwd_step", thd_attn_fwd_step(q, k, v, o, l, cu_seqlens_q, cu_seqlens_kv, cu_seqlens_q_padded,

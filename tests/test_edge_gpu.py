@@ -94,6 +94,47 @@ def test_backward_on_metadata_edges(name):
         assert np.all(g[~valid] == 0), f"{gname}: rows without a valid token (pad, slack) must be 0"
 
 
+def _offset_buffer(shape, dtype, offset):
+    """A [shape] view that starts `offset` elements past a 256-byte aligned allocation."""
+    n = int(np.prod(shape))
+    big = torch.full((n + offset,), 7.0, dtype=dtype, device="cuda")
+    return big[offset:].view(*shape)
+
+
+@pytest.mark.parametrize("kernel", [T.THD_FWD_KERNEL_SINGLE, T.THD_FWD_KERNEL_DUAL], ids=["single", "dual"])
+def test_forward_into_16_byte_aligned_buffers_is_bit_identical(kernel):
+    """O buffers aligned to 16 bytes but not 32 (bf16 O and bf16 / fp32 step
+    partials): the forward kernels then write rows with 16-byte stores instead
+    of 32-byte ones; the results must be the same bits."""
+    w = _workload("mqa")
+    t = inputs.make_tensors(w)
+    d = device_inputs(w, t)
+    shape = (w.T, w.Hq, w.D)
+    assert T.thd_test_select_fwd_kernel(kernel) == T.THD_OK
+    try:
+        def run(offset_bf16, offset_f32):
+            o, _, st = T.attn_fwd(d["q"], d["k"], d["v"], d["cu"], d["cu"], d["cu_pad"], d["cu_pad"],
+                                  cp_size=w.cp_size, softmax_scale=w.softmax_scale,
+                                  out=_offset_buffer(shape, torch.bfloat16, offset_bf16))
+            ob, _, stb = T.attn_fwd_step_bf16(d["q"], d["k"], d["v"], d["cu"], d["cu"], d["cu_pad"], d["cu_pad"],
+                                              step=1, cp_size=w.cp_size, softmax_scale=w.softmax_scale,
+                                              out=_offset_buffer(shape, torch.bfloat16, offset_bf16))
+            of, _, stf = T.attn_fwd_step(d["q"], d["k"], d["v"], d["cu"], d["cu"], d["cu_pad"], d["cu_pad"],
+                                         step=1, cp_size=w.cp_size, softmax_scale=w.softmax_scale,
+                                         out=_offset_buffer(shape, torch.float32, offset_f32))
+            torch.cuda.synchronize()
+            assert int(st.item()) == 0 and int(stb.item()) == 0 and int(stf.item()) == 0
+            return o, ob, of
+
+        a = run(0, 0)
+        b = run(8, 4)  # 16 bytes past a 256-byte aligned allocation
+        assert b[0].data_ptr() % 32 == 16 and b[2].data_ptr() % 32 == 16
+        for x, y in zip(a, b):
+            assert torch.equal(x, y)
+    finally:
+        T.thd_test_select_fwd_kernel(0)
+
+
 def test_backward_into_16_byte_aligned_buffers_is_bit_identical():
     """dQ/dK/dV buffers aligned to 16 bytes but not 32 (the API's minimum):
     the kernels then write rows with 16-byte stores instead of 32-byte ones;
@@ -105,11 +146,8 @@ def test_backward_into_16_byte_aligned_buffers_is_bit_identical():
                             softmax_scale=w.softmax_scale)
 
     def run(offset):
-        out = []
-        for rows, H in ((w.dq_rows, w.Hq), (w.dkv_rows, w.Hkv), (w.dkv_rows, w.Hkv)):
-            n = rows * H * w.D
-            big = torch.full((n + offset,), 7.0, dtype=torch.bfloat16, device="cuda")
-            out.append(big[offset:].view(rows, H, w.D))
+        out = [_offset_buffer((rows, H, w.D), torch.bfloat16, offset)
+               for rows, H in ((w.dq_rows, w.Hq), (w.dkv_rows, w.Hkv), (w.dkv_rows, w.Hkv))]
         dq, dk, dv, st2 = T.attn_bwd(d["q"], d["k"], d["v"], o, lse, d["do"], d["cu"], d["cu"], d["cu_pad"],
                                      d["cu_pad"], cp_size=w.cp_size, softmax_scale=w.softmax_scale,
                                      dq_rows=w.dq_rows, dkv_rows=w.dkv_rows, dq=out[0], dk=out[1], dv=out[2])
@@ -119,6 +157,6 @@ def test_backward_into_16_byte_aligned_buffers_is_bit_identical():
 
     a = run(0)
     b = run(8)  # 8 bf16 = 16 bytes past a 256-byte aligned allocation
-    assert b[1].data_ptr() % 32 == 16
+    assert b[0].data_ptr() % 32 == 16 and b[1].data_ptr() % 32 == 16
     for x, y in zip(a, b):
         assert torch.equal(x, y)
