@@ -158,8 +158,12 @@ def _oracle_item(args):
 
 # The CPU legs time the oracle on whole sequences up to this length; a longer
 # sequence is sampled as the same problem on its first ORACLE_PREFIX tokens
-# (a 131072-token sequence would take the fp64 oracle hours per head).
+# (a 131072-token sequence would take the fp64 oracle hours per head).  The
+# cpu_baseline leg cuts at CPU_BASELINE_PREFIX, so that its sample of the
+# single-sequence workload holds 10-30 s of host work; the reference arm keeps
+# its steps at a few seconds each.
 ORACLE_PREFIX = 4096
+CPU_BASELINE_PREFIX = 8192
 
 
 def _sample_lengths(w, prefix=ORACLE_PREFIX):
@@ -203,11 +207,11 @@ def _spawn_pool(n):
     return mp.get_context("spawn").Pool(n)
 
 
-def cpu_baseline(w, t, target_s=15.0):
+def cpu_baseline(w, t, target_s=15.0, prefix=CPU_BASELINE_PREFIX):
     """Time the oracle (as it stands) on a bounded sample of the workload:
     fwd+bwd of query heads 0, 1, 2, ... over every sequence (long sequences
-    cut to ORACLE_PREFIX tokens), adding batches of heads until about
-    `target_s` seconds of host time (or the whole workload)."""
+    cut to `prefix` tokens), adding batches of heads until about `target_s`
+    seconds of host time (or the whole workload)."""
     cores = os.cpu_count() or 1
     n_seq = max(1, sum(1 for L in w.lengths if L))
     per_batch = max(1, cores // n_seq)
@@ -215,16 +219,16 @@ def cpu_baseline(w, t, target_s=15.0):
     with _spawn_pool(cores) as pool:
         while done < w.Hq and spent < target_s:
             heads = list(range(done, min(w.Hq, done + per_batch)))
-            items = _oracle_items(w, t, heads)
+            items = _oracle_items(w, t, heads, prefix)
             t0 = time.perf_counter()
             pool.map(_oracle_item, items)
             spent += time.perf_counter() - t0
             done += len(heads)
-    flops = _sample_flops(w, list(range(done)))
+    flops = _sample_flops(w, list(range(done)), prefix)
     scope = "all" if done == w.Hq else f"0..{done - 1} of {w.Hq}"
     return {"value": flops / spent / 1e12, "unit": UNIT, "cores": cores, "kind": "oracle",
             "sample": f"fp64 oracle fwd+bwd of query heads {scope} on the '{w.name}' workload: "
-                      f"{_sample_scope(w)} ({spent:.1f} s, process pool of {cores}, one BLAS thread each); "
+                      f"{_sample_scope(w, prefix)} ({spent:.1f} s, process pool of {cores}, one BLAS thread each); "
                       f"TFLOPS counted on the sample's own valid pairs",
             "seconds": spent}
 
