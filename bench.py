@@ -43,6 +43,10 @@ def _args():
     ap.add_argument("--steps", type=int, default=20)
     ap.add_argument("--warmup", type=int, default=5)
     ap.add_argument("--config", default="long", help="tiny|packed|padded|long|fwdbwd (or C1..C5)")
+    ap.add_argument("--lengths", default=None,
+                    help="comma-separated sequence lengths replacing the named workload's (its heads, head "
+                         "dimension, cp size and padding rule kept), e.g. a smaller case of the same kernels "
+                         "for a profiler capture; the workload is then named config[lengths]")
     ap.add_argument("--no-extras", action="store_true",
                     help="time only the named workload (no per_config, HBM-kernel, ring or ABBA keys)")
     ap.add_argument("--impl", default="ours", choices=["ours", "reference"])
@@ -55,6 +59,17 @@ def _args():
                     help="a2a group size: time the step through the emulated Ulysses (a2a = cp) or hierarchical "
                          "a2a+p2p layer (thd_attn_fwd_a2a / thd_attn_bwd_a2a on per-rank shards)")
     return ap.parse_args()
+
+
+def _workload(a):
+    """The named workload, or its --lengths variant (named config[lengths])."""
+    from packed_sequence_context_gb300 import inputs
+    if not a.lengths:
+        return inputs.make_workload(a.config)
+    L = [int(x) for x in a.lengths.split(",") if x.strip()]
+    w = inputs.make_workload(a.config, lengths=L)
+    w.name = f"{a.config}[{','.join(str(x) for x in L)}]"
+    return w
 
 
 def _kernel_traffic(kernel: str, workload: str):
@@ -239,7 +254,7 @@ def run_reference(a):
     if rank != 0:
         return 0
     from packed_sequence_context_gb300 import inputs
-    w = inputs.make_workload(a.config)
+    w = _workload(a)
     t = inputs.make_tensors(w, with_grad=True)
     cores = os.cpu_count() or 1
     n_seq = max(1, sum(1 for L in w.lengths if L))
@@ -441,7 +456,7 @@ def run_ours(a):
     peaks = _peaks()
     peak, peak_sus, hbm, peak_kind = peaks
 
-    w = inputs.make_workload(a.config)
+    w = _workload(a)
     t = inputs.make_tensors(w, with_grad=True)
     # the CPU leg runs first, before this process touches the GPU with work
     cpu = None
@@ -564,7 +579,7 @@ def run_a2a(a):
         raise SystemExit("bench.py needs a CUDA GPU")
     T.lib()
     peak, _, hbm, _ = _peaks()
-    w = inputs.make_workload(a.config)
+    w = _workload(a)
     t = inputs.make_tensors(w, with_grad=True)
     dev = torch.device("cuda", 0)
     cp, A = w.cp_size, a.a2a
