@@ -853,7 +853,9 @@ def run_hbm_kernels(a):
 def _split_copy(dst, src, streams, after):
     """dst.copy_(src) as one slice per copy stream (dimension 0), each slice
     started after the event `after`; returns the events that mark them done.
-    Several host<->device copies in flight use several copy engines."""
+    Several host<->device copies in flight use several copy engines.  A
+    device source is recorded on the copy streams, so that its memory is not
+    handed to a later allocation before the copy has read it."""
     import torch
     n = len(streams)
     rows = src.shape[0]
@@ -865,6 +867,8 @@ def _split_copy(dst, src, streams, after):
         cs.wait_event(after)
         with torch.cuda.stream(cs):
             dst[lo:hi].copy_(src[lo:hi], non_blocking=True)
+        if src.is_cuda:
+            src.record_stream(cs)
         ev = torch.cuda.Event()
         ev.record(cs)
         done.append(ev)
@@ -874,10 +878,17 @@ def _split_copy(dst, src, streams, after):
 def e2e_measure(a, w, t, dev, stream, step_flops):
     """Same metric through the public API with host buffers: every step, the
     pinned H2D of its inputs and metadata, the calls, and the D2H of O, lse,
-    dQ, dK, dV, all inside the events.  Copies run on four copy streams, one
-    slice each (q, k, v before the forward; dO during the forward; O and lse
-    during the backward; dQ, dK, dV after it); the compute stream waits for
-    the copies it needs and, before the closing event, for every D2H."""
+    dQ, dK, dV, all inside the timed region.  Copies run on four copy
+    streams, one slice of each tensor per stream.
+
+    The value is a pipelined run of K steps, the way a training loop feeds
+    the library: two device input buffers, step i+1's inputs uploaded while
+    step i computes (once step i-1, the buffer's last reader, is done), step
+    i's outputs downloaded while step i+1 computes; the events open before
+    the first upload and close after the last download.  `serial` is the
+    same step with each step's copies and calls alone between its events
+    (inputs before the forward, dO during it, O and lse during the backward,
+    gradients after it)."""
     import torch
 
     from packed_sequence_context_gb300 import thd_attn as T
@@ -885,61 +896,105 @@ def e2e_measure(a, w, t, dev, stream, step_flops):
     host = {x: t[x].pin_memory() for x in ("q", "k", "v", "do")}
     cu_h = torch.from_numpy(w.cu_seqlens).pin_memory()
     cup_h = torch.from_numpy(w.cu_seqlens_padded).pin_memory()
-    dev_in = {x: torch.empty_like(host[x], device=dev) for x in host}
-    cu_d = torch.empty_like(cu_h, device=dev)
-    cup_d = torch.empty_like(cup_h, device=dev)
+    bufs = []
+    for _ in range(2):
+        b = {x: torch.empty_like(host[x], device=dev) for x in host}
+        b["cu"] = torch.empty_like(cu_h, device=dev)
+        b["cup"] = torch.empty_like(cup_h, device=dev)
+        bufs.append(b)
     copy_streams = [torch.cuda.Stream(device=dev) for _ in range(4)]
     h2d = sum(x.numel() * x.element_size() for x in host.values()) + 2 * cu_h.numel() * 4
     n = max(3, min(a.steps, 20))
-    evs = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)) for _ in range(n + 2)]
-    host_out = None
-    times = []
+    out_shapes = [((w.T, w.Hq, w.D), torch.bfloat16), ((w.Hq, w.T), torch.float32)]
+    if not a.fwd_only:
+        out_shapes += [((w.dq_rows, w.Hq, w.D), torch.bfloat16), ((w.dkv_rows, w.Hkv, w.D), torch.bfloat16),
+                       ((w.dkv_rows, w.Hkv, w.D), torch.bfloat16)]
+    host_out = [torch.empty(shape, dtype=dt, pin_memory=True) for shape, dt in out_shapes]
+    d2h_bytes = sum(x.numel() * x.element_size() for x in host_out)
 
     def wait_all(events):
         for ev in events:
             stream.wait_event(ev)
 
-    for i, (e0, e1) in enumerate(evs):
-        e0.record(stream)
-        cu_d.copy_(cu_h, non_blocking=True)
-        cup_d.copy_(cup_h, non_blocking=True)
+    def upload(b, after):
+        """H2D of one step's inputs into buffer b; returns (q/k/v/metadata events, dO events)."""
+        ev = []
+        with torch.cuda.stream(copy_streams[0]):
+            copy_streams[0].wait_event(after)
+            b["cu"].copy_(cu_h, non_blocking=True)
+            b["cup"].copy_(cup_h, non_blocking=True)
+            e = torch.cuda.Event()
+            e.record(copy_streams[0])
+            ev.append(e)
         for x in ("q", "k", "v"):
-            wait_all(_split_copy(dev_in[x], host[x], copy_streams, e0))
-        do_done = [] if a.fwd_only else _split_copy(dev_in["do"], host["do"], copy_streams, e0)
-        o, lse, st = T.attn_fwd(dev_in["q"], dev_in["k"], dev_in["v"], cu_d, cu_d, cup_d, cup_d,
+            ev += _split_copy(b[x], host[x], copy_streams, after)
+        do_ev = [] if a.fwd_only else _split_copy(b["do"], host["do"], copy_streams, after)
+        return ev, do_ev
+
+    def compute(b, in_ev, do_ev):
+        """The calls on the compute stream, then the D2H of their results;
+        returns (the event after the step's last call, the D2H events)."""
+        wait_all(in_ev)
+        o, lse, st = T.attn_fwd(b["q"], b["k"], b["v"], b["cu"], b["cu"], b["cup"], b["cup"],
                                 cp_size=w.cp_size, softmax_scale=w.softmax_scale)
         fwd_done = torch.cuda.Event()
         fwd_done.record(stream)
-        res = [o, lse]
-        if host_out is None:
-            shapes = [o, lse]
-            if not a.fwd_only:
-                shapes += [torch.empty((w.dq_rows, w.Hq, w.D), dtype=o.dtype),
-                           torch.empty((w.dkv_rows, w.Hkv, w.D), dtype=o.dtype),
-                           torch.empty((w.dkv_rows, w.Hkv, w.D), dtype=o.dtype)]
-            host_out = [torch.empty(r.shape, dtype=r.dtype, pin_memory=True) for r in shapes]
         d2h = _split_copy(host_out[0], o, copy_streams, fwd_done) + \
             _split_copy(host_out[1], lse, copy_streams, fwd_done)
+        last = fwd_done
         if not a.fwd_only:
-            wait_all(do_done)
-            dq, dk, dv, st2 = T.attn_bwd(dev_in["q"], dev_in["k"], dev_in["v"], o, lse, dev_in["do"], cu_d, cu_d,
-                                         cup_d, cup_d, cp_size=w.cp_size, softmax_scale=w.softmax_scale,
+            wait_all(do_ev)
+            dq, dk, dv, st2 = T.attn_bwd(b["q"], b["k"], b["v"], o, lse, b["do"], b["cu"], b["cu"], b["cup"],
+                                         b["cup"], cp_size=w.cp_size, softmax_scale=w.softmax_scale,
                                          dq_rows=w.dq_rows, dkv_rows=w.dkv_rows)
-            bwd_done = torch.cuda.Event()
-            bwd_done.record(stream)
+            last = torch.cuda.Event()
+            last.record(stream)
             for hd, r in zip(host_out[2:], (dq, dk, dv)):
-                d2h += _split_copy(hd, r, copy_streams, bwd_done)
-            res += [dq, dk, dv]
+                d2h += _split_copy(hd, r, copy_streams, last)
+        return last, d2h
+
+    # serial: each step alone between its events
+    serial = []
+    for i in range(n + 2):
+        e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+        e0.record(stream)
+        in_ev, do_ev = upload(bufs[0], e0)
+        _, d2h = compute(bufs[0], in_ev, do_ev)
         wait_all(d2h)
         e1.record(stream)
         stream.synchronize()
         if i >= 2:
-            times.append(e0.elapsed_time(e1))
-    d2h_bytes = sum(x.numel() * x.element_size() for x in host_out)
-    ms = sum(times) / len(times)
+            serial.append(e0.elapsed_time(e1))
+
+    # pipelined: n steps in flight through two input buffers
+    def pipelined(steps):
+        e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+        e0.record(stream)
+        pending = [upload(bufs[0], e0)]
+        done, d2h_all = [], []
+        for i in range(steps):
+            if i + 1 < steps:   # the next step's buffer is free once step i-1 is done
+                pending.append(upload(bufs[(i + 1) % 2], done[i - 1] if i >= 1 else e0))
+            last, d2h = compute(bufs[i % 2], *pending[i])
+            done.append(last)
+            d2h_all += d2h
+        wait_all(d2h_all)
+        e1.record(stream)
+        stream.synchronize()
+        return e0.elapsed_time(e1) / steps
+
+    pipelined(3)   # warm-up
+    ms = pipelined(n)
+    ms_serial = sum(serial) / len(serial)
     return {"value": step_flops / (ms * 1e-3) / 1e12, "unit": UNIT, "ms_per_step": ms,
             "h2d_bytes_per_step": int(h2d), "d2h_bytes_per_step": int(d2h_bytes),
-            "copies": "4 copy streams, one slice each per tensor; dO overlaps the forward, O and lse the backward"}
+            "steps": n,
+            "copies": ("pipelined: step i+1's inputs uploaded and step i-1's outputs downloaded while step i "
+                       "computes (two device input buffers, 4 copy streams, one slice each per tensor); the "
+                       "events open before the first upload and close after the last download"),
+            "serial": {"value": step_flops / (ms_serial * 1e-3) / 1e12, "ms_per_step": ms_serial,
+                       "copies": "each step alone: q/k/v before the forward, dO during it, O and lse during "
+                                 "the backward, dQ/dK/dV after it"}}
 
 
 def main():
