@@ -383,7 +383,9 @@ __global__ void __launch_bounds__(kGrouped ? 352 : 384, 1)
             mma_ts(tmem + C::kColDV, pcol + 64 * (ks >> 2) + 8 * (ks & 3), sdesc_sw128(dob + ks * 2048, 16384, 1024),
                    idesc_kv, (pv_first && ks == 0) ? 0u : 1u);
           tc_commit(&bar_do_empty[pv_stage]);
-          tc_commit(bar_dk_done);  // both of the step's products (this thread's MMAs complete in order)
+          // the item's last step: dk_done completes once per item, when every
+          // product of the item has (this thread's MMAs complete in order)
+          if (last) tc_commit(bar_dk_done);
           pv_stage = -1;
           return true;
         };
@@ -413,9 +415,9 @@ __global__ void __launch_bounds__(kGrouped ? 352 : 384, 1)
               return;
             }
             // dP^T = V dO^T -> the buffer P^T(s-1) and dS^T(s-1) leave once dV(s-1)
-            // and dK(s-1) have read them
-            if ((su > 0 && !mbar_wait(bar_dk_done, (su - 1) & 1u, s_abort)) ||
-                !mbar_wait(&bar_do_full[stage], ph, s_abort)) {
+            // and dK(s-1) have read them: this thread issued those just before,
+            // and the tensor pipe executes one thread's MMAs in issue order
+            if (!mbar_wait(&bar_do_full[stage], ph, s_abort)) {
               ok = false;
               return;
             }
@@ -459,7 +461,7 @@ __global__ void __launch_bounds__(kGrouped ? 352 : 384, 1)
     // dK/dV rows start at multiples of 128 bytes: with 32-byte aligned buffers
     // the epilogue stores whole 32-byte sectors (the API asks for 16)
     const bool v8_ok = ((reinterpret_cast<uintptr_t>(p.dk) | reinterpret_cast<uintptr_t>(p.dv)) & 31u) == 0;
-    uint32_t su = 0;
+    uint32_t su = 0, n_done = 0;
     bool ok = true;
     for (uint32_t kit = 0; ok; ++kit) {
       int w;
@@ -585,7 +587,8 @@ __global__ void __launch_bounds__(kGrouped ? 352 : 384, 1)
       // ---- epilogue: dK (scaled) and dV of this key tile, zeros on pad rows,
       // once the item's last dK (and with it every product before) completed
       if (nsteps > 0) {
-        if (!mbar_wait(bar_dk_done, (su - 1) & 1u, s_abort)) break;
+        if (!mbar_wait(bar_dk_done, n_done & 1u, s_abort)) break;  // one phase per item with steps
+        ++n_done;
         tc_fence_after();
       }
 #pragma unroll 1
