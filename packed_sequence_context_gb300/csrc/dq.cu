@@ -26,12 +26,13 @@
 //   warp 8     producer: gathers the item's Q and dO rows (cp.async) and
 //              issues the K tile TMA loads into a 3-slot ring
 //   warp 10    producer of the V tiles (2-slot ring)
-//   warp 9     TMEM allocator and S = Q K^T issuer (one thread)
-//   warp 11    dP = dO V^T and dQ += dS K issuer (one thread)
+//   warp 9     TMEM allocator, S = Q K^T and dQ += dS K issuer (one thread)
+//   warp 11    dP = dO V^T issuer (one thread)
 // TMEM: S buffers [0,128) and [128,256), dP [256,384), dQ [384, 384+D).  A K
 // slot is read by S of its tile and by dQ of that tile, so it frees after the
-// dQ product; S buffer b is overwritten once the dQ product that read its dS
-// has completed (s_free).
+// dQ product; S buffer b is overwritten by an S issued after the dQ that read
+// its dS, by the same thread (the tensor pipe runs one thread's MMAs in issue
+// order).
 #include "common.cuh"
 #include "ptx.cuh"
 #include "sched.cuh"
@@ -71,7 +72,6 @@ __global__ void __launch_bounds__(384, 1)
   __shared__ __align__(8) uint64_t bar_v_full[VS];
   __shared__ __align__(8) uint64_t bar_v_empty[VS];
   __shared__ __align__(8) uint64_t bar_s_full[2];
-  __shared__ __align__(8) uint64_t bar_s_free[2];
   __shared__ __align__(8) uint64_t bar_ds_ready[2];
   __shared__ __align__(8) uint64_t bar_dp_full;
   __shared__ __align__(8) uint64_t bar_dp_free;  // the dS warps have read dP into registers
@@ -100,7 +100,6 @@ __global__ void __launch_bounds__(384, 1)
     }
     for (int s = 0; s < 2; ++s) {
       mbar_init(&bar_s_full[s], 1);
-      mbar_init(&bar_s_free[s], 1);
       mbar_init(&bar_ds_ready[s], 8);  // one arrival per dS warp
     }
     mbar_init(&bar_dp_full, 1);
@@ -239,69 +238,21 @@ __global__ void __launch_bounds__(384, 1)
       }
       __syncwarp();
     } else if (warp == 9) {
-      // ------------------------------------------------------------ S = Q K^T issuer
+      // ------------------------------------------------------------ S = Q K^T and dQ += dS K issuer
       // Two issuing threads, as in the forward: a barrier wait in one does not
       // leave the tensor pipe idle while the other has products to issue.
-      if (lane == 0) {
-        const uint64_t qdesc = sdesc_sw128(smem_u32(sQ), 16, 1024);
-        const uint64_t kdesc = sdesc_sw128(smem_u32(sK), 16, 1024);
-        int ks = 0;
-        uint32_t kph = 0, g = 0, q_iter = 0;
-        bool ok = true;
-        for (uint32_t kit = 0; ok; ++kit) {
-          int w;
-          if (!item_take_one(&ring, kit, w, &s_abort) || w >= n_items) break;
-          const QItem it = q_item<kGrouped>(p, n_entries, w);
-          int n = 0;
-          for_each_kv_tile(it, p, [&](int, int) { ++n; });
-          if (!mbar_wait(&bar_q_full, q_iter & 1u, &s_abort)) break;
-          ++q_iter;
-          tc_fence_after();
-          if (n == 0) tc_commit(&bar_q_empty);
-          int j = 0;
-          for_each_kv_tile(it, p, [&](int c, int jt) {
-            if (!ok) return;
-            const int ncols = q_tile_ncols(it, p, c, jt);
-            const uint32_t b = g & 1u;
-            if (!mbar_wait(&bar_k_full[ks], kph, &s_abort) ||
-                (g >= 2 && !mbar_wait(&bar_s_free[b], ((g >> 1) - 1) & 1u, &s_abort))) {
-              ok = false;
-              return;
-            }
-            tc_fence_after();
-            const uint32_t idesc_s = idesc_bf16(128, ncols, false, false);
-            const uint64_t kd = kdesc + (uint64_t)((ks * C::kKVBytes) >> 4);
-#pragma unroll
-            for (int kk = 0; kk < D / 16; ++kk) {
-              const uint64_t off = (uint64_t)(((kk >> 2) * 16384 + (kk & 3) * 32) >> 4);
-              mma_ss(tmem + b * 128u, qdesc + off, kd + off, idesc_s, kk > 0 ? 1u : 0u);
-            }
-            tc_commit(&bar_s_full[b]);
-            if (++j == n) tc_commit(&bar_q_empty);  // the item's last read of Q
-            if (++ks == KS) {
-              ks = 0;
-              kph ^= 1u;
-            }
-            ++g;
-          });
-        }
-        tc_commit(&bar_drain);
-        drain_wait(&bar_drain, 0);
-      }
-      __syncwarp();
-    } else if (warp == 11) {
-      // ------------------------------------------------------------ dP = dO V^T and dQ += dS K issuer
-      // Per tile g: once the dS warps have read dP of tile g-1 into registers
-      // (dp_free: early in their work on g-1), dP of tile g -- so it is ready
-      // when they come to g -- then, once their dS of g-1 is in TMEM, dQ of
-      // tile g-1.  The item's last dQ follows its last dS.
+      // This one issues, per tile g of an item, S(g) and then dQ(g-1) once the
+      // dS warps have written dS(g-1) (ds_ready): S(g+1) thus follows dQ(g-1)
+      // at once and is ready one tile ahead.  S(g) goes into S buffer g % 2,
+      // whose dS(g-2) the dQ(g-2) issued before it by this same thread reads:
+      // the tensor pipe runs one thread's MMAs in issue order, so no wait.
       if (lane == 0) {
         constexpr uint32_t idesc_dq = idesc_bf16(128, D, false, true);
-        const uint64_t dodesc = sdesc_sw128(smem_u32(sDO), 16, 1024);
-        const uint64_t vdesc = sdesc_sw128(smem_u32(sV), 16, 1024);
+        const uint64_t qdesc = sdesc_sw128(smem_u32(sQ), 16, 1024);
+        const uint64_t kdesc = sdesc_sw128(smem_u32(sK), 16, 1024);
         const uint64_t kmn = sdesc_sw128(smem_u32(sK), 16384, 1024);  // K read MN-major
-        int vs = 0;
-        uint32_t vph = 0, g = 0, q_iter = 0;
+        int ks = 0;
+        uint32_t kph = 0, g = 0, q_iter = 0;
         bool ok = true;
         // issue dQ += dS K for tile gg (its dS in S buffer gg % 2, its K in ring slot gg % KS)
         auto issue_dq = [&](uint32_t gg, int ncols, bool first) -> bool {
@@ -314,8 +265,7 @@ __global__ void __launch_bounds__(384, 1)
           for (int kk = 0; kk < ncols / 16; ++kk)
             mma_ts(tmem + C::kColDQ, tmem + b * 128u + 64 * (kk >> 2) + 8 * (kk & 3),
                    kd + (uint64_t)(kk * (2048 >> 4)), idesc_dq, (first && kk == 0) ? 0u : 1u);
-          tc_commit(&bar_s_free[b]);
-          tc_commit(&bar_k_empty[kslot]);
+          tc_commit(&bar_k_empty[kslot]);  // the K slot's last reader
           return true;
         };
         for (uint32_t kit = 0; ok; ++kit) {
@@ -335,12 +285,72 @@ __global__ void __launch_bounds__(384, 1)
           for_each_kv_tile(it, p, [&](int c, int jt) {
             if (!ok) return;
             const int ncols = q_tile_ncols(it, p, c, jt);
-            // the dP buffer is free once the dS warps have read tile g-1's dP
-            if (g > 0 && !mbar_wait(&bar_dp_free, (g - 1) & 1u, &s_abort)) {
+            const uint32_t b = g & 1u;
+            if (!mbar_wait(&bar_k_full[ks], kph, &s_abort)) {
               ok = false;
               return;
             }
-            if (!mbar_wait(&bar_v_full[vs], vph, &s_abort)) {
+            tc_fence_after();
+            const uint32_t idesc_s = idesc_bf16(128, ncols, false, false);
+            const uint64_t kd = kdesc + (uint64_t)((ks * C::kKVBytes) >> 4);
+#pragma unroll
+            for (int kk = 0; kk < D / 16; ++kk) {
+              const uint64_t off = (uint64_t)(((kk >> 2) * 16384 + (kk & 3) * 32) >> 4);
+              mma_ss(tmem + b * 128u, qdesc + off, kd + off, idesc_s, kk > 0 ? 1u : 0u);
+            }
+            tc_commit(&bar_s_full[b]);
+            if (j == n - 1) tc_commit(&bar_q_empty);  // the item's last read of Q
+            if (++ks == KS) {
+              ks = 0;
+              kph ^= 1u;
+            }
+            if (j > 0 && !issue_dq(g - 1, prev_cols, j == 1)) {
+              ok = false;
+              return;
+            }
+            prev_cols = ncols;
+            ++g;
+            ++j;
+          });
+          if (!ok) break;
+          if (!issue_dq(g - 1, prev_cols, n == 1)) break;
+          tc_commit(&bar_dq_done);
+        }
+        tc_commit(&bar_drain);
+        drain_wait(&bar_drain, 0);
+      }
+      __syncwarp();
+    } else if (warp == 11) {
+      // ------------------------------------------------------------ dP = dO V^T issuer
+      // Per tile g: once the dS warps have read dP of tile g-1 into registers
+      // (dp_free: early in their work on g-1), dP of tile g -- so it is ready
+      // when they come to g.
+      if (lane == 0) {
+        const uint64_t dodesc = sdesc_sw128(smem_u32(sDO), 16, 1024);
+        const uint64_t vdesc = sdesc_sw128(smem_u32(sV), 16, 1024);
+        int vs = 0;
+        uint32_t vph = 0, g = 0, q_iter = 0;
+        bool ok = true;
+        for (uint32_t kit = 0; ok; ++kit) {
+          int w;
+          if (!item_take_one(&ring, kit, w, &s_abort) || w >= n_items) break;
+          const QItem it = q_item<kGrouped>(p, n_entries, w);
+          int n = 0;
+          for_each_kv_tile(it, p, [&](int, int) { ++n; });
+          if (!mbar_wait(&bar_q_full, q_iter & 1u, &s_abort)) break;
+          ++q_iter;
+          tc_fence_after();
+          if (n == 0) {
+            tc_commit(&bar_q_empty);
+            continue;
+          }
+          int j = 0;
+          for_each_kv_tile(it, p, [&](int c, int jt) {
+            if (!ok) return;
+            const int ncols = q_tile_ncols(it, p, c, jt);
+            // the dP buffer is free once the dS warps have read tile g-1's dP
+            if ((g > 0 && !mbar_wait(&bar_dp_free, (g - 1) & 1u, &s_abort)) ||
+                !mbar_wait(&bar_v_full[vs], vph, &s_abort)) {
               ok = false;
               return;
             }
@@ -359,17 +369,9 @@ __global__ void __launch_bounds__(384, 1)
               vs = 0;
               vph ^= 1u;
             }
-            if (j > 0 && !issue_dq(g - 1, prev_cols, j == 1)) {
-              ok = false;
-              return;
-            }
-            prev_cols = ncols;
             ++g;
             ++j;
           });
-          if (!ok) break;
-          if (!issue_dq(g - 1, prev_cols, n == 1)) break;
-          tc_commit(&bar_dq_done);
         }
         tc_commit(&bar_drain2);
         drain_wait(&bar_drain2, 0);
