@@ -45,3 +45,17 @@ def test_a2a_bytes_from_tensor_shapes():
     backward = 2 * (3 * q.nbytes + 2 * kv.nbytes) + 2 * (q.nbytes + 2 * kv.nbytes)   # in: q, O, dO; k, v. out
     step = forward + backward
     assert bench.a2a_step_bytes(T, Hq, Hkv, D) == step
+
+
+def test_lengths_override_keeps_the_workload_shape_and_renames_it():
+    """bench.py --lengths: the named workload's heads, head dimension and cp
+    size on other sequence lengths, under a name of its own (so that no
+    per-workload record of the named workload applies to it)."""
+    import argparse
+    a = argparse.Namespace(config="long", lengths="32768")
+    w = bench._workload(a)
+    assert w.name == "long[32768]" and w.lengths == [32768] and w.T == 32768
+    assert (w.Hq, w.Hkv, w.D, w.cp_size) == (32, 8, 128, 4)
+    assert bench._kernel_traffic("bwd_kernel", w.name) is None
+    a = argparse.Namespace(config="long", lengths=None)
+    assert bench._workload(a).name == "long" and bench._workload(a).T == 131072
