@@ -294,8 +294,8 @@ __global__ void __launch_bounds__(kGrouped ? 352 : 384, 1)
       //   warp 9:  S^T(s), as soon as the compute warps hold dP^T(s-1), which sat
       //            in the same buffer, in registers (y_free)
       //   warp 10: once the compute warps have written P^T(s-1) and dS(s-1),
-      //            dK(s-1) and dV(s-1); then, at once, dP^T(s) into the buffer
-      //            they read (this thread's MMAs run in issue order).
+      //            dV(s-1) and dK(s-1); then dP^T(s) into the buffer P^T(s-1)
+      //            leaves once dV(s-1) has read it.
       // The compute warps of step s compute P from S^T(s) while dV/dK(s-1) run
       // and dS once dP^T(s) is there.  P^T(s) and dS^T(s) both go back over
       // S^T(s) as packed bf16 (each thread into the S^T columns it has read) and
